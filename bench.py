@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the GDN mixer core on one GB300 (or N replicas under torchrun).
+
+Prints ONE JSON line.  The headline is prefill tokens/s on the T=4096,
+Hk=16, Hv=32, d_k=d_v=128 bf16 workload ("value"); the same line carries
+decode tokens/s (256 sequences x 1 token), the packed variable-length prefill
+(16 sequences, lengths U{128..8192}) and the speculative-verify decode
+(64 sequences x 4 tokens, every intermediate state emitted), each with its
+roofline against the measured peaks, the dominant kernel's per-launch time from
+CUDA events recorded by libgdn on the launching stream, and an end-to-end
+figure through the public API with pinned host buffers.
+
+``--impl reference`` times the CPU oracle instead (the only baseline: the pages
+publish no GPU implementation of this core), on a bounded sample per step.
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and a
+device synchronize; a 256 MiB buffer (2x L2) is written between timed steps
+and each step is bracketed by CUDA events on the launching stream.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------- workloads
+# Algorithmic bytes: what the core must read and write at minimum (inputs once,
+# outputs once, states once each way).  Activations are bf16.
+
+def _act_bytes_per_token(c):
+    cd, vd, hv = c.conv_dim, c.n_v_heads * c.d_v, c.n_v_heads
+    return 2 * (cd + vd + 2 * hv + vd)  # x, z, a, b in; out
+
+
+def _state_bytes(c):
+    return 4 * c.n_v_heads * c.d_k * c.d_v
+
+
+def _conv_state_bytes(c):
+    return 2 * c.conv_dim * (c.conv_k - 1)
+
+
+WORKLOADS = {
+    # key: (config index, description)
+    "prefill": 1,
+    "decode": 2,
+    "varlen": 3,
+    "spec_verify": 4,
+}
+
+
+class Runner:
+    """Holds device buffers of one workload and runs one step of it."""
+
+    def __init__(self, key, case, device):
+        import torch
+        import gated_deltanet_linear_mixer_gb300 as gdn
+        self.key, self.case, self.dev = key, case, device
+        self.gdn, self.torch = gdn, torch
+        c = case
+        self.d = gdn.Dims(c.n_k_heads, c.n_v_heads, c.d_k, c.d_v, c.conv_k, torch.bfloat16, c.act)
+        bf = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.bfloat16)  # noqa: E731
+        f32 = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.float32)  # noqa: E731
+        self.x, self.z, self.a, self.b = bf(c.x), bf(c.z), bf(c.a), bf(c.b)
+        self.params = gdn.Params(f32(c.conv_w), f32(c.A_log), f32(c.dt_bias), f32(c.norm_w))
+        n = c.n_seq
+        self.cu_host = torch.from_numpy(c.cu_seqlens.copy())
+        self.cu_dev = self.cu_host.to(device)
+        vd = c.n_v_heads * c.d_v
+        self.out = torch.empty((c.n_tokens, vd), dtype=torch.bfloat16, device=device)
+        self.state0 = None if c.state is None else f32(c.state)
+        self.state = None if c.state is None else self.state0.clone()
+        self.conv0 = None if c.conv_state is None else bf(c.conv_state)
+        self.conv = None if c.conv_state is None else self.conv0.clone()
+        self.final = torch.empty((n, c.n_v_heads, c.d_k, c.d_v), device=device)
+        self.conv_out = torch.empty((n, c.conv_dim, c.conv_k - 1), dtype=torch.bfloat16, device=device)
+        self.inter = None
+        if key == "spec_verify":
+            self.inter = torch.empty((n, c.tokens_per_seq, c.n_v_heads, c.d_k, c.d_v), device=device)
+        ws = gdn.prefill_workspace_size(self.d, self.cu_host) if c.mode == "prefill" else 0
+        self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
+
+    # -- one step through the public API (device-resident inputs)
+    def step(self):
+        gdn, c = self.gdn, self.case
+        if c.mode == "prefill":
+            gdn.prefill(self.d, self.params, (self.cu_dev, self.cu_host), self.x, self.z, self.a,
+                        self.b, initial_state=self.state0, final_state=self.final,
+                        conv_state_in=None, conv_state_out=self.conv_out, out=self.out,
+                        workspace=self.ws)
+        else:
+            n, t = c.n_seq, c.tokens_per_seq
+            gdn.decode(self.d, self.params, self.x.view(n, t, -1), self.z.view(n, t, -1),
+                       self.a.view(n, t, -1), self.b.view(n, t, -1), self.state, self.conv,
+                       self.inter, self.out.view(n, t, -1))
+
+    @property
+    def tokens(self):
+        return self.case.n_tokens
+
+    def algorithmic_bytes(self):
+        c = self.case
+        act = _act_bytes_per_token(c) * c.n_tokens
+        n = c.n_seq
+        if self.key == "prefill":      # zero initial state (not read); final state + conv state out
+            return act + n * (_state_bytes(c) + _conv_state_bytes(c))
+        if self.key == "varlen":       # initial state in, final state out, conv state out
+            return act + n * (2 * _state_bytes(c) + _conv_state_bytes(c))
+        if self.key == "decode":       # state and conv state read and written in place
+            return act + n * (2 * _state_bytes(c) + 2 * _conv_state_bytes(c))
+        if self.key == "spec_verify":  # state read once, T states written, conv state read
+            return act + n * ((1 + c.tokens_per_seq) * _state_bytes(c) + _conv_state_bytes(c))
+        raise KeyError(self.key)
+
+    def kernel_bytes(self, name):
+        """Algorithmic bytes of one launch of kernel `name` (for the roofline).
+
+        The conv-state kernel moves the K-1 history rows; every other kernel of
+        a step is charged the rest of the step's algorithmic bytes."""
+        c = self.case
+        conv = c.n_seq * _conv_state_bytes(c)
+        hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0}[self.key]
+        if name == "conv_state":
+            return hist
+        return self.algorithmic_bytes() - hist
+
+    def useful_flops(self, chunk=64):
+        """Useful flops of the chunked form per step (prefill), else of the recurrence."""
+        c = self.case
+        dk, dv = c.d_k, c.d_v
+        if c.mode == "prefill":
+            per_tok_head = 6 * dk * dv + chunk * (3 * dk + 2 * dv) + chunk * chunk / 3
+        else:
+            per_tok_head = 5 * dk * dv
+        return per_tok_head * c.n_v_heads * c.n_tokens
+
+    # -- end to end: pinned host buffers, H2D of the step's inputs, the call,
+    # D2H of the step's outputs.
+    def setup_e2e(self):
+        torch = self.torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
+        self.h_in = [pin(t) for t in (self.x, self.z, self.a, self.b)]
+        self.d_in = [self.x, self.z, self.a, self.b]
+        # the step's result read back by the caller: the mixer output (states
+        # stay resident on the device for the next call)
+        outs = [self.out]
+        self.d_out = outs
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def e2e_step(self):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        for d, h in zip(self.d_out, self.h_out):
+            h.copy_(d, non_blocking=True)
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.samples, self.proc = index, [], None
+        self._thr = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._thr = threading.Thread(target=self._read, daemon=True)
+        self._thr.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        rows = [p for (ts, p) in self.samples if (t0 is None or ts >= t0) and (t1 is None or ts <= t1)]
+        if not rows:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        busy = [r for r in rows if (num(r[3]) or 0) >= 50] or rows
+        sm = [num(r[0]) for r in busy if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(busy)}
+
+
+# -------------------------------------------------------------------- timing
+
+def _flush(buf):
+    buf.add_(1)
+
+
+def time_steps(fn, steps, warmup, flush_buf, stream, barrier):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        _flush(flush_buf)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def cpu_baseline(key, case, max_seconds=10.0):
+    """Time the CPU oracle as it stands on a bounded sample of the workload."""
+    import oracle
+    od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act)
+    cu = case.cu_seqlens
+    if case.mode == "prefill":
+        # leading tokens of the first sequence, with its initial state
+        take = min(int(cu[1] - cu[0]), 256)
+        sl = slice(0, take)
+        args = ([0, take], case.x[sl], case.z[sl], case.a[sl], case.b[sl])
+        st = None if case.state is None else case.state[:1]
+        cs = None if case.conv_state is None else case.conv_state[:1]
+        sample = f"first {take} tokens of sequence 0 (all {case.n_v_heads} heads)"
+        tokens = take
+    else:
+        nseq = min(case.n_seq, 16)
+        t = case.tokens_per_seq
+        rows = slice(0, nseq * t)
+        args = (cu[:nseq + 1], case.x[rows], case.z[rows], case.a[rows], case.b[rows])
+        st = case.state[:nseq]
+        cs = None if case.conv_state is None else case.conv_state[:nseq]
+        sample = f"{nseq} of {case.n_seq} sequences x {t} tokens"
+        tokens = nseq * t
+    times = []
+    t_end = time.time() + max_seconds
+    while len(times) < 3 and (not times or time.time() < t_end):
+        t0 = time.perf_counter()
+        oracle.gdn(od, args[0], *args[1:], case.conv_w, case.A_log, case.dt_bias, case.norm_w,
+                   cs, st, want_inter=(key == "spec_verify"))
+        times.append(time.perf_counter() - t0)
+    med = statistics.median(times)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": tokens / med, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample + f", f64 C oracle with OpenMP over (sequence, value head), "
+                               f"median of {len(times)} runs"}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    import gated_deltanet_linear_mixer_gb300 as gdn
+    from gated_deltanet_linear_mixer_gb300 import _build, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier()
+    gdn.load()
+    peaks = _peaks()
+    stream = torch.cuda.current_stream(device)
+    flush_buf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    sampler = ClockSampler(index=local)
+    sampler.start()
+
+    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify") if k in args.extras]
+    results = {}
+    total_launches = 0
+    for key in keys:
+        case = workloads.config(WORKLOADS[key])
+        r = Runner(key, case, device)
+        t_start = time.time()
+        gdn.timing_enable(True)
+        ms = time_steps(r.step, args.steps, args.warmup, flush_buf, stream, barrier)
+        rep = gdn.timing_report()
+        gdn.timing_enable(False)
+        t_stop = time.time()
+        # timing_report counts warm-up launches too: scale to the timed steps
+        per_step_launch = {k: v[0] / (args.steps + args.warmup) for k, v in rep.items()}
+        launches = int(round(sum(per_step_launch.values()) * args.steps))
+        mean_ms = statistics.mean(ms)
+        t_max = mean_ms
+        if world > 1:
+            tt = torch.tensor([mean_ms], device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_max = float(tt.item())
+        tok_s = world * r.tokens / (t_max / 1e3)
+        # dominant kernel: largest total time
+        dom = max(rep.items(), key=lambda kv: kv[1][1])
+        dom_name, (dom_n, dom_ms) = dom
+        dom_avg_ms = dom_ms / dom_n
+        kb = r.kernel_bytes(dom_name)
+        achieved = kb / (dom_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": kb,
+                "kernel_ms": dom_avg_ms,
+                "kernel_share": dom_ms / sum(v[1] for v in rep.values())}
+        step_bytes = r.algorithmic_bytes()
+        res = {
+            "value": tok_s, "unit": UNIT, "ms_per_step": t_max,
+            "config": {"workload": case.name, "n_seq": case.n_seq, "tokens": r.tokens,
+                       "Hk": case.n_k_heads, "Hv": case.n_v_heads, "d_k": case.d_k,
+                       "d_v": case.d_v, "K": case.conv_k, "act": case.act,
+                       "l2": "256 MiB buffer written between timed steps"},
+            "roofline": roof,
+            "step_hbm": {"algorithmic_bytes": step_bytes,
+                         "achieved_gbs": step_bytes / (t_max / 1e3) / 1e9,
+                         "frac": step_bytes / (t_max / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "kernels": {k: {"launches_per_step": per_step_launch[k], "ms_per_launch": v[1] / v[0]}
+                        for k, v in rep.items()},
+            "gpu_launches": launches,
+            "clocks": sampler.summary(t_start, t_stop),
+        }
+        if case.mode == "prefill":
+            fl = r.useful_flops()
+            res["roofline_tensor"] = {
+                "useful_flops_per_step": fl, "chunk": 64,
+                "achieved_tflops": fl / (t_max / 1e3) / 1e12,
+                "peak": peaks["bf16_tflops"],
+                "frac": fl / (t_max / 1e3) / 1e12 / peaks["bf16_tflops"]}
+        # end to end through the public API with host buffers
+        r.setup_e2e()
+        e2e_ms = time_steps(r.e2e_step, max(2, args.steps // 2), 1, flush_buf, stream, barrier)
+        e2e_mean = statistics.mean(e2e_ms)
+        if world > 1:
+            tt = torch.tensor([e2e_mean], device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_mean = float(tt.item())
+        res["e2e"] = {"value": world * r.tokens / (e2e_mean / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": r.h2d, "d2h_bytes_per_step": r.d2h,
+                      "ms_per_step": e2e_mean}
+        if rank == 0 and not args.no_cpu_baseline and key in ("prefill", "decode"):
+            res["cpu_baseline"] = cpu_baseline(key, case)
+        results[key] = res
+        total_launches += launches
+        del r
+        torch.cuda.empty_cache()
+    sampler.stop()
+
+    head = results["prefill"]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": dict(head["config"], parallelism="replicas" if world > 1 else "single",
+                       compute="bf16 activations, fp32 state and accumulation"),
+        "roofline": head["roofline"],
+        "roofline_tensor": head.get("roofline_tensor"),
+        "step_hbm": head["step_hbm"],
+        "cpu_baseline": head.get("cpu_baseline"),
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "kernels": head["kernels"],
+        "clocks": head["clocks"] or sampler.summary(),
+    }
+    for k in keys[1:]:
+        line[k] = results[k]
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on the prefill workload's config."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gated_deltanet_linear_mixer_gb300 import workloads
+    import oracle
+    case = workloads.config(1)
+    od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act)
+    take = 128
+    sl = slice(0, take)
+    run = lambda: oracle.gdn(od, [0, take], case.x[sl], case.z[sl], case.a[sl], case.b[sl],  # noqa: E731
+                             case.conv_w, case.A_log, case.dt_bias, case.norm_w)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    mean_s = statistics.mean(times)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    v = take / mean_s
+    sample = (f"first {take} of the {case.n_tokens} tokens per step (all {case.n_v_heads} heads), "
+              "f64 C oracle with OpenMP over (sequence, value head)")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": case.name, "n_seq": case.n_seq, "tokens": case.n_tokens,
+                       "Hk": case.n_k_heads, "Hv": case.n_v_heads, "d_k": case.d_k,
+                       "d_v": case.d_v, "K": case.conv_k, "act": case.act},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--extras", default="decode,varlen,spec_verify",
+                    help="comma list of extra workloads in the same line")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    args.extras = [e for e in args.extras.split(",") if e]
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+// Prologue kernels of the GDN core: causal depthwise conv + SiLU, q/k L2
+// normalisation with the q scale, the decay/write gates, and the conv-state
+// update (oxinfer 0.0.5 src/qwen.rs, fn gdn_forward and DeltaRule::run;
+// cherenkov qwen4_exp/cpu.rs, fn causal_conv).
+//
+// Work split: one CTA = one head's channels ("unit": a q head, a k head or a
+// v head) x a tile of 64 tokens.  Each thread owns one 16-byte vector of
+// channels (8 bf16 / 4 fp32) of one token row, so loads and stores of x and
+// qkv_out are 16-byte, fully coalesced; the d-wide L2 norm of a q/k head is a
+// shuffle reduction over the d/VEC lanes that share the token.  One extra
+// unit per token tile computes g and beta.  The whole pass reads x once and
+// writes qkv_out once, so it is bound by HBM bandwidth.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+constexpr int kConvThreads = 128;
+constexpr int kConvTokTile = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(kConvThreads)
+conv_prologue_kernel(ConvArgs p) {
+    using V = Vec16<T>;
+    constexpr int VEC = V::N;
+    const int n_units = 2 * p.n_k_heads + p.n_v_heads;
+    const int unit = blockIdx.y;
+    const int tile0 = blockIdx.x * kConvTokTile;
+    const int cd = 2 * p.n_k_heads * p.d_k + p.n_v_heads * p.d_v;
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+
+    if (unit == n_units) {  // gates for this token tile
+        const int hv_n = p.n_v_heads;
+        const T* __restrict__ a = static_cast<const T*>(p.a);
+        const T* __restrict__ b = static_cast<const T*>(p.b);
+        for (int i = threadIdx.x; i < kConvTokTile * hv_n; i += kConvThreads) {
+            const int t = tile0 + i / hv_n;
+            const int h = i % hv_n;
+            if (t >= p.n_tokens) break;
+            const size_t idx = (size_t)t * hv_n + h;
+            p.g_out[idx] = log_decay(to_f32(a[idx]), p.A_log[h], p.dt_bias[h]);
+            p.beta_out[idx] = sigmoidf_(to_f32(b[idx]));
+        }
+        return;
+    }
+
+    const bool is_q = unit < p.n_k_heads;
+    const bool is_k = !is_q && unit < 2 * p.n_k_heads;
+    const int D = (is_q || is_k) ? p.d_k : p.d_v;
+    const int ch0 = (is_q || is_k) ? unit * p.d_k
+                                   : 2 * p.n_k_heads * p.d_k + (unit - 2 * p.n_k_heads) * p.d_v;
+    const int tpr = D / VEC;               // threads per token row (power of 2, <= 32)
+    const int rows_per_pass = kConvThreads / tpr;
+    const int lane_in_row = threadIdx.x % tpr;
+    const int row = threadIdx.x / tpr;
+    const int c = ch0 + lane_in_row * VEC;  // first channel of this thread
+    const int K = p.conv_k;
+    const int keep = K - 1;
+
+    float w[VEC][4];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[e][j] = j < K ? p.conv_w[(size_t)(c + e) * K + j] : 0.0f;
+
+    const float qscale = rsqrtf((float)p.d_k);
+    const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
+    T* __restrict__ out = static_cast<T*>(p.qkv_out);
+
+    for (int r = row; r < kConvTokTile; r += rows_per_pass) {
+        const int t = tile0 + r;
+        const bool valid = t < p.n_tokens;
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+        if (valid) {
+            const int n = seq_of_token(p.cu_seqlens, p.n_seq, t);
+            const int bos = p.cu_seqlens[n];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j >= K) break;
+                const int src = t - keep + j;
+                float v[VEC];
+                if (src >= bos) {
+                    V::load(x + (size_t)src * cd + c, v);
+                } else if (cs_in) {
+                    const int slot = keep + (src - bos);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        v[e] = to_f32(cs_in[((size_t)n * cd + c + e) * keep + slot]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) v[e] = 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w[e][j], v[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] = siluf_(acc[e]);
+        }
+        if (is_q || is_k) {
+            float ss = 0.0f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) ss = fmaf(acc[e], acc[e], ss);
+            for (int off = tpr / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            float inv = rsqrtf(ss + p.l2_eps);
+            if (is_q) inv *= qscale;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] *= inv;
+        }
+        if (valid) V::store(out + (size_t)t * cd + c, acc);
+    }
+}
+
+// New history of each sequence = its last K-1 raw inputs, oldest first,
+// shifted in from the old history when the sequence is shorter than K-1.
+template <typename T>
+__global__ void conv_state_kernel(ConvStateArgs p) {
+    const int n = blockIdx.y;
+    const int ch = blockIdx.x * blockDim.x + threadIdx.x;
+    const int cd = 2 * p.n_k_heads * p.d_k + p.n_v_heads * p.d_v;
+    if (ch >= cd) return;
+    const int keep = p.conv_k - 1;
+    int bos, len;
+    if (p.cu_seqlens) {
+        bos = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - bos;
+    } else {
+        bos = n * p.uniform_T;
+        len = p.uniform_T;
+    }
+    if (p.lengths) len = min(max(p.lengths[n], 0), len);  // accepted prefix (commit)
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
+    T* __restrict__ cs_out = static_cast<T*>(p.conv_state_out);
+    T nw[3];
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+        if (s >= keep) break;
+        const int ti = len - keep + s;
+        if (ti >= 0)
+            nw[s] = x[(size_t)(bos + ti) * cd + ch];
+        else if (cs_in)
+            nw[s] = cs_in[((size_t)n * cd + ch) * keep + keep + ti];
+        else
+            nw[s] = from_f32<T>(0.0f);
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+        if (s >= keep) break;
+        cs_out[((size_t)n * cd + ch) * keep + s] = nw[s];
+    }
+}
+
+cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream) {
+    if (p.n_tokens == 0) return cudaSuccess;
+    dim3 grid((p.n_tokens + kConvTokTile - 1) / kConvTokTile, 2 * p.n_k_heads + p.n_v_heads + 1);
+    if (bf16)
+        conv_prologue_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, stream>>>(p);
+    else
+        conv_prologue_kernel<float><<<grid, kConvThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t stream) {
+    if (p.n_seq == 0 || p.conv_k < 2) return cudaSuccess;
+    const int cd = 2 * p.n_k_heads * p.d_k + p.n_v_heads * p.d_v;
+    dim3 grid((cd + 255) / 256, p.n_seq);
+    if (bf16)
+        conv_state_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+    else
+        conv_state_kernel<float><<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,188 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) mixer core for GB300 (sm_103a).
+ *
+ * The core is what runs between a GDN layer's input projections and its
+ * out_proj (oxinfer 0.0.5 src/qwen.rs, fn gdn_forward; cherenkov
+ * qwen4_exp/cpu.rs, fn deltanet):
+ *   a1  causal depthwise conv over the packed [q | k | v] channels, then SiLU
+ *   a2  conv-state update: the last K-1 raw inputs of each sequence
+ *   a3  per key head, q and k L2-normalised over d_k; q scaled by d_k^-1/2
+ *   a4  beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias)
+ *   a5  per value head, token by token: S <- exp(g) S; u = beta (v - S^T k);
+ *       S <- S + k u^T; o = S^T q    (qwen.rs DeltaRule::run, cpu.rs deltanet)
+ *   a6  y = norm_w * o * (mean(o^2) + eps)^-1/2 * act(z), act = SiLU or sigmoid
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer is a DEVICE pointer unless its name ends in _host.  The
+ *   caller allocates and owns every buffer; no call allocates device memory
+ *   or keeps a pointer after it returns.
+ * - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *   is the legacy default stream).  Returning GDN_OK means the work was
+ *   validated and enqueued, not that it has finished.
+ * - Layouts are row-major and token-major ("packed"): sequence i owns tokens
+ *   [cu_seqlens[i], cu_seqlens[i+1]) of every [T, ...] array.
+ *     x       [T, CD]   CD = 2*Hk*dk + Hv*dv, channels [q | k | v]
+ *     z       [T, Hv*dv]
+ *     a, b    [T, Hv]
+ *     out     [T, Hv*dv]
+ *     state   [N, Hv, dk, dv]  fp32, key lane major (row = key lane)
+ *     conv_state [N, CD, K-1]  activation dtype, oldest input first
+ *   Activations (x, z, a, b, out, conv_state, qkv_out) are all fp32 or all
+ *   bf16 (gdn_dims.dtype).  Parameters and recurrent states are always fp32.
+ * - Value head h reads key head h / (Hv/Hk) (contiguous groups).
+ * - Errors: each call returns a gdn_status; on failure nothing was enqueued
+ *   (or, for GDN_ERR_CUDA, a launch failed), and gdn_last_error() returns a
+ *   message naming the call and the reason.  No call aborts the process.
+ * - Buffers must be 16-byte aligned (x, z, out, states, qkv_out).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size or cu_seqlens, misalignment */
+    GDN_ERR_UNSUPPORTED = 2, /* geometry the kernels are not built for */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    GDN_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+/* Output-gate activation: qwen.rs gdn_forward uses SiLU, cpu.rs deltanet and
+ * the qwen4_exp config (output_gate_sigmoid) use sigmoid. */
+typedef enum gdn_act { GDN_ACT_SILU = 0, GDN_ACT_SIGMOID = 1 } gdn_act;
+
+/* Geometry (names of qwen4_exp.rs GdnCfg / qwen.rs QwenConfig).
+ * Supported: d_k, d_v in {32, 64, 128}; 2 <= conv_k <= 4;
+ * n_v_heads a multiple of n_k_heads; eps > 0. */
+typedef struct gdn_dims {
+    int32_t n_k_heads; /* Hk  linear_num_key_heads */
+    int32_t n_v_heads; /* Hv  linear_num_value_heads */
+    int32_t d_k;       /* linear_key_head_dim */
+    int32_t d_v;       /* linear_value_head_dim */
+    int32_t conv_k;    /* K   linear_conv_kernel_dim */
+    int32_t dtype;     /* gdn_dtype of the activations */
+    int32_t act;       /* gdn_act of the output gate */
+    float l2_eps;      /* q/k L2-norm eps (1e-6 on the pages) */
+    float rms_eps;     /* gated RMSNorm eps (1e-6 / rms_norm_eps) */
+} gdn_dims;
+
+/* Per-layer parameters, fp32 device pointers (qwen.rs loader: conv1d.weight
+ * [CD,1,K], A_log [Hv], dt_bias [Hv], norm.weight [dv], plain weight). */
+typedef struct gdn_params {
+    const float* conv_w;  /* [CD, K]; tap K-1 multiplies the current token */
+    const float* A_log;   /* [Hv] */
+    const float* dt_bias; /* [Hv] */
+    const float* norm_w;  /* [dv] */
+} gdn_params;
+
+/*
+ * gdn_conv -- steps a1..a4 only (the prologue), for callers that run their
+ * own recurrence, and for tests.
+ *   x [T, CD]; a, b [T, Hv]; cu_seqlens [n_seq+1] (device) and the same values
+ *   on the host (cu_seqlens_host), which is validated and used for sizing.
+ *   conv_state_in [N, CD, K-1] or NULL (all-zero history).
+ *   conv_state_out [N, CD, K-1] or NULL (not written); may equal conv_state_in.
+ *   qkv_out [T, CD]: [q_hat (already scaled by d_k^-1/2) | k_hat | v], in the
+ *   activation dtype.  g_out, beta_out [T, Hv] fp32 (g is the log-decay).
+ * Defined by qwen.rs gdn_forward (conv, conv-state update) and
+ * DeltaRule::run (normalisation, gates).
+ */
+gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_seq,
+                    const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                    const void* x, const void* a, const void* b,
+                    const void* conv_state_in, void* conv_state_out,
+                    void* qkv_out, float* g_out, float* beta_out, void* stream);
+
+/*
+ * gdn_prefill_workspace_size -- bytes of device workspace gdn_prefill needs
+ * for this geometry and sequence layout (written to *bytes; may be 0).
+ */
+gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
+                                      const int32_t* cu_seqlens_host, size_t* bytes);
+
+/*
+ * gdn_prefill -- the whole core (a1..a6) over n_seq packed sequences of any
+ * lengths (qwen.rs gdn_forward over t tokens; each sequence independent, with
+ * its own conv history and recurrent state).
+ *   initial_state [N, Hv, dk, dv] or NULL (zeros).  final_state: same shape,
+ *   or NULL (not written); may equal initial_state.
+ *   conv_state_in / conv_state_out as in gdn_conv (NULL allowed).
+ *   out [T, Hv*dv] in the activation dtype.
+ *   workspace: at least gdn_prefill_workspace_size() bytes, 256-byte aligned.
+ * bf16 activations run the chunked form on tensor cores (bf16 operands, fp32
+ * accumulation and fp32 state); fp32 activations run the token recurrence in
+ * fp32 on CUDA cores.
+ */
+gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n_seq,
+                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                       const void* x, const void* z, const void* a, const void* b,
+                       const void* conv_state_in, void* conv_state_out,
+                       const float* initial_state, float* final_state, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_decode -- T tokens (1 <= T <= 16) for each of n_seq sequences against a
+ * resident fp32 state: cpu.rs deltanet (one token) run T times, or a short
+ * speculative-verify chunk.  Layouts are [n_seq, T, ...] (packed with uniform
+ * lengths).
+ *   inter_states == NULL: state [N, Hv, dk, dv] and conv_state [N, CD, K-1]
+ *     are updated in place to their values after the T tokens.
+ *   inter_states != NULL ([N, T, Hv, dk, dv]): the state after every token is
+ *     written there and state and conv_state are only read, so the caller
+ *     can keep any accepted prefix (gdn_decode_commit does that on the GPU).
+ *   conv_state may be NULL (zero history, nothing written).
+ */
+gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_seq,
+                      int32_t T, const void* x, const void* z, const void* a, const void* b,
+                      float* state, void* conv_state, float* inter_states, void* out,
+                      void* stream);
+
+/*
+ * gdn_decode_commit -- after a verify call of gdn_decode that wrote
+ * inter_states, keep the first accepted[i] of the T tokens of sequence i:
+ * state[i] becomes inter_states[i, accepted[i]-1] (left as is when
+ * accepted[i] == 0) and conv_state[i] the last K-1 raw inputs of
+ * (old history ++ x[i, :accepted[i]]).  This is the rewind of qwen.rs
+ * QwenSession::rewind, done by selecting a kept state instead of replaying.
+ *   accepted [n_seq] int32 device array; values are clamped to [0, T].
+ *   x is the [n_seq, T, CD] input of the verify call; conv_state may be NULL.
+ */
+gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,
+                             const int32_t* accepted, const void* x,
+                             const float* inter_states, float* state, void* conv_state,
+                             void* stream);
+
+/*
+ * gdn_timing_enable / gdn_timing_report -- per-kernel device timing (the
+ * library's tracing hook; the pages time their GDN phases with scoped timers,
+ * qwen.rs gdn_forward prof::start).  While enabled, every kernel launch the
+ * library makes is bracketed by CUDA events recorded on its stream.
+ *   gdn_timing_enable(1) clears the totals and starts recording; (0) stops.
+ *   gdn_timing_report waits for the recorded events, then writes one line per
+ *   kernel, "<name> <launches> <total_ms>\n", into buf (NUL-terminated,
+ *   truncated to buf_len) and returns the bytes the full report needs.
+ * Process-wide; thread-safe; not for use while a CUDA graph is captured.
+ */
+gdn_status gdn_timing_enable(int32_t enable);
+size_t gdn_timing_report(char* buf, size_t buf_len);
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* gdn_last_error(void);
+
+/* Library version string. */
+const char* gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

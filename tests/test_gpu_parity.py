@@ -1,0 +1,263 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Every comparison is element by element on the same seeded inputs, with the
+error metric max|gpu - ref| / rms(ref) and the tolerances 1e-4 (fp32
+activations) and 2e-2 (bf16 activations, fp32 state).
+"""
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_mixer_gb300 as gdn
+from gated_deltanet_linear_mixer_gb300 import workloads
+from gdn_cases import TOL, dims, gpu_decode, gpu_prefill, rel_err, run_oracle, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_deltanet_linear_mixer_gb300 import _build
+    _build.build()
+    gdn.load()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _gen(name, **kw):
+    base = dict(n_k_heads=2, n_v_heads=4, d_k=128, d_v=128, conv_k=4, dtype="bf16", act="silu",
+                seed=11)
+    base.update(kw)
+    return workloads.generate(name, **base)
+
+
+def _subcase(case, seqs):
+    """The same workload restricted to some sequences (they are independent)."""
+    c = copy.copy(case)
+    cu = case.cu_seqlens
+    rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs]).astype(np.int64)
+    lens = [int(cu[i + 1] - cu[i]) for i in seqs]
+    c.cu_seqlens = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    c.x, c.z, c.a, c.b = case.x[rows], case.z[rows], case.a[rows], case.b[rows]
+    c.state = None if case.state is None else case.state[list(seqs)]
+    c.conv_state = None if case.conv_state is None else case.conv_state[list(seqs)]
+    return c, rows
+
+
+PREFILL_CASES = {
+    "tiny_fp32": lambda: workloads.config(0),
+    "tiny_fp32_slow_decay": lambda: workloads.config(0, slow_decay=True),
+    "ragged_bf16_d128_states": lambda: _gen("r1", lengths=[1, 0, 2, 3, 130, 77, 64],
+                                            state_std=0.05, conv_state_std=1.0),
+    "ragged_f32_dk64_dv128_sigmoid": lambda: _gen("r2", d_k=64, d_v=128, dtype="f32",
+                                                  act="sigmoid", lengths=[5, 64, 129, 1],
+                                                  state_std=0.05, conv_state_std=1.0, seed=12),
+    "bf16_dk128_dv32_K3": lambda: _gen("r3", d_k=128, d_v=32, conv_k=3, lengths=[40, 200],
+                                       seed=13, conv_state_std=1.0),
+    "bf16_dk32_dv64_K2_gqa4": lambda: _gen("r4", n_k_heads=1, n_v_heads=4, d_k=32, d_v=64,
+                                           conv_k=2, lengths=[33, 65], seed=14, state_std=0.1),
+    "bf16_slow_decay_long": lambda: _gen("r5", lengths=[700, 333], state_std=0.05, seed=15,
+                                         slow_decay=True),
+    "f32_slow_decay": lambda: _gen("r6", dtype="f32", lengths=[300, 17], state_std=0.05,
+                                   conv_state_std=1.0, seed=16, slow_decay=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_CASES))
+def test_prefill_matches_oracle(name):
+    case = PREFILL_CASES[name]()
+    ref = run_oracle(case)
+    got = gpu_prefill(case)
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0  # a copy of raw inputs
+
+
+@pytest.mark.parametrize("name", ["ragged_bf16_d128_states", "ragged_f32_dk64_dv128_sigmoid"])
+def test_prefill_in_place_states(name):
+    case = PREFILL_CASES[name]()
+    ref = run_oracle(case)
+    got = gpu_prefill(case, in_place=True)
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
+def test_prefill_without_optional_states():
+    """NULL initial state / conv state in, no outputs for them: out still matches."""
+    case = _gen("r7", lengths=[50, 3], seed=17)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    t = upload(case)
+    out = gdn.prefill(d, t["params"], case.cu_seqlens, t["x"], t["z"], t["a"], t["b"])
+    torch.cuda.synchronize()
+    assert rel_err(out, ref["out"]) <= TOL["bf16"]
+
+
+def test_prefill_zero_sequences_and_empty():
+    d, _ = dims(_gen("e", lengths=[1]))
+    case = _gen("e", lengths=[0, 0])
+    t = upload(case)
+    st = torch.full((2, 4, 128, 128), float("nan"), device="cuda")
+    gdn.prefill(d, t["params"], [0, 0, 0], t["x"], t["z"], t["a"], t["b"], final_state=st)
+    torch.cuda.synchronize()
+    assert torch.all(st == 0)   # empty sequences: final state = (zero) initial state
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (32, 128)])
+def test_conv_prologue_matches_oracle_stages(dtype, dk, dv):
+    case = _gen("c", d_k=dk, d_v=dv, dtype=dtype, lengths=[1, 2, 70, 0, 129, 5],
+                conv_state_std=1.0, seed=18)
+    ref = run_oracle(case, want_stages=True)
+    d, _ = dims(case)
+    t = upload(case)
+    cs_out = torch.full_like(t["conv_state"], float("nan"))
+    qkv, g, beta = gdn.conv(d, t["params"], case.cu_seqlens, t["x"], t["a"], t["b"],
+                            conv_state_in=t["conv_state"], conv_state_out=cs_out)
+    torch.cuda.synchronize()
+    kd = d.n_k_heads * dk
+    tol = TOL[dtype]
+    tt = case.n_tokens
+    assert rel_err(qkv[:, :kd], ref["q_hat"].reshape(tt, -1)) <= tol
+    assert rel_err(qkv[:, kd:2 * kd], ref["k_hat"].reshape(tt, -1)) <= tol
+    assert rel_err(qkv[:, 2 * kd:], ref["v"].reshape(tt, -1)) <= tol
+    assert rel_err(g, ref["g"]) <= 1e-5
+    assert rel_err(beta, ref["beta"]) <= 1e-6
+    assert rel_err(cs_out, ref["conv_state"]) == 0.0
+
+
+DECODE_CASES = {
+    "bf16_T1_sigmoid": lambda: _gen("d1", mode="decode", n_seq=6, tokens_per_seq=1,
+                                    act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=21),
+    "bf16_T4_inter": lambda: _gen("d2", mode="decode", n_seq=5, tokens_per_seq=4,
+                                  act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=22,
+                                  want_inter=True),
+    "f32_T3_silu_dk64": lambda: _gen("d3", mode="decode", n_seq=3, tokens_per_seq=3, d_k=64,
+                                     dtype="f32", state_std=0.05, conv_state_std=1.0, seed=23),
+    "bf16_T16_max": lambda: _gen("d4", mode="decode", n_seq=2, tokens_per_seq=16,
+                                 act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=24,
+                                 want_inter=True),
+    "f32_T2_slow_decay": lambda: _gen("d5", mode="decode", n_seq=4, tokens_per_seq=2,
+                                      dtype="f32", state_std=0.05, conv_state_std=1.0, seed=25,
+                                      slow_decay=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DECODE_CASES))
+def test_decode_matches_oracle(name):
+    case = DECODE_CASES[name]()
+    ref = run_oracle(case, want_inter=case.want_inter)
+    got = gpu_decode(case, inter=case.want_inter)
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    if case.want_inter:
+        n, tt = case.n_seq, case.tokens_per_seq
+        inter_ref = ref["inter"].reshape(n, tt, *ref["inter"].shape[1:])
+        assert rel_err(got["inter"], inter_ref) <= tol
+        # verify mode: resident state and conv state are read only
+        assert rel_err(got["state"], case.state) == 0.0
+        assert rel_err(got["conv_state"], case.conv_state) == 0.0
+    else:
+        assert rel_err(got["state"], ref["state"]) <= tol
+        assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
+def test_decode_commit_keeps_accepted_prefix():
+    case = _gen("cm", mode="decode", n_seq=5, tokens_per_seq=4, act="sigmoid", state_std=0.05,
+                conv_state_std=1.0, seed=26, want_inter=True)
+    got = gpu_decode(case, inter=True)
+    d, _ = dims(case)
+    t = upload(case)
+    accepted = torch.tensor([0, 1, 2, 3, 4], dtype=torch.int32, device="cuda")
+    state = t["state"].clone()
+    cs = t["conv_state"].clone()
+    gdn.decode_commit(d, accepted, t["x"].view(5, 4, -1), got["inter"], state, cs)
+    torch.cuda.synchronize()
+    for i, j in enumerate([0, 1, 2, 3, 4]):
+        sub, _ = _subcase(case, [i])
+        sub.cu_seqlens = np.array([0, j], dtype=np.int32)
+        sub.x, sub.z, sub.a, sub.b = sub.x[:j], sub.z[:j], sub.a[:j], sub.b[:j]
+        ref = run_oracle(sub)
+        assert rel_err(state[i], ref["state"][0]) <= TOL["bf16"]
+        assert rel_err(cs[i], ref["conv_state"][0]) == 0.0
+
+
+def test_decode_equals_prefill_of_same_tokens():
+    """T decode tokens against a state == prefill of those T tokens from that state."""
+    case = _gen("dp", mode="decode", n_seq=3, tokens_per_seq=4, state_std=0.05,
+                conv_state_std=1.0, seed=27)
+    dec = gpu_decode(case)
+    pre = gpu_prefill(case)
+    assert rel_err(dec["out"], pre["out"].float().cpu().numpy()) <= 1e-2
+    assert rel_err(dec["state"], pre["state"].cpu().numpy()) <= 1e-4
+    assert rel_err(dec["conv_state"], pre["conv_state"].float().cpu().numpy()) == 0.0
+
+
+def test_invalid_arguments_raise():
+    case = _gen("iv", lengths=[4])
+    d, _ = dims(case)
+    t = upload(case)
+    with pytest.raises(gdn.GDNError, match="cu_seqlens"):
+        gdn.prefill(d, t["params"], torch.tensor([1, 4], dtype=torch.int32), t["x"], t["z"], t["a"], t["b"])
+    with pytest.raises(gdn.GDNError, match="T must be"):
+        st = torch.zeros((1, 4, 128, 128), device="cuda")
+        x = torch.zeros((1, 17, d.conv_dim), dtype=d.dtype, device="cuda")
+        gdn.decode(d, t["params"], x, torch.zeros((1, 17, 512), dtype=d.dtype, device="cuda"),
+                   torch.zeros((1, 17, 4), dtype=d.dtype, device="cuda"),
+                   torch.zeros((1, 17, 4), dtype=d.dtype, device="cuda"), st)
+
+
+# ---------------------------------------------------------------- full sizes
+
+def test_full_size_prefill_T4096():
+    case = workloads.config(1)
+    ref = run_oracle(case)
+    got = gpu_prefill(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+
+
+def test_full_size_prefill_T4096_slow_decay():
+    case = workloads.config(1, slow_decay=True)
+    ref = run_oracle(case)
+    got = gpu_prefill(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_full_size_varlen_prefill_sampled_sequences(slow):
+    """The whole 16-sequence workload runs on the GPU; the oracle checks the
+    shortest, a middle and the longest sequence (sequences are independent)."""
+    case = workloads.config(3, slow_decay=slow)
+    got = gpu_prefill(case)
+    lens = np.diff(case.cu_seqlens)
+    order = np.argsort(lens)
+    pick = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    sub, rows = _subcase(case, pick)
+    ref = run_oracle(sub)
+    assert rel_err(got["out"][torch.from_numpy(rows).cuda()], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"][pick], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"][pick].float(), ref["conv_state"]) == 0.0
+
+
+def test_full_size_decode_256():
+    case = workloads.config(2)
+    ref = run_oracle(case)
+    got = gpu_decode(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
+def test_full_size_spec_verify_64x4():
+    case = workloads.config(4)
+    ref = run_oracle(case, want_inter=True)
+    got = gpu_decode(case, inter=True)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    inter_ref = ref["inter"].reshape(64, 4, 32, 128, 128)
+    assert rel_err(got["inter"], inter_ref) <= TOL["bf16"]
