@@ -407,3 +407,14 @@ def test_workload_generator_shapes_and_bf16_rounding():
                                   [1.0 + 2 ** -6])
     ref = torch.tensor(c4.z.ravel()[:100] + np.float32(1e-3)).to(torch.bfloat16).float().numpy()
     np.testing.assert_array_equal(workloads.round_bf16(c4.z.ravel()[:100] + np.float32(1e-3)), ref)
+
+
+def test_bf16_half_ulp_helper():
+    """The test metric's storage-rounding allowance: exact half ulps of bf16 values."""
+    from gdn_cases import bf16_half_ulp
+    v = np.array([1.0, 1.5, -2.0, 3.0, 0.0, 2.0 ** -10])
+    np.testing.assert_array_equal(bf16_half_ulp(v), [2 ** -8, 2 ** -8, 2 ** -7, 2 ** -7, 0.0, 2 ** -18])
+    # any float32 rounds to bf16 within half an ulp of the result
+    x = np.random.default_rng(0).normal(size=1000).astype(np.float32) * 37
+    r = workloads.round_bf16(x).astype(np.float64)
+    assert np.all(np.abs(r - x) <= bf16_half_ulp(r) * (1 + 1e-12))
