@@ -29,8 +29,8 @@ ACT_SILU, ACT_SIGMOID = 0, 1
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_decode",
-           "gdn_decode_commit", "gdn_timing_enable", "gdn_timing_report", "gdn_last_error",
-           "gdn_version")
+           "gdn_decode_commit", "gdn_timing_enable", "gdn_timing_report", "gdn_device_error",
+           "gdn_last_error", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -80,6 +80,8 @@ def load(path: str | None = None):
     lib.gdn_timing_enable.restype = ctypes.c_int
     lib.gdn_timing_report.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
     lib.gdn_timing_report.restype = ctypes.c_size_t
+    lib.gdn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), I32]
+    lib.gdn_device_error.restype = ctypes.c_int
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_last_error.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
@@ -204,6 +206,13 @@ def timing_report() -> dict:
         name, n, ms = line.split()
         rep[name] = (int(n), float(ms))
     return rep
+
+
+def device_error(reset: bool = True) -> int:
+    """The sticky device-side error word (0 = none); waits for the device."""
+    code = ctypes.c_int32(0)
+    _check("gdn_device_error", load().gdn_device_error(ctypes.byref(code), 1 if reset else 0))
+    return int(code.value)
 
 
 def conv(d: Dims, params: Params, cu_seqlens, x, a, b, conv_state_in=None, conv_state_out=None,

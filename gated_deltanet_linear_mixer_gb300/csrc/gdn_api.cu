@@ -115,29 +115,6 @@ cudaEvent_t take_event() {
     return e;
 }
 
-// Runs `launch` (returning cudaError_t) and, when timing is on, brackets it.
-template <typename F>
-cudaError_t timed(const char* name, cudaStream_t stream, F&& launch) {
-    bool on;
-    {
-        std::lock_guard<std::mutex> lk(g_timing_mu);
-        on = g_timing_on;
-    }
-    if (!on) return launch();
-    cudaEvent_t a, b;
-    {
-        std::lock_guard<std::mutex> lk(g_timing_mu);
-        a = take_event();
-        b = take_event();
-    }
-    if (a) cudaEventRecord(a, stream);
-    cudaError_t e = launch();
-    if (b) cudaEventRecord(b, stream);
-    std::lock_guard<std::mutex> lk(g_timing_mu);
-    if (a && b) g_pending.push_back({name, a, b});
-    return e;
-}
-
 void drain_pending_locked() {
     for (auto& r : g_pending) {
         float ms = 0.f;
@@ -159,9 +136,35 @@ void drain_pending_locked() {
     g_pending.clear();
 }
 
-int conv_dim(const gdn_dims* d) { return 2 * d->n_k_heads * d->d_k + d->n_v_heads * d->d_v; }
 
 }  // namespace
+
+namespace gdn {
+
+void* timing_start(const char* name, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    if (!g_timing_on) return nullptr;
+    cudaEvent_t a = take_event(), b = take_event();
+    if (!a || !b) {
+        if (a) g_event_pool.push_back(a);
+        if (b) g_event_pool.push_back(b);
+        return nullptr;
+    }
+    cudaEventRecord(a, stream);
+    g_pending.push_back({name, a, b});
+    return reinterpret_cast<void*>(g_pending.size());  // 1-based index
+}
+
+void timing_stop(void* handle, cudaStream_t stream) {
+    if (!handle) return;
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    const size_t idx = reinterpret_cast<size_t>(handle) - 1;
+    if (idx < g_pending.size()) cudaEventRecord(g_pending[idx].stop, stream);
+}
+
+}  // namespace gdn
+
+using gdn::timed_launch;
 
 extern "C" {
 
@@ -188,6 +191,15 @@ size_t gdn_timing_report(char* buf, size_t buf_len) {
         buf[n] = '\0';
     }
     return text.size() + 1;
+}
+
+gdn_status gdn_device_error(int32_t* code, int32_t reset) {
+    const char* fn = "gdn_device_error";
+    if (!code) return fail(GDN_ERR_INVALID_ARG, fn, "code is NULL");
+    int v = 0;
+    gdn_status st = cuda_status(gdn::read_device_error(&v, reset != 0), fn, "reading the error word");
+    *code = v;
+    return st;
 }
 
 const char* gdn_last_error(void) { return g_err; }
@@ -221,7 +233,7 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_se
     p.cu_seqlens = cu_seqlens; p.x = x; p.a = a; p.b = b;
     p.conv_w = params->conv_w; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
     p.conv_state_in = conv_state_in; p.qkv_out = qkv_out; p.g_out = g_out; p.beta_out = beta_out;
-    if ((st = cuda_status(timed("conv_prologue", s, [&] { return gdn::launch_conv_prologue(p, bf16, s); }), fn, "conv prologue launch")) != GDN_OK)
+    if ((st = cuda_status(timed_launch("conv_prologue", s, [&] { return gdn::launch_conv_prologue(p, bf16, s); }), fn, "conv prologue launch")) != GDN_OK)
         return st;
     if (conv_state_out && n_seq > 0) {
         gdn::ConvStateArgs c{};
@@ -229,7 +241,7 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_se
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
         c.cu_seqlens = cu_seqlens; c.x = x; c.conv_state_in = conv_state_in;
         c.conv_state_out = conv_state_out;
-        if ((st = cuda_status(timed("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
+        if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
             return st;
     }
     return GDN_OK;
@@ -244,6 +256,14 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
     if (n_seq < 0) return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
     if (n_seq > 0 && !cu_seqlens_host) return fail(GDN_ERR_INVALID_ARG, fn, "cu_seqlens_host is NULL");
     *bytes = 0;
+    if (gdn::chunked_supported(dims->d_k, dims->d_v, dims->n_k_heads, dims->n_v_heads,
+                               dims->dtype == GDN_DTYPE_BF16) && n_seq > 0) {
+        int total = 0;
+        if ((st = check_cu(n_seq, cu_seqlens_host, cu_seqlens_host, &total, fn)) != GDN_OK)
+            return st;
+        *bytes = gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads,
+                                              dims->n_v_heads, nullptr);
+    }
     g_err[0] = '\0';
     return GDN_OK;
 }
@@ -270,12 +290,29 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(GDN_ERR_WORKSPACE, fn, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
-    (void)workspace;
     g_err[0] = '\0';
     if (n_seq == 0) return GDN_OK;
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    if (gdn::chunked_supported(dims->d_k, dims->d_v, dims->n_k_heads, dims->n_v_heads, bf16)) {
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(GDN_ERR_WORKSPACE, fn, "workspace must be 256-byte aligned");
+        gdn::ChunkLaunch c{};
+        c.n_seq = n_seq; c.n_tokens = total; c.n_k_heads = dims->n_k_heads;
+        c.n_v_heads = dims->n_v_heads; c.conv_k = dims->conv_k; c.act = dims->act;
+        c.l2_eps = dims->l2_eps; c.rms_eps = dims->rms_eps; c.cu_seqlens = cu_seqlens;
+        c.x = x; c.z = z; c.a = a; c.b = b;
+        c.conv_w = params->conv_w; c.A_log = params->A_log; c.dt_bias = params->dt_bias;
+        c.norm_w = params->norm_w; c.conv_state_in = conv_state_in;
+        c.state_in = initial_state; c.state_out = final_state; c.out = out;
+        c.workspace = workspace;
+        gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads, dims->n_v_heads,
+                                     &c.layout);
+        if ((st = cuda_status(gdn::launch_chunked_prefill(c, s), fn, "chunked prefill launch")) !=
+            GDN_OK)
+            return st;
+    } else {
     gdn::RecurrentArgs r{};
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
@@ -284,16 +321,17 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
     r.norm_w = params->norm_w; r.conv_state_in = conv_state_in;
     r.state_in = initial_state; r.state_out = final_state; r.inter = nullptr; r.out = out;
-    if ((st = cuda_status(timed("recurrent", s, [&] { return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s); }), fn,
+    if ((st = cuda_status(timed_launch("recurrent", s, [&] { return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s); }), fn,
                           "recurrent launch")) != GDN_OK)
         return st;
+    }
     if (conv_state_out) {
         gdn::ConvStateArgs c{};
         c.n_seq = n_seq; c.n_k_heads = dims->n_k_heads; c.n_v_heads = dims->n_v_heads;
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
         c.cu_seqlens = cu_seqlens; c.x = x; c.conv_state_in = conv_state_in;
         c.conv_state_out = conv_state_out;
-        if ((st = cuda_status(timed("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
+        if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
             return st;
     }
     return GDN_OK;
@@ -330,7 +368,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     r.state_out = inter_states ? nullptr : state;
     r.inter = inter_states;
     r.out = out;
-    if ((st = cuda_status(timed("recurrent", s, [&] { return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s); }), fn,
+    if ((st = cuda_status(timed_launch("recurrent", s, [&] { return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s); }), fn,
                           "recurrent launch")) != GDN_OK)
         return st;
     if (conv_state && !inter_states) {
@@ -339,7 +377,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
         c.cu_seqlens = nullptr; c.uniform_T = T; c.x = x;
         c.conv_state_in = conv_state; c.conv_state_out = conv_state;
-        if ((st = cuda_status(timed("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
+        if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
             return st;
     }
     return GDN_OK;
@@ -364,14 +402,14 @@ gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,
     gdn::CommitArgs c{};
     c.n_seq = n_seq; c.n_v_heads = dims->n_v_heads; c.d_k = dims->d_k; c.d_v = dims->d_v;
     c.T = T; c.accepted = accepted; c.inter = inter_states; c.state = state;
-    if ((st = cuda_status(timed("commit_state", s, [&] { return gdn::launch_commit_state(c, s); }), fn, "commit launch")) != GDN_OK) return st;
+    if ((st = cuda_status(timed_launch("commit_state", s, [&] { return gdn::launch_commit_state(c, s); }), fn, "commit launch")) != GDN_OK) return st;
     if (conv_state) {
         gdn::ConvStateArgs cs{};
         cs.n_seq = n_seq; cs.n_k_heads = dims->n_k_heads; cs.n_v_heads = dims->n_v_heads;
         cs.d_k = dims->d_k; cs.d_v = dims->d_v; cs.conv_k = dims->conv_k;
         cs.cu_seqlens = nullptr; cs.uniform_T = T; cs.lengths = accepted; cs.x = x;
         cs.conv_state_in = conv_state; cs.conv_state_out = conv_state;
-        if ((st = cuda_status(timed("conv_state", s, [&] { return gdn::launch_conv_state(cs, dims->dtype == GDN_DTYPE_BF16, s); }), fn,
+        if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(cs, dims->dtype == GDN_DTYPE_BF16, s); }), fn,
                               "conv state launch")) != GDN_OK)
             return st;
     }

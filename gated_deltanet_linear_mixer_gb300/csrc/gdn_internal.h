@@ -2,6 +2,7 @@
 // kernels.  Host-visible plain structs; pointers are device pointers.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -60,6 +61,68 @@ struct CommitArgs {
     const float* inter;       // [n_seq, T, Hv, dk, dv]
     float* state;             // [n_seq, Hv, dk, dv]
 };
+
+// Arguments of the chunked (tensor-core) kernels.
+struct ChunkArgs {
+    int n_seq, n_tokens, n_chunks, n_k_heads, n_v_heads, act;
+    float rms_eps;
+    const int32_t* cu_seqlens;  // [n_seq+1]
+    const int32_t* cu_chunks;   // [n_seq+1] chunk offsets (workspace)
+    const __nv_bfloat16* qkv;   // [T, CD] normalised q | k | v (workspace)
+    const float* g;             // [T, Hv] log-decay (workspace)
+    const float* beta;          // [T, Hv] (workspace)
+    const __nv_bfloat16* z;     // [T, Hv*dv]
+    const float* norm_w;        // [dv]
+    const float* state_in;      // [N, Hv, dk, dv] or null
+    float* state_out;           // or null
+    __nv_bfloat16* w_ws;        // [chunks, Hv, 64, dk]
+    __nv_bfloat16* u_ws;        // [chunks, Hv, 64, dv]
+    __nv_bfloat16* qk_ws;       // [chunks, Hv, 64, 64]
+    float* gcum_ws;             // [chunks, Hv, 64]
+    __nv_bfloat16* out;         // [T, Hv*dv]
+};
+
+// Byte offsets of the chunked path's workspace regions.
+struct ChunkLayout {
+    size_t qkv, g, beta, cu_chunks, w, u, qk, gcum, total;
+    int n_chunks;
+};
+
+// Per-kernel timing hook (CUDA events on the launching stream when enabled).
+void* timing_start(const char* name, cudaStream_t stream);
+void timing_stop(void* handle, cudaStream_t stream);
+template <typename F>
+cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
+    void* h = timing_start(name, stream);
+    cudaError_t e = launch();
+    timing_stop(h, stream);
+    return e;
+}
+
+struct ChunkLaunch {
+    int n_seq, n_tokens, n_k_heads, n_v_heads, conv_k, act;
+    float l2_eps, rms_eps;
+    const int32_t* cu_seqlens;
+    const void *x, *z, *a, *b;
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    const void* conv_state_in;
+    const float* state_in;
+    float* state_out;
+    void* out;
+    void* workspace;
+    ChunkLayout layout;
+};
+
+// Workspace size (and layout) of the chunked path for this sequence layout.
+size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads, int n_v_heads,
+                               ChunkLayout* layout);
+// Whether the chunked tensor-core path serves this geometry.
+inline bool chunked_supported(int d_k, int d_v, int n_k_heads, int n_v_heads, bool bf16) {
+    return bf16 && d_k == 128 && d_v == 128 && n_v_heads / n_k_heads <= 4;
+}
+cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t stream);
+// Sticky device-side error word set by a kernel whose bounded wait gave up.
+cudaError_t read_device_error(int* code, bool reset);
 
 cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t stream);
