@@ -39,8 +39,6 @@ using namespace tc;
 constexpr int kC = 64;             // chunk length
 constexpr int kD = 128;            // d_k = d_v on this path
 constexpr int kChunkThreads = 256;
-constexpr uint32_t kPrepSmemFixed = 81920;   // Ag 32K + T 16K + B 32K
-constexpr uint32_t kScanSmem = 131072;       // Bs 32K + Aw 32K + Aq 16K + Bu 16K + Ak 16K + Ut 16K
 
 __device__ int g_device_error = 0;
 
@@ -127,18 +125,54 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu_seq
     }
 }
 
+// Split arithmetic.  Every tensor-core operand is carried as a pair of bf16
+// tiles, hi = bf16(x) and lo = bf16(x - hi), which together hold ~16
+// significant bits; a product A.B is formed as hi.hi + hi.lo + lo.hi with
+// fp32 accumulation (the dropped lo.lo term is ~2^-16 relative).  The gated
+// outputs are heavy-tailed (up to ~50x their RMS), so plain bf16 operands
+// (2^-9 relative) would put the largest outputs' error far above 2e-2 of the
+// output RMS.
+__device__ __forceinline__ void split_store(const float* f, uint8_t* hi, uint8_t* lo) {
+    float h[8], l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        h[e] = __bfloat162float(__float2bfloat16_rn(f[e]));
+        l[e] = f[e] - h[e];
+    }
+    *reinterpret_cast<uint4*>(hi) = pack_bf16x8(h);
+    *reinterpret_cast<uint4*>(lo) = pack_bf16x8(l);
+}
+__device__ __forceinline__ void load_pair(const uint8_t* hi, const uint8_t* lo, float* f) {
+    float l[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(hi), f);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(lo), l);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] += l[e];
+}
+// D (+)= A.B with A, B given as (hi, lo) descriptor pairs.
+__device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
+                                     uint32_t idesc, uint32_t accumulate) {
+    mma_bf16(d, ah, bh, idesc, accumulate);
+    mma_bf16(d, ah, bl, idesc, 1u);
+    mma_bf16(d, al, bh, idesc, 1u);
+}
+
 // --------------------------------------------------------------- chunk_prep
+constexpr uint32_t kPrepAgH = 0, kPrepAgL = 32768, kPrepTH = 65536, kPrepTL = 81920,
+                   kPrepBH = 98304, kPrepBL = 131072, kPrepAt = 163840, kPrepVec = 180224;
+
 __global__ void __launch_bounds__(kChunkThreads, 1)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
+chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                  ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sAg = smem;            // [Q; K] K-major, 2 column blocks of 128 rows x 128 B
-    uint8_t* sT = smem + 32768;     // T, K-major 128 rows (64..127 zero) x 128 B
-    uint8_t* sB = smem + 49152;     // [beta e^G K | beta V], MN-major 64 rows x 256
+    uint8_t* sAg[2] = {smem + kPrepAgH, smem + kPrepAgL};  // [Q; K] K-major (hi, lo)
+    uint8_t* sT[2] = {smem + kPrepTH, smem + kPrepTL};     // T K-major, rows 64.. zero
+    uint8_t* sB[2] = {smem + kPrepBH, smem + kPrepBL};     // [beta e^G K | beta V] MN-major
+    float* sAt = reinterpret_cast<float*>(smem + kPrepAt); // A^T [s][t] of one head
     const int R = p.n_v_heads / p.n_k_heads;
-    float* sAt = reinterpret_cast<float*>(smem + kPrepSmemFixed);  // per head A^T [s][t]
-    float* sG = sAt + R * kC * kC;
+    float* sG = reinterpret_cast<float*>(smem + kPrepVec);
     float* sBeta = sG + R * kC;
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_slot;
@@ -155,9 +189,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_slot, 256);
-    for (int i = tid; i < 512; i += kChunkThreads)
-        reinterpret_cast<uint4*>(sT + 8192)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (warp == 0) tmem_alloc(&tmem_slot, 512);
+    for (int i = tid; i < 1024; i += kChunkThreads)
+        reinterpret_cast<uint4*>(sT[i >> 9] + 8192)[i & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp < R) {  // cumulative log-decay and write strength of value head hk*R + warp
         const int h = hk * R + warp;
         const int s0 = 2 * lane, s1 = 2 * lane + 1;
@@ -186,33 +220,36 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;
+    const uint32_t tmem = tmem_slot;        // cols 0..255: [W | U~]
+    const uint32_t tmem_g = tmem + 256;     // cols 256..319: Gram
     uint32_t mma_phase = 0;
-    bool tma_issued = false, mma_pending = false;
+    bool tma_pending = false, mma_pending = false;
 
     do {
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_tma, 4 * 8192);
+            mbar_arrive_expect_tx(&bar_tma, 8 * 8192);
             const int qc = hk * kD, kc = p.n_k_heads * kD + hk * kD;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                tma_load_2d(sAg + b * 16384, &map_qkv, &bar_tma, qc + 64 * b, t0);
-                tma_load_2d(sAg + b * 16384 + 8192, &map_qkv, &bar_tma, kc + 64 * b, t0);
+                tma_load_2d(sAg[0] + b * 16384, &map_qh, &bar_tma, qc + 64 * b, t0);
+                tma_load_2d(sAg[0] + b * 16384 + 8192, &map_qh, &bar_tma, kc + 64 * b, t0);
+                tma_load_2d(sAg[1] + b * 16384, &map_ql, &bar_tma, qc + 64 * b, t0);
+                tma_load_2d(sAg[1] + b * 16384 + 8192, &map_ql, &bar_tma, kc + 64 * b, t0);
             }
         }
-        tma_issued = true;
+        tma_pending = true;
         if (any_failed(mbar_wait(&bar_tma, 0))) {
             if (tid == 0) report_error(1);
             break;
         }
-        tma_issued = false;
+        tma_pending = false;
         if (L < kC) {  // rows past the chunk belong to another sequence: zero them
             const int nr = kC - L;
-            for (int i = tid; i < nr * 32; i += kChunkThreads) {
+            for (int i = tid; i < nr * 64; i += kChunkThreads) {
                 const int ch = i & 7, rest = i >> 3;
-                const int r = L + rest % nr, pb = rest / nr;  // pb: part (q/k) x block
-                *reinterpret_cast<uint4*>(sAg + (pb >> 1) * 16384 + ((pb & 1) * 64 + r) * 128 +
-                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                const int r = L + rest % nr, pb = rest / nr;  // pb: hi/lo x part x block
+                *reinterpret_cast<uint4*>(sAg[pb >> 2] + ((pb >> 1) & 1) * 16384 +
+                                          ((pb & 1) * 64 + r) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
         fence_proxy_async_smem();
@@ -222,9 +259,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
         if (tid == 0) {  // Gram: rows 0..63 = Q K^T, rows 64..127 = K K^T
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const uint32_t a = smem_u32(sAg) + (k >> 2) * 16384 + (k & 3) * 32;
-                mma_bf16(tmem, desc_kmajor_sw128(a), desc_kmajor_sw128(a + 8192),
-                         idesc_bf16_f32(128, 64), k > 0 ? 1u : 0u);
+                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                const uint32_t ah = smem_u32(sAg[0]) + off, al = smem_u32(sAg[1]) + off;
+                mma3(tmem_g, desc_kmajor_sw128(ah), desc_kmajor_sw128(al),
+                     desc_kmajor_sw128(ah + 8192), desc_kmajor_sw128(al + 8192),
+                     idesc_bf16_f32(128, 64), k > 0 ? 1u : 0u);
             }
             mma_commit(&bar_mma);
         }
@@ -236,50 +275,70 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
         mma_pending = false;
         mma_phase ^= 1;
         tc_fence_after_sync();
-        if (warp < 4) {
-            float v[64];
-            tmem_ld32(tmem + ((32u * warp) << 16), v);
-            tmem_ld32(tmem + ((32u * warp) << 16) + 32, v + 32);
-            if (warp < 2) {  // masked decayed Q K^T rows -> workspace
-                const int t = 32 * warp + lane;
-                for (int r = 0; r < R; ++r) {
-                    const float Gt = sG[r * kC + t];
-                    uint4* dst = reinterpret_cast<uint4*>(
-                        p.qk_ws + ((size_t)(c * hv_n + hk * R + r) * kC + t) * kC);
+
+        bool failed = false;
+        for (int r = 0; r < R; ++r) {
+            const int h = hk * R + r;
+            const float* Gr = sG + r * kC;
+            const float* Br = sBeta + r * kC;
+            if (warp < 4) {
+                float v[64];
+                tmem_ld32(tmem_g + ((32u * warp) << 16), v);
+                tmem_ld32(tmem_g + ((32u * warp) << 16) + 32, v + 32);
+                if (warp < 2) {  // masked decayed Q K^T row t -> workspace (hi, lo)
+                    const int t = 32 * warp + lane;
+                    const float Gt = Gr[t];
+                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kC;
 #pragma unroll
                     for (int q8 = 0; q8 < 8; ++q8) {
                         float f[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int s = q8 * 8 + e;
-                            f[e] = s <= t ? expf(Gt - sG[r * kC + s]) * v[s] : 0.f;
+                            f[e] = s <= t ? expf(Gt - Gr[s]) * v[s] : 0.f;
                         }
-                        dst[q8] = pack_bf16x8(f);
+                        split_store(f, reinterpret_cast<uint8_t*>(p.qk_hi + o + 8 * q8),
+                                    reinterpret_cast<uint8_t*>(p.qk_lo + o + 8 * q8));
                     }
-                }
-            } else {  // A = strictly-lower beta_t e^{G_t-G_s} k_t.k_s, stored transposed
-                const int t = 32 * (warp - 2) + lane;
-                for (int r = 0; r < R; ++r) {
-                    const float Gt = sG[r * kC + t], bt = sBeta[r * kC + t];
-                    float* At = sAt + r * kC * kC;
+                } else {  // A = strictly-lower beta_t e^{G_t-G_s} k_t.k_s, stored transposed
+                    const int t = 32 * (warp - 2) + lane;
+                    const float Gt = Gr[t], bt = Br[t];
 #pragma unroll
                     for (int s = 0; s < kC; ++s)
-                        At[s * kC + t] = s < t ? bt * expf(Gt - sG[r * kC + s]) * v[s] : 0.f;
+                        sAt[s * kC + t] = s < t ? bt * expf(Gt - Gr[s]) * v[s] : 0.f;
+                }
+            } else {
+                // B rows s: [beta_s e^{G_s} k_s | beta_s v_s], MN-major, hi/lo
+                for (int it = tid - 128; it < kC * 32; it += 128) {
+                    const int ch = it & 7, blk = (it >> 3) & 3, s = it >> 5;
+                    const uint32_t pos = static_cast<uint32_t>((ch ^ (s & 7)) << 4);
+                    const float bt = Br[s];
+                    float f[8];
+                    if (blk < 2) {
+                        const uint32_t so = blk * 16384 + (64 + s) * 128 + pos;
+                        load_pair(sAg[0] + so, sAg[1] + so, f);
+                        const float sc = bt * expf(Gr[s]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] *= sc;
+                    } else if (s < L) {
+                        const size_t go = (size_t)(t0 + s) * cd + 2 * p.n_k_heads * kD + h * kD +
+                                          (blk - 2) * 64 + ch * 8;
+                        load_pair(reinterpret_cast<const uint8_t*>(p.qkv_hi + go),
+                                  reinterpret_cast<const uint8_t*>(p.qkv_lo + go), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] *= bt;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                    }
+                    split_store(f, sB[0] + blk * 8192 + s * 128 + pos, sB[1] + blk * 8192 + s * 128 + pos);
                 }
             }
-        }
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-
-        bool failed = false;
-        for (int r = 0; r < R && !failed; ++r) {
-            const int h = hk * R + r;
+            __syncthreads();
             if (warp < 2) {
                 // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
                 // substitution, eliminating one known entry at a time.
                 const int j = tid;
-                const float* At = sAt + r * kC * kC;
                 float x[kC];
 #pragma unroll
                 for (int t = 0; t < kC; ++t) x[t] = t == j ? 1.f : 0.f;
@@ -287,30 +346,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
                 for (int s = 0; s < kC - 1; ++s) {
                     const float xs = x[s];
 #pragma unroll
-                    for (int t = s + 1; t < kC; ++t) x[t] = fmaf(-At[s * kC + t], xs, x[t]);
+                    for (int t = s + 1; t < kC; ++t) x[t] = fmaf(-sAt[s * kC + t], xs, x[t]);
                 }
 #pragma unroll
-                for (int t = 0; t < kC; ++t)
-                    *reinterpret_cast<__nv_bfloat16*>(sT + t * 128 + ((((j >> 3) ^ (t & 7))) << 4) +
-                                                      (j & 7) * 2) = __float2bfloat16_rn(x[t]);
-            } else if (warp >= 4) {
-                // B rows s: [beta_s e^{G_s} k_s | beta_s v_s], MN-major
-                for (int it = tid - 128; it < kC * 32; it += 128) {
-                    const int ch = it & 7, blk = (it >> 3) & 3, s = it >> 5;
-                    const uint32_t pos = static_cast<uint32_t>((ch ^ (s & 7)) << 4);
-                    const float bt = sBeta[r * kC + s];
-                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                    if (blk < 2) {
-                        const uint4 src =
-                            *reinterpret_cast<const uint4*>(sAg + blk * 16384 + (64 + s) * 128 + pos);
-                        val = scale_bf16x8(src, bt * expf(sG[r * kC + s]));
-                    } else if (s < L) {
-                        const uint4 src = *reinterpret_cast<const uint4*>(
-                            p.qkv + (size_t)(t0 + s) * cd + 2 * p.n_k_heads * kD + h * kD +
-                            (blk - 2) * 64 + ch * 8);
-                        val = scale_bf16x8(src, bt);
-                    }
-                    *reinterpret_cast<uint4*>(sB + blk * 8192 + s * 128 + pos) = val;
+                for (int t = 0; t < kC; ++t) {
+                    const uint32_t o = t * 128 + ((((j >> 3) ^ (t & 7))) << 4) + (j & 7) * 2;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(x[t]);
+                    *reinterpret_cast<__nv_bfloat16*>(sT[0] + o) = hi;
+                    *reinterpret_cast<__nv_bfloat16*>(sT[1] + o) =
+                        __float2bfloat16_rn(x[t] - __bfloat162float(hi));
                 }
             }
             fence_proxy_async_smem();
@@ -320,9 +364,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
             if (tid == 0) {  // [W | U~] = T [beta e^G K | beta V]   (M padded to 128)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sT) + k * 32),
-                             desc_mnmajor_sw128(smem_u32(sB) + k * 2048, 8192),
-                             idesc_bf16_f32(128, 256, false, true), k > 0 ? 1u : 0u);
+                    mma3(tmem, desc_kmajor_sw128(smem_u32(sT[0]) + k * 32),
+                         desc_kmajor_sw128(smem_u32(sT[1]) + k * 32),
+                         desc_mnmajor_sw128(smem_u32(sB[0]) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(sB[1]) + k * 2048, 8192),
+                         idesc_bf16_f32(128, 256, false, true), k > 0 ? 1u : 0u);
                 mma_commit(&bar_mma);
             }
             mma_pending = true;
@@ -334,238 +380,293 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qkv, ChunkArgs p) {
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
-            if ((warp & 3) < 2) {  // rows t of W (warps 0,1) and of U~ (warps 4,5)
+            if ((warp & 3) < 2) {  // rows t of W (warps 0,1, hi/lo) and of U~ (warps 4,5, fp32)
                 const int t = 32 * (warp & 3) + lane;
-                const int col0 = (warp >> 2) * 128;
-                __nv_bfloat16* dst =
-                    (warp < 4 ? p.w_ws : p.u_ws) + ((size_t)(c * hv_n + h) * kC + t) * kD;
+                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD;
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     float v[32];
-                    tmem_ld32(tmem + ((32u * (warp & 3)) << 16) + col0 + 32 * cb, v);
+                    tmem_ld32(tmem + ((32u * (warp & 3)) << 16) + (warp >> 2) * 128 + 32 * cb, v);
+                    if (warp < 4) {
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8)
-                        reinterpret_cast<uint4*>(dst + 32 * cb)[q8] = pack_bf16x8(v + 8 * q8);
+                        for (int q8 = 0; q8 < 4; ++q8)
+                            split_store(v + 8 * q8,
+                                        reinterpret_cast<uint8_t*>(p.w_hi + o + 32 * cb + 8 * q8),
+                                        reinterpret_cast<uint8_t*>(p.w_lo + o + 32 * cb + 8 * q8));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(p.u_ws + o + 32 * cb);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                    }
                 }
             }
-            if (tid < kC) p.gcum_ws[(size_t)(c * hv_n + h) * kC + tid] = sG[r * kC + tid];
+            if (tid < kC) p.gcum_ws[(size_t)(c * hv_n + h) * kC + tid] = Gr[tid];
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
         }
+        (void)failed;
     } while (false);
 
     // Unwind after a give-up: let in-flight copies and MMAs land first.
-    if (tma_issued) mbar_wait(&bar_tma, 0);
+    if (tma_pending) mbar_wait(&bar_tma, 0);
     if (mma_pending) mbar_wait(&bar_mma, mma_phase);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // --------------------------------------------------------------- chunk_scan
-__global__ void __launch_bounds__(kChunkThreads, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_w,
-                  const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_qk,
+// A cluster of kSplit CTAs shares one (sequence, value head): CTA p owns value
+// lanes [64p, 64p+64) of the state, the outputs and U.  The per-token sums of
+// squares of the gated RMSNorm are exchanged through distributed shared memory.
+constexpr int kSplit = 2;
+constexpr int kDS = kD / kSplit;   // value lanes per CTA
+constexpr uint32_t kScanBsH = 0, kScanBsL = 16384, kScanAwH = 32768, kScanAwL = 65536,
+                   kScanAqH = 98304, kScanAqL = 114688, kScanBuH = 131072, kScanBuL = 139264,
+                   kScanAkH = 147456, kScanAkL = 163840, kScanEnd = 180224;
+
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
+chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                  const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                   ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sBs = smem;            // S (bf16), MN-major: 128 key rows x 128 value lanes
-    uint8_t* sAw = smem + 32768;    // [W; e^G Q] K-major, 2 column blocks x 128 rows
-    uint8_t* sAq = smem + 65536;    // [0; M o QK^T] K-major, 128 rows x 64
-    uint8_t* sBu = smem + 81920;    // U (bf16), MN-major: 64 token rows x 128 value lanes
-    uint8_t* sAk = smem + 98304;    // e^{G_last-G} K, MN-major: 64 token rows x 128 key lanes
-    uint8_t* sUt = smem + 114688;   // U~ rows (K-major, 2 column blocks x 64 rows)
+    uint8_t* sBs[2] = {smem + kScanBsH, smem + kScanBsL};  // S slice, MN-major 128 x 64
+    uint8_t* sAw[2] = {smem + kScanAwH, smem + kScanAwL};  // [W; e^G Q] K-major 128 x 128
+    uint8_t* sAq[2] = {smem + kScanAqH, smem + kScanAqL};  // [0; M o QK^T] K-major 128 x 64
+    uint8_t* sBu[2] = {smem + kScanBuH, smem + kScanBuL};  // U slice, MN-major 64 x 64
+    uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // e^{G_last-G} K, MN-major 64 x 128
     __shared__ float sG[kC];
     __shared__ float sSsq[2][kC];
+    __shared__ float sSsqC[2][kC];
     __shared__ __align__(8) uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, hf = warp >> 2;
     const int row = 32 * q + lane;  // tensor-memory lane this thread reads
-    const int h = blockIdx.x, n = blockIdx.y;
+    const uint32_t rank = cluster_ctarank();
+    const int h = blockIdx.x / kSplit, n = blockIdx.y;
+    const int j0 = static_cast<int>(rank) * kDS + 32 * hf;  // first value lane of this thread
     const int hv_n = p.n_v_heads;
     const int R = hv_n / p.n_k_heads, hk = h / R;
     const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
     const int c_begin = p.cu_chunks[n], c_end = p.cu_chunks[n + 1];
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
 
-    // fp32 state: this thread owns S[row][64*hf .. 64*hf+63]
-    float S[64];
+    // fp32 state: this thread owns S[row][j0 .. j0+31]
+    float S[32];
     if (p.state_in) {
-        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + 64 * hf);
+        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + j0);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const float4 v = src[i];
             S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = 0.f;
+        for (int i = 0; i < 32; ++i) S[i] = 0.f;
     }
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(sBs + hf * 16384 + row * 128 + ((ch ^ (row & 7)) << 4)) =
-            pack_bf16x8(S + 8 * ch);
-    for (int i = tid; i < 512; i += kChunkThreads)
-        reinterpret_cast<uint4*>(sAq)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
+        split_store(S + 8 * ch, sBs[0] + o, sBs[1] + o);
+    }
+    for (int i = tid; i < 1024; i += kChunkThreads)
+        reinterpret_cast<uint4*>(sAq[i >> 9])[i & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_slot, 256);
+    if (warp == 0) tmem_alloc(&tmem_slot, 128);
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;               // cols 0..127: [W S; Q S + (M o QK^T) U]
-    const uint32_t tmem_s = tmem + 128;            // cols 128..255: K'^T U
+    const uint32_t tmem = tmem_slot;     // cols 0..63: [W S ; e^G Q S + (M o QK^T) U]
+    const uint32_t tmem_s = tmem + 64;   // cols 64..127: K'^T U
     const uint32_t lane_off = (32u * q) << 16;
+    const uint32_t peer_ssq = map_to_rank(smem_u32(&sSsqC[0][0]), rank ^ 1u);
     uint32_t ld_phase = 0, mma_phase = 0;
-    bool ld_pending = false, mma_pending = false;
-    const bool act_is_sigmoid = p.act == 1;
+    bool ld_pending = false, mma_pending = false, dead = false;
+    const bool sigmoid_gate = p.act == 1;
+    const uint32_t id_p4 = idesc_bf16_f32(128, kDS, false, true);
+    const uint32_t id_p7 = idesc_bf16_f32(128, kDS, true, true);
 
     for (int c = c_begin; c < c_end; ++c) {
         const int t0 = bos + (c - c_begin) * kC;
         const int L = min(kC, eos - t0);
         const int wrow = (c * hv_n + h) * kC;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 8 * 8192 + 8192);
+        const int buf = (c - c_begin) & 1;
+        do {
+            if (dead) break;
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&bar_ld, 14 * 8192);
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                tma_load_2d(sAw + b * 16384, &map_w, &bar_ld, 64 * b, wrow);
-                tma_load_2d(sAw + b * 16384 + 8192, &map_qkv, &bar_ld, hk * kD + 64 * b, t0);
-                tma_load_2d(sAk + b * 8192, &map_qkv, &bar_ld,
-                            p.n_k_heads * kD + hk * kD + 64 * b, t0);
-                tma_load_2d(sUt + b * 8192, &map_u, &bar_ld, 64 * b, wrow);
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_2d(sAw[0] + b * 16384, &map_wh, &bar_ld, 64 * b, wrow);
+                    tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_ld, 64 * b, wrow);
+                    tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qh, &bar_ld, hk * kD + 64 * b, t0);
+                    tma_load_2d(sAw[1] + b * 16384 + 8192, &map_ql, &bar_ld, hk * kD + 64 * b, t0);
+                    tma_load_2d(sAk[0] + b * 8192, &map_qh, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
+                    tma_load_2d(sAk[1] + b * 8192, &map_ql, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
+                }
+                tma_load_2d(sAq[0] + 8192, &map_kqh, &bar_ld, 0, wrow);
+                tma_load_2d(sAq[1] + 8192, &map_kql, &bar_ld, 0, wrow);
             }
-            tma_load_2d(sAq + 8192, &map_qk, &bar_ld, 0, wrow);
-        }
-        ld_pending = true;
-        if (tid < kC) sG[tid] = p.gcum_ws[(size_t)wrow + tid];
-        if (any_failed(mbar_wait(&bar_ld, ld_phase))) {
-            if (tid == 0) report_error(4);
-            break;
-        }
-        ld_pending = false;
-        ld_phase ^= 1;
-        const float GL = sG[L - 1];
-        // Scale Q rows by e^{G_t} and K rows by e^{G_last-G_s}; zero rows >= L.
-        for (int it = tid; it < 2048; it += kChunkThreads) {
-            const int ch = it & 7, b = (it >> 3) & 1, r = (it >> 4) & 63, which = it >> 10;
-            uint8_t* ptr = which == 0 ? sAw + b * 16384 + (64 + r) * 128 + ch * 16
-                                      : sAk + b * 8192 + r * 128 + ch * 16;
-            const float f = r < L ? expf(which == 0 ? sG[r] : GL - sG[r]) : 0.f;
-            *reinterpret_cast<uint4*>(ptr) = scale_bf16x8(*reinterpret_cast<const uint4*>(ptr), f);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-        if (tid == 0) {  // [W S ; e^G Q S]
+            ld_pending = true;
+            if (tid < kC) sG[tid] = p.gcum_ws[(size_t)wrow + tid];
+            float ut[32];
+            if (q < 2) {  // U~ row `row`, value lanes j0 .. j0+31 (fp32)
+                const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow + row) * kD + j0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sAw) + (k >> 2) * 16384 + (k & 3) * 32),
-                         desc_mnmajor_sw128(smem_u32(sBs) + k * 2048, 16384),
-                         idesc_bf16_f32(128, 128, false, true), k > 0 ? 1u : 0u);
-            mma_commit(&bar_mma);
-        }
-        mma_pending = true;
-        if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
-            if (tid == 0) report_error(5);
-            break;
-        }
-        mma_pending = false;
-        mma_phase ^= 1;
-        tc_fence_after_sync();
-        if (q < 2) {  // U = U~ - W S for token row `row`, value lanes of half hf
-            float u[64];
-            tmem_ld32(tmem + lane_off + 64 * hf, u);
-            tmem_ld32(tmem + lane_off + 64 * hf + 32, u + 32);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint32_t pos = static_cast<uint32_t>((ch ^ (row & 7)) << 4);
-                float ut[8];
-                unpack_bf16x8(*reinterpret_cast<const uint4*>(sUt + hf * 8192 + row * 128 + pos), ut);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ut[e] -= u[8 * ch + e];
-                *reinterpret_cast<uint4*>(sBu + hf * 8192 + row * 128 + pos) = pack_bf16x8(ut);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = src[i];
+                    ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
+                }
             }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-        if (tid == 0) {
-            // O rows: e^G Q S + (M o QK^T) U  (rows 0..63 of A are zero)
+            if (any_failed(mbar_wait(&bar_ld, ld_phase))) {
+                if (tid == 0) report_error(4);
+                dead = true;
+                break;
+            }
+            ld_pending = false;
+            ld_phase ^= 1;
+            const float GL = sG[L - 1];
+            // Scale Q rows by e^{G_t} and K rows by e^{G_last-G_s}; zero rows >= L.
+            for (int it = tid; it < 2048; it += kChunkThreads) {
+                const int ch = it & 7, b = (it >> 3) & 1, r = (it >> 4) & 63, which = it >> 10;
+                const uint32_t o = which == 0 ? kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16
+                                              : kScanAkH + b * 8192 + r * 128 + ch * 16;
+                const uint32_t lo_off = which == 0 ? (kScanAwL - kScanAwH) : (kScanAkL - kScanAkH);
+                const float f = r < L ? expf(which == 0 ? sG[r] : GL - sG[r]) : 0.f;
+                float v[8];
+                load_pair(smem + o, smem + o + lo_off, v);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem, desc_kmajor_sw128(smem_u32(sAq) + k * 32),
-                         desc_mnmajor_sw128(smem_u32(sBu) + k * 2048, 8192),
-                         idesc_bf16_f32(128, 128, false, true), 1u);
-            // state increment: (e^{G_last-G} K)^T U
+                for (int e = 0; e < 8; ++e) v[e] *= f;
+                split_store(v, smem + o, smem + o + lo_off);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            tc_fence_after_sync();
+            if (tid == 0) {  // [W S ; e^G Q S]
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem_s, desc_mnmajor_sw128(smem_u32(sAk) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(sBu) + k * 2048, 8192),
-                         idesc_bf16_f32(128, 128, true, true), k > 0 ? 1u : 0u);
-            mma_commit(&bar_mma);
-        }
-        mma_pending = true;
-        if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
-            if (tid == 0) report_error(6);
-            break;
-        }
-        mma_pending = false;
-        mma_phase ^= 1;
-        tc_fence_after_sync();
-        {  // S <- e^{G_last} S + K'^T U ; refresh the bf16 copy
-            const float gam = expf(GL);
-            float ds[64];
-            tmem_ld32(tmem_s + lane_off + 64 * hf, ds);
-            tmem_ld32(tmem_s + lane_off + 64 * hf + 32, ds + 32);
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma3(tmem, desc_kmajor_sw128(smem_u32(sAw[0]) + ao),
+                         desc_kmajor_sw128(smem_u32(sAw[1]) + ao),
+                         desc_mnmajor_sw128(smem_u32(sBs[0]) + k * 2048, 16384),
+                         desc_mnmajor_sw128(smem_u32(sBs[1]) + k * 2048, 16384), id_p4,
+                         k > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_mma);
+            }
+            mma_pending = true;
+            if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
+                if (tid == 0) report_error(5);
+                dead = true;
+                break;
+            }
+            mma_pending = false;
+            mma_phase ^= 1;
+            tc_fence_after_sync();
+            if (q < 2) {  // U = U~ - W S for token row `row`, value lanes j0..j0+31
+                float ws[32];
+                tmem_ld32(tmem + lane_off + 32 * hf, ws);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) S[j] = fmaf(gam, S[j], ds[j]);
+                for (int i = 0; i < 32; ++i) ut[i] -= ws[i];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(sBs + hf * 16384 + row * 128 + ((ch ^ (row & 7)) << 4)) =
-                    pack_bf16x8(S + 8 * ch);
-        }
-        if (q >= 2) {  // output rows: partial sum of squares over this half
-            float o[64];
-            tmem_ld32(tmem + lane_off + 64 * hf, o);
-            tmem_ld32(tmem + lane_off + 64 * hf + 32, o + 32);
-            float ss = 0.f;
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
+                    split_store(ut + 8 * ch, sBu[0] + o, sBu[1] + o);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            tc_fence_after_sync();
+            if (tid == 0) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) ss = fmaf(o[j], o[j], ss);
-            sSsq[hf][row - 64] = ss;
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
-        tc_fence_after_sync();
-        if (q >= 2) {  // gated RMSNorm epilogue for token t
+                for (int k = 0; k < 4; ++k) {  // O += (M o QK^T) U   (rows 0..63 of A are zero)
+                    const uint64_t bh = desc_mnmajor_sw128(smem_u32(sBu[0]) + k * 2048, 8192);
+                    const uint64_t bl = desc_mnmajor_sw128(smem_u32(sBu[1]) + k * 2048, 8192);
+                    mma3(tmem, desc_kmajor_sw128(smem_u32(sAq[0]) + k * 32),
+                         desc_kmajor_sw128(smem_u32(sAq[1]) + k * 32), bh, bl, id_p4, 1u);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {  // state increment (e^{G_last-G} K)^T U
+                    const uint64_t bh = desc_mnmajor_sw128(smem_u32(sBu[0]) + k * 2048, 8192);
+                    const uint64_t bl = desc_mnmajor_sw128(smem_u32(sBu[1]) + k * 2048, 8192);
+                    mma3(tmem_s, desc_mnmajor_sw128(smem_u32(sAk[0]) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(sAk[1]) + k * 2048, 8192), bh, bl, id_p7,
+                         k > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_mma);
+            }
+            mma_pending = true;
+            if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
+                if (tid == 0) report_error(6);
+                dead = true;
+                break;
+            }
+            mma_pending = false;
+            mma_phase ^= 1;
+            tc_fence_after_sync();
+            {  // S <- e^{G_last} S + K'^T U ; refresh the split copy
+                const float gam = expf(GL);
+                float ds[32];
+                tmem_ld32(tmem_s + lane_off + 32 * hf, ds);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], ds[j]);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
+                    split_store(S + 8 * ch, sBs[0] + o, sBs[1] + o);
+                }
+            }
+            if (q >= 2) {  // output rows: partial sum of squares over 32 value lanes
+                float o[32];
+                tmem_ld32(tmem + lane_off + 32 * hf, o);
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+                sSsq[hf][row - 64] = ss;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncthreads();
+            tc_fence_after_sync();
+            if (tid < kC) sSsqC[buf][tid] = sSsq[0][tid] + sSsq[1][tid];
+        } while (false);
+        // Exchange the CTA's partial sums with its peer; every CTA of the
+        // cluster passes this barrier once per chunk, also after an error.
+        cluster_arrive();
+        cluster_wait();
+        if (!dead && q >= 2) {  // gated RMSNorm epilogue for token t, value lanes j0..j0+31
             const int t = row - 64;
             if (t < L) {
-                float o[64];
-                tmem_ld32(tmem + lane_off + 64 * hf, o);
-                tmem_ld32(tmem + lane_off + 64 * hf + 32, o + 32);
-                const float rr = rsqrtf((sSsq[0][t] + sSsq[1][t]) * (1.f / kD) + p.rms_eps);
-                const size_t base = (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + 64 * hf;
+                float o[32];
+                tmem_ld32(tmem + lane_off + 32 * hf, o);
+                const float tot = sSsqC[buf][t] + ld_cluster_f32(peer_ssq + (uint32_t)(buf * kC + t) * 4u);
+                const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
+                const size_t base = (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + j0;
                 const uint4* zp = reinterpret_cast<const uint4*>(p.z + base);
                 uint4* op = reinterpret_cast<uint4*>(p.out + base);
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = 0; ch < 4; ++ch) {
                     float zz[8], y[8];
                     unpack_bf16x8(zp[ch], zz);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float gate = act_is_sigmoid ? sigmoidf_(zz[e]) : siluf_(zz[e]);
-                        y[e] = o[8 * ch + e] * rr * p.norm_w[64 * hf + 8 * ch + e] * gate;
+                        const float gate = sigmoid_gate ? sigmoidf_(zz[e]) : siluf_(zz[e]);
+                        y[e] = o[8 * ch + e] * rr * p.norm_w[j0 + 8 * ch + e] * gate;
                     }
                     op[ch] = pack_bf16x8(y);
                 }
@@ -577,15 +678,18 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_cons
     if (ld_pending) mbar_wait(&bar_ld, ld_phase);
     if (mma_pending) mbar_wait(&bar_mma, mma_phase);
     if (p.state_out) {
-        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + 64 * hf);
+        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + j0);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     }
+    // No CTA may leave while its peer can still read its shared memory.
+    cluster_arrive();
+    cluster_wait();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ------------------------------------------------------------------- host
@@ -596,16 +700,20 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     long long chunks = 0;
     for (int i = 0; i < n_seq; ++i) chunks += (cu_host[i + 1] - cu_host[i] + kC - 1) / kC;
     const size_t cd = 2 * (size_t)n_k_heads * kD + (size_t)n_v_heads * kD;
+    const size_t crow = (size_t)chunks * n_v_heads * kC;  // rows of the per-chunk arrays
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     size_t off = 0;
-    l.qkv = off; off = up(off + (size_t)T * cd * 2);
+    l.qkv_hi = off; off = up(off + (size_t)T * cd * 2);
+    l.qkv_lo = off; off = up(off + (size_t)T * cd * 2);
     l.g = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.beta = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.cu_chunks = off; off = up(off + (size_t)(n_seq + 1) * 4);
-    l.w = off; off = up(off + (size_t)chunks * n_v_heads * kC * kD * 2);
-    l.u = off; off = up(off + (size_t)chunks * n_v_heads * kC * kD * 2);
-    l.qk = off; off = up(off + (size_t)chunks * n_v_heads * kC * kC * 2);
-    l.gcum = off; off = up(off + (size_t)chunks * n_v_heads * kC * 4);
+    l.w_hi = off; off = up(off + crow * kD * 2);
+    l.w_lo = off; off = up(off + crow * kD * 2);
+    l.u = off; off = up(off + crow * kD * 4);
+    l.qk_hi = off; off = up(off + crow * kC * 2);
+    l.qk_lo = off; off = up(off + crow * kC * 2);
+    l.gcum = off; off = up(off + crow * 4);
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
     if (lay) *lay = l;
@@ -620,14 +728,15 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     const int T = a.n_tokens;
     const int R = hv_n / hk_n;
 
-    // 1. prologue: conv + SiLU + L2 norm + gates -> qkv, g, beta (workspace)
+    // 1. prologue: conv + SiLU + L2 norm + gates -> q|k|v (hi, lo), g, beta
     ConvArgs cv{};
     cv.n_seq = a.n_seq; cv.n_tokens = T; cv.n_k_heads = hk_n; cv.n_v_heads = hv_n;
     cv.d_k = kD; cv.d_v = kD; cv.conv_k = a.conv_k; cv.l2_eps = a.l2_eps;
     cv.cu_seqlens = a.cu_seqlens; cv.x = a.x; cv.a = a.a; cv.b = a.b;
     cv.conv_w = a.conv_w; cv.A_log = a.A_log; cv.dt_bias = a.dt_bias;
     cv.conv_state_in = a.conv_state_in;
-    cv.qkv_out = ws + l.qkv;
+    cv.qkv_out = ws + l.qkv_hi;
+    cv.qkv_lo_out = ws + l.qkv_lo;
     cv.g_out = reinterpret_cast<float*>(ws + l.g);
     cv.beta_out = reinterpret_cast<float*>(ws + l.beta);
     cudaError_t e = timed_launch("conv_prologue", st, [&] { return launch_conv_prologue(cv, true, st); });
@@ -645,52 +754,57 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.n_seq = a.n_seq; p.n_tokens = T; p.n_chunks = l.n_chunks;
     p.n_k_heads = hk_n; p.n_v_heads = hv_n; p.act = a.act; p.rms_eps = a.rms_eps;
     p.cu_seqlens = a.cu_seqlens; p.cu_chunks = cu_chunks;
-    p.qkv = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv);
+    p.qkv_hi = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_hi);
+    p.qkv_lo = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_lo);
     p.g = reinterpret_cast<const float*>(ws + l.g);
     p.beta = reinterpret_cast<const float*>(ws + l.beta);
     p.z = static_cast<const __nv_bfloat16*>(a.z);
     p.norm_w = a.norm_w;
     p.state_in = a.state_in; p.state_out = a.state_out;
-    p.w_ws = reinterpret_cast<__nv_bfloat16*>(ws + l.w);
-    p.u_ws = reinterpret_cast<__nv_bfloat16*>(ws + l.u);
-    p.qk_ws = reinterpret_cast<__nv_bfloat16*>(ws + l.qk);
+    p.w_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.w_hi);
+    p.w_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.w_lo);
+    p.u_ws = reinterpret_cast<float*>(ws + l.u);
+    p.qk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_hi);
+    p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qkv, m_w, m_u, m_qk;
-    std::memset(&m_qkv, 0, sizeof(m_qkv));
-    m_w = m_u = m_qk = m_qkv;
-    const uint64_t wrows = (uint64_t)l.n_chunks * hv_n * kC;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql;
+    std::memset(&m_qh, 0, sizeof(m_qh));
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qh;
+    const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
-        if (!make_tma_map_bf16_2d(&m_qkv, ws + l.qkv, T, cd, cd, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_w, ws + l.w, wrows, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_u, ws + l.u, wrows, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_qk, ws + l.qk, wrows, kC, kC, 64, 64))
+        if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, T, cd, cd, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_ql, ws + l.qkv_lo, T, cd, cd, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64))
             return cudaErrorInvalidValue;
     }
 
-    const size_t prep_smem = 1024 + kPrepSmemFixed + (size_t)R * (kC * kC * 4 + 2 * kC * 4);
-    const size_t scan_smem = 1024 + kScanSmem;
+    const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 2 * kC * 4;
+    const size_t scan_smem = 1024 + kScanEnd;
     static bool attrs_set = false;
     if (!attrs_set) {
         cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             1024 + kPrepSmemFixed + 4 * (kC * kC * 4 + 2 * kC * 4));
+                             static_cast<int>(1024 + kPrepVec + 8 * 2 * kC * 4));
         cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(scan_smem));
         attrs_set = true;
     }
     if (l.n_chunks > 0) {
         e = timed_launch("chunk_prep", st, [&] {
-            chunk_prep_kernel<<<dim3(l.n_chunks, hk_n), kChunkThreads, prep_smem, st>>>(m_qkv, p);
+            chunk_prep_kernel<<<dim3(l.n_chunks, hk_n), kChunkThreads, prep_smem, st>>>(m_qh, m_ql, p);
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;
     }
     e = timed_launch("chunk_scan", st, [&] {
-        chunk_scan_kernel<<<dim3(hv_n, a.n_seq), kChunkThreads, scan_smem, st>>>(m_qkv, m_w, m_u,
-                                                                                m_qk, p);
+        chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
+            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, p);
         return cudaGetLastError();
     });
     return e;

@@ -66,6 +66,7 @@ conv_prologue_kernel(ConvArgs p) {
     const float qscale = rsqrtf((float)p.d_k);
     const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
     T* __restrict__ out = static_cast<T*>(p.qkv_out);
+    T* __restrict__ out_lo = static_cast<T*>(p.qkv_lo_out);
 
     for (int r = row; r < kConvTokTile; r += rows_per_pass) {
         const int t = tile0 + r;
@@ -108,7 +109,15 @@ conv_prologue_kernel(ConvArgs p) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[e] *= inv;
         }
-        if (valid) V::store(out + (size_t)t * cd + c, acc);
+        if (valid) {
+            V::store(out + (size_t)t * cd + c, acc);
+            if (out_lo) {  // bf16 residual: acc = hi + lo to ~16 significant bits
+                float lo[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) lo[e] = acc[e] - to_f32(from_f32<T>(acc[e]));
+                V::store(out_lo + (size_t)t * cd + c, lo);
+            }
+        }
     }
 }
 

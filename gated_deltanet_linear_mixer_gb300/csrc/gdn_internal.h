@@ -21,6 +21,7 @@ struct ConvArgs {
     const float* dt_bias;       // [Hv]
     const void* conv_state_in;  // [N, CD, K-1] or null
     void* qkv_out;              // [T, CD]
+    void* qkv_lo_out;           // [T, CD] bf16 residual x - bf16(x), or null (bf16 only)
     float* g_out;               // [T, Hv]
     float* beta_out;            // [T, Hv]
 };
@@ -62,29 +63,33 @@ struct CommitArgs {
     float* state;             // [n_seq, Hv, dk, dv]
 };
 
-// Arguments of the chunked (tensor-core) kernels.
+// Arguments of the chunked (tensor-core) kernels.  Operands that feed the
+// tensor cores are kept as bf16 (hi, lo) pairs: hi = bf16(x), lo = bf16(x - hi).
 struct ChunkArgs {
     int n_seq, n_tokens, n_chunks, n_k_heads, n_v_heads, act;
     float rms_eps;
-    const int32_t* cu_seqlens;  // [n_seq+1]
-    const int32_t* cu_chunks;   // [n_seq+1] chunk offsets (workspace)
-    const __nv_bfloat16* qkv;   // [T, CD] normalised q | k | v (workspace)
-    const float* g;             // [T, Hv] log-decay (workspace)
-    const float* beta;          // [T, Hv] (workspace)
-    const __nv_bfloat16* z;     // [T, Hv*dv]
-    const float* norm_w;        // [dv]
-    const float* state_in;      // [N, Hv, dk, dv] or null
-    float* state_out;           // or null
-    __nv_bfloat16* w_ws;        // [chunks, Hv, 64, dk]
-    __nv_bfloat16* u_ws;        // [chunks, Hv, 64, dv]
-    __nv_bfloat16* qk_ws;       // [chunks, Hv, 64, 64]
-    float* gcum_ws;             // [chunks, Hv, 64]
-    __nv_bfloat16* out;         // [T, Hv*dv]
+    const int32_t* cu_seqlens;    // [n_seq+1]
+    const int32_t* cu_chunks;     // [n_seq+1] chunk offsets (workspace)
+    const __nv_bfloat16* qkv_hi;  // [T, CD] normalised q | k | v, hi part (workspace)
+    const __nv_bfloat16* qkv_lo;  // [T, CD] lo part (workspace)
+    const float* g;               // [T, Hv] log-decay (workspace)
+    const float* beta;            // [T, Hv] (workspace)
+    const __nv_bfloat16* z;       // [T, Hv*dv]
+    const float* norm_w;          // [dv]
+    const float* state_in;        // [N, Hv, dk, dv] or null
+    float* state_out;             // or null
+    __nv_bfloat16* w_hi;          // [chunks, Hv, 64, dk] W (hi, lo)
+    __nv_bfloat16* w_lo;
+    float* u_ws;                  // [chunks, Hv, 64, dv] U~ (fp32)
+    __nv_bfloat16* qk_hi;         // [chunks, Hv, 64, 64] masked decayed Q K^T (hi, lo)
+    __nv_bfloat16* qk_lo;
+    float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
+    __nv_bfloat16* out;           // [T, Hv*dv]
 };
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv, g, beta, cu_chunks, w, u, qk, gcum, total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, gcum, total;
     int n_chunks;
 };
 
@@ -118,7 +123,7 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
                                ChunkLayout* layout);
 // Whether the chunked tensor-core path serves this geometry.
 inline bool chunked_supported(int d_k, int d_v, int n_k_heads, int n_v_heads, bool bf16) {
-    return bf16 && d_k == 128 && d_v == 128 && n_v_heads / n_k_heads <= 4;
+    return bf16 && d_k == 128 && d_v == 128 && n_v_heads / n_k_heads <= 8;
 }
 cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t stream);
 // Sticky device-side error word set by a kernel whose bounded wait gave up.

@@ -61,7 +61,25 @@ PREFILL_CASES = {
                                          slow_decay=True),
     "f32_slow_decay": lambda: _gen("r6", dtype="f32", lengths=[300, 17], state_std=0.05,
                                    conv_state_std=1.0, seed=16, slow_decay=True),
+    # tensor-core path (bf16, d_k = d_v = 128): GQA ratios 1, 2, 4, ragged chunks
+    "tc_mha_R1": lambda: _gen("t1", n_k_heads=2, n_v_heads=2, lengths=[150, 64, 65],
+                              state_std=0.05, conv_state_std=1.0, seed=31, act="sigmoid"),
+    "tc_gqa_R4": lambda: _gen("t2", n_k_heads=1, n_v_heads=4, lengths=[200, 1, 127],
+                              state_std=0.05, seed=32),
+    "tc_many_short": lambda: _gen("t3", n_k_heads=2, n_v_heads=4,
+                                  lengths=[1, 2, 3, 4, 5, 63, 64, 65, 0, 7, 130, 31],
+                                  state_std=0.05, conv_state_std=1.0, seed=33),
+    "tc_slow_decay_g0": lambda: _gen("t4", n_k_heads=2, n_v_heads=4, lengths=[1000],
+                                     state_std=0.05, seed=34, slow_decay=True),
 }
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    """Every test must leave the library's sticky device error word at 0."""
+    gdn.device_error(reset=True)
+    yield
+    assert gdn.device_error(reset=True) == 0, "a bounded device wait gave up"
 
 
 @pytest.mark.parametrize("name", sorted(PREFILL_CASES))
