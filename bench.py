@@ -313,6 +313,7 @@ def run_gpu(args):
     import torch.distributed as dist
     import gated_deltanet_linear_mixer_gb300 as gdn
     from gated_deltanet_linear_mixer_gb300 import _build, workloads
+    from gated_deltanet_linear_mixer_gb300.sharding import max_over_ranks
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -353,11 +354,7 @@ def run_gpu(args):
         per_step_launch = {k: v[0] / (args.steps + args.warmup) for k, v in rep.items()}
         launches = int(round(sum(per_step_launch.values()) * args.steps))
         mean_ms = statistics.mean(ms)
-        t_max = mean_ms
-        if world > 1:
-            tt = torch.tensor([mean_ms], device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_max = float(tt.item())
+        t_max = max_over_ranks(mean_ms, device=device)
         tok_s = world * r.tokens / (t_max / 1e3)
         # dominant kernel: largest total time
         dom = max(rep.items(), key=lambda kv: kv[1][1])
@@ -396,11 +393,7 @@ def run_gpu(args):
         # end to end through the public API with host buffers
         r.setup_e2e()
         e2e_ms = time_steps(r.e2e_step, max(2, args.steps // 2), 1, flush_buf, stream, barrier)
-        e2e_mean = statistics.mean(e2e_ms)
-        if world > 1:
-            tt = torch.tensor([e2e_mean], device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_mean = float(tt.item())
+        e2e_mean = max_over_ranks(statistics.mean(e2e_ms), device=device)
         res["e2e"] = {"value": world * r.tokens / (e2e_mean / 1e3), "unit": UNIT,
                       "h2d_bytes_per_step": r.h2d, "d2h_bytes_per_step": r.d2h,
                       "ms_per_step": e2e_mean}
