@@ -17,14 +17,16 @@
 //               factors, the unit-lower-triangular inverse T in fp32 on CUDA
 //               cores, then [W | U~] = T [beta e^G K | beta V] on the tensor
 //               core, for each value head of the group.
-//   chunk_scan  one CTA per (sequence, value head): carries S in fp32
-//               registers across the chunks; per chunk three MMA groups
-//               ([W; e^G Q] S,  then (M o QK^T) U and (e^{G_last-G} K)^T U),
-//               the state update and the fused gated RMSNorm epilogue.
+//   chunk_scan  a 2-CTA cluster per (sequence, value head), each CTA owning
+//               64 value lanes: carries S in fp32 registers across the chunks;
+//               per chunk three MMA groups ([W; e^G Q] S, then (M o QK^T) U and
+//               (e^{G_last-G} K)^T U), the state update and the fused gated
+//               RMSNorm epilogue.
 // Every operand tile is either loaded by TMA with the 128-byte swizzle or
-// written by threads in the same layout; operands whose contraction runs
-// along a tile's rows use the MN-major descriptor, so no tile is ever
-// transposed.
+// written by threads in the same layout.  B operands whose contraction runs
+// along a tile's rows (S, U, [K|V] rows) use the MN-major descriptor; every A
+// operand is K-major (the one A that would be MN-major, the scaled keys of the
+// state increment, is transposed by threads).
 #include <cstring>
 
 #include "gdn_common.cuh"
@@ -361,14 +363,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
-            if (tid == 0) {  // [W | U~] = T [beta e^G K | beta V]   (M padded to 128)
+            if (tid == 0) {  // W = T beta e^G K (cols 0..127), U~ = T beta V (cols 128..255)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma3(tmem, desc_kmajor_sw128(smem_u32(sT[0]) + k * 32),
-                         desc_kmajor_sw128(smem_u32(sT[1]) + k * 32),
-                         desc_mnmajor_sw128(smem_u32(sB[0]) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(sB[1]) + k * 2048, 8192),
-                         idesc_bf16_f32(128, 256, false, true), k > 0 ? 1u : 0u);
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma3(tmem + 128 * half, desc_kmajor_sw128(smem_u32(sT[0]) + k * 32),
+                             desc_kmajor_sw128(smem_u32(sT[1]) + k * 32),
+                             desc_mnmajor_sw128(smem_u32(sB[0]) + half * 16384 + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(sB[1]) + half * 16384 + k * 2048, 8192),
+                             idesc_bf16_f32(128, 128, false, true), k > 0 ? 1u : 0u);
                 mma_commit(&bar_mma);
             }
             mma_pending = true;
@@ -426,7 +430,8 @@ constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;   // value lanes per CTA
 constexpr uint32_t kScanBsH = 0, kScanBsL = 16384, kScanAwH = 32768, kScanAwL = 65536,
                    kScanAqH = 98304, kScanAqL = 114688, kScanBuH = 131072, kScanBuL = 139264,
-                   kScanAkH = 147456, kScanAkL = 163840, kScanEnd = 180224;
+                   kScanAkH = 147456, kScanAkL = 163840, kScanKsH = 180224, kScanKsL = 196608,
+                   kScanEnd = 212992;
 
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
@@ -440,7 +445,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     uint8_t* sAw[2] = {smem + kScanAwH, smem + kScanAwL};  // [W; e^G Q] K-major 128 x 128
     uint8_t* sAq[2] = {smem + kScanAqH, smem + kScanAqL};  // [0; M o QK^T] K-major 128 x 64
     uint8_t* sBu[2] = {smem + kScanBuH, smem + kScanBuL};  // U slice, MN-major 64 x 64
-    uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // e^{G_last-G} K, MN-major 64 x 128
+    uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // (e^{G_last-G} K)^T, K-major 128 x 64
+    uint8_t* sKs[2] = {smem + kScanKsH, smem + kScanKsL};  // K rows as loaded (64 x 128, 2 blocks)
     __shared__ float sG[kC];
     __shared__ float sSsq[2][kC];
     __shared__ float sSsqC[2][kC];
@@ -497,7 +503,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     bool ld_pending = false, mma_pending = false, dead = false;
     const bool sigmoid_gate = p.act == 1;
     const uint32_t id_p4 = idesc_bf16_f32(128, kDS, false, true);
-    const uint32_t id_p7 = idesc_bf16_f32(128, kDS, true, true);
 
     for (int c = c_begin; c < c_end; ++c) {
         const int t0 = bos + (c - c_begin) * kC;
@@ -514,8 +519,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_ld, 64 * b, wrow);
                     tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qh, &bar_ld, hk * kD + 64 * b, t0);
                     tma_load_2d(sAw[1] + b * 16384 + 8192, &map_ql, &bar_ld, hk * kD + 64 * b, t0);
-                    tma_load_2d(sAk[0] + b * 8192, &map_qh, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
-                    tma_load_2d(sAk[1] + b * 8192, &map_ql, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
+                    tma_load_2d(sKs[0] + b * 8192, &map_qh, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
+                    tma_load_2d(sKs[1] + b * 8192, &map_ql, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
                 }
                 tma_load_2d(sAq[0] + 8192, &map_kqh, &bar_ld, 0, wrow);
                 tma_load_2d(sAq[1] + 8192, &map_kql, &bar_ld, 0, wrow);
@@ -539,18 +544,36 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             ld_pending = false;
             ld_phase ^= 1;
             const float GL = sG[L - 1];
-            // Scale Q rows by e^{G_t} and K rows by e^{G_last-G_s}; zero rows >= L.
-            for (int it = tid; it < 2048; it += kChunkThreads) {
-                const int ch = it & 7, b = (it >> 3) & 1, r = (it >> 4) & 63, which = it >> 10;
-                const uint32_t o = which == 0 ? kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16
-                                              : kScanAkH + b * 8192 + r * 128 + ch * 16;
-                const uint32_t lo_off = which == 0 ? (kScanAwL - kScanAwH) : (kScanAkL - kScanAkH);
-                const float f = r < L ? expf(which == 0 ? sG[r] : GL - sG[r]) : 0.f;
+            // Scale Q rows by e^{G_t} in place; zero rows >= L.
+            for (int it = tid; it < 1024; it += kChunkThreads) {
+                const int ch = it & 7, b = (it >> 3) & 1, r = it >> 4;
+                const uint32_t o = kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16;
+                const float f = r < L ? expf(sG[r]) : 0.f;
                 float v[8];
-                load_pair(smem + o, smem + o + lo_off, v);
+                load_pair(smem + o, smem + o + (kScanAwL - kScanAwH), v);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] *= f;
-                split_store(v, smem + o, smem + o + lo_off);
+                split_store(v, smem + o, smem + o + (kScanAwL - kScanAwH));
+            }
+            {   // (e^{G_last-G_s} k_s)^T: thread (i, half) transposes 32 tokens of key lane i
+                const int i = tid & 127, s0 = 32 * (tid >> 7);
+                const uint32_t col = (i >> 6) * 8192 + (i & 7) * 2;
+                const uint32_t chunk = (i & 63) >> 3;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = s0 + 8 * c8 + e;
+                        const uint32_t o = col + s * 128 + ((chunk ^ (s & 7)) << 4);
+                        const float kv =
+                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[0] + o)) +
+                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[1] + o));
+                        v[e] = s < L ? kv * expf(GL - sG[s]) : 0.f;
+                    }
+                    const uint32_t d = i * 128 + (((4 * (tid >> 7) + c8) ^ (i & 7)) << 4);
+                    split_store(v, sAk[0] + d, sAk[1] + d);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -604,8 +627,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 for (int k = 0; k < 4; ++k) {  // state increment (e^{G_last-G} K)^T U
                     const uint64_t bh = desc_mnmajor_sw128(smem_u32(sBu[0]) + k * 2048, 8192);
                     const uint64_t bl = desc_mnmajor_sw128(smem_u32(sBu[1]) + k * 2048, 8192);
-                    mma3(tmem_s, desc_mnmajor_sw128(smem_u32(sAk[0]) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(sAk[1]) + k * 2048, 8192), bh, bl, id_p7,
+                    mma3(tmem_s, desc_kmajor_sw128(smem_u32(sAk[0]) + k * 32),
+                         desc_kmajor_sw128(smem_u32(sAk[1]) + k * 32), bh, bl, id_p4,
                          k > 0 ? 1u : 0u);
                 }
                 mma_commit(&bar_mma);
