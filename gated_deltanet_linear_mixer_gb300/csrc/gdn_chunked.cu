@@ -548,11 +548,16 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             for (int it = tid; it < 1024; it += kChunkThreads) {
                 const int ch = it & 7, b = (it >> 3) & 1, r = it >> 4;
                 const uint32_t o = kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16;
-                const float f = r < L ? expf(sG[r]) : 0.f;
                 float v[8];
-                load_pair(smem + o, smem + o + (kScanAwL - kScanAwH), v);
+                if (r < L) {
+                    const float f = expf(sG[r]);
+                    load_pair(smem + o, smem + o + (kScanAwL - kScanAwH), v);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= f;
+                    for (int e = 0; e < 8; ++e) v[e] *= f;
+                } else {  // rows past the chunk: zeros (they may hold any bits)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                }
                 split_store(v, smem + o, smem + o + (kScanAwL - kScanAwH));
             }
             {   // (e^{G_last-G_s} k_s)^T: thread (i, half) transposes 32 tokens of key lane i
@@ -726,8 +731,10 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     const size_t crow = (size_t)chunks * n_v_heads * kC;  // rows of the per-chunk arrays
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     size_t off = 0;
-    l.qkv_hi = off; off = up(off + (size_t)T * cd * 2);
-    l.qkv_lo = off; off = up(off + (size_t)T * cd * 2);
+    // q|k|v rows are padded by one chunk so that every 64-row TMA box that
+    // starts inside the batch stays inside the tensor (no out-of-bounds boxes).
+    l.qkv_hi = off; off = up(off + ((size_t)T + kC) * cd * 2);
+    l.qkv_lo = off; off = up(off + ((size_t)T + kC) * cd * 2);
     l.g = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.beta = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.cu_chunks = off; off = up(off + (size_t)(n_seq + 1) * 4);
@@ -799,8 +806,8 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     m_ql = m_wh = m_wl = m_kqh = m_kql = m_qh;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
-        if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, T, cd, cd, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_ql, ws + l.qkv_lo, T, cd, cd, 64, 64) ||
+        if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_ql, ws + l.qkv_lo, (uint64_t)T + kC, cd, cd, 64, 64) ||
             !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||

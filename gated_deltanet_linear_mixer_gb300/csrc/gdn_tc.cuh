@@ -65,12 +65,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Gives up after
 // `timeout_ns` and returns false (the caller records an error and unwinds),
 // so that a lost arrival can never hang the GPU.
+// Two independent bounds: the global nanosecond timer and the SM cycle
+// counter (2^32 cycles, ~2 s at 2 GHz), whichever runs out first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t timeout_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > timeout_ns) return false;
+        if (clock64() - c0 > (1ll << 32)) return false;
     }
     return true;
 }
