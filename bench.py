@@ -140,17 +140,17 @@ class Runner:
             return act + n * ((1 + c.tokens_per_seq) * _state_bytes(c) + _conv_state_bytes(c))
         raise KeyError(self.key)
 
-    def kernel_bytes(self, name):
+    def kernel_bytes(self, name, kernels=()):
         """Algorithmic bytes of one launch of kernel `name` (for the roofline).
 
-        The conv-state kernel moves the K-1 history rows; every other kernel of
-        a step is charged the rest of the step's algorithmic bytes."""
+        A separate conv-state kernel, when the step launches one, is charged the
+        K-1 history rows; the step's other kernels share the rest."""
         c = self.case
         conv = c.n_seq * _conv_state_bytes(c)
         hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0}[self.key]
         if name == "conv_state":
             return hist
-        return self.algorithmic_bytes() - hist
+        return self.algorithmic_bytes() - (hist if "conv_state" in kernels else 0)
 
     def useful_flops(self, chunk=64):
         """Useful flops of the chunked form per step (prefill), else of the recurrence."""
@@ -360,7 +360,7 @@ def run_gpu(args):
         dom = max(rep.items(), key=lambda kv: kv[1][1])
         dom_name, (dom_n, dom_ms) = dom
         dom_avg_ms = dom_ms / dom_n
-        kb = r.kernel_bytes(dom_name)
+        kb = r.kernel_bytes(dom_name, rep.keys())
         achieved = kb / (dom_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,

@@ -679,9 +679,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         cluster_wait();
         if (!dead && q >= 2) {  // gated RMSNorm epilogue for token t, value lanes j0..j0+31
             const int t = row - 64;
+            float o[32];
+            tmem_ld32(tmem + lane_off + 32 * hf, o);  // warp-collective: every lane loads
             if (t < L) {
-                float o[32];
-                tmem_ld32(tmem + lane_off + 32 * hf, o);
                 const float tot = sSsqC[buf][t] + ld_cluster_f32(peer_ssq + (uint32_t)(buf * kC + t) * 4u);
                 const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
                 const size_t base = (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + j0;

@@ -133,7 +133,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
  * gdn_decode -- T tokens (1 <= T <= 16) for each of n_seq sequences against a
  * resident fp32 state: cpu.rs deltanet (one token) run T times, or a short
  * speculative-verify chunk.  Layouts are [n_seq, T, ...] (packed with uniform
- * lengths).
+ * lengths).  conv_state, when given, must be 16-byte aligned.
  *   inter_states == NULL: state [N, Hv, dk, dv] and conv_state [N, CD, K-1]
  *     are updated in place to their values after the T tokens.
  *   inter_states != NULL ([N, T, Hv, dk, dv]): the state after every token is
@@ -179,8 +179,8 @@ size_t gdn_timing_report(char* buf, size_t buf_len);
  * gdn_device_error -- the library's sticky device-side error word.  Kernels
  * whose waits are bounded (the tensor-core prefill waits on its own TMA copies
  * and MMAs) give up after ~2 s instead of hanging, store a nonzero code here
- * (1..6 name the wait that gave up) and exit cleanly; their outputs are then
- * invalid.  Waits for the device (cudaMemcpyFromSymbol), writes the code to
+ * (1..6: the tensor-core prefill's waits; 101: the decode kernel's
+ * prefetch wait) and exit cleanly; their outputs are then invalid.  Waits for the device (cudaMemcpyFromSymbol), writes the code to
  * *code (0 = no error) and clears it when reset != 0.
  */
 gdn_status gdn_device_error(int32_t* code, int32_t reset);
