@@ -161,7 +161,8 @@ __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint6
 
 // --------------------------------------------------------------- chunk_prep
 constexpr uint32_t kPrepAgH = 0, kPrepAgL = 32768, kPrepTH = 65536, kPrepTL = 81920,
-                   kPrepBH = 98304, kPrepBL = 131072, kPrepAt = 163840, kPrepVec = 180224;
+                   kPrepBH = 98304, kPrepBL = 131072, kPrepAt = 163840, kPrepVH = 180224,
+                   kPrepVL = 196608, kPrepVec = 212992;
 
 __global__ void __launch_bounds__(kChunkThreads, 1)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
@@ -173,10 +174,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     uint8_t* sT[2] = {smem + kPrepTH, smem + kPrepTL};     // T K-major, rows 64.. zero
     uint8_t* sB[2] = {smem + kPrepBH, smem + kPrepBL};     // [beta e^G K | beta V] MN-major
     float* sAt = reinterpret_cast<float*>(smem + kPrepAt); // A^T [s][t] of one head
+    uint8_t* sV[2] = {smem + kPrepVH, smem + kPrepVL};     // v rows of one head (hi, lo)
     const int R = p.n_v_heads / p.n_k_heads;
     float* sG = reinterpret_cast<float*>(smem + kPrepVec);
     float* sBeta = sG + R * kC;
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_v;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -189,6 +191,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_v, 1);
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
@@ -226,9 +229,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const uint32_t tmem_g = tmem + 256;     // cols 256..319: Gram
     uint32_t mma_phase = 0;
     bool tma_pending = false, mma_pending = false;
+    int v_issued = 0, v_done = 0;  // value heads whose v tiles were requested / consumed
+    // v rows of value head hk*R + r (both column blocks, hi and lo) -> sV
+    auto issue_v = [&](int r) {
+        const int vc = 2 * p.n_k_heads * kD + (hk * R + r) * kD;
+        mbar_arrive_expect_tx(&bar_v, 4 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_2d(sV[0] + b * 8192, &map_qh, &bar_v, vc + 64 * b, t0);
+            tma_load_2d(sV[1] + b * 8192, &map_ql, &bar_v, vc + 64 * b, t0);
+        }
+    };
 
     do {
         if (tid == 0) {
+            issue_v(0);
             mbar_arrive_expect_tx(&bar_tma, 8 * 8192);
             const int qc = hk * kD, kc = p.n_k_heads * kD + hk * kD;
 #pragma unroll
@@ -240,6 +255,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             }
         }
         tma_pending = true;
+        v_issued = 1;
         if (any_failed(mbar_wait(&bar_tma, 0))) {
             if (tid == 0) report_error(1);
             break;
@@ -283,6 +299,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             const int h = hk * R + r;
             const float* Gr = sG + r * kC;
             const float* Br = sBeta + r * kC;
+            if (any_failed(mbar_wait(&bar_v, r & 1))) {  // this head's v tiles
+                if (tid == 0) report_error(7);
+                failed = true;
+                break;
+            }
+            v_done = r + 1;
             if (warp < 4) {
                 float v[64];
                 tmem_ld32(tmem_g + ((32u * warp) << 16), v);
@@ -323,10 +345,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] *= sc;
                     } else if (s < L) {
-                        const size_t go = (size_t)(t0 + s) * cd + 2 * p.n_k_heads * kD + h * kD +
-                                          (blk - 2) * 64 + ch * 8;
-                        load_pair(reinterpret_cast<const uint8_t*>(p.qkv_hi + go),
-                                  reinterpret_cast<const uint8_t*>(p.qkv_lo + go), f);
+                        const uint32_t so = (blk - 2) * 8192 + s * 128 + pos;
+                        load_pair(sV[0] + so, sV[1] + so, f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] *= bt;
                     } else {
@@ -337,6 +357,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 }
             }
             __syncthreads();
+            if (tid == 0 && r + 1 < R) {  // next head's v tiles land during this head's solve
+                issue_v(r + 1);
+                v_issued = r + 2;
+            }
             if (warp < 2) {
                 // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
                 // substitution, eliminating one known entry at a time.
@@ -414,7 +438,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     } while (false);
 
     // Unwind after a give-up: let in-flight copies and MMAs land first.
+    v_issued = __syncthreads_or(v_issued > v_done) ? v_done + 1 : v_done;
     if (tma_pending) mbar_wait(&bar_tma, 0);
+    if (v_issued > v_done) mbar_wait(&bar_v, v_done & 1);
     if (mma_pending) mbar_wait(&bar_mma, mma_phase);
     tc_fence_before_sync();
     __syncthreads();
@@ -447,10 +473,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     uint8_t* sBu[2] = {smem + kScanBuH, smem + kScanBuL};  // U slice, MN-major 64 x 64
     uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // (e^{G_last-G} K)^T, K-major 128 x 64
     uint8_t* sKs[2] = {smem + kScanKsH, smem + kScanKsL};  // K rows as loaded (64 x 128, 2 blocks)
-    __shared__ float sG[kC];
+    __shared__ float sG[2][kC];       // in-chunk cumulative log-decay, double-buffered
     __shared__ float sSsq[2][kC];
     __shared__ float sSsqC[2][kC];
-    __shared__ __align__(8) uint64_t bar_ld, bar_mma;
+    __shared__ __align__(8) uint64_t bar_wq, bar_k, bar_kq, bar_mma;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -462,7 +488,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const int hv_n = p.n_v_heads;
     const int R = hv_n / p.n_k_heads, hk = h / R;
     const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
-    const int c_begin = p.cu_chunks[n], c_end = p.cu_chunks[n + 1];
+    const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
 
     // fp32 state: this thread owns S[row][j0 .. j0+31]
@@ -486,11 +512,14 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     for (int i = tid; i < 1024; i += kChunkThreads)
         reinterpret_cast<uint4*>(sAq[i >> 9])[i & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
-        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_wq, 1);
+        mbar_init(&bar_k, 1);
+        mbar_init(&bar_kq, 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 128);
+    if (tid < kC && n_ch > 0) sG[0][tid] = p.gcum_ws[(size_t)(c_begin * hv_n + h) * kC + tid];
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -499,58 +528,94 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const uint32_t tmem_s = tmem + 64;   // cols 64..127: K'^T U
     const uint32_t lane_off = (32u * q) << 16;
     const uint32_t peer_ssq = map_to_rank(smem_u32(&sSsqC[0][0]), rank ^ 1u);
-    uint32_t ld_phase = 0, mma_phase = 0;
-    bool ld_pending = false, mma_pending = false, dead = false;
     const bool sigmoid_gate = p.act == 1;
     const uint32_t id_p4 = idesc_bf16_f32(128, kDS, false, true);
+    const int kcol = p.n_k_heads * kD + hk * kD;
 
-    for (int c = c_begin; c < c_end; ++c) {
-        const int t0 = bos + (c - c_begin) * kC;
+    // Loads of chunk i (within this sequence), three groups with their own
+    // barriers so that each can be issued as soon as its buffer is free.
+    auto issue_wq = [&](int i) {  // W and q rows -> [W; Q]
+        const int wrow = ((c_begin + i) * hv_n + h) * kC, t0 = bos + i * kC;
+        mbar_arrive_expect_tx(&bar_wq, 8 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_2d(sAw[0] + b * 16384, &map_wh, &bar_wq, 64 * b, wrow);
+            tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_wq, 64 * b, wrow);
+            tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qh, &bar_wq, hk * kD + 64 * b, t0);
+            tma_load_2d(sAw[1] + b * 16384 + 8192, &map_ql, &bar_wq, hk * kD + 64 * b, t0);
+        }
+    };
+    auto issue_k = [&](int i) {  // k rows -> staging
+        const int t0 = bos + i * kC;
+        mbar_arrive_expect_tx(&bar_k, 4 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_2d(sKs[0] + b * 8192, &map_qh, &bar_k, kcol + 64 * b, t0);
+            tma_load_2d(sKs[1] + b * 8192, &map_ql, &bar_k, kcol + 64 * b, t0);
+        }
+    };
+    auto issue_kq = [&](int i) {  // masked decayed Q K^T -> rows 64..127 of [0; M o QK^T]
+        const int wrow = ((c_begin + i) * hv_n + h) * kC;
+        mbar_arrive_expect_tx(&bar_kq, 2 * 8192);
+        tma_load_2d(sAq[0] + 8192, &map_kqh, &bar_kq, 0, wrow);
+        tma_load_2d(sAq[1] + 8192, &map_kql, &bar_kq, 0, wrow);
+    };
+    // issued[g] / done[g]: loads of each group requested / waited for
+    int issued_wq = 0, issued_k = 0, issued_kq = 0, done_wq = 0, done_k = 0, done_kq = 0;
+    uint32_t mma_phase = 0;
+    bool mma_pending = false, dead = false;
+    if (n_ch > 0) {
+        if (tid == 0) {
+            issue_wq(0);
+            issue_k(0);
+            issue_kq(0);
+        }
+        issued_wq = issued_k = issued_kq = 1;
+    }
+    float ut[32];  // U~ row `row`, value lanes j0..j0+31, of the current chunk (q < 2)
+    if (q < 2 && n_ch > 0) {
+        const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)(c_begin * hv_n + h) * kC + row) * kD + j0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = src[i];
+            ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
+        }
+    }
+
+    for (int i = 0; i < n_ch; ++i) {
+        const int t0 = bos + i * kC;
         const int L = min(kC, eos - t0);
-        const int wrow = (c * hv_n + h) * kC;
-        const int buf = (c - c_begin) & 1;
+        const int buf = i & 1;
+        const float* Gc = sG[buf];
+        float g_next = 0.f;
+        uint4 zr[4];
         do {
             if (dead) break;
-            if (tid == 0) {
-                mbar_arrive_expect_tx(&bar_ld, 14 * 8192);
+            // prefetch: next chunk's G, this chunk's z rows for the epilogue
+            if (tid < kC && i + 1 < n_ch)
+                g_next = p.gcum_ws[(size_t)((c_begin + i + 1) * hv_n + h) * kC + tid];
+            if (q >= 2 && row - 64 < L) {
+                const uint4* zp = reinterpret_cast<const uint4*>(
+                    p.z + (size_t)(t0 + row - 64) * hv_n * kD + (size_t)h * kD + j0);
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    tma_load_2d(sAw[0] + b * 16384, &map_wh, &bar_ld, 64 * b, wrow);
-                    tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_ld, 64 * b, wrow);
-                    tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qh, &bar_ld, hk * kD + 64 * b, t0);
-                    tma_load_2d(sAw[1] + b * 16384 + 8192, &map_ql, &bar_ld, hk * kD + 64 * b, t0);
-                    tma_load_2d(sKs[0] + b * 8192, &map_qh, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
-                    tma_load_2d(sKs[1] + b * 8192, &map_ql, &bar_ld, p.n_k_heads * kD + hk * kD + 64 * b, t0);
-                }
-                tma_load_2d(sAq[0] + 8192, &map_kqh, &bar_ld, 0, wrow);
-                tma_load_2d(sAq[1] + 8192, &map_kql, &bar_ld, 0, wrow);
+                for (int ch = 0; ch < 4; ++ch) zr[ch] = zp[ch];
             }
-            ld_pending = true;
-            if (tid < kC) sG[tid] = p.gcum_ws[(size_t)wrow + tid];
-            float ut[32];
-            if (q < 2) {  // U~ row `row`, value lanes j0 .. j0+31 (fp32)
-                const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow + row) * kD + j0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 v = src[i];
-                    ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
-                }
-            }
-            if (any_failed(mbar_wait(&bar_ld, ld_phase))) {
+            const bool okk = mbar_wait(&bar_k, i & 1);
+            const bool okw = mbar_wait(&bar_wq, i & 1);
+            if (any_failed(okk && okw)) {
                 if (tid == 0) report_error(4);
                 dead = true;
                 break;
             }
-            ld_pending = false;
-            ld_phase ^= 1;
-            const float GL = sG[L - 1];
+            done_k = done_wq = i + 1;
+            const float GL = Gc[L - 1];
             // Scale Q rows by e^{G_t} in place; zero rows >= L.
             for (int it = tid; it < 1024; it += kChunkThreads) {
                 const int ch = it & 7, b = (it >> 3) & 1, r = it >> 4;
                 const uint32_t o = kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16;
                 float v[8];
                 if (r < L) {
-                    const float f = expf(sG[r]);
+                    const float f = expf(Gc[r]);
                     load_pair(smem + o, smem + o + (kScanAwL - kScanAwH), v);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v[e] *= f;
@@ -561,9 +626,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 split_store(v, smem + o, smem + o + (kScanAwL - kScanAwH));
             }
             {   // (e^{G_last-G_s} k_s)^T: thread (i, half) transposes 32 tokens of key lane i
-                const int i = tid & 127, s0 = 32 * (tid >> 7);
-                const uint32_t col = (i >> 6) * 8192 + (i & 7) * 2;
-                const uint32_t chunk = (i & 63) >> 3;
+                const int ki = tid & 127, s0 = 32 * (tid >> 7);
+                const uint32_t col = (ki >> 6) * 8192 + (ki & 7) * 2;
+                const uint32_t chunk = (ki & 63) >> 3;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     float v[8];
@@ -574,9 +639,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                         const float kv =
                             __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[0] + o)) +
                             __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[1] + o));
-                        v[e] = s < L ? kv * expf(GL - sG[s]) : 0.f;
+                        v[e] = s < L ? kv * expf(GL - Gc[s]) : 0.f;
                     }
-                    const uint32_t d = i * 128 + (((4 * (tid >> 7) + c8) ^ (i & 7)) << 4);
+                    const uint32_t d = ki * 128 + (((4 * (tid >> 7) + c8) ^ (ki & 7)) << 4);
                     split_store(v, sAk[0] + d, sAk[1] + d);
                 }
             }
@@ -584,9 +649,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
-            if (tid == 0) {  // [W S ; e^G Q S]
+            if (tid == 0) {
+                if (i + 1 < n_ch) issue_k(i + 1);  // staging is free again
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < 8; ++k) {  // [W S ; e^G Q S]
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
                     mma3(tmem, desc_kmajor_sw128(smem_u32(sAw[0]) + ao),
                          desc_kmajor_sw128(smem_u32(sAw[1]) + ao),
@@ -596,6 +662,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 }
                 mma_commit(&bar_mma);
             }
+            if (i + 1 < n_ch) issued_k = i + 2;
             mma_pending = true;
             if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(5);
@@ -605,20 +672,37 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
+            if (tid == 0 && i + 1 < n_ch) issue_wq(i + 1);  // [W; Q] consumed
+            if (i + 1 < n_ch) issued_wq = i + 2;
             if (q < 2) {  // U = U~ - W S for token row `row`, value lanes j0..j0+31
                 float ws[32];
                 tmem_ld32(tmem + lane_off + 32 * hf, ws);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) ut[i] -= ws[i];
+                for (int e = 0; e < 32; ++e) ut[e] -= ws[e];
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
                     split_store(ut + 8 * ch, sBu[0] + o, sBu[1] + o);
                 }
+                if (i + 1 < n_ch) {  // next chunk's U~ row
+                    const float4* src = reinterpret_cast<const float4*>(
+                        p.u_ws + ((size_t)((c_begin + i + 1) * hv_n + h) * kC + row) * kD + j0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 v = src[e];
+                        ut[4 * e] = v.x; ut[4 * e + 1] = v.y; ut[4 * e + 2] = v.z; ut[4 * e + 3] = v.w;
+                    }
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            __syncthreads();
+            const bool okq = mbar_wait(&bar_kq, i & 1);
+            if (any_failed(okq)) {
+                if (tid == 0) report_error(8);
+                dead = true;
+                break;
+            }
+            done_kq = i + 1;
             tc_fence_after_sync();
             if (tid == 0) {
 #pragma unroll
@@ -647,6 +731,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
+            if (tid == 0 && i + 1 < n_ch) issue_kq(i + 1);  // [0; M o QK^T] consumed
+            if (i + 1 < n_ch) issued_kq = i + 2;
             {  // S <- e^{G_last} S + K'^T U ; refresh the split copy
                 const float gam = expf(GL);
                 float ds[32];
@@ -667,6 +753,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
                 sSsq[hf][row - 64] = ss;
             }
+            if (tid < kC && i + 1 < n_ch) sG[buf ^ 1][tid] = g_next;
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
@@ -684,13 +771,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             if (t < L) {
                 const float tot = sSsqC[buf][t] + ld_cluster_f32(peer_ssq + (uint32_t)(buf * kC + t) * 4u);
                 const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
-                const size_t base = (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + j0;
-                const uint4* zp = reinterpret_cast<const uint4*>(p.z + base);
-                uint4* op = reinterpret_cast<uint4*>(p.out + base);
+                uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + j0);
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     float zz[8], y[8];
-                    unpack_bf16x8(zp[ch], zz);
+                    unpack_bf16x8(zr[ch], zz);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float gate = sigmoid_gate ? sigmoidf_(zz[e]) : siluf_(zz[e]);
@@ -703,7 +788,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         }
     }
 
-    if (ld_pending) mbar_wait(&bar_ld, ld_phase);
+    // Unwind: let every copy and MMA still in flight land before leaving.
+    if (__syncthreads_or(issued_k > done_k)) mbar_wait(&bar_k, done_k & 1);
+    if (__syncthreads_or(issued_wq > done_wq)) mbar_wait(&bar_wq, done_wq & 1);
+    if (__syncthreads_or(issued_kq > done_kq)) mbar_wait(&bar_kq, done_kq & 1);
     if (mma_pending) mbar_wait(&bar_mma, mma_phase);
     if (p.state_out) {
         float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + j0);

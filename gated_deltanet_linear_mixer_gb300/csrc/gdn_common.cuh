@@ -21,6 +21,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
     static constexpr int N = 4;
+    __device__ __forceinline__ static uint4 load_raw(const float* p) {
+        return *reinterpret_cast<const uint4*>(p);
+    }
+    __device__ __forceinline__ static void unpack(uint4 v, float* out) {
+        out[0] = __uint_as_float(v.x); out[1] = __uint_as_float(v.y);
+        out[2] = __uint_as_float(v.z); out[3] = __uint_as_float(v.w);
+    }
     __device__ __forceinline__ static void load(const float* p, float* out) {
         float4 v = *reinterpret_cast<const float4*>(p);
         out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
@@ -31,6 +38,17 @@ template <> struct Vec16<float> {
 };
 template <> struct Vec16<__nv_bfloat16> {
     static constexpr int N = 8;
+    __device__ __forceinline__ static uint4 load_raw(const __nv_bfloat16* p) {
+        return *reinterpret_cast<const uint4*>(p);
+    }
+    __device__ __forceinline__ static void unpack(uint4 v, float* out) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
     __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* out) {
         uint4 v = *reinterpret_cast<const uint4*>(p);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};

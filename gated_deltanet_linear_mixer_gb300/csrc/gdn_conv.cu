@@ -5,9 +5,10 @@
 //
 // Work split: one CTA = one head's channels ("unit": a q head, a k head or a
 // v head) x a tile of 64 tokens.  Each thread owns one 16-byte vector of
-// channels (8 bf16 / 4 fp32) of one token row, so loads and stores of x and
-// qkv_out are 16-byte, fully coalesced; the d-wide L2 norm of a q/k head is a
-// shuffle reduction over the d/VEC lanes that share the token.  One extra
+// channels (8 bf16 / 4 fp32) and a run of consecutive tokens; it loads each
+// raw row of its window once (all loads issued up front), so loads and stores
+// of x and qkv_out are 16-byte and coalesced; the d-wide L2 norm of a q/k head
+// is a shuffle reduction over the d/VEC lanes that share the token.  One extra
 // unit per token tile computes g and beta.  The whole pass reads x once and
 // writes qkv_out once, so it is bound by HBM bandwidth.
 #include "gdn_common.cuh"
@@ -49,52 +50,79 @@ conv_prologue_kernel(ConvArgs p) {
     const int D = (is_q || is_k) ? p.d_k : p.d_v;
     const int ch0 = (is_q || is_k) ? unit * p.d_k
                                    : 2 * p.n_k_heads * p.d_k + (unit - 2 * p.n_k_heads) * p.d_v;
-    const int tpr = D / VEC;               // threads per token row (power of 2, <= 32)
-    const int rows_per_pass = kConvThreads / tpr;
+    const int tpr = D / VEC;                 // threads per token row (power of 2, <= 32)
+    const int runs = kConvThreads / tpr;     // token runs per tile
+    const int TR = kConvTokTile / runs;      // consecutive tokens per thread (2..16)
     const int lane_in_row = threadIdx.x % tpr;
-    const int row = threadIdx.x / tpr;
-    const int c = ch0 + lane_in_row * VEC;  // first channel of this thread
+    const int run = threadIdx.x / tpr;
+    const int c = ch0 + lane_in_row * VEC;   // first channel of this thread
     const int K = p.conv_k;
     const int keep = K - 1;
+    const int tr0 = tile0 + run * TR;        // first token of this thread's run
 
+    // Taps padded to 4 with leading zero weights: padded tap k multiplies
+    // raw row t-3+k, so every window index below is a compile-time constant.
+    const int pad = 4 - K;
     float w[VEC][4];
 #pragma unroll
     for (int e = 0; e < VEC; ++e)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[e][j] = j < K ? p.conv_w[(size_t)(c + e) * K + j] : 0.0f;
+        for (int k = 0; k < 4; ++k)
+            w[e][k] = k >= pad ? p.conv_w[(size_t)(c + e) * K + (k - pad)] : 0.0f;
 
     const float qscale = rsqrtf((float)p.d_k);
     const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
     T* __restrict__ out = static_cast<T*>(p.qkv_out);
     T* __restrict__ out_lo = static_cast<T*>(p.qkv_lo_out);
 
-    for (int r = row; r < kConvTokTile; r += rows_per_pass) {
-        const int t = tile0 + r;
+    // Sliding window: the raw rows tr0-3 .. tr0+TR-1 are loaded once each,
+    // all issued before any is used.
+    constexpr int kMaxTR = 16;
+    uint4 raw[kMaxTR + 3];  // packed rows, unpacked at use
+#pragma unroll
+    for (int i = 0; i < kMaxTR + 3; ++i) {
+        const int row = tr0 - 3 + i;
+        raw[i] = (i < TR + 3 && row >= 0 && row < p.n_tokens) ? V::load_raw(x + (size_t)row * cd + c)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+    }
+    int n = 0, bos = 0, eos = 0;
+    if (tr0 < p.n_tokens) {
+        n = seq_of_token(p.cu_seqlens, p.n_seq, tr0);
+        bos = p.cu_seqlens[n];
+        eos = p.cu_seqlens[n + 1];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTR; ++j) {
+        if (j >= TR) break;  // uniform across the warp: TR is per CTA
+        const int t = tr0 + j;
         const bool valid = t < p.n_tokens;
+        if (valid) {
+            while (t >= eos) {  // crossed into the next non-empty sequence
+                ++n;
+                bos = p.cu_seqlens[n];
+                eos = p.cu_seqlens[n + 1];
+            }
+        }
         float acc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
         if (valid) {
-            const int n = seq_of_token(p.cu_seqlens, p.n_seq, t);
-            const int bos = p.cu_seqlens[n];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j >= K) break;
-                const int src = t - keep + j;
-                float v[VEC];
+            for (int k = 0; k < 4; ++k) {
+                if (k < pad) continue;
+                const int src = t - 3 + k;               // raw row j + k of the window
                 if (src >= bos) {
-                    V::load(x + (size_t)src * cd + c, v);
+                    float v[VEC];
+                    V::unpack(raw[j + k], v);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w[e][k], v[e], acc[e]);
                 } else if (cs_in) {
                     const int slot = keep + (src - bos);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e)
-                        v[e] = to_f32(cs_in[((size_t)n * cd + c + e) * keep + slot]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) v[e] = 0.0f;
+                        acc[e] = fmaf(w[e][k], to_f32(cs_in[((size_t)n * cd + c + e) * keep + slot]),
+                                      acc[e]);
                 }
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w[e][j], v[e], acc[e]);
             }
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[e] = siluf_(acc[e]);

@@ -38,7 +38,7 @@ recurrent_kernel(RecurrentArgs p) {
     __shared__ float cbuf[kRecTokBlock][CH];
     __shared__ float gam[kRecTokBlock], bet[kRecTokBlock], kqs[kRecTokBlock];
     __shared__ float red[NW][2][DV];
-    __shared__ float dlt[DV];
+    __shared__ __align__(16) float dlt[DV];  // read back as float4
     __shared__ float ysum[DV / 32];
 
     const int hv = blockIdx.x;
@@ -302,7 +302,7 @@ decode_stream_kernel(DecodeArgs p) {
     __shared__ __align__(8) uint64_t bars[3];
     __shared__ float gam[16], bet[16], kqs[16];
     __shared__ float red[NW][2][DV];
-    __shared__ float dlt[DV];
+    __shared__ __align__(16) float dlt[DV];  // read back as float4
     __shared__ float ysum[DV / 32];
     __shared__ float s_norm_w[DV];
 
