@@ -468,6 +468,30 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """One warm-up call and one profiled call of a workload, untimed (for ncu)."""
+    import torch
+    import gated_deltanet_linear_mixer_gb300 as gdn
+    from gated_deltanet_linear_mixer_gb300 import _build, workloads
+    _build.build()
+    gdn.load()
+    key = args.profile
+    if key == "decode64":  # a 64-sequence decode step: 128 MiB of state (> L2)
+        case = workloads.generate("decode_N64_T1_Hk16_Hv32_d128_bf16", n_k_heads=16, n_v_heads=32,
+                                  d_k=128, d_v=128, mode="decode", n_seq=64, tokens_per_seq=1,
+                                  dtype="bf16", act="sigmoid", seed=2, state_std=0.05,
+                                  conv_state_std=1.0)
+        key = "decode"
+    else:
+        case = workloads.config(WORKLOADS[key])
+    r = Runner(key, case, torch.device("cuda", 0))
+    for _ in range(2):
+        r.step()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "workload": case.name,
+                      "device_error": gdn.device_error()}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,10 +501,14 @@ def main():
     ap.add_argument("--extras", default="decode,varlen,spec_verify",
                     help="comma list of extra workloads in the same line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64"],
+                    help="run one warm-up and one call of a workload, untimed (for ncu)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     args.extras = [e for e in args.extras.split(",") if e]
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -196,11 +196,9 @@ size_t gdn_timing_report(char* buf, size_t buf_len) {
 gdn_status gdn_device_error(int32_t* code, int32_t reset) {
     const char* fn = "gdn_device_error";
     if (!code) return fail(GDN_ERR_INVALID_ARG, fn, "code is NULL");
-    int v = 0, w = 0;
+    int v = 0;
     gdn_status st = cuda_status(gdn::read_device_error(&v, reset != 0), fn, "reading the error word");
-    if (st == GDN_OK)
-        st = cuda_status(gdn::read_decode_error(&w, reset != 0), fn, "reading the error word");
-    *code = v ? v : (w ? 100 + w : 0);
+    *code = v;
     return st;
 }
 
@@ -359,23 +357,30 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (conv_state && !aligned16(conv_state))
-        return fail(GDN_ERR_INVALID_ARG, fn, "conv_state must be 16-byte aligned");
-    gdn::DecodeArgs d{};
-    d.n_seq = n_seq; d.T = T; d.n_k_heads = dims->n_k_heads; d.n_v_heads = dims->n_v_heads;
-    d.conv_k = dims->conv_k; d.act = dims->act; d.l2_eps = dims->l2_eps; d.rms_eps = dims->rms_eps;
-    d.x = x; d.z = z; d.a = a; d.b = b;
-    d.conv_w = params->conv_w; d.A_log = params->A_log; d.dt_bias = params->dt_bias;
-    d.norm_w = params->norm_w;
-    d.conv_state = conv_state;
-    d.write_conv = inter_states ? 0 : 1;
-    d.state = state;
-    d.inter = inter_states;
-    d.out = out;
-    if ((st = cuda_status(timed_launch("decode_stream", s, [&] {
-             return gdn::launch_decode_stream(d, dims->d_k, dims->d_v, bf16, s);
-         }), fn, "decode launch")) != GDN_OK)
+    gdn::RecurrentArgs r{};
+    r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
+    r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
+    r.cu_seqlens = nullptr; r.uniform_T = T;
+    r.x = x; r.z = z; r.a = a; r.b = b;
+    r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
+    r.norm_w = params->norm_w; r.conv_state_in = conv_state;
+    r.state_in = state;
+    r.state_out = inter_states ? nullptr : state;
+    r.inter = inter_states;
+    r.out = out;
+    if ((st = cuda_status(timed_launch("recurrent", s, [&] {
+             return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s);
+         }), fn, "recurrent launch")) != GDN_OK)
         return st;
+    if (conv_state && !inter_states) {
+        gdn::ConvStateArgs c{};
+        c.n_seq = n_seq; c.n_k_heads = dims->n_k_heads; c.n_v_heads = dims->n_v_heads;
+        c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
+        c.cu_seqlens = nullptr; c.uniform_T = T; c.x = x;
+        c.conv_state_in = conv_state; c.conv_state_out = conv_state;
+        if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
+            return st;
+    }
     return GDN_OK;
 }
 

@@ -56,23 +56,6 @@ struct RecurrentArgs {
     void* out;                  // [T, Hv*dv]
 };
 
-// Persistent decode: one CTA per SM walks (sequence, key head) groups and
-// their value heads, prefetching each head's state and inputs with bulk
-// copies into a ring of shared-memory stages.
-struct DecodeArgs {
-    int n_seq, T, n_k_heads, n_v_heads, conv_k, act;
-    float l2_eps, rms_eps;
-    const void *x, *z, *a, *b;   // [N*T, CD], [N*T, Hv*dv], [N*T, Hv] x2
-    const float *conv_w, *A_log, *dt_bias, *norm_w;
-    void* conv_state;            // [N, CD, K-1] or null
-    int write_conv;              // update the conv history in place
-    float* state;                // [N, Hv, dk, dv]
-    float* inter;                // [N, T, Hv, dk, dv] or null (then state is updated in place)
-    void* out;                   // [N, T, Hv*dv]
-    uint32_t stage_bytes;        // bytes of one pipeline stage
-    int n_stages;
-};
-
 struct CommitArgs {
     int n_seq, n_v_heads, d_k, d_v, T;
     const int32_t* accepted;  // [n_seq]
@@ -151,8 +134,5 @@ cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t st
 cudaError_t launch_recurrent(const RecurrentArgs& p, int d_k, int d_v, bool bf16,
                              cudaStream_t stream);
 cudaError_t launch_commit_state(const CommitArgs& p, cudaStream_t stream);
-cudaError_t launch_decode_stream(DecodeArgs p, int d_k, int d_v, bool bf16, cudaStream_t stream);
-// Sticky error word of the decode kernel's bounded waits.
-cudaError_t read_decode_error(int* code, bool reset);
 
 }  // namespace gdn

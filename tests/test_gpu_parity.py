@@ -209,9 +209,9 @@ def test_decode_equals_prefill_of_same_tokens():
     case = _gen("dp", mode="decode", n_seq=3, tokens_per_seq=4, state_std=0.05,
                 conv_state_std=1.0, seed=27)
     dec = gpu_decode(case)
-    pre = gpu_prefill(case)
-    assert rel_err(dec["out"], pre["out"].float().cpu().numpy()) <= 1e-2
-    assert rel_err(dec["state"], pre["state"].cpu().numpy()) <= 1e-4
+    pre = gpu_prefill(case)  # bf16, d=128: the tensor-core path
+    assert rel_err(dec["out"], pre["out"].float().cpu().numpy()) <= TOL["bf16"]
+    assert rel_err(dec["state"], pre["state"].cpu().numpy()) <= TOL["bf16"]
     assert rel_err(dec["conv_state"], pre["conv_state"].float().cpu().numpy()) == 0.0
 
 
