@@ -141,6 +141,16 @@ void drain_pending_locked() {
 
 namespace gdn {
 
+gdn_status set_error(gdn_status st, const char* fn, const char* fmt, ...) {
+    int n = std::snprintf(g_err, sizeof(g_err), "%s: ", fn);
+    if (n < 0) n = 0;
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err + n, sizeof(g_err) - (size_t)n, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 void* timing_start(const char* name, cudaStream_t stream) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     if (!g_timing_on) return nullptr;

@@ -361,6 +361,45 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 issue_v(r + 1);
                 v_issued = r + 2;
             }
+            if (warp >= 2 && warp < 4) {
+                // operand rows the state scan needs, prepared here off its chain:
+                // q~_t = e^{G_t} q_t (zero past the chunk), hi/lo
+                const int t = 32 * (warp - 2) + lane;
+                const float f = t < L ? expf(Gr[t]) : 0.f;
+                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD;
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch) {
+                    const uint32_t so = (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
+                    float v[8];
+                    load_pair(sAg[0] + so, sAg[1] + so, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
+                    split_store(v, reinterpret_cast<uint8_t*>(p.qt_hi + o + 8 * ch),
+                                reinterpret_cast<uint8_t*>(p.qt_lo + o + 8 * ch));
+                }
+            } else if (warp >= 4) {
+                // (e^{G_last-G_s} k_s)^T: thread i writes key lane i over the tokens
+                const int ki = tid - 128;
+                const float GL = Gr[L - 1];
+                const uint32_t col = (ki >> 6) * 16384 + (ki & 7) * 2;
+                const uint32_t chunk = (ki & 63) >> 3;
+                const size_t o = ((size_t)(c * hv_n + h) * kD + ki) * kC;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int sidx = 8 * c8 + e;
+                        const uint32_t so = col + (64 + sidx) * 128 + ((chunk ^ (sidx & 7)) << 4);
+                        const float kv =
+                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sAg[0] + so)) +
+                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sAg[1] + so));
+                        v[e] = sidx < L ? kv * expf(GL - Gr[sidx]) : 0.f;
+                    }
+                    split_store(v, reinterpret_cast<uint8_t*>(p.kt_hi + o + 8 * c8),
+                                reinterpret_cast<uint8_t*>(p.kt_lo + o + 8 * c8));
+                }
+            }
             if (warp < 2) {
                 // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
                 // substitution, eliminating one known entry at a time.
@@ -456,13 +495,13 @@ constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;   // value lanes per CTA
 constexpr uint32_t kScanBsH = 0, kScanBsL = 16384, kScanAwH = 32768, kScanAwL = 65536,
                    kScanAqH = 98304, kScanAqL = 114688, kScanBuH = 131072, kScanBuL = 139264,
-                   kScanAkH = 147456, kScanAkL = 163840, kScanKsH = 180224, kScanKsL = 196608,
-                   kScanEnd = 212992;
+                   kScanAkH = 147456, kScanAkL = 163840, kScanEnd = 180224;
 
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qth, const __grid_constant__ CUtensorMap map_qtl,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                  const __grid_constant__ CUtensorMap map_kth, const __grid_constant__ CUtensorMap map_ktl,
                   ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -472,8 +511,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     uint8_t* sAq[2] = {smem + kScanAqH, smem + kScanAqL};  // [0; M o QK^T] K-major 128 x 64
     uint8_t* sBu[2] = {smem + kScanBuH, smem + kScanBuL};  // U slice, MN-major 64 x 64
     uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // (e^{G_last-G} K)^T, K-major 128 x 64
-    uint8_t* sKs[2] = {smem + kScanKsH, smem + kScanKsL};  // K rows as loaded (64 x 128, 2 blocks)
-    __shared__ float sG[2][kC];       // in-chunk cumulative log-decay, double-buffered
     __shared__ float sSsq[2][kC];
     __shared__ float sSsqC[2][kC];
     __shared__ __align__(8) uint64_t bar_wq, bar_k, bar_kq, bar_mma;
@@ -519,7 +556,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 128);
-    if (tid < kC && n_ch > 0) sG[0][tid] = p.gcum_ws[(size_t)(c_begin * hv_n + h) * kC + tid];
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
@@ -530,28 +566,32 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const uint32_t peer_ssq = map_to_rank(smem_u32(&sSsqC[0][0]), rank ^ 1u);
     const bool sigmoid_gate = p.act == 1;
     const uint32_t id_p4 = idesc_bf16_f32(128, kDS, false, true);
-    const int kcol = p.n_k_heads * kD + hk * kD;
+    // in-chunk log-decay at the chunk's last token, e^{.} of which decays the state
+    auto last_g = [&](int i) {
+        const int L = min(kC, eos - (bos + i * kC));
+        return p.gcum_ws[(size_t)((c_begin + i) * hv_n + h) * kC + L - 1];
+    };
 
     // Loads of chunk i (within this sequence), three groups with their own
     // barriers so that each can be issued as soon as its buffer is free.
-    auto issue_wq = [&](int i) {  // W and q rows -> [W; Q]
-        const int wrow = ((c_begin + i) * hv_n + h) * kC, t0 = bos + i * kC;
+    auto issue_wq = [&](int i) {  // W rows and e^{G} q rows -> [W; Q~]
+        const int wrow = ((c_begin + i) * hv_n + h) * kC;
         mbar_arrive_expect_tx(&bar_wq, 8 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             tma_load_2d(sAw[0] + b * 16384, &map_wh, &bar_wq, 64 * b, wrow);
             tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_wq, 64 * b, wrow);
-            tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qh, &bar_wq, hk * kD + 64 * b, t0);
-            tma_load_2d(sAw[1] + b * 16384 + 8192, &map_ql, &bar_wq, hk * kD + 64 * b, t0);
+            tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qth, &bar_wq, 64 * b, wrow);
+            tma_load_2d(sAw[1] + b * 16384 + 8192, &map_qtl, &bar_wq, 64 * b, wrow);
         }
     };
-    auto issue_k = [&](int i) {  // k rows -> staging
-        const int t0 = bos + i * kC;
+    auto issue_k = [&](int i) {  // (e^{G_last-G} K)^T rows -> A of the state increment
+        const int krow = ((c_begin + i) * hv_n + h) * kD;
         mbar_arrive_expect_tx(&bar_k, 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(sKs[0] + b * 8192, &map_qh, &bar_k, kcol + 64 * b, t0);
-            tma_load_2d(sKs[1] + b * 8192, &map_ql, &bar_k, kcol + 64 * b, t0);
+            tma_load_2d(sAk[0] + b * 8192, &map_kth, &bar_k, 0, krow + 64 * b);
+            tma_load_2d(sAk[1] + b * 8192, &map_ktl, &bar_k, 0, krow + 64 * b);
         }
     };
     auto issue_kq = [&](int i) {  // masked decayed Q K^T -> rows 64..127 of [0; M o QK^T]
@@ -572,6 +612,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         }
         issued_wq = issued_k = issued_kq = 1;
     }
+    float gl_cur = n_ch > 0 ? last_g(0) : 0.f, gl_next = 0.f;
     float ut[32];  // U~ row `row`, value lanes j0..j0+31, of the current chunk (q < 2)
     if (q < 2 && n_ch > 0) {
         const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)(c_begin * hv_n + h) * kC + row) * kD + j0);
@@ -586,15 +627,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         const int t0 = bos + i * kC;
         const int L = min(kC, eos - t0);
         const int buf = i & 1;
-        const float* Gc = sG[buf];
-        float g_next = 0.f;
+        const float GL = gl_cur;
         uint4 zr[4];
         do {
             if (dead) break;
-            // prefetch: next chunk's G, this chunk's z rows for the epilogue
-            if (tid < kC && i + 1 < n_ch)
-                g_next = p.gcum_ws[(size_t)((c_begin + i + 1) * hv_n + h) * kC + tid];
-            if (q >= 2 && row - 64 < L) {
+            if (i + 1 < n_ch) gl_next = last_g(i + 1);  // prefetched for the next chunk
+            if (q >= 2 && row - 64 < L) {  // this chunk's z rows for the epilogue
                 const uint4* zp = reinterpret_cast<const uint4*>(
                     p.z + (size_t)(t0 + row - 64) * hv_n * kD + (size_t)h * kD + j0);
 #pragma unroll
@@ -608,49 +646,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 break;
             }
             done_k = done_wq = i + 1;
-            const float GL = Gc[L - 1];
-            // Scale Q rows by e^{G_t} in place; zero rows >= L.
-            for (int it = tid; it < 1024; it += kChunkThreads) {
-                const int ch = it & 7, b = (it >> 3) & 1, r = it >> 4;
-                const uint32_t o = kScanAwH + b * 16384 + (64 + r) * 128 + ch * 16;
-                float v[8];
-                if (r < L) {
-                    const float f = expf(Gc[r]);
-                    load_pair(smem + o, smem + o + (kScanAwL - kScanAwH), v);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] *= f;
-                } else {  // rows past the chunk: zeros (they may hold any bits)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-                }
-                split_store(v, smem + o, smem + o + (kScanAwL - kScanAwH));
-            }
-            {   // (e^{G_last-G_s} k_s)^T: thread (i, half) transposes 32 tokens of key lane i
-                const int ki = tid & 127, s0 = 32 * (tid >> 7);
-                const uint32_t col = (ki >> 6) * 8192 + (ki & 7) * 2;
-                const uint32_t chunk = (ki & 63) >> 3;
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = s0 + 8 * c8 + e;
-                        const uint32_t o = col + s * 128 + ((chunk ^ (s & 7)) << 4);
-                        const float kv =
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[0] + o)) +
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sKs[1] + o));
-                        v[e] = s < L ? kv * expf(GL - Gc[s]) : 0.f;
-                    }
-                    const uint32_t d = ki * 128 + (((4 * (tid >> 7) + c8) ^ (ki & 7)) << 4);
-                    split_store(v, sAk[0] + d, sAk[1] + d);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            __syncthreads();
             tc_fence_after_sync();
             if (tid == 0) {
-                if (i + 1 < n_ch) issue_k(i + 1);  // staging is free again
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {  // [W S ; e^G Q S]
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
@@ -662,7 +659,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 }
                 mma_commit(&bar_mma);
             }
-            if (i + 1 < n_ch) issued_k = i + 2;
             mma_pending = true;
             if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(5);
@@ -731,8 +727,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
-            if (tid == 0 && i + 1 < n_ch) issue_kq(i + 1);  // [0; M o QK^T] consumed
-            if (i + 1 < n_ch) issued_kq = i + 2;
+            if (tid == 0 && i + 1 < n_ch) {  // [0; M o QK^T] and the keys are consumed
+                issue_kq(i + 1);
+                issue_k(i + 1);
+            }
+            if (i + 1 < n_ch) issued_kq = issued_k = i + 2;
             {  // S <- e^{G_last} S + K'^T U ; refresh the split copy
                 const float gam = expf(GL);
                 float ds[32];
@@ -753,13 +752,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
                 sSsq[hf][row - 64] = ss;
             }
-            if (tid < kC && i + 1 < n_ch) sG[buf ^ 1][tid] = g_next;
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
             if (tid < kC) sSsqC[buf][tid] = sSsq[0][tid] + sSsq[1][tid];
         } while (false);
+        gl_cur = gl_next;
         // Exchange the CTA's partial sums with its peer; every CTA of the
         // cluster passes this barrier once per chunk, also after an error.
         cluster_arrive();
@@ -831,6 +830,10 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.u = off; off = up(off + crow * kD * 4);
     l.qk_hi = off; off = up(off + crow * kC * 2);
     l.qk_lo = off; off = up(off + crow * kC * 2);
+    l.qt_hi = off; off = up(off + crow * kD * 2);
+    l.qt_lo = off; off = up(off + crow * kD * 2);
+    l.kt_hi = off; off = up(off + (size_t)chunks * n_v_heads * kD * kC * 2);
+    l.kt_lo = off; off = up(off + (size_t)chunks * n_v_heads * kD * kC * 2);
     l.gcum = off; off = up(off + crow * 4);
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
@@ -884,14 +887,18 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.u_ws = reinterpret_cast<float*>(ws + l.u);
     p.qk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_hi);
     p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
+    p.qt_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qt_hi);
+    p.qt_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qt_lo);
+    p.kt_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.kt_hi);
+    p.kt_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.kt_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_qth, m_qtl, m_kth, m_ktl;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qth = m_qtl = m_kth = m_ktl = m_qh;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
@@ -899,7 +906,11 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64))
+            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_qth, ws + l.qt_hi, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_qtl, ws + l.qt_lo, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kth, ws + l.kt_hi, (uint64_t)l.n_chunks * hv_n * kD, kC, kC, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_ktl, ws + l.kt_lo, (uint64_t)l.n_chunks * hv_n * kD, kC, kC, 64, 64))
             return cudaErrorInvalidValue;
     }
 
@@ -922,7 +933,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     }
     e = timed_launch("chunk_scan", st, [&] {
         chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
-            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, p);
+            m_qth, m_qtl, m_wh, m_wl, m_kqh, m_kql, m_kth, m_ktl, p);
         return cudaGetLastError();
     });
     return e;

@@ -75,75 +75,78 @@ conv_prologue_kernel(ConvArgs p) {
     T* __restrict__ out = static_cast<T*>(p.qkv_out);
     T* __restrict__ out_lo = static_cast<T*>(p.qkv_lo_out);
 
-    // Sliding window: the raw rows tr0-3 .. tr0+TR-1 are loaded once each,
-    // all issued before any is used.
-    constexpr int kMaxTR = 16;
-    uint4 raw[kMaxTR + 3];  // packed rows, unpacked at use
+    // Sliding window in passes of up to 8 tokens: the raw rows t-3 .. t+7 of a
+    // pass are loaded once each, all issued before any is used.
+    constexpr int kPass = 8;
+    for (int p0 = 0; p0 < TR; p0 += kPass) {
+        const int tp = tr0 + p0;
+        uint4 raw[kPass + 3];  // packed rows, unpacked at use
 #pragma unroll
-    for (int i = 0; i < kMaxTR + 3; ++i) {
-        const int row = tr0 - 3 + i;
-        raw[i] = (i < TR + 3 && row >= 0 && row < p.n_tokens) ? V::load_raw(x + (size_t)row * cd + c)
-                                                              : make_uint4(0u, 0u, 0u, 0u);
-    }
-    int n = 0, bos = 0, eos = 0;
-    if (tr0 < p.n_tokens) {
-        n = seq_of_token(p.cu_seqlens, p.n_seq, tr0);
-        bos = p.cu_seqlens[n];
-        eos = p.cu_seqlens[n + 1];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTR; ++j) {
-        if (j >= TR) break;  // uniform across the warp: TR is per CTA
-        const int t = tr0 + j;
-        const bool valid = t < p.n_tokens;
-        if (valid) {
-            while (t >= eos) {  // crossed into the next non-empty sequence
-                ++n;
-                bos = p.cu_seqlens[n];
-                eos = p.cu_seqlens[n + 1];
-            }
+        for (int i = 0; i < kPass + 3; ++i) {
+            const int row = tp - 3 + i;
+            raw[i] = (i < TR - p0 + 3 && row >= 0 && row < p.n_tokens)
+                         ? V::load_raw(x + (size_t)row * cd + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float acc[VEC];
+        int n = 0, bos = 0, eos = 0;
+        if (tp < p.n_tokens) {
+            n = seq_of_token(p.cu_seqlens, p.n_seq, tp);
+            bos = p.cu_seqlens[n];
+            eos = p.cu_seqlens[n + 1];
+        }
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
-        if (valid) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (k < pad) continue;
-                const int src = t - 3 + k;               // raw row j + k of the window
-                if (src >= bos) {
-                    float v[VEC];
-                    V::unpack(raw[j + k], v);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w[e][k], v[e], acc[e]);
-                } else if (cs_in) {
-                    const int slot = keep + (src - bos);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e)
-                        acc[e] = fmaf(w[e][k], to_f32(cs_in[((size_t)n * cd + c + e) * keep + slot]),
-                                      acc[e]);
+        for (int j = 0; j < kPass; ++j) {
+            if (p0 + j >= TR) break;  // uniform across the warp: TR is per CTA
+            const int t = tp + j;
+            const bool valid = t < p.n_tokens;
+            if (valid) {
+                while (t >= eos) {  // crossed into the next non-empty sequence
+                    ++n;
+                    bos = p.cu_seqlens[n];
+                    eos = p.cu_seqlens[n + 1];
                 }
             }
+            float acc[VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] = siluf_(acc[e]);
-        }
-        if (is_q || is_k) {
-            float ss = 0.0f;
+            for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+            if (valid) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) ss = fmaf(acc[e], acc[e], ss);
-            for (int off = tpr / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            float inv = rsqrtf(ss + p.l2_eps);
-            if (is_q) inv *= qscale;
+                for (int k = 0; k < 4; ++k) {
+                    if (k < pad) continue;
+                    const int src = t - 3 + k;           // raw row j + k of the window
+                    if (src >= bos) {
+                        float v[VEC];
+                        V::unpack(raw[j + k], v);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] *= inv;
-        }
-        if (valid) {
-            V::store(out + (size_t)t * cd + c, acc);
-            if (out_lo) {  // bf16 residual: acc = hi + lo to ~16 significant bits
-                float lo[VEC];
+                        for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w[e][k], v[e], acc[e]);
+                    } else if (cs_in) {
+                        const int slot = keep + (src - bos);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) lo[e] = acc[e] - to_f32(from_f32<T>(acc[e]));
-                V::store(out_lo + (size_t)t * cd + c, lo);
+                        for (int e = 0; e < VEC; ++e)
+                            acc[e] = fmaf(w[e][k], to_f32(cs_in[((size_t)n * cd + c + e) * keep + slot]),
+                                          acc[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = siluf_(acc[e]);
+            }
+            if (is_q || is_k) {
+                float ss = 0.0f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) ss = fmaf(acc[e], acc[e], ss);
+                for (int off = tpr / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                float inv = rsqrtf(ss + p.l2_eps);
+                if (is_q) inv *= qscale;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] *= inv;
+            }
+            if (valid) {
+                V::store(out + (size_t)t * cd + c, acc);
+                if (out_lo) {  // bf16 residual: acc = hi + lo to ~16 significant bits
+                    float lo[VEC];
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) lo[e] = acc[e] - to_f32(from_f32<T>(acc[e]));
+                    V::store(out_lo + (size_t)t * cd + c, lo);
+                }
             }
         }
     }
