@@ -28,9 +28,10 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_SILU, ACT_SIGMOID = 0, 1
 
 # Every symbol include/gdn.h declares.
-EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_decode",
-           "gdn_decode_commit", "gdn_timing_enable", "gdn_timing_report", "gdn_device_error",
-           "gdn_last_error", "gdn_version")
+EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
+           "gdn_prefill_noalloc_scratch_bytes", "gdn_decode", "gdn_decode_commit",
+           "gdn_timing_enable", "gdn_timing_report", "gdn_device_error", "gdn_last_error",
+           "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -71,10 +72,13 @@ def load(path: str | None = None):
     lib.gdn_conv.argtypes = [PD, PP, I32, P, P, P, P, P, P, P, P, P, P, P]
     lib.gdn_prefill_workspace_size.argtypes = [PD, I32, P, ctypes.POINTER(ctypes.c_size_t)]
     lib.gdn_prefill.argtypes = [PD, PP, I32, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.gdn_prefill_noalloc.argtypes = [PD, PP, I32, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.gdn_prefill_noalloc_scratch_bytes.argtypes = []
+    lib.gdn_prefill_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.gdn_decode.argtypes = [PD, PP, I32, I32, P, P, P, P, P, P, P, P, P]
     lib.gdn_decode_commit.argtypes = [PD, I32, I32, P, P, P, P, P, P]
-    for f in ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_decode",
-              "gdn_decode_commit"):
+    for f in ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
+              "gdn_decode", "gdn_decode_commit"):
         getattr(lib, f).restype = ctypes.c_int
     lib.gdn_timing_enable.argtypes = [I32]
     lib.gdn_timing_enable.restype = ctypes.c_int

@@ -130,6 +130,37 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_prefill_noalloc -- gdn_prefill for callers that cannot allocate device
+ * memory: an engine plugin that is given its inputs and outputs but no
+ * workspace, or a serving loop whose memory is fixed before the first request
+ * and that may not call cudaMalloc (or a framework allocator) on its path.
+ * The pages have no counterpart: their CPU loop needs no scratch memory.
+ *   Arguments are those of gdn_prefill without the workspace; the scratch is
+ *   a built-in device array of gdn_prefill_noalloc_scratch_bytes() bytes
+ *   (64 MiB) that every GPU loading the library holds until the process exits.
+ *   A sequence layout needing more (gdn_prefill_workspace_size) is refused
+ *   with GDN_ERR_WORKSPACE and nothing is enqueued; at Hk=16, Hv=32,
+ *   d_k=d_v=128 the limit is a few hundred tokens per call.
+ *   No call allocates: the first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current, so make
+ *   that first call before any stream capture begins.
+ *   Every call on a device shares the one array: calls that can overlap on
+ *   the GPU (on different streams, or from different threads without an
+ *   ordering between them) race and give wrong results.  Calls ordered on one
+ *   stream are safe; each call writes every scratch region it reads, so the
+ *   previous call's contents never need clearing.
+ */
+gdn_status gdn_prefill_noalloc(const gdn_dims* dims, const gdn_params* params, int32_t n_seq,
+                               const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                               const void* x, const void* z, const void* a, const void* b,
+                               const void* conv_state_in, void* conv_state_out,
+                               const float* initial_state, float* final_state, void* out,
+                               void* stream);
+
+/* Bytes of the built-in scratch array of gdn_prefill_noalloc. */
+size_t gdn_prefill_noalloc_scratch_bytes(void);
+
+/*
  * gdn_decode -- T tokens (1 <= T <= 16) for each of n_seq sequences against a
  * resident fp32 state: cpu.rs deltanet (one token) run T times, or a short
  * speculative-verify chunk.  Layouts are [n_seq, T, ...] (packed with uniform
