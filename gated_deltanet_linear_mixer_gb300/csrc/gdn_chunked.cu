@@ -361,45 +361,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 issue_v(r + 1);
                 v_issued = r + 2;
             }
-            if (warp >= 2 && warp < 4) {
-                // operand rows the state scan needs, prepared here off its chain:
-                // q~_t = e^{G_t} q_t (zero past the chunk), hi/lo
-                const int t = 32 * (warp - 2) + lane;
-                const float f = t < L ? expf(Gr[t]) : 0.f;
-                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD;
-#pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const uint32_t so = (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
-                    float v[8];
-                    load_pair(sAg[0] + so, sAg[1] + so, v);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
-                    split_store(v, reinterpret_cast<uint8_t*>(p.qt_hi + o + 8 * ch),
-                                reinterpret_cast<uint8_t*>(p.qt_lo + o + 8 * ch));
-                }
-            } else if (warp >= 4) {
-                // (e^{G_last-G_s} k_s)^T: thread i writes key lane i over the tokens
-                const int ki = tid - 128;
-                const float GL = Gr[L - 1];
-                const uint32_t col = (ki >> 6) * 16384 + (ki & 7) * 2;
-                const uint32_t chunk = (ki & 63) >> 3;
-                const size_t o = ((size_t)(c * hv_n + h) * kD + ki) * kC;
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int sidx = 8 * c8 + e;
-                        const uint32_t so = col + (64 + sidx) * 128 + ((chunk ^ (sidx & 7)) << 4);
-                        const float kv =
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sAg[0] + so)) +
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sAg[1] + so));
-                        v[e] = sidx < L ? kv * expf(GL - Gr[sidx]) : 0.f;
-                    }
-                    split_store(v, reinterpret_cast<uint8_t*>(p.kt_hi + o + 8 * c8),
-                                reinterpret_cast<uint8_t*>(p.kt_lo + o + 8 * c8));
-                }
-            }
             if (warp < 2) {
                 // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
                 // substitution, eliminating one known entry at a time.
@@ -489,322 +450,410 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 
 // --------------------------------------------------------------- chunk_scan
 // A cluster of kSplit CTAs shares one (sequence, value head): CTA p owns value
-// lanes [64p, 64p+64) of the state, the outputs and U.  The per-token sums of
-// squares of the gated RMSNorm are exchanged through distributed shared memory.
+// lanes [64p, 64p+64) of the state, of U and of the outputs.  The state
+// recurrence per chunk is a chain of two tensor-core products,
+//   U = U~ - W S   (rows 0..63 of P4 = [W; Q] S),   S <- e^{G_last} S + K''^T U
+// (P7, K'' = diag(e^{G_last-G}) K), and only that chain is serialised.  Warp
+// roles, handing work over through mbarriers:
+//   warps 0-3  state: hold S (row = key lane, 64 value lanes) in registers,
+//              scale the chunk's keys into K'', update and re-store S; thread 0
+//              issues every MMA of the CTA (so one commit covers all before it)
+//   warps 4-5  U: token rows 0..63 of the accumulator -> U (hi/lo) in smem
+//   warps 6-7  output: rows 64..127, o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t,
+//              the gated RMSNorm with the peer CTA's sums of squares exchanged
+//              through distributed shared memory, and the output store.
+// Accumulators are double-buffered per chunk so that the output of chunk c is
+// read while chunk c+1's chain runs.  Every wait is bounded; a wait that gives
+// up records an error and the CTA unwinds (see wait_or_dead).
 constexpr int kSplit = 2;
-constexpr int kDS = kD / kSplit;   // value lanes per CTA
-constexpr uint32_t kScanBsH = 0, kScanBsL = 16384, kScanAwH = 32768, kScanAwL = 65536,
-                   kScanAqH = 98304, kScanAqL = 114688, kScanBuH = 131072, kScanBuL = 139264,
-                   kScanAkH = 147456, kScanAkL = 163840, kScanEnd = 180224;
+constexpr int kDS = kD / kSplit;  // value lanes per CTA
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64
+constexpr uint32_t kScanA4 = 32768, kScanA4Stage = 65536;   // [W; Q] K-major 128 x 128, 2 stages (hi, lo)
+constexpr uint32_t kScanKH = 163840, kScanKL = 180224;      // K'' as MN-major A (dk 128 x t 64)
+constexpr uint32_t kScanBuH = 196608, kScanBuL = 204800;    // U, MN-major 64 x 64
+constexpr uint32_t kScanQkH = 212992, kScanQkL = 221184;    // M o QK^T rows (K-major 64 x 64)
+constexpr uint32_t kScanEnd = 229376;
+// tensor-memory columns
+constexpr uint32_t kTmD4 = 0, kTmD6 = 128, kTmDs = 256;
+
+struct ScanSync {
+    uint64_t a4[2], k, qk, p4, p7, p6, u, kk, of[2], x[2], xf[2];
+    int dead;
+    int n_a4[2], n_k, n_qk;  // TMA loads issued per barrier
+};
+
+// Bounded wait that also gives up as soon as another thread of this CTA (or,
+// with peer_dead != 0, of the peer CTA) has recorded a failure.
+__device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, ScanSync& sy,
+                                             int code, bool cluster_scope = false,
+                                             uint32_t peer_dead = 0) {
+    auto tryw = [&] {
+        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (tryw()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+        if (tryw()) return true;
+        if (*reinterpret_cast<volatile int*>(&sy.dead)) return false;
+        if (peer_dead && (it & 63u) == 63u && ld_cluster_s32(peer_dead)) {
+            atomicExch(&sy.dead, 1);
+            return false;
+        }
+        if (globaltimer_ns() - t0 > 2000000000ull || clock64() - c0 > (1ll << 32)) {
+            atomicExch(&sy.dead, 1);
+            report_error(code);
+            return false;
+        }
+    }
+}
 
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qth, const __grid_constant__ CUtensorMap map_qtl,
+chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
-                  const __grid_constant__ CUtensorMap map_kth, const __grid_constant__ CUtensorMap map_ktl,
                   ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sBs[2] = {smem + kScanBsH, smem + kScanBsL};  // S slice, MN-major 128 x 64
-    uint8_t* sAw[2] = {smem + kScanAwH, smem + kScanAwL};  // [W; e^G Q] K-major 128 x 128
-    uint8_t* sAq[2] = {smem + kScanAqH, smem + kScanAqL};  // [0; M o QK^T] K-major 128 x 64
-    uint8_t* sBu[2] = {smem + kScanBuH, smem + kScanBuL};  // U slice, MN-major 64 x 64
-    uint8_t* sAk[2] = {smem + kScanAkH, smem + kScanAkL};  // (e^{G_last-G} K)^T, K-major 128 x 64
-    __shared__ float sSsq[2][kC];
-    __shared__ float sSsqC[2][kC];
-    __shared__ __align__(8) uint64_t bar_wq, bar_k, bar_kq, bar_mma;
+    __shared__ ScanSync sy;
+    __shared__ float sx[2][kC];   // the peer's per-token sums of squares
+    __shared__ float sNw[kDS];    // this CTA's norm weights
     __shared__ uint32_t tmem_slot;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, hf = warp >> 2;
-    const int row = 32 * q + lane;  // tensor-memory lane this thread reads
-    const uint32_t rank = cluster_ctarank();
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int h = blockIdx.x / kSplit, n = blockIdx.y;
-    const int j0 = static_cast<int>(rank) * kDS + 32 * hf;  // first value lane of this thread
+    const int v0 = static_cast<int>(rank) * kDS;  // first value lane of this CTA
     const int hv_n = p.n_v_heads;
     const int R = hv_n / p.n_k_heads, hk = h / R;
     const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
     const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
+    const int qcol = hk * kD, kcol = p.n_k_heads * kD + hk * kD;
 
-    // fp32 state: this thread owns S[row][j0 .. j0+31]
-    float S[32];
-    if (p.state_in) {
-        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + j0);
+    float S[kDS];  // state warps: S[row][v0 .. v0+63], row = key lane tid
+    if (warp < 4) {
+        if (p.state_in) {
+            const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)tid * kD + v0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = src[i];
-            S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
+            for (int i = 0; i < 16; ++i) {
+                const float4 v = src[i];
+                S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kDS; ++i) S[i] = 0.f;
         }
-    } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) S[i] = 0.f;
+        for (int ch = 0; ch < 8; ++ch) {
+            const uint32_t o = tid * 128 + ((ch ^ (tid & 7)) << 4);
+            split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
+        }
     }
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
-        split_store(S + 8 * ch, sBs[0] + o, sBs[1] + o);
-    }
-    for (int i = tid; i < 1024; i += kChunkThreads)
-        reinterpret_cast<uint4*>(sAq[i >> 9])[i & 511] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kDS) sNw[tid] = p.norm_w[v0 + tid];
     if (tid == 0) {
-        mbar_init(&bar_wq, 1);
-        mbar_init(&bar_k, 1);
-        mbar_init(&bar_kq, 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&sy.a4[0], 1); mbar_init(&sy.a4[1], 1);
+        mbar_init(&sy.k, 1); mbar_init(&sy.qk, 1);
+        mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1); mbar_init(&sy.p6, 1);
+        mbar_init(&sy.u, 64); mbar_init(&sy.kk, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sy.of[i], 64);
+            mbar_init(&sy.x[i], 64);
+            mbar_init(&sy.xf[i], 64);
+        }
+        sy.dead = 0;
+        sy.n_a4[0] = sy.n_a4[1] = sy.n_k = sy.n_qk = 0;
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_slot, 128);
+    if (warp == 0) tmem_alloc(&tmem_slot, 512);
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
+    cluster_arrive();  // the peer's barriers are initialised before any remote arrive
+    cluster_wait();
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;     // cols 0..63: [W S ; e^G Q S + (M o QK^T) U]
-    const uint32_t tmem_s = tmem + 64;   // cols 64..127: K'^T U
-    const uint32_t lane_off = (32u * q) << 16;
-    const uint32_t peer_ssq = map_to_rank(smem_u32(&sSsqC[0][0]), rank ^ 1u);
-    const bool sigmoid_gate = p.act == 1;
-    const uint32_t id_p4 = idesc_bf16_f32(128, kDS, false, true);
-    // in-chunk log-decay at the chunk's last token, e^{.} of which decays the state
-    auto last_g = [&](int i) {
-        const int L = min(kC, eos - (bos + i * kC));
-        return p.gcum_ws[(size_t)((c_begin + i) * hv_n + h) * kC + L - 1];
-    };
+    const uint32_t tmem = tmem_slot;
+    const uint32_t peer_dead = map_to_rank(smem_u32(&sy.dead), peer);
 
-    // Loads of chunk i (within this sequence), three groups with their own
-    // barriers so that each can be issued as soon as its buffer is free.
-    auto issue_wq = [&](int i) {  // W rows and e^{G} q rows -> [W; Q~]
-        const int wrow = ((c_begin + i) * hv_n + h) * kC;
-        mbar_arrive_expect_tx(&bar_wq, 8 * 8192);
+    auto wrow = [&](int c) { return ((c_begin + c) * hv_n + h) * kC; };
+    auto tok0 = [&](int c) { return bos + c * kC; };
+    auto issue_a4 = [&](int c) {  // W rows (0..63) and Q rows (64..127), both column blocks
+        const int s = c & 1;
+        uint8_t* bh = smem + kScanA4 + s * kScanA4Stage;
+        uint8_t* bl = bh + 32768;
+        uint64_t* bar = &sy.a4[s];
+        mbar_arrive_expect_tx(bar, 8 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(sAw[0] + b * 16384, &map_wh, &bar_wq, 64 * b, wrow);
-            tma_load_2d(sAw[1] + b * 16384, &map_wl, &bar_wq, 64 * b, wrow);
-            tma_load_2d(sAw[0] + b * 16384 + 8192, &map_qth, &bar_wq, 64 * b, wrow);
-            tma_load_2d(sAw[1] + b * 16384 + 8192, &map_qtl, &bar_wq, 64 * b, wrow);
+            tma_load_2d(bh + b * 16384, &map_wh, bar, 64 * b, wrow(c));
+            tma_load_2d(bl + b * 16384, &map_wl, bar, 64 * b, wrow(c));
+            tma_load_2d(bh + b * 16384 + 8192, &map_qh, bar, qcol + 64 * b, tok0(c));
+            tma_load_2d(bl + b * 16384 + 8192, &map_ql, bar, qcol + 64 * b, tok0(c));
         }
+        sy.n_a4[s] += 1;
     };
-    auto issue_k = [&](int i) {  // (e^{G_last-G} K)^T rows -> A of the state increment
-        const int krow = ((c_begin + i) * hv_n + h) * kD;
-        mbar_arrive_expect_tx(&bar_k, 4 * 8192);
+    auto issue_k = [&](int c) {  // key rows, both key-lane blocks (MN-major A)
+        mbar_arrive_expect_tx(&sy.k, 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(sAk[0] + b * 8192, &map_kth, &bar_k, 0, krow + 64 * b);
-            tma_load_2d(sAk[1] + b * 8192, &map_ktl, &bar_k, 0, krow + 64 * b);
+            tma_load_2d(smem + kScanKH + b * 8192, &map_qh, &sy.k, kcol + 64 * b, tok0(c));
+            tma_load_2d(smem + kScanKL + b * 8192, &map_ql, &sy.k, kcol + 64 * b, tok0(c));
         }
+        sy.n_k += 1;
     };
-    auto issue_kq = [&](int i) {  // masked decayed Q K^T -> rows 64..127 of [0; M o QK^T]
-        const int wrow = ((c_begin + i) * hv_n + h) * kC;
-        mbar_arrive_expect_tx(&bar_kq, 2 * 8192);
-        tma_load_2d(sAq[0] + 8192, &map_kqh, &bar_kq, 0, wrow);
-        tma_load_2d(sAq[1] + 8192, &map_kql, &bar_kq, 0, wrow);
+    auto issue_qk = [&](int c) {  // masked decayed Q K^T rows
+        mbar_arrive_expect_tx(&sy.qk, 2 * 8192);
+        tma_load_2d(smem + kScanQkH, &map_kqh, &sy.qk, 0, wrow(c));
+        tma_load_2d(smem + kScanQkL, &map_kql, &sy.qk, 0, wrow(c));
+        sy.n_qk += 1;
     };
-    // issued[g] / done[g]: loads of each group requested / waited for
-    int issued_wq = 0, issued_k = 0, issued_kq = 0, done_wq = 0, done_k = 0, done_kq = 0;
-    uint32_t mma_phase = 0;
-    bool mma_pending = false, dead = false;
-    if (n_ch > 0) {
-        if (tid == 0) {
-            issue_wq(0);
-            issue_k(0);
-            issue_kq(0);
-        }
-        issued_wq = issued_k = issued_kq = 1;
-    }
-    float gl_cur = n_ch > 0 ? last_g(0) : 0.f, gl_next = 0.f;
-    float ut[32];  // U~ row `row`, value lanes j0..j0+31, of the current chunk (q < 2)
-    if (q < 2 && n_ch > 0) {
-        const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)(c_begin * hv_n + h) * kC + row) * kD + j0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = src[i];
-            ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
-        }
+    auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
+    auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
+
+    if (tid == 0 && n_ch > 0) {
+        issue_a4(0);
+        if (n_ch > 1) issue_a4(1);
+        issue_k(0);
+        issue_qk(0);
     }
 
-    for (int i = 0; i < n_ch; ++i) {
-        const int t0 = bos + i * kC;
-        const int L = min(kC, eos - t0);
-        const int buf = i & 1;
-        const float GL = gl_cur;
-        uint4 zr[4];
-        do {
-            if (dead) break;
-            if (i + 1 < n_ch) gl_next = last_g(i + 1);  // prefetched for the next chunk
-            if (q >= 2 && row - 64 < L) {  // this chunk's z rows for the epilogue
-                const uint4* zp = reinterpret_cast<const uint4*>(
-                    p.z + (size_t)(t0 + row - 64) * hv_n * kD + (size_t)h * kD + j0);
+    // Thread 0's commits: the last one covers every MMA it issued.
+    uint64_t* last_commit = nullptr;
+    uint32_t last_parity = 0;
+
+    if (warp < 4) {
+        // ---------------------------------------------------------- state
+        const int t_row = tid & 63, kb = tid >> 6;  // K'' scaling: token row, key-lane block
+        for (int c = 0; c < n_ch; ++c) {
+            const int L = chunk_len(c);
+            bool ok0 = true;
+            if (tid == 0) {  // P4_c = [W; Q] S into D4[c%2]
+                ok0 = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4) &&
+                      (c < 2 || wait_or_dead(&sy.of[c & 1], ((c - 2) >> 1) & 1, sy, 9));
+                if (ok0) {
+                    tc_fence_after_sync();
+                    const uint32_t ah = smem_u32(smem + kScanA4 + (c & 1) * kScanA4Stage);
+                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) zr[ch] = zp[ch];
-            }
-            const bool okk = mbar_wait(&bar_k, i & 1);
-            const bool okw = mbar_wait(&bar_wq, i & 1);
-            if (any_failed(okk && okw)) {
-                if (tid == 0) report_error(4);
-                dead = true;
-                break;
-            }
-            done_k = done_wq = i + 1;
-            tc_fence_after_sync();
-            if (tid == 0) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // [W S ; e^G Q S]
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma3(tmem, desc_kmajor_sw128(smem_u32(sAw[0]) + ao),
-                         desc_kmajor_sw128(smem_u32(sAw[1]) + ao),
-                         desc_mnmajor_sw128(smem_u32(sBs[0]) + k * 2048, 16384),
-                         desc_mnmajor_sw128(smem_u32(sBs[1]) + k * 2048, 16384), id_p4,
-                         k > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_mma);
-            }
-            mma_pending = true;
-            if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
-                if (tid == 0) report_error(5);
-                dead = true;
-                break;
-            }
-            mma_pending = false;
-            mma_phase ^= 1;
-            tc_fence_after_sync();
-            if (tid == 0 && i + 1 < n_ch) issue_wq(i + 1);  // [W; Q] consumed
-            if (i + 1 < n_ch) issued_wq = i + 2;
-            if (q < 2) {  // U = U~ - W S for token row `row`, value lanes j0..j0+31
-                float ws[32];
-                tmem_ld32(tmem + lane_off + 32 * hf, ws);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) ut[e] -= ws[e];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
-                    split_store(ut + 8 * ch, sBu[0] + o, sBu[1] + o);
-                }
-                if (i + 1 < n_ch) {  // next chunk's U~ row
-                    const float4* src = reinterpret_cast<const float4*>(
-                        p.u_ws + ((size_t)((c_begin + i + 1) * hv_n + h) * kC + row) * kD + j0);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 v = src[e];
-                        ut[4 * e] = v.x; ut[4 * e + 1] = v.y; ut[4 * e + 2] = v.z; ut[4 * e + 3] = v.w;
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                        mma3(tmem + kTmD4 + (c & 1) * 64, desc_kmajor_sw128(ah + ao),
+                             desc_kmajor_sw128(ah + 32768 + ao),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBsH) + k * 2048, 16384),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBsL) + k * 2048, 16384), id,
+                             k > 0 ? 1u : 0u);
                     }
+                    mma_commit(&sy.p4);
+                    last_commit = &sy.p4;
+                    last_parity = c & 1;
+                }
+            }
+            __syncwarp();
+            // K''_c = diag(e^{G_last - G_t}) K_c, rows past the chunk zeroed
+            bool ok = wait_or_dead(&sy.k, c & 1, sy, 5);
+            if (!group_all(ok && ok0, 1, 128)) break;
+            {
+                const float GL = gcum(c, L - 1);
+                const float f = t_row < L ? __expf(GL - gcum(c, t_row)) : 0.f;
+                uint8_t* kh = smem + kScanKH + kb * 8192;
+                uint8_t* kl = smem + kScanKL + kb * 8192;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t o = t_row * 128 + ((ch ^ (t_row & 7)) << 4);
+                    float v[8];
+                    load_pair(kh + o, kl + o, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = t_row < L ? v[e] * f : 0.f;
+                    split_store(v, kh + o, kl + o);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&sy.kk);
+            if (tid == 0) {  // P7_c = K''^T U -> Ds, then P6_c = (M o QK^T) U -> D6[c%2]
+                ok0 = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.kk, c & 1, sy, 6);
+                if (ok0) {
+                    tc_fence_after_sync();
+                    const uint32_t id = idesc_bf16_f32(128, kDS, true, true);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma3(tmem + kTmDs,
+                             desc_mnmajor_sw128(smem_u32(smem + kScanKH) + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanKL) + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
+                             k > 0 ? 1u : 0u);
+                    mma_commit(&sy.p7);
+                    last_commit = &sy.p7;
+                    last_parity = c & 1;
+                    ok0 = wait_or_dead(&sy.qk, c & 1, sy, 8);
+                }
+                if (ok0) {
+                    tc_fence_after_sync();
+                    // A rows 0..63 of this M=128 operand are whatever precedes the
+                    // QK^T rows in shared memory: they only reach accumulator rows
+                    // 0..63 of D6, which nothing reads.
+                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma3(tmem + kTmD6 + (c & 1) * 64,
+                             desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
+                             desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
+                             k > 0 ? 1u : 0u);
+                    mma_commit(&sy.p6);
+                    last_commit = &sy.p6;
+                    last_parity = c & 1;
+                }
+            }
+            __syncwarp();
+            ok = wait_or_dead(&sy.p7, c & 1, sy, 6);
+            if (!group_all(ok && ok0, 1, 128)) break;
+            tc_fence_after_sync();
+            {  // S <- e^{G_last} S + K''^T U ; refresh the split copy
+                const float gam = __expf(gcum(c, L - 1));
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float ds[32];
+                    tmem_ld32(tmem + kTmDs + ((32u * warp) << 16) + 32 * hf, ds);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) S[32 * hf + j] = fmaf(gam, S[32 * hf + j], ds[j]);
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint32_t o = tid * 128 + ((ch ^ (tid & 7)) << 4);
+                    split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            const bool okq = mbar_wait(&bar_kq, i & 1);
-            if (any_failed(okq)) {
-                if (tid == 0) report_error(8);
-                dead = true;
-                break;
-            }
-            done_kq = i + 1;
+            group_sync(1, 128);
             tc_fence_after_sync();
-            if (tid == 0) {
+            if (tid == 0 && c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K''_c
+        }
+    } else if (warp < 6) {
+        // -------------------------------------------------------------- U
+        const int t = tid - 128;  // token row = accumulator lane
+        float ut[kDS];
+        auto load_ut = [&](int c) {
+            const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow(c) + t) * kD + v0);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {  // O += (M o QK^T) U   (rows 0..63 of A are zero)
-                    const uint64_t bh = desc_mnmajor_sw128(smem_u32(sBu[0]) + k * 2048, 8192);
-                    const uint64_t bl = desc_mnmajor_sw128(smem_u32(sBu[1]) + k * 2048, 8192);
-                    mma3(tmem, desc_kmajor_sw128(smem_u32(sAq[0]) + k * 32),
-                         desc_kmajor_sw128(smem_u32(sAq[1]) + k * 32), bh, bl, id_p4, 1u);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {  // state increment (e^{G_last-G} K)^T U
-                    const uint64_t bh = desc_mnmajor_sw128(smem_u32(sBu[0]) + k * 2048, 8192);
-                    const uint64_t bl = desc_mnmajor_sw128(smem_u32(sBu[1]) + k * 2048, 8192);
-                    mma3(tmem_s, desc_kmajor_sw128(smem_u32(sAk[0]) + k * 32),
-                         desc_kmajor_sw128(smem_u32(sAk[1]) + k * 32), bh, bl, id_p4,
-                         k > 0 ? 1u : 0u);
-                }
-                mma_commit(&bar_mma);
+            for (int i = 0; i < 16; ++i) {
+                const float4 v = src[i];
+                ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
             }
-            mma_pending = true;
-            if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
-                if (tid == 0) report_error(6);
-                dead = true;
-                break;
-            }
-            mma_pending = false;
-            mma_phase ^= 1;
+        };
+        if (n_ch > 0) load_ut(0);
+        for (int c = 0; c < n_ch; ++c) {
+            const bool ok = wait_or_dead(&sy.p4, c & 1, sy, 5);
+            if (!group_all(ok, 2, 64)) break;
             tc_fence_after_sync();
-            if (tid == 0 && i + 1 < n_ch) {  // [0; M o QK^T] and the keys are consumed
-                issue_kq(i + 1);
-                issue_k(i + 1);
+            if (tid == 128 && c + 2 < n_ch) issue_a4(c + 2);  // P4_c has read stage c%2
+            __syncwarp();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float ws[32];
+                tmem_ld32(tmem + kTmD4 + (c & 1) * 64 + ((32u * (warp - 4)) << 16) + 32 * hf, ws);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ut[32 * hf + j] -= ws[j];
             }
-            if (i + 1 < n_ch) issued_kq = issued_k = i + 2;
-            {  // S <- e^{G_last} S + K'^T U ; refresh the split copy
-                const float gam = expf(GL);
-                float ds[32];
-                tmem_ld32(tmem_s + lane_off + 32 * hf, ds);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], ds[j]);
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t o = row * 128 + (((4 * hf + ch) ^ (row & 7)) << 4);
-                    split_store(S + 8 * ch, sBs[0] + o, sBs[1] + o);
-                }
-            }
-            if (q >= 2) {  // output rows: partial sum of squares over 32 value lanes
-                float o[32];
-                tmem_ld32(tmem + lane_off + 32 * hf, o);
-                float ss = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
-                sSsq[hf][row - 64] = ss;
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint32_t o = t * 128 + ((ch ^ (t & 7)) << 4);
+                split_store(ut + 8 * ch, smem + kScanBuH + o, smem + kScanBuL + o);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            __syncthreads();
+            mbar_arrive(&sy.u);
+            if (c + 1 < n_ch) load_ut(c + 1);
+        }
+    } else {
+        // --------------------------------------------------------- output
+        const int t = tid - 192;  // token row; accumulator lane 64 + t
+        const bool sigmoid_gate = p.act == 1;
+        const uint32_t lane_off = (32u * (warp - 4)) << 16;
+        uint4 zr[8];
+        auto load_z = [&](int c) {
+            if (t < chunk_len(c)) {
+                const uint4* zp = reinterpret_cast<const uint4*>(
+                    p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) zr[i] = zp[i];
+            }
+        };
+        if (n_ch > 0) load_z(0);
+        for (int c = 0; c < n_ch; ++c) {
+            const int L = chunk_len(c), s = c & 1;
+            const float eg = __expf(gcum(c, t));
+            bool ok = wait_or_dead(&sy.p6, c & 1, sy, 7);
+            if (!group_all(ok, 3, 64)) break;
             tc_fence_after_sync();
-            if (tid < kC) sSsqC[buf][tid] = sSsq[0][tid] + sSsq[1][tid];
-        } while (false);
-        gl_cur = gl_next;
-        // Exchange the CTA's partial sums with its peer; every CTA of the
-        // cluster passes this barrier once per chunk, also after an error.
-        cluster_arrive();
-        cluster_wait();
-        if (!dead && q >= 2) {  // gated RMSNorm epilogue for token t, value lanes j0..j0+31
-            const int t = row - 64;
-            float o[32];
-            tmem_ld32(tmem + lane_off + 32 * hf, o);  // warp-collective: every lane loads
-            if (t < L) {
-                const float tot = sSsqC[buf][t] + ld_cluster_f32(peer_ssq + (uint32_t)(buf * kC + t) * 4u);
+            if (tid == 192 && c + 1 < n_ch) issue_qk(c + 1);  // P6_c has read QK^T
+            __syncwarp();
+            float o[kDS];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float a[32], b[32];
+                tmem_ld32(tmem + kTmD4 + s * 64 + lane_off + 32 * hf, a);
+                tmem_ld32(tmem + kTmD6 + s * 64 + lane_off + 32 * hf, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[32 * hf + j] = fmaf(eg, a[j], b[j]);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&sy.of[s]);  // D4[s] and D6[s] may be overwritten
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < kDS; ++j) ss = fmaf(o[j], o[j], ss);
+            ok = c < 2 || wait_or_dead(&sy.xf[s], ((c - 2) >> 1) & 1, sy, 10, true, peer_dead);
+            if (!group_all(ok, 3, 64)) break;
+            st_cluster_f32(map_to_rank(smem_u32(&sx[s][t]), peer), ss);
+            mbar_arrive_remote(map_to_rank(smem_u32(&sy.x[s]), peer));
+            ok = wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, true, peer_dead);
+            if (!group_all(ok, 3, 64)) break;
+            const float tot = ss + sx[s][t];
+            mbar_arrive_remote(map_to_rank(smem_u32(&sy.xf[s]), peer));
+            if (t < L) {  // gated RMSNorm of token t over all d_v lanes
                 const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
-                uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(t0 + t) * hv_n * kD + (size_t)h * kD + j0);
+                uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
+                                                     (size_t)h * kD + v0);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int i = 0; i < 8; ++i) {
                     float zz[8], y[8];
-                    unpack_bf16x8(zr[ch], zz);
+                    unpack_bf16x8(zr[i], zz);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float gate = sigmoid_gate ? sigmoidf_(zz[e]) : siluf_(zz[e]);
-                        y[e] = o[8 * ch + e] * rr * p.norm_w[j0 + 8 * ch + e] * gate;
+                        y[e] = o[8 * i + e] * rr * sNw[8 * i + e] * gate;
                     }
-                    op[ch] = pack_bf16x8(y);
+                    op[i] = pack_bf16x8(y);
                 }
             }
-            tc_fence_before_sync();
+            if (c + 1 < n_ch) load_z(c + 1);
         }
     }
 
-    // Unwind: let every copy and MMA still in flight land before leaving.
-    if (__syncthreads_or(issued_k > done_k)) mbar_wait(&bar_k, done_k & 1);
-    if (__syncthreads_or(issued_wq > done_wq)) mbar_wait(&bar_wq, done_wq & 1);
-    if (__syncthreads_or(issued_kq > done_kq)) mbar_wait(&bar_kq, done_kq & 1);
-    if (mma_pending) mbar_wait(&bar_mma, mma_phase);
-    if (p.state_out) {
-        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + j0);
+    // Unwind: no copy or MMA of this CTA may still be in flight when it leaves.
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s)
+            if (sy.n_a4[s] > 0) mbar_wait(&sy.a4[s], (sy.n_a4[s] - 1) & 1);
+        if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
+        if (sy.n_qk > 0) mbar_wait(&sy.qk, (sy.n_qk - 1) & 1);
+        if (last_commit) mbar_wait(last_commit, last_parity);
+    }
+    if (warp < 4 && p.state_out && !sy.dead) {
+        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)tid * kD + v0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 16; ++i)
             dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     }
-    // No CTA may leave while its peer can still read its shared memory.
+    // No CTA may leave while its peer can still reach its shared memory.
+    tc_fence_before_sync();
     cluster_arrive();
     cluster_wait();
-    tc_fence_before_sync();
-    __syncthreads();
     tc_fence_after_sync();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------- host
@@ -830,10 +879,6 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.u = off; off = up(off + crow * kD * 4);
     l.qk_hi = off; off = up(off + crow * kC * 2);
     l.qk_lo = off; off = up(off + crow * kC * 2);
-    l.qt_hi = off; off = up(off + crow * kD * 2);
-    l.qt_lo = off; off = up(off + crow * kD * 2);
-    l.kt_hi = off; off = up(off + (size_t)chunks * n_v_heads * kD * kC * 2);
-    l.kt_lo = off; off = up(off + (size_t)chunks * n_v_heads * kD * kC * 2);
     l.gcum = off; off = up(off + crow * 4);
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
@@ -887,18 +932,14 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.u_ws = reinterpret_cast<float*>(ws + l.u);
     p.qk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_hi);
     p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
-    p.qt_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qt_hi);
-    p.qt_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qt_lo);
-    p.kt_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.kt_hi);
-    p.kt_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.kt_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_qth, m_qtl, m_kth, m_ktl;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qth = m_qtl = m_kth = m_ktl = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qh;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
@@ -906,11 +947,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_qth, ws + l.qt_hi, crow, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_qtl, ws + l.qt_lo, crow, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kth, ws + l.kt_hi, (uint64_t)l.n_chunks * hv_n * kD, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_ktl, ws + l.kt_lo, (uint64_t)l.n_chunks * hv_n * kD, kC, kC, 64, 64))
+            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64))
             return cudaErrorInvalidValue;
     }
 
@@ -933,7 +970,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     }
     e = timed_launch("chunk_scan", st, [&] {
         chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
-            m_qth, m_qtl, m_wh, m_wl, m_kqh, m_kql, m_kth, m_ktl, p);
+            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, p);
         return cudaGetLastError();
     });
     return e;

@@ -83,18 +83,13 @@ struct ChunkArgs {
     float* u_ws;                  // [chunks, Hv, 64, dv] U~ (fp32)
     __nv_bfloat16* qk_hi;         // [chunks, Hv, 64, 64] masked decayed Q K^T (hi, lo)
     __nv_bfloat16* qk_lo;
-    __nv_bfloat16* qt_hi;         // [chunks, Hv, 64, dk] e^{G_t} q_t rows (hi, lo)
-    __nv_bfloat16* qt_lo;
-    __nv_bfloat16* kt_hi;         // [chunks, Hv, dk, 64] (e^{G_last-G_s} k_s)^T rows (hi, lo)
-    __nv_bfloat16* kt_lo;
     float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
     __nv_bfloat16* out;           // [T, Hv*dv]
 };
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, qt_hi, qt_lo, kt_hi,
-        kt_lo, gcum, total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, gcum, total;
     int n_chunks;
 };
 
