@@ -361,6 +361,24 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 issue_v(r + 1);
                 v_issued = r + 2;
             }
+            if (warp >= 2) {
+                // decayed keys of the state increment, K''_t = e^{G_last-G_t} k_t
+                // (zero past the chunk), hi/lo: an operand of the state scan
+                // prepared here, off its serial chain
+                const float GL = Gr[L - 1];
+                for (int i = tid - 64; i < kC * 16; i += kChunkThreads - 64) {
+                    const int t = i >> 4, ch = i & 15;
+                    const float f = t < L ? __expf(GL - Gr[t]) : 0.f;
+                    const uint32_t so = (ch >> 3) * 16384 + (64 + t) * 128 + (((ch & 7) ^ (t & 7)) << 4);
+                    float v[8];
+                    load_pair(sAg[0] + so, sAg[1] + so, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
+                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 8 * ch;
+                    split_store(v, reinterpret_cast<uint8_t*>(p.kk_hi + o),
+                                reinterpret_cast<uint8_t*>(p.kk_lo + o));
+                }
+            }
             if (warp < 2) {
                 // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
                 // substitution, eliminating one known entry at a time.
@@ -453,13 +471,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // lanes [64p, 64p+64) of the state, of U and of the outputs.  The state
 // recurrence per chunk is a chain of two tensor-core products,
 //   U = U~ - W S   (rows 0..63 of P4 = [W; Q] S),   S <- e^{G_last} S + K''^T U
-// (P7, K'' = diag(e^{G_last-G}) K), and only that chain is serialised.  Warp
+// (P7, K'' = diag(e^{G_last-G}) K, written by chunk_prep), and only that chain
+// is serialised.  Warp
 // roles, handing work over through mbarriers:
 //   warps 0-3  state: hold S (row = key lane, 64 value lanes) in registers,
-//              scale the chunk's keys into K'', update and re-store S; thread 0
-//              issues every MMA of the CTA (so one commit covers all before it)
+//              update and re-store it; thread 0 issues the chain's MMAs (P4, P7)
 //   warps 4-5  U: token rows 0..63 of the accumulator -> U (hi/lo) in smem
-//   warps 6-7  output: rows 64..127, o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t,
+//   warps 6-7  output: thread 192 issues P6 = (M o QK^T) U after P7 is done;
+//              rows 64..127, o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t,
 //              the gated RMSNorm with the peer CTA's sums of squares exchanged
 //              through distributed shared memory, and the output store.
 // Accumulators are double-buffered per chunk so that the output of chunk c is
@@ -478,26 +497,35 @@ constexpr uint32_t kScanEnd = 229376;
 constexpr uint32_t kTmD4 = 0, kTmD6 = 128, kTmDs = 256;
 
 struct ScanSync {
-    uint64_t a4[2], k, qk, p4, p7, p6, u, kk, of[2], x[2], xf[2];
+    uint64_t a4[2], k, qk, p4, p7, p6, u, of[2], x[2], xf[2];
     int dead;
     int n_a4[2], n_k, n_qk;  // TMA loads issued per barrier
 };
 
+#ifndef GDN_WAIT_HINT_NS
+#define GDN_WAIT_HINT_NS 0
+#endif
 // Bounded wait that also gives up as soon as another thread of this CTA (or,
-// with peer_dead != 0, of the peer CTA) has recorded a failure.
+// with peer_dead != 0, of the peer CTA) has recorded a failure.  The waiting
+// thread mostly sits in try_wait, which may suspend it; the failure and
+// timeout checks run every 16th round.
 __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, ScanSync& sy,
                                              int code, bool cluster_scope = false,
                                              uint32_t peer_dead = 0) {
     auto tryw = [&] {
-        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+        if (GDN_WAIT_HINT_NS == 0)
+            return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+        return cluster_scope ? mbar_try_wait_cluster_sleep(bar, parity, GDN_WAIT_HINT_NS)
+                             : mbar_try_wait_sleep(bar, parity, GDN_WAIT_HINT_NS);
     };
     if (tryw()) return true;
     const uint64_t t0 = globaltimer_ns();
     const long long c0 = clock64();
     for (uint32_t it = 0;; ++it) {
         if (tryw()) return true;
+        if ((it & 15u) != 15u) continue;
         if (*reinterpret_cast<volatile int*>(&sy.dead)) return false;
-        if (peer_dead && (it & 63u) == 63u && ld_cluster_s32(peer_dead)) {
+        if (peer_dead && ld_cluster_s32(peer_dead)) {
             atomicExch(&sy.dead, 1);
             return false;
         }
@@ -513,6 +541,7 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 
 chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                  const __grid_constant__ CUtensorMap map_kkh, const __grid_constant__ CUtensorMap map_kkl,
                   ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -531,7 +560,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
     const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
-    const int qcol = hk * kD, kcol = p.n_k_heads * kD + hk * kD;
+    const int qcol = hk * kD;
 
     float S[kDS];  // state warps: S[row][v0 .. v0+63], row = key lane tid
     if (warp < 4) {
@@ -557,10 +586,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         mbar_init(&sy.a4[0], 1); mbar_init(&sy.a4[1], 1);
         mbar_init(&sy.k, 1); mbar_init(&sy.qk, 1);
         mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1); mbar_init(&sy.p6, 1);
-        mbar_init(&sy.u, 64); mbar_init(&sy.kk, 128);
+        mbar_init(&sy.u, 64);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sy.of[i], 64);
-            mbar_init(&sy.x[i], 64);
+            mbar_init(&sy.x[i], 1);
             mbar_init(&sy.xf[i], 64);
         }
         sy.dead = 0;
@@ -593,12 +622,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         }
         sy.n_a4[s] += 1;
     };
-    auto issue_k = [&](int c) {  // key rows, both key-lane blocks (MN-major A)
+    auto issue_k = [&](int c) {  // decayed key rows K'', both key-lane blocks (MN-major A)
         mbar_arrive_expect_tx(&sy.k, 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(smem + kScanKH + b * 8192, &map_qh, &sy.k, kcol + 64 * b, tok0(c));
-            tma_load_2d(smem + kScanKL + b * 8192, &map_ql, &sy.k, kcol + 64 * b, tok0(c));
+            tma_load_2d(smem + kScanKH + b * 8192, &map_kkh, &sy.k, 64 * b, wrow(c));
+            tma_load_2d(smem + kScanKL + b * 8192, &map_kkl, &sy.k, 64 * b, wrow(c));
         }
         sy.n_k += 1;
     };
@@ -618,15 +647,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         issue_qk(0);
     }
 
-    // Thread 0's commits: the last one covers every MMA it issued.
+    // The MMA issuers (threads 0 and 192): their last commit covers every MMA
+    // the thread issued.
     uint64_t* last_commit = nullptr;
     uint32_t last_parity = 0;
 
     if (warp < 4) {
         // ---------------------------------------------------------- state
-        const int t_row = tid & 63, kb = tid >> 6;  // K'' scaling: token row, key-lane block
         for (int c = 0; c < n_ch; ++c) {
-            const int L = chunk_len(c);
+            const float gam = __expf(gcum(c, chunk_len(c) - 1));  // state decay over the chunk
             bool ok0 = true;
             if (tid == 0) {  // P4_c = [W; Q] S into D4[c%2]
                 ok0 = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4) &&
@@ -648,30 +677,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     last_commit = &sy.p4;
                     last_parity = c & 1;
                 }
-            }
-            __syncwarp();
-            // K''_c = diag(e^{G_last - G_t}) K_c, rows past the chunk zeroed
-            bool ok = wait_or_dead(&sy.k, c & 1, sy, 5);
-            if (!group_all(ok && ok0, 1, 128)) break;
-            {
-                const float GL = gcum(c, L - 1);
-                const float f = t_row < L ? __expf(GL - gcum(c, t_row)) : 0.f;
-                uint8_t* kh = smem + kScanKH + kb * 8192;
-                uint8_t* kl = smem + kScanKL + kb * 8192;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t o = t_row * 128 + ((ch ^ (t_row & 7)) << 4);
-                    float v[8];
-                    load_pair(kh + o, kl + o, v);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = t_row < L ? v[e] * f : 0.f;
-                    split_store(v, kh + o, kl + o);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&sy.kk);
-            if (tid == 0) {  // P7_c = K''^T U -> Ds, then P6_c = (M o QK^T) U -> D6[c%2]
-                ok0 = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.kk, c & 1, sy, 6);
+                // P7_c = K''^T U -> Ds once U_c and K''_c are in shared memory
+                ok0 = ok0 && wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
                 if (ok0) {
                     tc_fence_after_sync();
                     const uint32_t id = idesc_bf16_f32(128, kDS, true, true);
@@ -686,40 +693,17 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     mma_commit(&sy.p7);
                     last_commit = &sy.p7;
                     last_parity = c & 1;
-                    ok0 = wait_or_dead(&sy.qk, c & 1, sy, 8);
-                }
-                if (ok0) {
-                    tc_fence_after_sync();
-                    // A rows 0..63 of this M=128 operand are whatever precedes the
-                    // QK^T rows in shared memory: they only reach accumulator rows
-                    // 0..63 of D6, which nothing reads.
-                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma3(tmem + kTmD6 + (c & 1) * 64,
-                             desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
-                             desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
-                             k > 0 ? 1u : 0u);
-                    mma_commit(&sy.p6);
-                    last_commit = &sy.p6;
-                    last_parity = c & 1;
                 }
             }
             __syncwarp();
-            ok = wait_or_dead(&sy.p7, c & 1, sy, 6);
+            const bool ok = wait_or_dead(&sy.p7, c & 1, sy, 6);
             if (!group_all(ok && ok0, 1, 128)) break;
             tc_fence_after_sync();
             {  // S <- e^{G_last} S + K''^T U ; refresh the split copy
-                const float gam = __expf(gcum(c, L - 1));
+                float ds[kDS];
+                tmem_ld64(tmem + kTmDs + ((32u * warp) << 16), ds);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float ds[32];
-                    tmem_ld32(tmem + kTmDs + ((32u * warp) << 16) + 32 * hf, ds);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) S[32 * hf + j] = fmaf(gam, S[32 * hf + j], ds[j]);
-                }
+                for (int j = 0; j < kDS; ++j) S[j] = fmaf(gam, S[j], ds[j]);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     const uint32_t o = tid * 128 + ((ch ^ (tid & 7)) << 4);
@@ -746,17 +730,18 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         };
         if (n_ch > 0) load_ut(0);
         for (int c = 0; c < n_ch; ++c) {
-            const bool ok = wait_or_dead(&sy.p4, c & 1, sy, 5);
+            // P4_c done; P6_{c-1} (issued by the output warps) has read U_{c-1}
+            bool ok = wait_or_dead(&sy.p4, c & 1, sy, 5) &&
+                      (c == 0 || wait_or_dead(&sy.p6, (c - 1) & 1, sy, 7));
             if (!group_all(ok, 2, 64)) break;
             tc_fence_after_sync();
             if (tid == 128 && c + 2 < n_ch) issue_a4(c + 2);  // P4_c has read stage c%2
             __syncwarp();
+            {
+                float ws[kDS];
+                tmem_ld64(tmem + kTmD4 + (c & 1) * 64 + ((32u * (warp - 4)) << 16), ws);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float ws[32];
-                tmem_ld32(tmem + kTmD4 + (c & 1) * 64 + ((32u * (warp - 4)) << 16) + 32 * hf, ws);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) ut[32 * hf + j] -= ws[j];
+                for (int j = 0; j < kDS; ++j) ut[j] -= ws[j];
             }
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
@@ -786,49 +771,90 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         for (int c = 0; c < n_ch; ++c) {
             const int L = chunk_len(c), s = c & 1;
             const float eg = __expf(gcum(c, t));
-            bool ok = wait_or_dead(&sy.p6, c & 1, sy, 7);
+            bool ok = true;
+            if (tid == 192) {
+                // P6_c = (M o QK^T) U_c -> D6[c%2], issued once P7_c is done so
+                // that it never delays the state chain.  A rows 0..63 of this
+                // M=128 operand are whatever precedes the QK^T rows in shared
+                // memory: they only reach accumulator rows 0..63, never read.
+                ok = wait_or_dead(&sy.p7, c & 1, sy, 6) && wait_or_dead(&sy.qk, c & 1, sy, 8);
+                if (ok) {
+                    tc_fence_after_sync();
+                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma3(tmem + kTmD6 + s * 64,
+                             desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
+                             desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
+                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
+                             k > 0 ? 1u : 0u);
+                    mma_commit(&sy.p6);
+                    last_commit = &sy.p6;
+                    last_parity = c & 1;
+                }
+            }
+            __syncwarp();
+            ok = ok && wait_or_dead(&sy.p6, c & 1, sy, 7);
             if (!group_all(ok, 3, 64)) break;
             tc_fence_after_sync();
             if (tid == 192 && c + 1 < n_ch) issue_qk(c + 1);  // P6_c has read QK^T
             __syncwarp();
             float o[kDS];
+            tmem_ld64(tmem + kTmD4 + s * 64 + lane_off, o);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                float a[32], b[32];
-                tmem_ld32(tmem + kTmD4 + s * 64 + lane_off + 32 * hf, a);
+                float b[32];
                 tmem_ld32(tmem + kTmD6 + s * 64 + lane_off + 32 * hf, b);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[32 * hf + j] = fmaf(eg, a[j], b[j]);
+                for (int j = 0; j < 32; ++j) o[32 * hf + j] = fmaf(eg, o[32 * hf + j], b[j]);
             }
             tc_fence_before_sync();
             mbar_arrive(&sy.of[s]);  // D4[s] and D6[s] may be overwritten
             float ss = 0.f;
 #pragma unroll
             for (int j = 0; j < kDS; ++j) ss = fmaf(o[j], o[j], ss);
+            // the peer's slot s is free once it has read chunk c-2 from it
             ok = c < 2 || wait_or_dead(&sy.xf[s], ((c - 2) >> 1) & 1, sy, 10, true, peer_dead);
             if (!group_all(ok, 3, 64)) break;
-            st_cluster_f32(map_to_rank(smem_u32(&sx[s][t]), peer), ss);
-            mbar_arrive_remote(map_to_rank(smem_u32(&sy.x[s]), peer));
-            ok = wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, true, peer_dead);
+            if (tid == 192) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
+            st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), ss,
+                         map_to_rank(smem_u32(&sy.x[s]), peer));
+            // while the peer's sums travel: o * norm_w * act(z)
+            if (sigmoid_gate) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float zz[8];
+                    unpack_bf16x8(zr[i], zz);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[8 * i + e] * sigmoidf_(zz[e]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float zz[8];
+                    unpack_bf16x8(zr[i], zz);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[8 * i + e] * siluf_(zz[e]);
+                }
+            }
+            ok = wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
             if (!group_all(ok, 3, 64)) break;
             const float tot = ss + sx[s][t];
-            mbar_arrive_remote(map_to_rank(smem_u32(&sy.xf[s]), peer));
+            mbar_arrive_remote_relaxed(map_to_rank(smem_u32(&sy.xf[s]), peer), tot);
             if (t < L) {  // gated RMSNorm of token t over all d_v lanes
                 const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
                 uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
                                                      (size_t)h * kD + v0);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    float zz[8], y[8];
-                    unpack_bf16x8(zr[i], zz);
+                    float y[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float gate = sigmoid_gate ? sigmoidf_(zz[e]) : siluf_(zz[e]);
-                        y[e] = o[8 * i + e] * rr * sNw[8 * i + e] * gate;
-                    }
+                    for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
                     op[i] = pack_bf16x8(y);
                 }
             }
+            tc_fence_before_sync();
             if (c + 1 < n_ch) load_z(c + 1);
         }
     }
@@ -840,8 +866,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             if (sy.n_a4[s] > 0) mbar_wait(&sy.a4[s], (sy.n_a4[s] - 1) & 1);
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
         if (sy.n_qk > 0) mbar_wait(&sy.qk, (sy.n_qk - 1) & 1);
-        if (last_commit) mbar_wait(last_commit, last_parity);
     }
+    if ((tid == 0 || tid == 192) && last_commit) mbar_wait(last_commit, last_parity);
     if (warp < 4 && p.state_out && !sy.dead) {
         float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)tid * kD + v0);
 #pragma unroll
@@ -879,6 +905,8 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.u = off; off = up(off + crow * kD * 4);
     l.qk_hi = off; off = up(off + crow * kC * 2);
     l.qk_lo = off; off = up(off + crow * kC * 2);
+    l.kk_hi = off; off = up(off + crow * kD * 2);
+    l.kk_lo = off; off = up(off + crow * kD * 2);
     l.gcum = off; off = up(off + crow * 4);
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
@@ -932,14 +960,16 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.u_ws = reinterpret_cast<float*>(ws + l.u);
     p.qk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_hi);
     p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
+    p.kk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.kk_hi);
+    p.kk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.kk_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kkh = m_kkl = m_qh;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
@@ -947,7 +977,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64))
+            !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kkh, ws + l.kk_hi, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kkl, ws + l.kk_lo, crow, kD, kD, 64, 64))
             return cudaErrorInvalidValue;
     }
 
@@ -970,7 +1002,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     }
     e = timed_launch("chunk_scan", st, [&] {
         chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
-            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, p);
+            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl, p);
         return cudaGetLastError();
     });
     return e;

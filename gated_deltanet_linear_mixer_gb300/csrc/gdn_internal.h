@@ -83,13 +83,16 @@ struct ChunkArgs {
     float* u_ws;                  // [chunks, Hv, 64, dv] U~ (fp32)
     __nv_bfloat16* qk_hi;         // [chunks, Hv, 64, 64] masked decayed Q K^T (hi, lo)
     __nv_bfloat16* qk_lo;
+    __nv_bfloat16* kk_hi;         // [chunks, Hv, 64, dk] decayed keys e^{G_last-G_t} k_t (hi, lo)
+    __nv_bfloat16* kk_lo;
     float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
     __nv_bfloat16* out;           // [T, Hv*dv]
 };
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, gcum, total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, kk_hi, kk_lo, gcum,
+        total;
     int n_chunks;
 };
 
