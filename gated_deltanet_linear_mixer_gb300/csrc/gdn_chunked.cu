@@ -160,9 +160,28 @@ __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint6
 }
 
 // --------------------------------------------------------------- chunk_prep
-constexpr uint32_t kPrepAgH = 0, kPrepAgL = 32768, kPrepTH = 65536, kPrepTL = 81920,
-                   kPrepBH = 98304, kPrepBL = 131072, kPrepAt = 163840, kPrepVH = 180224,
-                   kPrepVL = 196608, kPrepVec = 212992;
+// One CTA per (chunk, key head); its R = Hv/Hk value heads are processed in
+// pairs so that every phase keeps all eight warps busy: the two heads of a
+// pair occupy rows 0..63 and 64..127 of each M=128 product.
+//   Gram     [Q; K] K^T on the tensor core (shared by the heads)
+//   per pair: M o QK^T rows -> workspace; A = strictly-lower beta_t
+//            e^{G_t-G_s} k_t.k_s; T = (I + A)^-1 by a blocked solve in fp32;
+//            W = (T diag(beta e^G)) K and U~ = (T diag(beta)) V on the tensor
+//            core (the row scalings of the right-hand sides are folded into
+//            T's columns); K''_t = e^{G_last-G_t} k_t; everything -> workspace.
+constexpr uint32_t kPrepAg = 0;          // [Q; K] K-major 128 x 128 (hi at +0, lo at +32768)
+constexpr uint32_t kPrepV = 65536;       // V of the pair: hi blocks (a0 a1 b0 b1) then lo blocks
+constexpr uint32_t kPrepT1 = 131072;     // [T'_a; T'_b] K-major 128 x 64 (hi, lo at +16384)
+constexpr uint32_t kPrepT2 = 163840;     // [T''_a; T''_b]
+constexpr uint32_t kPrepVec = 196608;    // G, beta per value head
+// tensor-memory columns
+constexpr uint32_t kTpW = 0, kTpUa = 128, kTpUb = 256, kTpGram = 384;
+
+// fp32 T of head hh (0/1) of the pair: rows live in the shared memory of the
+// (then dead) Q rows of the Gram operand, 32 rows per 8 KB piece.
+__device__ __forceinline__ float* prep_tf(uint8_t* smem, int hh, int row) {
+    return reinterpret_cast<float*>(smem + kPrepAg + (hh * 2 + (row >> 5)) * 16384 + (row & 31) * 256);
+}
 
 __global__ void __launch_bounds__(kChunkThreads, 1)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
@@ -170,11 +189,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sAg[2] = {smem + kPrepAgH, smem + kPrepAgL};  // [Q; K] K-major (hi, lo)
-    uint8_t* sT[2] = {smem + kPrepTH, smem + kPrepTL};     // T K-major, rows 64.. zero
-    uint8_t* sB[2] = {smem + kPrepBH, smem + kPrepBL};     // [beta e^G K | beta V] MN-major
-    float* sAt = reinterpret_cast<float*>(smem + kPrepAt); // A^T [s][t] of one head
-    uint8_t* sV[2] = {smem + kPrepVH, smem + kPrepVL};     // v rows of one head (hi, lo)
     const int R = p.n_v_heads / p.n_k_heads;
     float* sG = reinterpret_cast<float*>(smem + kPrepVec);
     float* sBeta = sG + R * kC;
@@ -184,9 +198,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, hk = blockIdx.y;
     const int hv_n = p.n_v_heads;
-    const int cd = 2 * p.n_k_heads * kD + hv_n * kD;
     const ChunkPos cp = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, c);
     const int t0 = cp.t0, L = cp.L;
+    const int n_pairs = (R + 1) / 2;
 
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
@@ -195,8 +209,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
-    for (int i = tid; i < 1024; i += kChunkThreads)
-        reinterpret_cast<uint4*>(sT[i >> 9] + 8192)[i & 511] = make_uint4(0u, 0u, 0u, 0u);
     if (warp < R) {  // cumulative log-decay and write strength of value head hk*R + warp
         const int h = hk * R + warp;
         const int s0 = 2 * lane, s1 = 2 * lane + 1;
@@ -225,19 +237,23 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;        // cols 0..255: [W | U~]
-    const uint32_t tmem_g = tmem + 256;     // cols 256..319: Gram
+    const uint32_t tmem = tmem_slot;
     uint32_t mma_phase = 0;
     bool tma_pending = false, mma_pending = false;
-    int v_issued = 0, v_done = 0;  // value heads whose v tiles were requested / consumed
-    // v rows of value head hk*R + r (both column blocks, hi and lo) -> sV
-    auto issue_v = [&](int r) {
-        const int vc = 2 * p.n_k_heads * kD + (hk * R + r) * kD;
-        mbar_arrive_expect_tx(&bar_v, 4 * 8192);
+    int v_issued = 0, v_done = 0;  // pairs whose v tiles were requested / consumed
+
+    // v rows of the pair's heads: hi blocks at kPrepV + (2*slot + b) * 8192,
+    // lo blocks 32 KB further, so [V_a | V_b] is one N=256 MN-major tile.
+    auto issue_v = [&](int pr) {
+        const int nb = min(2, R - 2 * pr);
+        mbar_arrive_expect_tx(&bar_v, nb * 4 * 8192);
+        for (int sl = 0; sl < nb; ++sl) {
+            const int vc = 2 * p.n_k_heads * kD + (hk * R + 2 * pr + sl) * kD;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tma_load_2d(sV[0] + b * 8192, &map_qh, &bar_v, vc + 64 * b, t0);
-            tma_load_2d(sV[1] + b * 8192, &map_ql, &bar_v, vc + 64 * b, t0);
+            for (int b = 0; b < 2; ++b) {
+                tma_load_2d(smem + kPrepV + (2 * sl + b) * 8192, &map_qh, &bar_v, vc + 64 * b, t0);
+                tma_load_2d(smem + kPrepV + 32768 + (2 * sl + b) * 8192, &map_ql, &bar_v, vc + 64 * b, t0);
+            }
         }
     };
 
@@ -248,10 +264,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             const int qc = hk * kD, kc = p.n_k_heads * kD + hk * kD;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                tma_load_2d(sAg[0] + b * 16384, &map_qh, &bar_tma, qc + 64 * b, t0);
-                tma_load_2d(sAg[0] + b * 16384 + 8192, &map_qh, &bar_tma, kc + 64 * b, t0);
-                tma_load_2d(sAg[1] + b * 16384, &map_ql, &bar_tma, qc + 64 * b, t0);
-                tma_load_2d(sAg[1] + b * 16384 + 8192, &map_ql, &bar_tma, kc + 64 * b, t0);
+                tma_load_2d(smem + kPrepAg + b * 16384, &map_qh, &bar_tma, qc + 64 * b, t0);
+                tma_load_2d(smem + kPrepAg + b * 16384 + 8192, &map_qh, &bar_tma, kc + 64 * b, t0);
+                tma_load_2d(smem + kPrepAg + 32768 + b * 16384, &map_ql, &bar_tma, qc + 64 * b, t0);
+                tma_load_2d(smem + kPrepAg + 32768 + b * 16384 + 8192, &map_ql, &bar_tma, kc + 64 * b, t0);
             }
         }
         tma_pending = true;
@@ -266,7 +282,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             for (int i = tid; i < nr * 64; i += kChunkThreads) {
                 const int ch = i & 7, rest = i >> 3;
                 const int r = L + rest % nr, pb = rest / nr;  // pb: hi/lo x part x block
-                *reinterpret_cast<uint4*>(sAg[pb >> 2] + ((pb >> 1) & 1) * 16384 +
+                *reinterpret_cast<uint4*>(smem + kPrepAg + (pb >> 2) * 32768 + ((pb >> 1) & 1) * 16384 +
                                           ((pb & 1) * 64 + r) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
@@ -278,8 +294,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                const uint32_t ah = smem_u32(sAg[0]) + off, al = smem_u32(sAg[1]) + off;
-                mma3(tmem_g, desc_kmajor_sw128(ah), desc_kmajor_sw128(al),
+                const uint32_t ah = smem_u32(smem + kPrepAg) + off, al = ah + 32768;
+                mma3(tmem + kTpGram, desc_kmajor_sw128(ah), desc_kmajor_sw128(al),
                      desc_kmajor_sw128(ah + 8192), desc_kmajor_sw128(al + 8192),
                      idesc_bf16_f32(128, 64), k > 0 ? 1u : 0u);
             }
@@ -294,165 +310,228 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         mma_phase ^= 1;
         tc_fence_after_sync();
 
-        bool failed = false;
-        for (int r = 0; r < R; ++r) {
-            const int h = hk * R + r;
-            const float* Gr = sG + r * kC;
-            const float* Br = sBeta + r * kC;
-            if (any_failed(mbar_wait(&bar_v, r & 1))) {  // this head's v tiles
+        for (int pr = 0; pr < n_pairs; ++pr) {
+            const int nb = min(2, R - 2 * pr);
+            if (any_failed(mbar_wait(&bar_v, pr & 1))) {  // this pair's v tiles
                 if (tid == 0) report_error(7);
-                failed = true;
                 break;
             }
-            v_done = r + 1;
-            if (warp < 4) {
-                float v[64];
-                tmem_ld32(tmem_g + ((32u * warp) << 16), v);
-                tmem_ld32(tmem_g + ((32u * warp) << 16) + 32, v + 32);
-                if (warp < 2) {  // masked decayed Q K^T row t -> workspace (hi, lo)
-                    const int t = 32 * warp + lane;
-                    const float Gt = Gr[t];
-                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kC;
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        float f[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int s = q8 * 8 + e;
-                            f[e] = s <= t ? expf(Gt - Gr[s]) * v[s] : 0.f;
-                        }
-                        split_store(f, reinterpret_cast<uint8_t*>(p.qk_hi + o + 8 * q8),
-                                    reinterpret_cast<uint8_t*>(p.qk_lo + o + 8 * q8));
-                    }
-                } else {  // A = strictly-lower beta_t e^{G_t-G_s} k_t.k_s, stored transposed
-                    const int t = 32 * (warp - 2) + lane;
-                    const float Gt = Gr[t], bt = Br[t];
-#pragma unroll
-                    for (int s = 0; s < kC; ++s)
-                        sAt[s * kC + t] = s < t ? bt * expf(Gt - Gr[s]) * v[s] : 0.f;
+            v_done = pr + 1;
+            if (L < kC) {  // v rows past the chunk: zero (they may hold anything)
+                const int nr = kC - L;
+                for (int i = tid; i < nr * 64; i += kChunkThreads) {
+                    const int ch = i & 7, rest = i >> 3;
+                    const int r = L + rest % nr, blk = rest / nr;  // blk: hi/lo x slot x block
+                    *reinterpret_cast<uint4*>(smem + kPrepV + blk * 8192 + r * 128 + ch * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
-            } else {
-                // B rows s: [beta_s e^{G_s} k_s | beta_s v_s], MN-major, hi/lo
-                for (int it = tid - 128; it < kC * 32; it += 128) {
-                    const int ch = it & 7, blk = (it >> 3) & 3, s = it >> 5;
-                    const uint32_t pos = static_cast<uint32_t>((ch ^ (s & 7)) << 4);
-                    const float bt = Br[s];
-                    float f[8];
-                    if (blk < 2) {
-                        const uint32_t so = blk * 16384 + (64 + s) * 128 + pos;
-                        load_pair(sAg[0] + so, sAg[1] + so, f);
-                        const float sc = bt * expf(Gr[s]);
+            }
+            // ---- phase A: M o QK^T rows (warps 0,1 / 4,5) and A^T (warps 2,3 / 6,7)
+            {
+                const int hh = warp >> 2;             // head of the pair this warp serves
+                const int q = warp & 3;
+                const int t = 32 * (q & 1) + lane;    // token row
+                float v[64];
+                tmem_ld64(tmem + kTpGram + ((32u * q) << 16), v);
+                if (hh < nb) {
+                    const int r = 2 * pr + hh, h = hk * R + r;
+                    const float* Gr = sG + r * kC;
+                    const float Gt = Gr[t];
+                    if (q < 2) {  // masked decayed Q K^T row t -> workspace (hi, lo)
+                        const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kC;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= sc;
-                    } else if (s < L) {
-                        const uint32_t so = (blk - 2) * 8192 + s * 128 + pos;
-                        load_pair(sV[0] + so, sV[1] + so, f);
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            float f[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] *= bt;
-                    } else {
+                            for (int e = 0; e < 8; ++e) {
+                                const int s = q8 * 8 + e;
+                                f[e] = s <= t ? __expf(Gt - Gr[s]) * v[s] : 0.f;
+                            }
+                            split_store(f, reinterpret_cast<uint8_t*>(p.qk_hi + o + 8 * q8),
+                                        reinterpret_cast<uint8_t*>(p.qk_lo + o + 8 * q8));
+                        }
+                    } else {  // A^T[s][t] = beta_t e^{G_t-G_s} k_t.k_s for s < t
+                        float* sAt = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384);
+                        const float bt = sBeta[r * kC + t];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                        for (int s = 0; s < kC; ++s)
+                            sAt[s * kC + t] = s < t ? bt * __expf(Gt - Gr[s]) * v[s] : 0.f;
                     }
-                    split_store(f, sB[0] + blk * 8192 + s * 128 + pos, sB[1] + blk * 8192 + s * 128 + pos);
                 }
             }
             __syncthreads();
-            if (tid == 0 && r + 1 < R) {  // next head's v tiles land during this head's solve
-                issue_v(r + 1);
-                v_issued = r + 2;
-            }
-            if (warp >= 2) {
-                // decayed keys of the state increment, K''_t = e^{G_last-G_t} k_t
-                // (zero past the chunk), hi/lo: an operand of the state scan
-                // prepared here, off its serial chain
-                const float GL = Gr[L - 1];
-                for (int i = tid - 64; i < kC * 16; i += kChunkThreads - 64) {
-                    const int t = i >> 4, ch = i & 15;
-                    const float f = t < L ? __expf(GL - Gr[t]) : 0.f;
-                    const uint32_t so = (ch >> 3) * 16384 + (64 + t) * 128 + (((ch & 7) ^ (t & 7)) << 4);
-                    float v[8];
-                    load_pair(sAg[0] + so, sAg[1] + so, v);
+            // ---- phase B: T = (I + A)^-1 per head, 16 x 16 blocks, fp32
+            {
+                const int hh = tid >> 7, e = tid & 127;
+                const float* sAt = reinterpret_cast<const float*>(smem + kPrepT1 + hh * 16384);
+                auto A = [&](int row, int col) { return sAt[col * kC + row]; };
+                if (e < 64) {  // diagonal blocks: column j of (I + A_ii)^-1
+                    const int i = e >> 4, j = e & 15;
+                    float x[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
-                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 8 * ch;
-                    split_store(v, reinterpret_cast<uint8_t*>(p.kk_hi + o),
-                                reinterpret_cast<uint8_t*>(p.kk_lo + o));
+                    for (int r = 0; r < 16; ++r) {
+                        float acc = r == j ? 1.f : 0.f;
+#pragma unroll
+                        for (int s = 0; s < r; ++s) acc = fmaf(-A(16 * i + r, 16 * i + s), x[s], acc);
+                        x[r] = acc;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) prep_tf(smem, hh, 16 * i + r)[16 * i + j] = x[r];
+                }
+                __syncthreads();
+                // block row i: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, j < i
+                for (int i = 1; i < 4; ++i) {
+                    float y[6];
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        if (m < 2 * i) {
+                            const int qq = e + 128 * m;
+                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
+                            float acc = 0.f;
+                            for (int k = j; k < i; ++k) {
+#pragma unroll
+                                for (int u = 0; u < 16; ++u)
+                                    acc = fmaf(A(16 * i + r, 16 * k + u), prep_tf(smem, hh, 16 * k + u)[16 * j + cc], acc);
+                            }
+                            y[m] = acc;
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        if (m < 2 * i) {
+                            const int qq = e + 128 * m;
+                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
+                            prep_tf(smem, hh, 16 * i + r)[16 * j + cc] = y[m];
+                        }
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        if (m < 2 * i) {
+                            const int qq = e + 128 * m;
+                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
+                            const float* tr = prep_tf(smem, hh, 16 * i + r) + 16 * i;
+                            float acc = 0.f;
+#pragma unroll
+                            for (int s = 0; s < 16; ++s)
+                                acc = fmaf(tr[s], prep_tf(smem, hh, 16 * i + s)[16 * j + cc], acc);
+                            y[m] = -acc;
+                        }
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        if (m < 2 * i) {
+                            const int qq = e + 128 * m;
+                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
+                            prep_tf(smem, hh, 16 * i + r)[16 * j + cc] = y[m];
+                        }
+                    }
+                    __syncthreads();
                 }
             }
-            if (warp < 2) {
-                // T = (I + A)^-1: thread j solves (I + A) x = e_j by forward
-                // substitution, eliminating one known entry at a time.
-                const int j = tid;
-                float x[kC];
+            // ---- T' = T diag(beta e^G), T'' = T diag(beta): split into the A tiles
+            for (int it = tid; it < 2 * kC * 8; it += kChunkThreads) {
+                const int hh = it >> 9, t = (it >> 3) & 63, ch = it & 7;
+                float f1[8], f2[8];
+                // blocks above the diagonal are zero (never written by the solve)
+                if (hh < nb && (ch >> 1) <= (t >> 4)) {
+                    const int r = 2 * pr + hh;
+                    const float* tr = prep_tf(smem, hh, t) + 8 * ch;
 #pragma unroll
-                for (int t = 0; t < kC; ++t) x[t] = t == j ? 1.f : 0.f;
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = 8 * ch + e;
+                        const float b = sBeta[r * kC + s];
+                        f2[e] = tr[e] * b;
+                        f1[e] = f2[e] * __expf(sG[r * kC + s]);
+                    }
+                } else {
 #pragma unroll
-                for (int s = 0; s < kC - 1; ++s) {
-                    const float xs = x[s];
-#pragma unroll
-                    for (int t = s + 1; t < kC; ++t) x[t] = fmaf(-sAt[s * kC + t], xs, x[t]);
+                    for (int e = 0; e < 8; ++e) f1[e] = f2[e] = 0.f;
                 }
-#pragma unroll
-                for (int t = 0; t < kC; ++t) {
-                    const uint32_t o = t * 128 + ((((j >> 3) ^ (t & 7))) << 4) + (j & 7) * 2;
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(x[t]);
-                    *reinterpret_cast<__nv_bfloat16*>(sT[0] + o) = hi;
-                    *reinterpret_cast<__nv_bfloat16*>(sT[1] + o) =
-                        __float2bfloat16_rn(x[t] - __bfloat162float(hi));
-                }
+                const int row = 64 * hh + t;
+                const uint32_t o = row * 128 + ((ch ^ (row & 7)) << 4);
+                split_store(f1, smem + kPrepT1 + o, smem + kPrepT1 + 16384 + o);
+                split_store(f2, smem + kPrepT2 + o, smem + kPrepT2 + 16384 + o);
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
-            if (tid == 0) {  // W = T beta e^G K (cols 0..127), U~ = T beta V (cols 128..255)
+            // ---- phase C: W = [T'_a; T'_b] K ; U~_x = [T''_a; T''_b] V_x
+            if (tid == 0) {
+                const uint32_t t1 = smem_u32(smem + kPrepT1), t2 = smem_u32(smem + kPrepT2);
+                const uint32_t kb = smem_u32(smem + kPrepAg) + 8192;   // K rows, MN-major B
+                const uint32_t vb = smem_u32(smem + kPrepV);
+                const uint32_t id = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
+                for (int k = 0; k < 4; ++k)
+                    mma3(tmem + kTpW, desc_kmajor_sw128(t1 + k * 32), desc_kmajor_sw128(t1 + 16384 + k * 32),
+                         desc_mnmajor_sw128(kb + k * 2048, 16384), desc_mnmajor_sw128(kb + 32768 + k * 2048, 16384),
+                         id, k > 0 ? 1u : 0u);
+                for (int sl = 0; sl < nb; ++sl) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma3(tmem + 128 * half, desc_kmajor_sw128(smem_u32(sT[0]) + k * 32),
-                             desc_kmajor_sw128(smem_u32(sT[1]) + k * 32),
-                             desc_mnmajor_sw128(smem_u32(sB[0]) + half * 16384 + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(sB[1]) + half * 16384 + k * 2048, 8192),
-                             idesc_bf16_f32(128, 128, false, true), k > 0 ? 1u : 0u);
+                        mma3(tmem + (sl ? kTpUb : kTpUa), desc_kmajor_sw128(t2 + k * 32),
+                             desc_kmajor_sw128(t2 + 16384 + k * 32),
+                             desc_mnmajor_sw128(vb + sl * 16384 + k * 2048, 8192),
+                             desc_mnmajor_sw128(vb + 32768 + sl * 16384 + k * 2048, 8192), id,
+                             k > 0 ? 1u : 0u);
+                }
                 mma_commit(&bar_mma);
             }
             mma_pending = true;
+            // while the products run: decayed keys K''_t = e^{G_last-G_t} k_t -> workspace
+            for (int it = tid; it < nb * kC * 16; it += kChunkThreads) {
+                const int hh = it >> 10, t = (it >> 4) & 63, ch = it & 15;
+                const int r = 2 * pr + hh, h = hk * R + r;
+                const float* Gr = sG + r * kC;
+                const float f = t < L ? __expf(Gr[L - 1] - Gr[t]) : 0.f;
+                const uint32_t so = (ch >> 3) * 16384 + 8192 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
+                float v[8];
+                load_pair(smem + kPrepAg + so, smem + kPrepAg + 32768 + so, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
+                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 8 * ch;
+                split_store(v, reinterpret_cast<uint8_t*>(p.kk_hi + o), reinterpret_cast<uint8_t*>(p.kk_lo + o));
+            }
             if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(3);
-                failed = true;
                 break;
             }
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
-            if ((warp & 3) < 2) {  // rows t of W (warps 0,1, hi/lo) and of U~ (warps 4,5, fp32)
-                const int t = 32 * (warp & 3) + lane;
-                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD;
+            if (tid == 0 && pr + 1 < n_pairs) {  // the next pair's v tiles (sV is free)
+                issue_v(pr + 1);
+                v_issued = pr + 2;
+            }
+            // ---- phase D: W rows (hi, lo) and U~ rows (fp32) -> workspace
+            {
+                const int q = warp & 3, half = warp >> 2;
+                const int hh = q >> 1, t = 32 * (q & 1) + lane;
+                float v[64];
+                tmem_ld64(tmem + kTpW + ((32u * q) << 16) + 64 * half, v);
+                float u[64];
+                tmem_ld64(tmem + (hh ? kTpUb : kTpUa) + ((32u * q) << 16) + 64 * half, u);
+                if (hh < nb) {
+                    const int h = hk * R + 2 * pr + hh;
+                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 64 * half;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    float v[32];
-                    tmem_ld32(tmem + ((32u * (warp & 3)) << 16) + (warp >> 2) * 128 + 32 * cb, v);
-                    if (warp < 4) {
+                    for (int q8 = 0; q8 < 8; ++q8)
+                        split_store(v + 8 * q8, reinterpret_cast<uint8_t*>(p.w_hi + o + 8 * q8),
+                                    reinterpret_cast<uint8_t*>(p.w_lo + o + 8 * q8));
+                    float4* dst = reinterpret_cast<float4*>(p.u_ws + o);
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8)
-                            split_store(v + 8 * q8,
-                                        reinterpret_cast<uint8_t*>(p.w_hi + o + 32 * cb + 8 * q8),
-                                        reinterpret_cast<uint8_t*>(p.w_lo + o + 32 * cb + 8 * q8));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(p.u_ws + o + 32 * cb);
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-                    }
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        dst[q4] = make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
+                    if (half == 0) p.gcum_ws[(size_t)(c * hv_n + h) * kC + t] = sG[(2 * pr + hh) * kC + t];
                 }
             }
-            if (tid < kC) p.gcum_ws[(size_t)(c * hv_n + h) * kC + tid] = Gr[tid];
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
         }
-        (void)failed;
     } while (false);
 
     // Unwind after a give-up: let in-flight copies and MMAs land first.

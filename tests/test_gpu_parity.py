@@ -61,11 +61,15 @@ PREFILL_CASES = {
                                          slow_decay=True),
     "f32_slow_decay": lambda: _gen("r6", dtype="f32", lengths=[300, 17], state_std=0.05,
                                    conv_state_std=1.0, seed=16, slow_decay=True),
-    # tensor-core path (bf16, d_k = d_v = 128): GQA ratios 1, 2, 4, ragged chunks
+    # tensor-core path (bf16, d_k = d_v = 128): GQA ratios 1, 2, 3, 4, 8, ragged chunks
     "tc_mha_R1": lambda: _gen("t1", n_k_heads=2, n_v_heads=2, lengths=[150, 64, 65],
                               state_std=0.05, conv_state_std=1.0, seed=31, act="sigmoid"),
     "tc_gqa_R4": lambda: _gen("t2", n_k_heads=1, n_v_heads=4, lengths=[200, 1, 127],
                               state_std=0.05, seed=32),
+    "tc_gqa_R3": lambda: _gen("t5", n_k_heads=1, n_v_heads=3, lengths=[96, 64, 33],
+                              state_std=0.05, conv_state_std=1.0, seed=35),
+    "tc_gqa_R8": lambda: _gen("t6", n_k_heads=1, n_v_heads=8, lengths=[129, 7],
+                              state_std=0.05, seed=36, act="sigmoid"),
     "tc_many_short": lambda: _gen("t3", n_k_heads=2, n_v_heads=4,
                                   lengths=[1, 2, 3, 4, 5, 63, 64, 65, 0, 7, 130, 31],
                                   state_std=0.05, conv_state_std=1.0, seed=33),
