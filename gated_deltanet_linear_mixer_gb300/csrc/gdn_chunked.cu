@@ -185,13 +185,17 @@ __device__ __forceinline__ float* prep_tf(uint8_t* smem, int hh, int row) {
 
 __global__ void __launch_bounds__(kChunkThreads, 1)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
-                  ChunkArgs p) {
+                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                  const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
+                  const __grid_constant__ CUtensorMap map_kql, ChunkArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const int R = p.n_v_heads / p.n_k_heads;
     float* sG = reinterpret_cast<float*>(smem + kPrepVec);
     float* sBeta = sG + R * kC;
+    float* sCs1 = sBeta + R * kC;  // beta_s e^{G_s}: column factors of T'
+    float* sCs2 = sCs1 + R * kC;   // beta_s: column factors of T''
     __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_v;
     __shared__ uint32_t tmem_slot;
 
@@ -233,6 +237,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         sG[warp * kC + s1] = excl + g0 + g1;
         sBeta[warp * kC + s0] = b0;
         sBeta[warp * kC + s1] = b1;
+        sCs1[warp * kC + s0] = b0 * __expf(excl + g0);
+        sCs1[warp * kC + s1] = b1 * __expf(excl + g0 + g1);
+        sCs2[warp * kC + s0] = b0;
+        sCs2[warp * kC + s1] = b1;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -337,8 +345,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     const int r = 2 * pr + hh, h = hk * R + r;
                     const float* Gr = sG + r * kC;
                     const float Gt = Gr[t];
-                    if (q < 2) {  // masked decayed Q K^T row t -> workspace (hi, lo)
-                        const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kC;
+                    if (q < 2) {  // masked decayed Q K^T row t -> staging tile (hi, lo)
+                        uint8_t* st = smem + kPrepT2 + hh * 16384;
 #pragma unroll
                         for (int q8 = 0; q8 < 8; ++q8) {
                             float f[8];
@@ -347,9 +355,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                                 const int s = q8 * 8 + e;
                                 f[e] = s <= t ? __expf(Gt - Gr[s]) * v[s] : 0.f;
                             }
-                            split_store(f, reinterpret_cast<uint8_t*>(p.qk_hi + o + 8 * q8),
-                                        reinterpret_cast<uint8_t*>(p.qk_lo + o + 8 * q8));
+                            const uint32_t o = sw128_offset(t, q8);
+                            split_store(f, st + o, st + 8192 + o);
                         }
+                        (void)h;
                     } else {  // A^T[s][t] = beta_t e^{G_t-G_s} k_t.k_s for s < t
                         float* sAt = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384);
                         const float bt = sBeta[r * kC + t];
@@ -359,7 +368,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     }
                 }
             }
+            fence_proxy_async_smem();
             __syncthreads();
+            if (tid == 0) {  // M o QK^T tiles -> workspace
+                for (int hh = 0; hh < nb; ++hh) {
+                    const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
+                    tma_store_2d(&map_kqh, smem + kPrepT2 + hh * 16384, 0, row);
+                    tma_store_2d(&map_kql, smem + kPrepT2 + hh * 16384 + 8192, 0, row);
+                }
+                bulk_commit();
+            }
             // ---- phase B: T = (I + A)^-1 per head, 16 x 16 blocks, fp32
             {
                 const int hh = tid >> 7, e = tid & 127;
@@ -379,57 +397,75 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     for (int r = 0; r < 16; ++r) prep_tf(smem, hh, 16 * i + r)[16 * i + j] = x[r];
                 }
                 __syncthreads();
-                // block row i: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, j < i
+                // block row i: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, j < i; a task
+                // is one row r of block j and four adjacent columns 4*c4 ..
                 for (int i = 1; i < 4; ++i) {
-                    float y[6];
+                    float4 y[2];
 #pragma unroll
-                    for (int m = 0; m < 6; ++m) {
-                        if (m < 2 * i) {
-                            const int qq = e + 128 * m;
-                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
-                            float acc = 0.f;
+                    for (int m = 0; m < 2; ++m) {
+                        const int qq = e + 128 * m;
+                        if (qq < 64 * i) {
+                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                             for (int k = j; k < i; ++k) {
+                                const float* ar = sAt + (16 * k) * kC + 16 * i + r;
+                                const float* tb = prep_tf(smem, hh, 16 * k) + 16 * j + 4 * c4;
 #pragma unroll
-                                for (int u = 0; u < 16; ++u)
-                                    acc = fmaf(A(16 * i + r, 16 * k + u), prep_tf(smem, hh, 16 * k + u)[16 * j + cc], acc);
+                                for (int u = 0; u < 16; ++u) {
+                                    const float a = ar[u * kC];
+                                    const float4 tv = *reinterpret_cast<const float4*>(tb + u * 64);
+                                    acc.x = fmaf(a, tv.x, acc.x); acc.y = fmaf(a, tv.y, acc.y);
+                                    acc.z = fmaf(a, tv.z, acc.z); acc.w = fmaf(a, tv.w, acc.w);
+                                }
                             }
                             y[m] = acc;
                         }
                     }
 #pragma unroll
-                    for (int m = 0; m < 6; ++m) {
-                        if (m < 2 * i) {
-                            const int qq = e + 128 * m;
-                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
-                            prep_tf(smem, hh, 16 * i + r)[16 * j + cc] = y[m];
+                    for (int m = 0; m < 2; ++m) {
+                        const int qq = e + 128 * m;
+                        if (qq < 64 * i) {
+                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
+                            *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
                         }
                     }
                     __syncthreads();
 #pragma unroll
-                    for (int m = 0; m < 6; ++m) {
-                        if (m < 2 * i) {
-                            const int qq = e + 128 * m;
-                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
+                    for (int m = 0; m < 2; ++m) {
+                        const int qq = e + 128 * m;
+                        if (qq < 64 * i) {
+                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
                             const float* tr = prep_tf(smem, hh, 16 * i + r) + 16 * i;
-                            float acc = 0.f;
+                            const float* pb = prep_tf(smem, hh, 16 * i) + 16 * j + 4 * c4;
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                            for (int s = 0; s < 16; ++s)
-                                acc = fmaf(tr[s], prep_tf(smem, hh, 16 * i + s)[16 * j + cc], acc);
-                            y[m] = -acc;
+                            for (int s4 = 0; s4 < 4; ++s4) {
+                                const float4 tv = *reinterpret_cast<const float4*>(tr + 4 * s4);
+                                const float ts[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const float4 pv = *reinterpret_cast<const float4*>(pb + (4 * s4 + q) * 64);
+                                    acc.x = fmaf(ts[q], pv.x, acc.x); acc.y = fmaf(ts[q], pv.y, acc.y);
+                                    acc.z = fmaf(ts[q], pv.z, acc.z); acc.w = fmaf(ts[q], pv.w, acc.w);
+                                }
+                            }
+                            y[m] = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                         }
                     }
                     __syncthreads();
 #pragma unroll
-                    for (int m = 0; m < 6; ++m) {
-                        if (m < 2 * i) {
-                            const int qq = e + 128 * m;
-                            const int j = qq >> 8, r = (qq >> 4) & 15, cc = qq & 15;
-                            prep_tf(smem, hh, 16 * i + r)[16 * j + cc] = y[m];
+                    for (int m = 0; m < 2; ++m) {
+                        const int qq = e + 128 * m;
+                        if (qq < 64 * i) {
+                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
+                            *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
                         }
                     }
                     __syncthreads();
                 }
             }
+            if (tid == 0) bulk_wait_read();  // the QK^T staging tiles may be overwritten
+            __syncthreads();
             // ---- T' = T diag(beta e^G), T'' = T diag(beta): split into the A tiles
             for (int it = tid; it < 2 * kC * 8; it += kChunkThreads) {
                 const int hh = it >> 9, t = (it >> 3) & 63, ch = it & 7;
@@ -441,9 +477,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = 8 * ch + e;
-                        const float b = sBeta[r * kC + s];
-                        f2[e] = tr[e] * b;
-                        f1[e] = f2[e] * __expf(sG[r * kC + s]);
+                        f1[e] = tr[e] * sCs1[r * kC + s];
+                        f2[e] = tr[e] * sCs2[r * kC + s];
                     }
                 } else {
 #pragma unroll
@@ -502,35 +537,54 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
-            if (tid == 0 && pr + 1 < n_pairs) {  // the next pair's v tiles (sV is free)
-                issue_v(pr + 1);
-                v_issued = pr + 2;
-            }
-            // ---- phase D: W rows (hi, lo) and U~ rows (fp32) -> workspace
+            // ---- phase D: W rows (hi, lo) and U~ rows (fp32), staged in the now
+            // free v / T tiles (head a / head b, 64 KB each), then TMA stores
             {
                 const int q = warp & 3, half = warp >> 2;
                 const int hh = q >> 1, t = 32 * (q & 1) + lane;
+                uint8_t* st = smem + (hh ? kPrepT1 : kPrepV);
                 float v[64];
                 tmem_ld64(tmem + kTpW + ((32u * q) << 16) + 64 * half, v);
-                float u[64];
-                tmem_ld64(tmem + (hh ? kTpUb : kTpUa) + ((32u * q) << 16) + 64 * half, u);
-                if (hh < nb) {
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const uint32_t o = half * 8192 + sw128_offset(t, q8);
+                    split_store(v + 8 * q8, st + o, st + 16384 + o);
+                }
+                tmem_ld64(tmem + (hh ? kTpUb : kTpUa) + ((32u * q) << 16) + 64 * half, v);
+#pragma unroll
+                for (int q4 = 0; q4 < 16; ++q4)
+                    *reinterpret_cast<float4*>(st + 32768 + (2 * half + (q4 >> 3)) * 8192 +
+                                               sw128_offset(t, q4 & 7)) =
+                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                if (hh < nb && half == 0) {
                     const int h = hk * R + 2 * pr + hh;
-                    const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 64 * half;
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8)
-                        split_store(v + 8 * q8, reinterpret_cast<uint8_t*>(p.w_hi + o + 8 * q8),
-                                    reinterpret_cast<uint8_t*>(p.w_lo + o + 8 * q8));
-                    float4* dst = reinterpret_cast<float4*>(p.u_ws + o);
-#pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4)
-                        dst[q4] = make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
-                    if (half == 0) p.gcum_ws[(size_t)(c * hv_n + h) * kC + t] = sG[(2 * pr + hh) * kC + t];
+                    p.gcum_ws[(size_t)(c * hv_n + h) * kC + t] = sG[(2 * pr + hh) * kC + t];
                 }
             }
+            fence_proxy_async_smem();
             tc_fence_before_sync();
             __syncthreads();
             tc_fence_after_sync();
+            if (tid == 0) {
+                for (int hh = 0; hh < nb; ++hh) {
+                    const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
+                    const uint8_t* st = smem + (hh ? kPrepT1 : kPrepV);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        tma_store_2d(&map_wh, st + b * 8192, 64 * b, row);
+                        tma_store_2d(&map_wl, st + 16384 + b * 8192, 64 * b, row);
+                    }
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) tma_store_2d(&map_u, st + 32768 + b * 8192, 32 * b, row);
+                }
+                bulk_commit();
+                if (pr + 1 < n_pairs) {  // staging read out: the next pair's v tiles may land
+                    bulk_wait_read();
+                    issue_v(pr + 1);
+                }
+            }
+            if (pr + 1 < n_pairs) v_issued = pr + 2;
+            __syncthreads();
         }
     } while (false);
 
@@ -539,6 +593,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     if (tma_pending) mbar_wait(&bar_tma, 0);
     if (v_issued > v_done) mbar_wait(&bar_v, v_done & 1);
     if (mma_pending) mbar_wait(&bar_mma, mma_phase);
+    if (tid == 0) bulk_wait_all();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -1046,9 +1101,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl, m_u;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kkh = m_kkl = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kkh = m_kkl = m_u = m_qh;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
@@ -1058,23 +1113,25 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kkh, ws + l.kk_hi, crow, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kkl, ws + l.kk_lo, crow, kD, kD, 64, 64))
+            !make_tma_map_bf16_2d(&m_kkl, ws + l.kk_lo, crow, kD, kD, 64, 64) ||
+            !make_tma_map_f32_2d(&m_u, ws + l.u, crow, kD, kD, 64, 32))
             return cudaErrorInvalidValue;
     }
 
-    const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 2 * kC * 4;
+    const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 4 * kC * 4;
     const size_t scan_smem = 1024 + kScanEnd;
     static bool attrs_set = false;
     if (!attrs_set) {
         cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(1024 + kPrepVec + 8 * 2 * kC * 4));
+                             static_cast<int>(1024 + kPrepVec + 8 * 4 * kC * 4));
         cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(scan_smem));
         attrs_set = true;
     }
     if (l.n_chunks > 0) {
         e = timed_launch("chunk_prep", st, [&] {
-            chunk_prep_kernel<<<dim3(l.n_chunks, hk_n), kChunkThreads, prep_smem, st>>>(m_qh, m_ql, p);
+            chunk_prep_kernel<<<dim3(l.n_chunks, hk_n), kChunkThreads, prep_smem, st>>>(
+                m_qh, m_ql, m_wh, m_wl, m_u, m_kqh, m_kql, p);
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;

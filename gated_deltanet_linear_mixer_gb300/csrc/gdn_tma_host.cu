@@ -25,19 +25,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool make_tma_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols) {
+namespace {
+
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType type, uint32_t elem_bytes,
+                 const void* base, uint64_t rows, uint64_t cols, uint64_t pitch_elems,
+                 uint32_t box_rows, uint32_t box_cols) {
     auto fn = encode_fn();
     if (!fn || rows == 0 || cols == 0) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {pitch_elems * 2};
+    cuuint64_t strides[1] = {pitch_elems * elem_bytes};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                    strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool make_tma_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols) {
+    return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, pitch_elems,
+                       box_rows, box_cols);
+}
+
+bool make_tma_map_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols) {
+    return make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, pitch_elems,
+                       box_rows, box_cols);
 }
 
 }  // namespace gdn

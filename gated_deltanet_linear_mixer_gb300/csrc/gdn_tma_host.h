@@ -14,5 +14,8 @@ namespace gdn {
 // (box_cols * 2 must be <= 128).  Returns false on failure.
 bool make_tma_map_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                           uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols);
+// The same for fp32 elements (box_cols * 4 <= 128).
+bool make_tma_map_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols);
 
 }  // namespace gdn
