@@ -88,6 +88,12 @@ __device__ __forceinline__ float log_decay(float a, float A_log, float dt_bias) 
     return -expf(A_log) * softplusf_(a + dt_bias);
 }
 
+// Two floats rounded to bf16 (nearest even) and packed, first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16_pair(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // ------------------------------------------------------------ reductions
 template <int WIDTH>
 __device__ __forceinline__ float group_sum(float v) {

@@ -152,6 +152,109 @@ conv_prologue_kernel(ConvArgs p) {
     }
 }
 
+// The prologue for bf16 activations with d_k = d_v = 128 (the tensor-core
+// prefill): one warp per (128-channel unit, 8-token run), 4 channels per lane,
+// four CTAs per SM.  The warp's 11 raw rows (3 of halo) are loaded up front with 8-byte
+// coalesced loads; per token the L2 norm of a q/k head is a full-warp
+// reduction.  Writes q|k|v as a (hi, lo) bf16 pair, g and beta like
+// conv_prologue_kernel.
+constexpr int kPro128Tok = 8;                   // tokens per warp
+constexpr int kPro128Tile = 8 * kPro128Tok;     // tokens per CTA
+
+__global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) {
+    const int n_units = 2 * p.n_k_heads + p.n_v_heads;
+    const int unit = blockIdx.y;
+    const int tile0 = blockIdx.x * kPro128Tile;
+    const int cd = n_units * 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(p.x);
+
+    if (unit == n_units) {  // gates for this token tile
+        const int hv_n = p.n_v_heads;
+        const __nv_bfloat16* __restrict__ a = static_cast<const __nv_bfloat16*>(p.a);
+        const __nv_bfloat16* __restrict__ b = static_cast<const __nv_bfloat16*>(p.b);
+        for (int i = tid; i < kPro128Tile * hv_n; i += 256) {
+            const int t = tile0 + i / hv_n;
+            const int h = i % hv_n;
+            if (t >= p.n_tokens) break;
+            const size_t idx = (size_t)t * hv_n + h;
+            p.g_out[idx] = log_decay(__bfloat162float(a[idx]), p.A_log[h], p.dt_bias[h]);
+            p.beta_out[idx] = sigmoidf_(__bfloat162float(b[idx]));
+        }
+        return;
+    }
+    const int tb = tile0 + warp * kPro128Tok;  // first token of this warp
+    if (tb >= p.n_tokens) return;              // warp-uniform
+    const bool is_q = unit < p.n_k_heads;
+    const bool norm = unit < 2 * p.n_k_heads;
+    const float scale = is_q ? rsqrtf(128.f) : 1.f;
+    const int c = unit * 128 + 4 * lane;  // first channel of this lane
+    const int K = p.conv_k, keep = K - 1, pad = 4 - K;
+    float w[4][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[e][k] = k >= pad ? p.conv_w[(size_t)(c + e) * K + (k - pad)] : 0.f;
+    uint2 raw[kPro128Tok + 3];  // rows tb-3 .. tb+15
+#pragma unroll
+    for (int i = 0; i < kPro128Tok + 3; ++i) {
+        const int rr = tb - 3 + i;
+        raw[i] = (rr >= 0 && rr < p.n_tokens) ? *reinterpret_cast<const uint2*>(x + (size_t)rr * cd + c)
+                                              : make_uint2(0u, 0u);
+    }
+    const __nv_bfloat16* __restrict__ cs_in = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(p.qkv_out);
+    __nv_bfloat16* __restrict__ out_lo = static_cast<__nv_bfloat16*>(p.qkv_lo_out);
+    int n = seq_of_token(p.cu_seqlens, p.n_seq, tb);
+    int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+#pragma unroll
+    for (int j = 0; j < kPro128Tok; ++j) {
+        const int t = tb + j;
+        if (t >= p.n_tokens) break;  // warp-uniform
+        while (t >= eos) {           // crossed into the next non-empty sequence
+            ++n;
+            bos = p.cu_seqlens[n];
+            eos = p.cu_seqlens[n + 1];
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int src = t - 3 + k;
+            float v[4];
+            if (src >= bos) {
+                const uint2 r = raw[j + k];
+                v[0] = __uint_as_float(r.x << 16); v[1] = __uint_as_float(r.x & 0xFFFF0000u);
+                v[2] = __uint_as_float(r.y << 16); v[3] = __uint_as_float(r.y & 0xFFFF0000u);
+            } else if (cs_in && src >= bos - keep) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[e] = __bfloat162float(cs_in[((size_t)n * cd + c + e) * keep + keep + (src - bos)]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = fmaf(w[e][k], v[e], acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = siluf_(acc[e]);
+        if (norm) {
+            float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss + p.l2_eps) * scale;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] *= inv;
+        }
+        const uint32_t h01 = pack_bf16_pair(acc[0], acc[1]), h23 = pack_bf16_pair(acc[2], acc[3]);
+        const float l0 = acc[0] - __uint_as_float(h01 << 16), l1 = acc[1] - __uint_as_float(h01 & 0xFFFF0000u);
+        const float l2 = acc[2] - __uint_as_float(h23 << 16), l3 = acc[3] - __uint_as_float(h23 & 0xFFFF0000u);
+        *reinterpret_cast<uint2*>(out + (size_t)t * cd + c) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2*>(out_lo + (size_t)t * cd + c) =
+            make_uint2(pack_bf16_pair(l0, l1), pack_bf16_pair(l2, l3));
+    }
+}
+
 // New history of each sequence = its last K-1 raw inputs, oldest first,
 // shifted in from the old history when the sequence is shorter than K-1.
 template <typename T>
@@ -194,6 +297,11 @@ __global__ void conv_state_kernel(ConvStateArgs p) {
 
 cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream) {
     if (p.n_tokens == 0) return cudaSuccess;
+    if (bf16 && p.d_k == 128 && p.d_v == 128 && p.qkv_lo_out) {
+        dim3 grid((p.n_tokens + kPro128Tile - 1) / kPro128Tile, 2 * p.n_k_heads + p.n_v_heads + 1);
+        conv_prologue_d128_kernel<<<grid, 256, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     dim3 grid((p.n_tokens + kConvTokTile - 1) / kConvTokTile, 2 * p.n_k_heads + p.n_v_heads + 1);
     if (bf16)
         conv_prologue_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, stream>>>(p);
