@@ -605,19 +605,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // lanes [64p, 64p+64) of the state, of U and of the outputs.  The state
 // recurrence per chunk is a chain of two tensor-core products,
 //   U = U~ - W S   (rows 0..63 of P4 = [W; Q] S),   S <- e^{G_last} S + K''^T U
-// (P7, K'' = diag(e^{G_last-G}) K, written by chunk_prep), and only that chain
-// is serialised.  Warp
-// roles, handing work over through mbarriers:
-//   warps 0-3  state: hold S (row = key lane, 64 value lanes) in registers,
-//              update and re-store it; thread 0 issues the chain's MMAs (P4, P7)
-//   warps 4-5  U: token rows 0..63 of the accumulator -> U (hi/lo) in smem
-//   warps 6-7  output: thread 192 issues P6 = (M o QK^T) U after P7 is done;
-//              rows 64..127, o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t,
-//              the gated RMSNorm with the peer CTA's sums of squares exchanged
-//              through distributed shared memory, and the output store.
-// Accumulators are double-buffered per chunk so that the output of chunk c is
-// read while chunk c+1's chain runs.  Every wait is bounded; a wait that gives
-// up records an error and the CTA unwinds (see wait_or_dead).
+// (P7, K'' = diag(e^{G_last-G}) K, written by chunk_prep).  Every step of the
+// chain is spread over all eight warps: thread (warp w, lane l) owns key lane
+// 32 (w%4) + l of the state and value lanes 32 (w/4) .. +31 of this CTA's
+// slice, which is exactly the part of the tensor-memory accumulators that the
+// warp may read.  Per chunk c:
+//   1. thread 0 issues P4_c = [W; Q] S into D4[c%2]
+//   2. warps 0,1,4,5 (accumulator rows 0..63): U_c = U~ - W S -> smem;
+//      warps 2,3,6,7 (rows 64..127), meanwhile: the output of chunk c-1,
+//      o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t, gated RMSNorm (sums of squares
+//      exchanged with the peer CTA through distributed shared memory), store
+//   3. thread 0 issues P7_c = K''^T U -> Ds and P6_c = (M o QK^T) U -> D6[c%2]
+//   4. all warps: S <- e^{G_last} S + Ds, re-split S into smem
+// Accumulators D4 and D6 are double-buffered so that step 2 reads chunk c-1's
+// while P4_c runs.  Every wait is bounded (wait_or_dead).
 constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;  // value lanes per CTA
 // shared memory (bytes from a 1024-aligned base)
@@ -631,26 +632,19 @@ constexpr uint32_t kScanEnd = 229376;
 constexpr uint32_t kTmD4 = 0, kTmD6 = 128, kTmDs = 256;
 
 struct ScanSync {
-    uint64_t a4[2], k, qk, p4, p7, p6, u, of[2], x[2], xf[2];
+    uint64_t a4[2], k, qk, p4, p7, p6, u, x[2], xf[2];
     int dead;
     int n_a4[2], n_k, n_qk;  // TMA loads issued per barrier
 };
 
-#ifndef GDN_WAIT_HINT_NS
-#define GDN_WAIT_HINT_NS 0
-#endif
 // Bounded wait that also gives up as soon as another thread of this CTA (or,
-// with peer_dead != 0, of the peer CTA) has recorded a failure.  The waiting
-// thread mostly sits in try_wait, which may suspend it; the failure and
-// timeout checks run every 16th round.
+// with peer_dead != 0, of the peer CTA) has recorded a failure; the failure
+// and timeout checks run every 16th round.
 __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, ScanSync& sy,
                                              int code, bool cluster_scope = false,
                                              uint32_t peer_dead = 0) {
     auto tryw = [&] {
-        if (GDN_WAIT_HINT_NS == 0)
-            return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-        return cluster_scope ? mbar_try_wait_cluster_sleep(bar, parity, GDN_WAIT_HINT_NS)
-                             : mbar_try_wait_sleep(bar, parity, GDN_WAIT_HINT_NS);
+        return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     };
     if (tryw()) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -682,10 +676,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                                                ~static_cast<uintptr_t>(1023));
     __shared__ ScanSync sy;
     __shared__ float sx[2][kC];   // the peer's per-token sums of squares
+    __shared__ float sSq[2][kC];  // this CTA's, per 32-lane half
     __shared__ float sNw[kDS];    // this CTA's norm weights
     __shared__ uint32_t tmem_slot;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, half = warp >> 2;
+    const int row = 32 * q + lane;       // accumulator lane: key lane / token row
+    const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice
+    const uint32_t lane_off = (32u * q) << 16;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int h = blockIdx.x / kSplit, n = blockIdx.y;
     const int v0 = static_cast<int>(rank) * kDS;  // first value lane of this CTA
@@ -695,34 +694,35 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
     const int qcol = hk * kD;
+    const bool is_u = q < 2;  // warps 0,1,4,5: accumulator rows 0..63
 
-    float S[kDS];  // state warps: S[row][v0 .. v0+63], row = key lane tid
-    if (warp < 4) {
-        if (p.state_in) {
-            const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)tid * kD + v0);
+    float S[32];  // S[row][v0 + cl .. +31]
+    if (p.state_in) {
+        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 v = src[i];
-                S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kDS; ++i) S[i] = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = src[i];
+            S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
         }
+    } else {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t o = tid * 128 + ((ch ^ (tid & 7)) << 4);
+        for (int i = 0; i < 32; ++i) S[i] = 0.f;
+    }
+    auto store_s = [&] {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
             split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
         }
-    }
+    };
+    store_s();
     if (tid < kDS) sNw[tid] = p.norm_w[v0 + tid];
     if (tid == 0) {
         mbar_init(&sy.a4[0], 1); mbar_init(&sy.a4[1], 1);
         mbar_init(&sy.k, 1); mbar_init(&sy.qk, 1);
         mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1); mbar_init(&sy.p6, 1);
-        mbar_init(&sy.u, 64);
+        mbar_init(&sy.u, 128);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sy.of[i], 64);
             mbar_init(&sy.x[i], 1);
             mbar_init(&sy.xf[i], 64);
         }
@@ -741,7 +741,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 
     auto wrow = [&](int c) { return ((c_begin + c) * hv_n + h) * kC; };
     auto tok0 = [&](int c) { return bos + c * kC; };
-    auto issue_a4 = [&](int c) {  // W rows (0..63) and Q rows (64..127), both column blocks
+    auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
+    auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
+    auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
         const int s = c & 1;
         uint8_t* bh = smem + kScanA4 + s * kScanA4Stage;
         uint8_t* bl = bh + 32768;
@@ -771,9 +773,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         tma_load_2d(smem + kScanQkL, &map_kql, &sy.qk, 0, wrow(c));
         sy.n_qk += 1;
     };
-    auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
-    auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
-
     if (tid == 0 && n_ch > 0) {
         issue_a4(0);
         if (n_ch > 1) issue_a4(1);
@@ -781,217 +780,213 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         issue_qk(0);
     }
 
-    // The MMA issuers (threads 0 and 192): their last commit covers every MMA
-    // the thread issued.
+    // thread 0 issues every MMA; its last commit covers all of them
     uint64_t* last_commit = nullptr;
     uint32_t last_parity = 0;
+    const bool sigmoid_gate = p.act == 1;
 
-    if (warp < 4) {
-        // ---------------------------------------------------------- state
-        for (int c = 0; c < n_ch; ++c) {
-            const float gam = __expf(gcum(c, chunk_len(c) - 1));  // state decay over the chunk
-            bool ok0 = true;
-            if (tid == 0) {  // P4_c = [W; Q] S into D4[c%2]
-                ok0 = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4) &&
-                      (c < 2 || wait_or_dead(&sy.of[c & 1], ((c - 2) >> 1) & 1, sy, 9));
-                if (ok0) {
-                    tc_fence_after_sync();
-                    const uint32_t ah = smem_u32(smem + kScanA4 + (c & 1) * kScanA4Stage);
-                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+    float ut[32];   // U~ row (U warps), prefetched one chunk ahead
+    uint4 zr[4];    // z row (output warps) of the chunk whose output is pending
+    auto load_ut = [&](int c) {
+        const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow(c) + row) * kD + v0 + cl);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                        mma3(tmem + kTmD4 + (c & 1) * 64, desc_kmajor_sw128(ah + ao),
-                             desc_kmajor_sw128(ah + 32768 + ao),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBsH) + k * 2048, 16384),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBsL) + k * 2048, 16384), id,
-                             k > 0 ? 1u : 0u);
-                    }
-                    mma_commit(&sy.p4);
-                    last_commit = &sy.p4;
-                    last_parity = c & 1;
-                }
-                // P7_c = K''^T U -> Ds once U_c and K''_c are in shared memory
-                ok0 = ok0 && wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
-                if (ok0) {
-                    tc_fence_after_sync();
-                    const uint32_t id = idesc_bf16_f32(128, kDS, true, true);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma3(tmem + kTmDs,
-                             desc_mnmajor_sw128(smem_u32(smem + kScanKH) + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanKL) + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
-                             k > 0 ? 1u : 0u);
-                    mma_commit(&sy.p7);
-                    last_commit = &sy.p7;
-                    last_parity = c & 1;
-                }
-            }
-            __syncwarp();
-            const bool ok = wait_or_dead(&sy.p7, c & 1, sy, 6);
-            if (!group_all(ok && ok0, 1, 128)) break;
-            tc_fence_after_sync();
-            {  // S <- e^{G_last} S + K''^T U ; refresh the split copy
-                float ds[kDS];
-                tmem_ld64(tmem + kTmDs + ((32u * warp) << 16), ds);
-#pragma unroll
-                for (int j = 0; j < kDS; ++j) S[j] = fmaf(gam, S[j], ds[j]);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t o = tid * 128 + ((ch ^ (tid & 7)) << 4);
-                    split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            group_sync(1, 128);
-            tc_fence_after_sync();
-            if (tid == 0 && c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K''_c
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = src[i];
+            ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
         }
-    } else if (warp < 6) {
-        // -------------------------------------------------------------- U
-        const int t = tid - 128;  // token row = accumulator lane
-        float ut[kDS];
-        auto load_ut = [&](int c) {
-            const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow(c) + t) * kD + v0);
+    };
+    auto load_z = [&](int c) {
+        const int t = row - 64;
+        if (t < chunk_len(c)) {
+            const uint4* zp = reinterpret_cast<const uint4*>(
+                p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0 + cl);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 v = src[i];
-                ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
-            }
-        };
-        if (n_ch > 0) load_ut(0);
-        for (int c = 0; c < n_ch; ++c) {
-            // P4_c done; P6_{c-1} (issued by the output warps) has read U_{c-1}
-            bool ok = wait_or_dead(&sy.p4, c & 1, sy, 5) &&
-                      (c == 0 || wait_or_dead(&sy.p6, (c - 1) & 1, sy, 7));
-            if (!group_all(ok, 2, 64)) break;
-            tc_fence_after_sync();
-            if (tid == 128 && c + 2 < n_ch) issue_a4(c + 2);  // P4_c has read stage c%2
-            __syncwarp();
-            {
-                float ws[kDS];
-                tmem_ld64(tmem + kTmD4 + (c & 1) * 64 + ((32u * (warp - 4)) << 16), ws);
-#pragma unroll
-                for (int j = 0; j < kDS; ++j) ut[j] -= ws[j];
-            }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint32_t o = t * 128 + ((ch ^ (t & 7)) << 4);
-                split_store(ut + 8 * ch, smem + kScanBuH + o, smem + kScanBuL + o);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            mbar_arrive(&sy.u);
-            if (c + 1 < n_ch) load_ut(c + 1);
+            for (int i = 0; i < 4; ++i) zr[i] = zp[i];
         }
-    } else {
-        // --------------------------------------------------------- output
-        const int t = tid - 192;  // token row; accumulator lane 64 + t
-        const bool sigmoid_gate = p.act == 1;
-        const uint32_t lane_off = (32u * (warp - 4)) << 16;
-        uint4 zr[8];
-        auto load_z = [&](int c) {
-            if (t < chunk_len(c)) {
-                const uint4* zp = reinterpret_cast<const uint4*>(
-                    p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) zr[i] = zp[i];
-            }
-        };
-        if (n_ch > 0) load_z(0);
-        for (int c = 0; c < n_ch; ++c) {
-            const int L = chunk_len(c), s = c & 1;
-            const float eg = __expf(gcum(c, t));
-            bool ok = true;
-            if (tid == 192) {
-                // P6_c = (M o QK^T) U_c -> D6[c%2], issued once P7_c is done so
-                // that it never delays the state chain.  A rows 0..63 of this
-                // M=128 operand are whatever precedes the QK^T rows in shared
-                // memory: they only reach accumulator rows 0..63, never read.
-                ok = wait_or_dead(&sy.p7, c & 1, sy, 6) && wait_or_dead(&sy.qk, c & 1, sy, 8);
-                if (ok) {
-                    tc_fence_after_sync();
-                    const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma3(tmem + kTmD6 + s * 64,
-                             desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
-                             desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
-                             desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
-                             k > 0 ? 1u : 0u);
-                    mma_commit(&sy.p6);
-                    last_commit = &sy.p6;
-                    last_parity = c & 1;
-                }
-            }
-            __syncwarp();
-            ok = ok && wait_or_dead(&sy.p6, c & 1, sy, 7);
-            if (!group_all(ok, 3, 64)) break;
+    };
+    if (n_ch > 0) {
+        if (is_u) load_ut(0);
+        else load_z(0);
+    }
+
+    // Output of chunk c (output warps, accumulator rows 64..127): needs P6_c done.
+    auto output = [&](int c) -> bool {
+        const int t = row - 64, s = c & 1, L = chunk_len(c);
+        const float eg = __expf(gcum(c, t));
+        bool ok = wait_or_dead(&sy.p6, c & 1, sy, 7);
+        float o[32];
+        if (ok) {
             tc_fence_after_sync();
-            if (tid == 192 && c + 1 < n_ch) issue_qk(c + 1);  // P6_c has read QK^T
-            __syncwarp();
-            float o[kDS];
-            tmem_ld64(tmem + kTmD4 + s * 64 + lane_off, o);
+            float b[32];
+            tmem_ld32(tmem + kTmD4 + s * 64 + lane_off + cl, o);
+            tmem_ld32(tmem + kTmD6 + s * 64 + lane_off + cl, b);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float b[32];
-                tmem_ld32(tmem + kTmD6 + s * 64 + lane_off + 32 * hf, b);
+            for (int j = 0; j < 32; ++j) o[j] = fmaf(eg, o[j], b[j]);
+        } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[32 * hf + j] = fmaf(eg, o[32 * hf + j], b[j]);
-            }
-            tc_fence_before_sync();
-            mbar_arrive(&sy.of[s]);  // D4[s] and D6[s] may be overwritten
-            float ss = 0.f;
+            for (int j = 0; j < 32; ++j) o[j] = 0.f;
+        }
+        float ss = 0.f;
 #pragma unroll
-            for (int j = 0; j < kDS; ++j) ss = fmaf(o[j], o[j], ss);
+        for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+        sSq[half][t] = ss;
+        group_sync(1, 128);  // the output warps' halves of each row are in sSq
+        const float tot = sSq[0][t] + sSq[1][t];
+        if (ok && half == 0) {
             // the peer's slot s is free once it has read chunk c-2 from it
             ok = c < 2 || wait_or_dead(&sy.xf[s], ((c - 2) >> 1) & 1, sy, 10, true, peer_dead);
-            if (!group_all(ok, 3, 64)) break;
-            if (tid == 192) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
-            st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), ss,
-                         map_to_rank(smem_u32(&sy.x[s]), peer));
-            // while the peer's sums travel: o * norm_w * act(z)
-            if (sigmoid_gate) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float zz[8];
-                    unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[8 * i + e] * sigmoidf_(zz[e]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float zz[8];
-                    unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[8 * i + e] * siluf_(zz[e]);
-                }
+            if (ok) {
+                if (t == 0) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
+                st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), tot,
+                             map_to_rank(smem_u32(&sy.x[s]), peer));
             }
-            ok = wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
-            if (!group_all(ok, 3, 64)) break;
-            const float tot = ss + sx[s][t];
-            mbar_arrive_remote_relaxed(map_to_rank(smem_u32(&sy.xf[s]), peer), tot);
-            if (t < L) {  // gated RMSNorm of token t over all d_v lanes
-                const float rr = rsqrtf(tot * (1.f / kD) + p.rms_eps);
-                uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
-                                                     (size_t)h * kD + v0);
+        }
+        // while the peer's sums travel: o * norm_w * act(z)
+        if (sigmoid_gate) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float y[8];
+            for (int i = 0; i < 4; ++i) {
+                float zz[8];
+                unpack_bf16x8(zr[i], zz);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
-                    op[i] = pack_bf16x8(y);
-                }
+                for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * sigmoidf_(zz[e]);
             }
-            tc_fence_before_sync();
-            if (c + 1 < n_ch) load_z(c + 1);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float zz[8];
+                unpack_bf16x8(zr[i], zz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * siluf_(zz[e]);
+            }
+        }
+        ok = ok && wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
+        const float peer_tot = sx[s][t];
+        group_sync(1, 128);  // both halves have read sx[s] for this chunk
+        if (ok && half == 0) mbar_arrive_remote_relaxed(map_to_rank(smem_u32(&sy.xf[s]), peer), peer_tot);
+        if (ok && t < L) {  // gated RMSNorm of token t over all d_v lanes
+            const float rr = rsqrtf((tot + peer_tot) * (1.f / kD) + p.rms_eps);
+            uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
+                                                 (size_t)h * kD + v0 + cl);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
+                op[i] = pack_bf16x8(y);
+            }
+        }
+        tc_fence_before_sync();
+        return ok;
+    };
+
+    for (int c = 0; c < n_ch; ++c) {
+        const float gam = __expf(gcum(c, chunk_len(c) - 1));  // state decay over the chunk
+        // 1. P4_c = [W; Q] S into D4[c%2]
+        if (tid == 0) {
+            bool ok = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4);
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t ah = smem_u32(smem + kScanA4 + (c & 1) * kScanA4Stage);
+                const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma3(tmem + kTmD4 + (c & 1) * 64, desc_kmajor_sw128(ah + ao),
+                         desc_kmajor_sw128(ah + 32768 + ao),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBsH) + k * 2048, 16384),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBsL) + k * 2048, 16384), id,
+                         k > 0 ? 1u : 0u);
+                }
+                mma_commit(&sy.p4);
+                last_commit = &sy.p4;
+                last_parity = c & 1;
+            }
+        }
+        __syncwarp();
+        // 2. U_c (rows 0..63) | output of chunk c-1 (rows 64..127)
+        if (is_u) {
+            if (wait_or_dead(&sy.p4, c & 1, sy, 5)) {
+                tc_fence_after_sync();
+                if (tid == 128 && c + 2 < n_ch) issue_a4(c + 2);  // P4_c has read stage c%2
+                __syncwarp();
+                float ws[32];
+                tmem_ld32(tmem + kTmD4 + (c & 1) * 64 + lane_off + cl, ws);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ut[j] -= ws[j];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                    split_store(ut + 8 * ch, smem + kScanBuH + o, smem + kScanBuL + o);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&sy.u);
+                if (c + 1 < n_ch) load_ut(c + 1);
+            }
+        } else if (c > 0) {
+            output(c - 1);
+            load_z(c);
+        }
+        // 3. P7_c = K''^T U -> Ds, then P6_c = (M o QK^T) U -> D6[c%2]
+        if (tid == 0) {
+            bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
+            if (ok) {
+                tc_fence_after_sync();
+                const uint32_t id = idesc_bf16_f32(128, kDS, true, true);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma3(tmem + kTmDs,
+                         desc_mnmajor_sw128(smem_u32(smem + kScanKH) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanKL) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
+                         k > 0 ? 1u : 0u);
+                mma_commit(&sy.p7);
+                last_commit = &sy.p7;
+                last_parity = c & 1;
+                ok = wait_or_dead(&sy.qk, c & 1, sy, 8);
+            }
+            if (ok) {
+                tc_fence_after_sync();
+                // A rows 0..63 of this M=128 operand are whatever precedes the
+                // QK^T rows in shared memory: they only reach accumulator rows
+                // 0..63 of D6, which nothing reads.
+                const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma3(tmem + kTmD6 + (c & 1) * 64,
+                         desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
+                         desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
+                         desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
+                         k > 0 ? 1u : 0u);
+                mma_commit(&sy.p6);
+                last_commit = &sy.p6;
+                last_parity = c & 1;
+            }
+        }
+        __syncwarp();
+        // 4. S <- e^{G_last} S + K''^T U ; refresh the split copy
+        if (wait_or_dead(&sy.p7, c & 1, sy, 6)) {
+            tc_fence_after_sync();
+            float ds[32];
+            tmem_ld32(tmem + kTmDs + lane_off + cl, ds);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], ds[j]);
+            store_s();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        if (__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead))) break;
+        tc_fence_after_sync();
+        if (tid == 0 && c + 1 < n_ch) {
+            issue_k(c + 1);  // P7_c has read K''_c
+            // sQK is free once P6_c is done (it runs during the state update)
+            if (wait_or_dead(&sy.p6, c & 1, sy, 7)) issue_qk(c + 1);
         }
     }
+    const bool alive = !__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead));
+    if (alive && n_ch > 0 && !is_u) output(n_ch - 1);  // the last chunk's output
 
     // Unwind: no copy or MMA of this CTA may still be in flight when it leaves.
     __syncthreads();
@@ -1000,12 +995,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             if (sy.n_a4[s] > 0) mbar_wait(&sy.a4[s], (sy.n_a4[s] - 1) & 1);
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
         if (sy.n_qk > 0) mbar_wait(&sy.qk, (sy.n_qk - 1) & 1);
+        if (last_commit) mbar_wait(last_commit, last_parity);
     }
-    if ((tid == 0 || tid == 192) && last_commit) mbar_wait(last_commit, last_parity);
-    if (warp < 4 && p.state_out && !sy.dead) {
-        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)tid * kD + v0);
+    if (p.state_out && !sy.dead) {
+        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     }
     // No CTA may leave while its peer can still reach its shared memory.
