@@ -780,6 +780,17 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         issue_qk(0);
     }
 
+    // Shared-memory descriptors, computed once: a descriptor for address a + o
+    // is the one for a plus o >> 4 (the 14-bit start field cannot carry over,
+    // every address here is below 256 KB).
+    const uint64_t dA4_0 = desc_kmajor_sw128(smem_u32(smem + kScanA4));
+    const uint64_t dA4_1 = desc_kmajor_sw128(smem_u32(smem + kScanA4 + kScanA4Stage));
+    const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
+    const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
+    const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBuH), 8192);
+    const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192);
+    constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
+
     // thread 0 issues every MMA; its last commit covers all of them
     uint64_t* last_commit = nullptr;
     uint32_t last_parity = 0;
@@ -886,16 +897,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             bool ok = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4);
             if (ok) {
                 tc_fence_after_sync();
-                const uint32_t ah = smem_u32(smem + kScanA4 + (c & 1) * kScanA4Stage);
+                const uint64_t da = (c & 1) ? dA4_1 : dA4_0;
                 const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma3(tmem + kTmD4 + (c & 1) * 64, desc_kmajor_sw128(ah + ao),
-                         desc_kmajor_sw128(ah + 32768 + ao),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBsH) + k * 2048, 16384),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBsL) + k * 2048, 16384), id,
-                         k > 0 ? 1u : 0u);
+                    const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                    mma3(tmem + kTmD4 + (c & 1) * 64, da + ao, da + kLoA4 + ao, dBs + k * 128,
+                         dBs + kLo16 + k * 128, id, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&sy.p4);
                 last_commit = &sy.p4;
@@ -929,37 +937,24 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         }
         // 3. P7_c = K''^T U -> Ds, then P6_c = (M o QK^T) U -> D6[c%2]
         if (tid == 0) {
-            bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
+            const bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5) &&
+                            wait_or_dead(&sy.qk, c & 1, sy, 8);
             if (ok) {
                 tc_fence_after_sync();
-                const uint32_t id = idesc_bf16_f32(128, kDS, true, true);
+                const uint32_t id7 = idesc_bf16_f32(128, kDS, true, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmDs,
-                         desc_mnmajor_sw128(smem_u32(smem + kScanKH) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanKL) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
-                         k > 0 ? 1u : 0u);
+                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, dBu + k * 128,
+                         dBu + kLo8 + k * 128, id7, k > 0 ? 1u : 0u);
                 mma_commit(&sy.p7);
-                last_commit = &sy.p7;
-                last_parity = c & 1;
-                ok = wait_or_dead(&sy.qk, c & 1, sy, 8);
-            }
-            if (ok) {
-                tc_fence_after_sync();
                 // A rows 0..63 of this M=128 operand are whatever precedes the
                 // QK^T rows in shared memory: they only reach accumulator rows
                 // 0..63 of D6, which nothing reads.
-                const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+                const uint32_t id6 = idesc_bf16_f32(128, kDS, false, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmD6 + (c & 1) * 64,
-                         desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192 + k * 32),
-                         desc_kmajor_sw128(smem_u32(smem + kScanQkL) - 8192 + k * 32),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBuH) + k * 2048, 8192),
-                         desc_mnmajor_sw128(smem_u32(smem + kScanBuL) + k * 2048, 8192), id,
-                         k > 0 ? 1u : 0u);
+                    mma3(tmem + kTmD6 + (c & 1) * 64, dQk + k * 2, dQk + kLo8 + k * 2, dBu + k * 128,
+                         dBu + kLo8 + k * 128, id6, k > 0 ? 1u : 0u);
                 mma_commit(&sy.p6);
                 last_commit = &sy.p6;
                 last_parity = c & 1;
@@ -979,7 +974,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         tc_fence_before_sync();
         if (__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead))) break;
         tc_fence_after_sync();
-        if (tid == 0 && c + 1 < n_ch) {
+        if (tid == 32 && c + 1 < n_ch) {  // off thread 0, which goes on to P4_{c+1}
             issue_k(c + 1);  // P7_c has read K''_c
             // sQK is free once P6_c is done (it runs during the state update)
             if (wait_or_dead(&sy.p6, c & 1, sy, 7)) issue_qk(c + 1);
