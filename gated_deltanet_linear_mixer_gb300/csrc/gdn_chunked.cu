@@ -890,8 +890,11 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         return ok;
     };
 
+    // log of the state decay over a chunk, loaded one chunk ahead
+    float gl_next = n_ch > 0 ? gcum(0, chunk_len(0) - 1) : 0.f;
     for (int c = 0; c < n_ch; ++c) {
-        const float gam = __expf(gcum(c, chunk_len(c) - 1));  // state decay over the chunk
+        const float gam = __expf(gl_next);  // state decay over chunk c
+        if (c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
         // 1. P4_c = [W; Q] S into D4[c%2]
         if (tid == 0) {
             bool ok = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4);
