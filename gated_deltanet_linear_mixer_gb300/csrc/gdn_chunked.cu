@@ -200,11 +200,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hk = blockIdx.y;
     const int hv_n = p.n_v_heads;
-    const ChunkPos cp = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, c);
-    const int t0 = cp.t0, L = cp.L;
     const int n_pairs = (R + 1) / 2;
+    const int n_items = p.n_chunks * p.n_k_heads;  // (chunk, key head), chunk-major
 
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
@@ -213,6 +211,55 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    uint32_t mma_phase = 0, tma_phase = 0, v_phase = 0;
+    bool tma_pending = false, mma_pending = false, v_pending = false;
+
+    // q rows (0..63) and k rows (64..127) of item it, both column blocks
+    auto issue_qk_tiles = [&](int it) {
+        const int ci = it / p.n_k_heads, hki = it % p.n_k_heads;
+        const int t0i = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, ci).t0;
+        mbar_arrive_expect_tx(&bar_tma, 8 * 8192);
+        const int qc = hki * kD, kc = p.n_k_heads * kD + hki * kD;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_2d(smem + kPrepAg + b * 16384, &map_qh, &bar_tma, qc + 64 * b, t0i);
+            tma_load_2d(smem + kPrepAg + b * 16384 + 8192, &map_qh, &bar_tma, kc + 64 * b, t0i);
+            tma_load_2d(smem + kPrepAg + 32768 + b * 16384, &map_ql, &bar_tma, qc + 64 * b, t0i);
+            tma_load_2d(smem + kPrepAg + 32768 + b * 16384 + 8192, &map_ql, &bar_tma, kc + 64 * b, t0i);
+        }
+    };
+    // v rows of pair pr of item it: hi blocks at kPrepV + (2*slot + b) * 8192,
+    // lo blocks 32 KB further
+    auto issue_v_item = [&](int it, int pr) {
+        const int ci = it / p.n_k_heads, hki = it % p.n_k_heads;
+        const int t0i = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, ci).t0;
+        const int nb = min(2, R - 2 * pr);
+        mbar_arrive_expect_tx(&bar_v, nb * 4 * 8192);
+        for (int sl = 0; sl < nb; ++sl) {
+            const int vc = 2 * p.n_k_heads * kD + (hki * R + 2 * pr + sl) * kD;
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                tma_load_2d(smem + kPrepV + (2 * sl + b) * 8192, &map_qh, &bar_v, vc + 64 * b, t0i);
+                tma_load_2d(smem + kPrepV + 32768 + (2 * sl + b) * 8192, &map_ql, &bar_v, vc + 64 * b, t0i);
+            }
+        }
+    };
+    if (tid == 0 && (int)blockIdx.x < n_items) {
+        issue_qk_tiles(blockIdx.x);
+        issue_v_item(blockIdx.x, 0);
+    }
+    tma_pending = v_pending = (int)blockIdx.x < n_items;
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int c = item / p.n_k_heads, hk = item % p.n_k_heads;
+    const int next = item + gridDim.x;
+    const ChunkPos cp = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, c);
+    const int t0 = cp.t0, L = cp.L;
+    bool failed = false;
     if (warp < R) {  // cumulative log-decay and write strength of value head hk*R + warp
         const int h = hk * R + warp;
         const int s0 = 2 * lane, s1 = 2 * lane + 1;
@@ -242,49 +289,14 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         sCs2[warp * kC + s0] = b0;
         sCs2[warp * kC + s1] = b1;
     }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    uint32_t mma_phase = 0;
-    bool tma_pending = false, mma_pending = false;
-    int v_issued = 0, v_done = 0;  // pairs whose v tiles were requested / consumed
-
-    // v rows of the pair's heads: hi blocks at kPrepV + (2*slot + b) * 8192,
-    // lo blocks 32 KB further, so [V_a | V_b] is one N=256 MN-major tile.
-    auto issue_v = [&](int pr) {
-        const int nb = min(2, R - 2 * pr);
-        mbar_arrive_expect_tx(&bar_v, nb * 4 * 8192);
-        for (int sl = 0; sl < nb; ++sl) {
-            const int vc = 2 * p.n_k_heads * kD + (hk * R + 2 * pr + sl) * kD;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                tma_load_2d(smem + kPrepV + (2 * sl + b) * 8192, &map_qh, &bar_v, vc + 64 * b, t0);
-                tma_load_2d(smem + kPrepV + 32768 + (2 * sl + b) * 8192, &map_ql, &bar_v, vc + 64 * b, t0);
-            }
-        }
-    };
-
     do {
-        if (tid == 0) {
-            issue_v(0);
-            mbar_arrive_expect_tx(&bar_tma, 8 * 8192);
-            const int qc = hk * kD, kc = p.n_k_heads * kD + hk * kD;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                tma_load_2d(smem + kPrepAg + b * 16384, &map_qh, &bar_tma, qc + 64 * b, t0);
-                tma_load_2d(smem + kPrepAg + b * 16384 + 8192, &map_qh, &bar_tma, kc + 64 * b, t0);
-                tma_load_2d(smem + kPrepAg + 32768 + b * 16384, &map_ql, &bar_tma, qc + 64 * b, t0);
-                tma_load_2d(smem + kPrepAg + 32768 + b * 16384 + 8192, &map_ql, &bar_tma, kc + 64 * b, t0);
-            }
-        }
-        tma_pending = true;
-        v_issued = 1;
-        if (any_failed(mbar_wait(&bar_tma, 0))) {
+        if (any_failed(mbar_wait(&bar_tma, tma_phase))) {  // this item's q, k tiles
             if (tid == 0) report_error(1);
+            failed = true;
             break;
         }
         tma_pending = false;
+        tma_phase ^= 1;
         if (L < kC) {  // rows past the chunk belong to another sequence: zero them
             const int nr = kC - L;
             for (int i = tid; i < nr * 64; i += kChunkThreads) {
@@ -312,6 +324,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         mma_pending = true;
         if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
             if (tid == 0) report_error(2);
+            failed = true;
             break;
         }
         mma_pending = false;
@@ -320,11 +333,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 
         for (int pr = 0; pr < n_pairs; ++pr) {
             const int nb = min(2, R - 2 * pr);
-            if (any_failed(mbar_wait(&bar_v, pr & 1))) {  // this pair's v tiles
+            if (any_failed(mbar_wait(&bar_v, v_phase))) {  // this pair's v tiles
                 if (tid == 0) report_error(7);
+                failed = true;
                 break;
             }
-            v_done = pr + 1;
+            v_pending = false;
+            v_phase ^= 1;
             if (L < kC) {  // v rows past the chunk: zero (they may hold anything)
                 const int nr = kC - L;
                 for (int i = tid; i < nr * 64; i += kChunkThreads) {
@@ -532,11 +547,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             }
             if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(3);
+                failed = true;
                 break;
             }
             mma_pending = false;
             mma_phase ^= 1;
             tc_fence_after_sync();
+            if (pr + 1 == n_pairs && next < n_items) {
+                // the q, k tiles are no longer read (K'' and the products are
+                // done): the next item's may land while this one is written out
+                if (tid == 0) issue_qk_tiles(next);
+                tma_pending = true;
+            }
             // ---- phase D: W rows (hi, lo) and U~ rows (fp32), staged in the now
             // free v / T tiles (head a / head b, 64 KB each), then TMA stores
             {
@@ -578,21 +600,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                     for (int b = 0; b < 4; ++b) tma_store_2d(&map_u, st + 32768 + b * 8192, 32 * b, row);
                 }
                 bulk_commit();
-                if (pr + 1 < n_pairs) {  // staging read out: the next pair's v tiles may land
-                    bulk_wait_read();
-                    issue_v(pr + 1);
-                }
+                // staging read out: the next v tiles (this item's next pair, or
+                // the next item's first) may land, T1/T2 may be rewritten
+                if (pr + 1 < n_pairs || next < n_items) bulk_wait_read();
+                if (pr + 1 < n_pairs) issue_v_item(item, pr + 1);
+                else if (next < n_items) issue_v_item(next, 0);
             }
-            if (pr + 1 < n_pairs) v_issued = pr + 2;
+            v_pending = pr + 1 < n_pairs || next < n_items;
             __syncthreads();
         }
     } while (false);
+    if (failed) break;
+    }
 
-    // Unwind after a give-up: let in-flight copies and MMAs land first.
-    v_issued = __syncthreads_or(v_issued > v_done) ? v_done + 1 : v_done;
-    if (tma_pending) mbar_wait(&bar_tma, 0);
-    if (v_issued > v_done) mbar_wait(&bar_v, v_done & 1);
-    if (mma_pending) mbar_wait(&bar_mma, mma_phase);
+    // Unwind (also after a give-up): in-flight copies and MMAs land first.
+    if (tid == 0) {
+        if (tma_pending) mbar_wait(&bar_tma, tma_phase);
+        if (v_pending) mbar_wait(&bar_v, v_phase);
+    }
+    if (__syncthreads_or(mma_pending) && tid == 0) mbar_wait(&bar_mma, mma_phase);
     if (tid == 0) bulk_wait_all();
     tc_fence_before_sync();
     __syncthreads();
@@ -1041,6 +1067,19 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     return off;
 }
 
+// SMs of the current device (the persistent prep kernel runs one CTA per SM).
+static int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     const ChunkLayout& l = a.layout;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -1121,9 +1160,10 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
                              static_cast<int>(scan_smem));
         attrs_set = true;
     }
+    const int n_items = l.n_chunks * hk_n;
     if (l.n_chunks > 0) {
         e = timed_launch("chunk_prep", st, [&] {
-            chunk_prep_kernel<<<dim3(l.n_chunks, hk_n), kChunkThreads, prep_smem, st>>>(
+            chunk_prep_kernel<<<dim3(std::min(n_items, sm_count())), kChunkThreads, prep_smem, st>>>(
                 m_qh, m_ql, m_wh, m_wl, m_u, m_kqh, m_kql, p);
             return cudaGetLastError();
         });
