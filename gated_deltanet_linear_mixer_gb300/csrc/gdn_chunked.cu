@@ -636,31 +636,38 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // 32 (w%4) + l of the state and value lanes 32 (w/4) .. +31 of this CTA's
 // slice, which is exactly the part of the tensor-memory accumulators that the
 // warp may read.  Per chunk c:
-//   1. thread 0 issues P4_c = [W; Q] S into D4[c%2]
+//   1. thread 0 issues P4_c = [W; Q] S into D4[c%3], then the previous chunk's
+//      output term P6_{c-1} = (M o QK^T) U_{c-1} into D6[(c-1)%3], which runs
+//      while the tensor pipe would otherwise wait for U_c
 //   2. warps 0,1,4,5 (accumulator rows 0..63): U_c = U~ - W S -> smem;
-//      warps 2,3,6,7 (rows 64..127), meanwhile: the output of chunk c-1,
+//      warps 2,3,6,7 (rows 64..127), meanwhile: the output of chunk c-2,
 //      o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t, gated RMSNorm (sums of squares
 //      exchanged with the peer CTA through distributed shared memory), store
-//   3. thread 0 issues P7_c = K''^T U -> Ds and P6_c = (M o QK^T) U -> D6[c%2]
+//   3. thread 0 issues P7_c = K''^T U -> Ds
 //   4. all warps: S <- e^{G_last} S + Ds, re-split S into smem
-// Accumulators D4 and D6 are double-buffered so that step 2 reads chunk c-1's
-// while P4_c runs.  Every wait is bounded (wait_or_dead).
+// Accumulators D4 and D6 have three slots and U two buffers, so that the
+// output can trail the chain by two chunks.  Every wait is bounded
+// (wait_or_dead).
 constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;  // value lanes per CTA
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64
-constexpr uint32_t kScanA4 = 32768, kScanA4Stage = 65536;   // [W; Q] K-major 128 x 128, 2 stages (hi, lo)
-constexpr uint32_t kScanKH = 163840, kScanKL = 180224;      // K'' as MN-major A (dk 128 x t 64)
-constexpr uint32_t kScanBuH = 196608, kScanBuL = 204800;    // U, MN-major 64 x 64
-constexpr uint32_t kScanQkH = 212992, kScanQkL = 221184;    // M o QK^T rows (K-major 64 x 64)
-constexpr uint32_t kScanEnd = 229376;
-// tensor-memory columns
-constexpr uint32_t kTmD4 = 0, kTmD6 = 128, kTmDs = 256;
+constexpr uint32_t kScanA4H = 32768, kScanA4L = 65536;      // [W; Q] K-major 128 x 128 (hi, lo)
+constexpr uint32_t kScanKH = 98304, kScanKL = 114688;       // K'' as MN-major A (dk 128 x t 64)
+constexpr uint32_t kScanBu = 131072;                        // U, MN-major 64 x 64: buffer b at
+                                                            //   +b*16384 (hi), +8192 (lo)
+constexpr uint32_t kScanQk = 163840;                        // M o QK^T rows (K-major 64 x 64):
+                                                            //   buffer b at +b*16384 (hi), +8192 (lo)
+constexpr uint32_t kScanEnd = 196608;
+// tensor-memory columns: D4 and D6 in three slots each (chunk c uses c%3)
+constexpr uint32_t kTmD4 = 0, kTmD6 = 192, kTmDs = 384;
 
 struct ScanSync {
-    uint64_t a4[2], k, qk, p4, p7, p6, u, x[2], xf[2];
+    // p6 per accumulator slot: the output warps wait for it chunks later, and
+    // a slot's barrier is re-armed only once that slot's output has been read
+    uint64_t a4, k, qk[2], p4, p7, p6[3], u, x[2], xf[2];
     int dead;
-    int n_a4[2], n_k, n_qk;  // TMA loads issued per barrier
+    int n_a4, n_k, n_qk[2];  // TMA loads issued per barrier
 };
 
 // Bounded wait that also gives up as soon as another thread of this CTA (or,
@@ -744,16 +751,17 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     store_s();
     if (tid < kDS) sNw[tid] = p.norm_w[v0 + tid];
     if (tid == 0) {
-        mbar_init(&sy.a4[0], 1); mbar_init(&sy.a4[1], 1);
-        mbar_init(&sy.k, 1); mbar_init(&sy.qk, 1);
-        mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1); mbar_init(&sy.p6, 1);
+        mbar_init(&sy.a4, 1);
+        mbar_init(&sy.k, 1); mbar_init(&sy.qk[0], 1); mbar_init(&sy.qk[1], 1);
+        mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&sy.p6[i], 1);
         mbar_init(&sy.u, 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sy.x[i], 1);
             mbar_init(&sy.xf[i], 64);
         }
         sy.dead = 0;
-        sy.n_a4[0] = sy.n_a4[1] = sy.n_k = sy.n_qk = 0;
+        sy.n_a4 = sy.n_k = sy.n_qk[0] = sy.n_qk[1] = 0;
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
@@ -770,19 +778,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
     auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
     auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
-        const int s = c & 1;
-        uint8_t* bh = smem + kScanA4 + s * kScanA4Stage;
-        uint8_t* bl = bh + 32768;
-        uint64_t* bar = &sy.a4[s];
-        mbar_arrive_expect_tx(bar, 8 * 8192);
+        mbar_arrive_expect_tx(&sy.a4, 8 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(bh + b * 16384, &map_wh, bar, 64 * b, wrow(c));
-            tma_load_2d(bl + b * 16384, &map_wl, bar, 64 * b, wrow(c));
-            tma_load_2d(bh + b * 16384 + 8192, &map_qh, bar, qcol + 64 * b, tok0(c));
-            tma_load_2d(bl + b * 16384 + 8192, &map_ql, bar, qcol + 64 * b, tok0(c));
+            tma_load_2d(smem + kScanA4H + b * 16384, &map_wh, &sy.a4, 64 * b, wrow(c));
+            tma_load_2d(smem + kScanA4L + b * 16384, &map_wl, &sy.a4, 64 * b, wrow(c));
+            tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_qh, &sy.a4, qcol + 64 * b, tok0(c));
+            tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_ql, &sy.a4, qcol + 64 * b, tok0(c));
         }
-        sy.n_a4[s] += 1;
+        sy.n_a4 += 1;
     };
     auto issue_k = [&](int c) {  // decayed key rows K'', both key-lane blocks (MN-major A)
         mbar_arrive_expect_tx(&sy.k, 4 * 8192);
@@ -793,29 +797,30 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         }
         sy.n_k += 1;
     };
-    auto issue_qk = [&](int c) {  // masked decayed Q K^T rows
-        mbar_arrive_expect_tx(&sy.qk, 2 * 8192);
-        tma_load_2d(smem + kScanQkH, &map_kqh, &sy.qk, 0, wrow(c));
-        tma_load_2d(smem + kScanQkL, &map_kql, &sy.qk, 0, wrow(c));
-        sy.n_qk += 1;
+    auto issue_qk = [&](int c) {  // masked decayed Q K^T rows, into buffer c%2
+        const int b = c & 1;
+        mbar_arrive_expect_tx(&sy.qk[b], 2 * 8192);
+        tma_load_2d(smem + kScanQk + b * 16384, &map_kqh, &sy.qk[b], 0, wrow(c));
+        tma_load_2d(smem + kScanQk + b * 16384 + 8192, &map_kql, &sy.qk[b], 0, wrow(c));
+        sy.n_qk[b] += 1;
     };
     if (tid == 0 && n_ch > 0) {
         issue_a4(0);
-        if (n_ch > 1) issue_a4(1);
         issue_k(0);
         issue_qk(0);
+        if (n_ch > 1) issue_qk(1);
     }
 
     // Shared-memory descriptors, computed once: a descriptor for address a + o
     // is the one for a plus o >> 4 (the 14-bit start field cannot carry over,
     // every address here is below 256 KB).
-    const uint64_t dA4_0 = desc_kmajor_sw128(smem_u32(smem + kScanA4));
-    const uint64_t dA4_1 = desc_kmajor_sw128(smem_u32(smem + kScanA4 + kScanA4Stage));
+    const uint64_t dA4 = desc_kmajor_sw128(smem_u32(smem + kScanA4H));
     const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
     const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
-    const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBuH), 8192);
-    const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQkH) - 8192);
+    const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
+    const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
     constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
+    auto bu = [&](int b, int k) { return dBu + (uint64_t)b * kLo16 + k * 128; };  // U buffer b
 
     // thread 0 issues every MMA; its last commit covers all of them
     uint64_t* last_commit = nullptr;
@@ -849,14 +854,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     // Output of chunk c (output warps, accumulator rows 64..127): needs P6_c done.
     auto output = [&](int c) -> bool {
         const int t = row - 64, s = c & 1, L = chunk_len(c);
+        const uint32_t slot = (uint32_t)(c % 3) * 64;
         const float eg = __expf(gcum(c, t));
-        bool ok = wait_or_dead(&sy.p6, c & 1, sy, 7);
+        bool ok = wait_or_dead(&sy.p6[c % 3], (c / 3) & 1, sy, 7);
         float o[32];
         if (ok) {
             tc_fence_after_sync();
             float b[32];
-            tmem_ld32(tmem + kTmD4 + s * 64 + lane_off + cl, o);
-            tmem_ld32(tmem + kTmD6 + s * 64 + lane_off + cl, b);
+            tmem_ld32(tmem + kTmD4 + slot + lane_off + cl, o);
+            tmem_ld32(tmem + kTmD6 + slot + lane_off + cl, b);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = fmaf(eg, o[j], b[j]);
         } else {
@@ -918,74 +924,81 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 
     // log of the state decay over a chunk, loaded one chunk ahead
     float gl_next = n_ch > 0 ? gcum(0, chunk_len(0) - 1) : 0.f;
+    // P6_c = (M o QK^T)_c U_c -> D6[c%3] (thread 0).  A rows 0..63 of this M=128
+    // operand are whatever precedes the QK^T rows in shared memory: they only
+    // reach accumulator rows 0..63 of D6, which nothing reads.
+    auto issue_p6 = [&](int c) {
+        if (!wait_or_dead(&sy.qk[c & 1], (c >> 1) & 1, sy, 8)) return;
+        tc_fence_after_sync();
+        const uint32_t id6 = idesc_bf16_f32(128, kDS, false, true);
+        const uint64_t dq = dQk + (uint64_t)(c & 1) * kLo16;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mma3(tmem + kTmD6 + (uint32_t)(c % 3) * 64, dq + k * 2, dq + kLo8 + k * 2, bu(c & 1, k),
+                 bu(c & 1, k) + kLo8, id6, k > 0 ? 1u : 0u);
+        mma_commit(&sy.p6[c % 3]);
+        last_commit = &sy.p6[c % 3];
+        last_parity = (c / 3) & 1;
+    };
     for (int c = 0; c < n_ch; ++c) {
         const float gam = __expf(gl_next);  // state decay over chunk c
         if (c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
-        // 1. P4_c = [W; Q] S into D4[c%2]
+        // 1. P4_c = [W; Q] S into D4[c%3], then P6_{c-1}
         if (tid == 0) {
-            bool ok = wait_or_dead(&sy.a4[c & 1], (c >> 1) & 1, sy, 4);
+            bool ok = wait_or_dead(&sy.a4, c & 1, sy, 4);
             if (ok) {
                 tc_fence_after_sync();
-                const uint64_t da = (c & 1) ? dA4_1 : dA4_0;
                 const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma3(tmem + kTmD4 + (c & 1) * 64, da + ao, da + kLoA4 + ao, dBs + k * 128,
-                         dBs + kLo16 + k * 128, id, k > 0 ? 1u : 0u);
+                    mma3(tmem + kTmD4 + (uint32_t)(c % 3) * 64, dA4 + ao, dA4 + kLoA4 + ao,
+                         dBs + k * 128, dBs + kLo16 + k * 128, id, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&sy.p4);
                 last_commit = &sy.p4;
                 last_parity = c & 1;
+                if (c > 0) issue_p6(c - 1);
             }
         }
         __syncwarp();
-        // 2. U_c (rows 0..63) | output of chunk c-1 (rows 64..127)
+        // 2. U_c (rows 0..63) | output of chunk c-2 (rows 64..127)
         if (is_u) {
             if (wait_or_dead(&sy.p4, c & 1, sy, 5)) {
                 tc_fence_after_sync();
-                if (tid == 128 && c + 2 < n_ch) issue_a4(c + 2);  // P4_c has read stage c%2
+                if (tid == 128 && c + 1 < n_ch) issue_a4(c + 1);  // P4_c has read the [W; Q] tile
                 __syncwarp();
                 float ws[32];
-                tmem_ld32(tmem + kTmD4 + (c & 1) * 64 + lane_off + cl, ws);
+                tmem_ld32(tmem + kTmD4 + (uint32_t)(c % 3) * 64 + lane_off + cl, ws);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ut[j] -= ws[j];
+                // buffer c%2 held U_{c-2}: its products finished before P4_c
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
-                    split_store(ut + 8 * ch, smem + kScanBuH + o, smem + kScanBuL + o);
+                    const uint32_t o = (c & 1) * 16384 + row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                    split_store(ut + 8 * ch, smem + kScanBu + o, smem + kScanBu + 8192 + o);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&sy.u);
                 if (c + 1 < n_ch) load_ut(c + 1);
             }
-        } else if (c > 0) {
-            output(c - 1);
-            load_z(c);
+        } else if (c > 1) {
+            output(c - 2);
+            load_z(c - 1);
         }
-        // 3. P7_c = K''^T U -> Ds, then P6_c = (M o QK^T) U -> D6[c%2]
+        // 3. P7_c = K''^T U -> Ds
         if (tid == 0) {
-            const bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5) &&
-                            wait_or_dead(&sy.qk, c & 1, sy, 8);
+            const bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
             if (ok) {
                 tc_fence_after_sync();
                 const uint32_t id7 = idesc_bf16_f32(128, kDS, true, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, dBu + k * 128,
-                         dBu + kLo8 + k * 128, id7, k > 0 ? 1u : 0u);
+                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, bu(c & 1, k),
+                         bu(c & 1, k) + kLo8, id7, k > 0 ? 1u : 0u);
                 mma_commit(&sy.p7);
-                // A rows 0..63 of this M=128 operand are whatever precedes the
-                // QK^T rows in shared memory: they only reach accumulator rows
-                // 0..63 of D6, which nothing reads.
-                const uint32_t id6 = idesc_bf16_f32(128, kDS, false, true);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmD6 + (c & 1) * 64, dQk + k * 2, dQk + kLo8 + k * 2, dBu + k * 128,
-                         dBu + kLo8 + k * 128, id6, k > 0 ? 1u : 0u);
-                mma_commit(&sy.p6);
-                last_commit = &sy.p6;
+                last_commit = &sy.p7;
                 last_parity = c & 1;
             }
         }
@@ -1003,22 +1016,33 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         tc_fence_before_sync();
         if (__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead))) break;
         tc_fence_after_sync();
-        if (tid == 32 && c + 1 < n_ch) {  // off thread 0, which goes on to P4_{c+1}
-            issue_k(c + 1);  // P7_c has read K''_c
-            // sQK is free once P6_c is done (it runs during the state update)
-            if (wait_or_dead(&sy.p6, c & 1, sy, 7)) issue_qk(c + 1);
+        if (tid == 32) {  // off thread 0, which goes on to P4_{c+1}
+            if (c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K''_c
+            // QK^T_{c+1} (for P6_{c+1}, issued in chunk c+2) into the buffer P6_{c-1} has read
+            if (c > 0 && c + 1 < n_ch && wait_or_dead(&sy.p6[(c - 1) % 3], ((c - 1) / 3) & 1, sy, 7))
+                issue_qk(c + 1);
         }
     }
     const bool alive = !__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead));
-    if (alive && n_ch > 0 && !is_u) output(n_ch - 1);  // the last chunk's output
+    if (alive && n_ch > 0) {
+        if (tid == 0) issue_p6(n_ch - 1);  // the last chunk's output term
+        __syncwarp();
+        if (!is_u) {  // the two outputs still pending
+            if (n_ch > 1) {
+                output(n_ch - 2);
+                load_z(n_ch - 1);
+            }
+            output(n_ch - 1);
+        }
+    }
 
     // Unwind: no copy or MMA of this CTA may still be in flight when it leaves.
     __syncthreads();
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s)
-            if (sy.n_a4[s] > 0) mbar_wait(&sy.a4[s], (sy.n_a4[s] - 1) & 1);
+        if (sy.n_a4 > 0) mbar_wait(&sy.a4, (sy.n_a4 - 1) & 1);
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
-        if (sy.n_qk > 0) mbar_wait(&sy.qk, (sy.n_qk - 1) & 1);
+        for (int b = 0; b < 2; ++b)
+            if (sy.n_qk[b] > 0) mbar_wait(&sy.qk[b], (sy.n_qk[b] - 1) & 1);
         if (last_commit) mbar_wait(last_commit, last_parity);
     }
     if (p.state_out && !sy.dead) {
