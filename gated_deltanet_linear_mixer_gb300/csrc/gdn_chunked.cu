@@ -27,6 +27,8 @@
 // along a tile's rows (S, U, [K|V] rows) use the MN-major descriptor; every A
 // operand is K-major (the one A that would be MN-major, the scaled keys of the
 // state increment, is transposed by threads).
+#include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "gdn_common.cuh"
@@ -87,12 +89,15 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
 __device__ __forceinline__ bool any_failed(bool ok) { return __syncthreads_or(ok ? 0 : 1) != 0; }
 
 // ------------------------------------------------------------ chunk table
-// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C).  One CTA.
+// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C).  One CTA; it
+// also clears the n_ready item flags of the fused launch.
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu_seqlens, int n_seq,
-                                                           int32_t* cu_chunks) {
+                                                           int32_t* cu_chunks, int* ready,
+                                                           int n_ready) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < n_ready; i += 1024) ready[i] = 0;
     if (tid == 0) {
         carry = 0;
         cu_chunks[0] = 0;
@@ -183,11 +188,22 @@ __device__ __forceinline__ float* prep_tf(uint8_t* smem, int hh, int row) {
     return reinterpret_cast<float*>(smem + kPrepAg + (hh * 2 + (row >> 5)) * 16384 + (row & 31) * 256);
 }
 
-__global__ void __launch_bounds__(kChunkThreads, 1)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
-                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
-                  const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
-                  const __grid_constant__ CUtensorMap map_kql, ChunkArgs p) {
+// An item is published (p.ready non-null) once all of its workspace writes
+// have landed: the TMA stores completed, then a gpu-scope release that also
+// covers the other threads' stores (they precede it through the CTA barrier).
+__device__ __forceinline__ void publish_item(int* flag) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+    __threadfence();
+    st_release_gpu(flag, 1);
+}
+
+// Items worker, worker + n_workers, ... (chunk-major).
+__device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
+                                                const CUtensorMap& map_wh, const CUtensorMap& map_wl,
+                                                const CUtensorMap& map_u, const CUtensorMap& map_kqh,
+                                                const CUtensorMap& map_kql, const ChunkArgs& p,
+                                                const int worker, const int n_workers) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -248,15 +264,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             }
         }
     };
-    if (tid == 0 && (int)blockIdx.x < n_items) {
-        issue_qk_tiles(blockIdx.x);
-        issue_v_item(blockIdx.x, 0);
+    if (tid == 0 && worker < n_items) {
+        issue_qk_tiles(worker);
+        issue_v_item(worker, 0);
     }
-    tma_pending = v_pending = (int)blockIdx.x < n_items;
+    tma_pending = v_pending = worker < n_items;
+    int pub = -1;  // finished item whose flag is still to be set
 
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    for (int item = worker; item < n_items; item += n_workers) {
     const int c = item / p.n_k_heads, hk = item % p.n_k_heads;
-    const int next = item + gridDim.x;
+    const int next = item + n_workers;
     const ChunkPos cp = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, c);
     const int t0 = cp.t0, L = cp.L;
     bool failed = false;
@@ -330,6 +347,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         mma_pending = false;
         mma_phase ^= 1;
         tc_fence_after_sync();
+        if (pub >= 0) {  // the previous item's stores were issued long ago
+            if (tid == 0) publish_item(p.ready + pub);
+            pub = -1;
+        }
 
         for (int pr = 0; pr < n_pairs; ++pr) {
             const int nb = min(2, R - 2 * pr);
@@ -609,6 +630,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
             v_pending = pr + 1 < n_pairs || next < n_items;
             __syncthreads();
         }
+        if (!failed && p.ready) pub = item;
     } while (false);
     if (failed) break;
     }
@@ -620,10 +642,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     }
     if (__syncthreads_or(mma_pending) && tid == 0) mbar_wait(&bar_mma, mma_phase);
     if (tid == 0) bulk_wait_all();
+    if (tid == 0 && pub >= 0) publish_item(p.ready + pub);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+__global__ void __launch_bounds__(kChunkThreads, 1)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                  const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
+                  const __grid_constant__ CUtensorMap map_kql, ChunkArgs p) {
+    chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_u, map_kqh, map_kql, p, blockIdx.x, gridDim.x);
 }
 
 // --------------------------------------------------------------- chunk_scan
@@ -698,12 +729,12 @@ __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, Sca
     }
 }
 
-__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
-                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
-                  const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
-                  const __grid_constant__ CUtensorMap map_kkh, const __grid_constant__ CUtensorMap map_kkl,
-                  ChunkArgs p) {
+// Value head h of sequence n, this CTA's half of the value lanes.
+__device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
+                                                const CUtensorMap& map_wh, const CUtensorMap& map_wl,
+                                                const CUtensorMap& map_kqh, const CUtensorMap& map_kql,
+                                                const CUtensorMap& map_kkh, const CUtensorMap& map_kkl,
+                                                const ChunkArgs& p, const int h, const int n) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -719,7 +750,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice
     const uint32_t lane_off = (32u * q) << 16;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
-    const int h = blockIdx.x / kSplit, n = blockIdx.y;
     const int v0 = static_cast<int>(rank) * kDS;  // first value lane of this CTA
     const int hv_n = p.n_v_heads;
     const int R = hv_n / p.n_k_heads, hk = h / R;
@@ -777,7 +807,27 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     auto tok0 = [&](int c) { return bos + c * kC; };
     auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
     auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
+    // Fused launch: chunk c's workspace rows come from prep CTAs running
+    // alongside; wait (bounded) for its item flag.  TMA loads of published
+    // rows follow a global proxy fence (in the issue_* helpers).
+    auto wait_chunk = [&](int c) -> bool {
+        const int* f = p.ready + (size_t)(c_begin + c) * p.n_k_heads + hk;
+        if (ld_acquire_gpu(f)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        const long long c0 = clock64();
+        for (;;) {
+            __nanosleep(100);
+            if (ld_acquire_gpu(f)) return true;
+            if (*reinterpret_cast<volatile int*>(&sy.dead)) return false;
+            if (globaltimer_ns() - t0 > 2000000000ull || clock64() - c0 > (1ll << 32)) {
+                atomicExch(&sy.dead, 1);
+                report_error(11);
+                return false;
+            }
+        }
+    };
     auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
+        if (p.ready) fence_proxy_async_global();
         mbar_arrive_expect_tx(&sy.a4, 8 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -789,6 +839,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
         sy.n_a4 += 1;
     };
     auto issue_k = [&](int c) {  // decayed key rows K'', both key-lane blocks (MN-major A)
+        if (p.ready) fence_proxy_async_global();
         mbar_arrive_expect_tx(&sy.k, 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -799,17 +850,19 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     };
     auto issue_qk = [&](int c) {  // masked decayed Q K^T rows, into buffer c%2
         const int b = c & 1;
+        if (p.ready) fence_proxy_async_global();
         mbar_arrive_expect_tx(&sy.qk[b], 2 * 8192);
         tma_load_2d(smem + kScanQk + b * 16384, &map_kqh, &sy.qk[b], 0, wrow(c));
         tma_load_2d(smem + kScanQk + b * 16384 + 8192, &map_kql, &sy.qk[b], 0, wrow(c));
         sy.n_qk[b] += 1;
     };
-    if (tid == 0 && n_ch > 0) {
+    if (tid == 0 && n_ch > 0 && (!p.ready || (wait_chunk(0) && (n_ch < 2 || wait_chunk(1))))) {
         issue_a4(0);
         issue_k(0);
         issue_qk(0);
         if (n_ch > 1) issue_qk(1);
     }
+    if (p.ready) __syncthreads();  // chunks 0 and 1 are readable by every thread
 
     // Shared-memory descriptors, computed once: a descriptor for address a + o
     // is the one for a plus o >> 4 (the 14-bit start field cannot carry over,
@@ -983,9 +1036,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                 mbar_arrive(&sy.u);
                 if (c + 1 < n_ch) load_ut(c + 1);
             }
-        } else if (c > 1) {
-            output(c - 2);
-            load_z(c - 1);
+        } else {
+            if (c > 1) {
+                output(c - 2);
+                load_z(c - 1);
+            }
+            // chunk c+2 is first read in chunk c+1 (its cumulative decay, its
+            // [W; Q] and U~ rows): its flag is awaited before this chunk's
+            // closing barrier
+            if (p.ready && tid == 64 && c + 2 < n_ch) wait_chunk(c + 2);
         }
         // 3. P7_c = K''^T U -> Ds
         if (tid == 0) {
@@ -1059,6 +1118,40 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
+chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                  const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                  const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                  const __grid_constant__ CUtensorMap map_kkh, const __grid_constant__ CUtensorMap map_kkl,
+                  ChunkArgs p) {
+    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kkh, map_kkl, p,
+                    blockIdx.x / kSplit, blockIdx.y);
+}
+
+// ------------------------------------------------------------- chunk_fused
+// Both phases in one launch, for batches whose scan alone would leave most of
+// the GPU idle (its clusters run one chunk after another).  CTAs [0, n_prep)
+// run chunk_prep over every item, chunk-major, and set each item's flag once
+// its rows have landed; the other CTAs run chunk_scan, one cluster per
+// (sequence, value head), and read a chunk's rows only after its flag is set,
+// so the scan of chunk c overlaps the prep of the chunks after it.  Prep CTAs
+// never wait for scan CTAs: the launch completes whichever of its CTAs are
+// resident at a time.
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
+chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                   const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
+                   const __grid_constant__ CUtensorMap map_kql, const __grid_constant__ CUtensorMap map_kkh,
+                   const __grid_constant__ CUtensorMap map_kkl, ChunkArgs p, int n_prep) {
+    if ((int)blockIdx.x < n_prep) {
+        chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_u, map_kqh, map_kql, p, blockIdx.x, n_prep);
+    } else {
+        const int s = ((int)blockIdx.x - n_prep) / kSplit;  // n_prep is even: clusters stay aligned
+        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kkh, map_kkl, p,
+                        s % p.n_v_heads, s / p.n_v_heads);
+    }
+}
+
 // ------------------------------------------------------------------- host
 size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads, int n_v_heads,
                                ChunkLayout* lay) {
@@ -1085,10 +1178,34 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.kk_hi = off; off = up(off + crow * kD * 2);
     l.kk_lo = off; off = up(off + crow * kD * 2);
     l.gcum = off; off = up(off + crow * 4);
+    l.ready = off; off = up(off + (size_t)chunks * n_k_heads * 4);
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
     if (lay) *lay = l;
     return off;
+}
+
+// CTAs of chunk_fused_kernel that can be resident at once (2 x its active
+// clusters), per device; 0 when the query fails.
+static int fused_capacity(size_t smem) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) {
+        cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * kSplit);
+        cfg.blockDim = dim3(kChunkThreads);
+        cfg.dynamicSmemBytes = smem;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, chunk_fused_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            nc = 0;
+        }
+        cached[dev] = nc > 0 ? 2 * nc : -1;
+    }
+    return cached[dev] > 0 ? cached[dev] : 0;
 }
 
 // SMs of the current device (the persistent prep kernel runs one CTA per SM).
@@ -1129,7 +1246,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
 
     int32_t* cu_chunks = reinterpret_cast<int32_t*>(ws + l.cu_chunks);
     e = timed_launch("chunk_table", st, [&] {
-        chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.n_seq, cu_chunks);
+        chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.n_seq, cu_chunks,
+                                               reinterpret_cast<int*>(ws + l.ready),
+                                               l.n_chunks * hk_n);
         return cudaGetLastError();
     });
     if (e != cudaSuccess) return e;
@@ -1176,15 +1295,35 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
 
     const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 4 * kC * 4;
     const size_t scan_smem = 1024 + kScanEnd;
+    const size_t prep_smem_max = 1024 + kPrepVec + 8 * 4 * kC * 4;
     static bool attrs_set = false;
     if (!attrs_set) {
         cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(1024 + kPrepVec + 8 * 4 * kC * 4));
+                             static_cast<int>(prep_smem_max));
         cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(scan_smem));
+        cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(std::max(prep_smem_max, scan_smem)));
         attrs_set = true;
     }
     const int n_items = l.n_chunks * hk_n;
+    // One fused launch when the scan's clusters leave at least 32 CTA slots
+    // of the co-resident capacity for prep (GDN_PREFILL_FUSED=0 turns it off).
+    const int scan_ctas = hv_n * kSplit * a.n_seq;
+    int n_prep = 0;
+    const char* fz = std::getenv("GDN_PREFILL_FUSED");
+    if (n_items > 0 && !(fz && fz[0] == '0')) {
+        const int cap = fused_capacity(std::max(prep_smem_max, scan_smem));
+        if (scan_ctas + 32 <= cap) n_prep = std::min(cap - scan_ctas, (n_items + 1) & ~1);
+    }
+    if (n_prep > 0) {
+        p.ready = reinterpret_cast<int*>(ws + l.ready);
+        return timed_launch("chunk_fused", st, [&] {
+            chunk_fused_kernel<<<dim3(n_prep + scan_ctas), kChunkThreads, std::max(prep_smem, scan_smem),
+                                 st>>>(m_qh, m_ql, m_wh, m_wl, m_u, m_kqh, m_kql, m_kkh, m_kkl, p, n_prep);
+            return cudaGetLastError();
+        });
+    }
     if (l.n_chunks > 0) {
         e = timed_launch("chunk_prep", st, [&] {
             chunk_prep_kernel<<<dim3(std::min(n_items, sm_count())), kChunkThreads, prep_smem, st>>>(

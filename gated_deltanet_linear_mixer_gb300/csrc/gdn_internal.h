@@ -87,12 +87,13 @@ struct ChunkArgs {
     __nv_bfloat16* kk_lo;
     float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
     __nv_bfloat16* out;           // [T, Hv*dv]
+    int* ready;                   // [chunks, Hk] item done flags (fused launch), else null
 };
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
     size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, kk_hi, kk_lo, gcum,
-        total;
+        ready, total;
     int n_chunks;
 };
 
