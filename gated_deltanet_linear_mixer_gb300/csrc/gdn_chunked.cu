@@ -168,12 +168,13 @@ __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint6
 // One CTA per (chunk, key head); its R = Hv/Hk value heads are processed in
 // pairs so that every phase keeps all eight warps busy: the two heads of a
 // pair occupy rows 0..63 and 64..127 of each M=128 product.
-//   Gram     [Q; K] K^T on the tensor core (shared by the heads)
+//   Gram     [Q; K] K^T on the tensor core (shared by the heads); the K tile
+//            itself -> workspace, rows in chunk order (the scan's K^T U')
 //   per pair: M o QK^T rows -> workspace; A = strictly-lower beta_t
 //            e^{G_t-G_s} k_t.k_s; T = (I + A)^-1 by a blocked solve in fp32;
 //            W = (T diag(beta e^G)) K and U~ = (T diag(beta)) V on the tensor
 //            core (the row scalings of the right-hand sides are folded into
-//            T's columns); K''_t = e^{G_last-G_t} k_t; everything -> workspace.
+//            T's columns); everything -> workspace.
 constexpr uint32_t kPrepAg = 0;          // [Q; K] K-major 128 x 128 (hi at +0, lo at +32768)
 constexpr uint32_t kPrepV = 65536;       // V of the pair: hi blocks (a0 a1 b0 b1) then lo blocks
 constexpr uint32_t kPrepT1 = 131072;     // [T'_a; T'_b] K-major 128 x 64 (hi, lo at +16384)
@@ -201,8 +202,9 @@ __device__ __forceinline__ void publish_item(int* flag) {
 // Items worker, worker + n_workers, ... (chunk-major).
 __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
-                                                const CUtensorMap& map_u, const CUtensorMap& map_kqh,
-                                                const CUtensorMap& map_kql, const ChunkArgs& p,
+                                                const CUtensorMap& map_kqh,
+                                                const CUtensorMap& map_kql, const CUtensorMap& map_kwh,
+                                                const CUtensorMap& map_kwl, const ChunkArgs& p,
                                                 const int worker, const int n_workers) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -337,6 +339,13 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                      idesc_bf16_f32(128, 64), k > 0 ? 1u : 0u);
             }
             mma_commit(&bar_mma);
+            const int krow = (c * p.n_k_heads + hk) * kC;  // K tile (rows past the chunk are 0)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                tma_store_2d(&map_kwh, smem + kPrepAg + b * 16384 + 8192, 64 * b, krow);
+                tma_store_2d(&map_kwl, smem + kPrepAg + 32768 + b * 16384 + 8192, 64 * b, krow);
+            }
+            bulk_commit();
         }
         mma_pending = true;
         if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
@@ -370,6 +379,8 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                         make_uint4(0u, 0u, 0u, 0u);
                 }
             }
+            if (tid == 0) bulk_wait_read();  // the last W stores have read T1 / T2
+            __syncthreads();
             // ---- phase A: M o QK^T rows (warps 0,1 / 4,5) and A^T (warps 2,3 / 6,7)
             {
                 const int hh = warp >> 2;             // head of the pair this warp serves
@@ -406,7 +417,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             }
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0) {  // M o QK^T tiles -> workspace
+            if (tid == 64) {  // M o QK^T tiles -> workspace (thread 64 idles in the diagonal solve)
                 for (int hh = 0; hh < nb; ++hh) {
                     const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
                     tma_store_2d(&map_kqh, smem + kPrepT2 + hh * 16384, 0, row);
@@ -500,7 +511,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                     __syncthreads();
                 }
             }
-            if (tid == 0) bulk_wait_read();  // the QK^T staging tiles may be overwritten
+            if (tid == 64) bulk_wait_all();  // the QK^T tiles have landed (T2 is rewritten next)
             __syncthreads();
             // ---- T' = T diag(beta e^G), T'' = T diag(beta): split into the A tiles
             for (int it = tid; it < 2 * kC * 8; it += kChunkThreads) {
@@ -552,20 +563,6 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 mma_commit(&bar_mma);
             }
             mma_pending = true;
-            // while the products run: decayed keys K''_t = e^{G_last-G_t} k_t -> workspace
-            for (int it = tid; it < nb * kC * 16; it += kChunkThreads) {
-                const int hh = it >> 10, t = (it >> 4) & 63, ch = it & 15;
-                const int r = 2 * pr + hh, h = hk * R + r;
-                const float* Gr = sG + r * kC;
-                const float f = t < L ? __expf(Gr[L - 1] - Gr[t]) : 0.f;
-                const uint32_t so = (ch >> 3) * 16384 + 8192 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
-                float v[8];
-                load_pair(smem + kPrepAg + so, smem + kPrepAg + 32768 + so, v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = t < L ? v[e] * f : 0.f;
-                const size_t o = ((size_t)(c * hv_n + h) * kC + t) * kD + 8 * ch;
-                split_store(v, reinterpret_cast<uint8_t*>(p.kk_hi + o), reinterpret_cast<uint8_t*>(p.kk_lo + o));
-            }
             if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(3);
                 failed = true;
@@ -575,17 +572,27 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             mma_phase ^= 1;
             tc_fence_after_sync();
             if (pr + 1 == n_pairs && next < n_items) {
-                // the q, k tiles are no longer read (K'' and the products are
+                // the q, k tiles are no longer read (the products are
                 // done): the next item's may land while this one is written out
-                if (tid == 0) issue_qk_tiles(next);
+                if (tid == 0) {
+                    bulk_wait_read();  // the K tile store has read the tile
+                    issue_qk_tiles(next);
+                }
                 tma_pending = true;
             }
-            // ---- phase D: W rows (hi, lo) and U~ rows (fp32), staged in the now
-            // free v / T tiles (head a / head b, 64 KB each), then TMA stores
+            if (tid == 0) {  // the products have read the v tiles: the next ones may land
+                if (pr + 1 < n_pairs) issue_v_item(item, pr + 1);
+                else if (next < n_items) issue_v_item(next, 0);
+            }
+            v_pending = pr + 1 < n_pairs || next < n_items;
+            // ---- phase D: W rows (hi, lo) staged in the free T tiles (head a in
+            // T1, head b in T2) for TMA stores; U~ rows (fp32) straight to the
+            // workspace, 4-column groups of 64 rows each ([group][row][4]), so
+            // that both these stores and the scan's row loads are coalesced
             {
                 const int q = warp & 3, half = warp >> 2;
                 const int hh = q >> 1, t = 32 * (q & 1) + lane;
-                uint8_t* st = smem + (hh ? kPrepT1 : kPrepV);
+                uint8_t* st = smem + (hh ? kPrepT2 : kPrepT1);
                 float v[64];
                 tmem_ld64(tmem + kTpW + ((32u * q) << 16) + 64 * half, v);
 #pragma unroll
@@ -594,14 +601,14 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                     split_store(v + 8 * q8, st + o, st + 16384 + o);
                 }
                 tmem_ld64(tmem + (hh ? kTpUb : kTpUa) + ((32u * q) << 16) + 64 * half, v);
-#pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4)
-                    *reinterpret_cast<float4*>(st + 32768 + (2 * half + (q4 >> 3)) * 8192 +
-                                               sw128_offset(t, q4 & 7)) =
-                        make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-                if (hh < nb && half == 0) {
+                if (hh < nb) {
                     const int h = hk * R + 2 * pr + hh;
-                    p.gcum_ws[(size_t)(c * hv_n + h) * kC + t] = sG[(2 * pr + hh) * kC + t];
+                    float4* dst = reinterpret_cast<float4*>(p.u_ws + (size_t)(c * hv_n + h) * kC * kD) +
+                                  (16 * half) * kC + t;
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; ++q4)
+                        dst[q4 * kC] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                    if (half == 0) p.gcum_ws[(size_t)(c * hv_n + h) * kC + t] = sG[(2 * pr + hh) * kC + t];
                 }
             }
             fence_proxy_async_smem();
@@ -611,23 +618,15 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             if (tid == 0) {
                 for (int hh = 0; hh < nb; ++hh) {
                     const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
-                    const uint8_t* st = smem + (hh ? kPrepT1 : kPrepV);
+                    const uint8_t* st = smem + (hh ? kPrepT2 : kPrepT1);
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
                         tma_store_2d(&map_wh, st + b * 8192, 64 * b, row);
                         tma_store_2d(&map_wl, st + 16384 + b * 8192, 64 * b, row);
                     }
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) tma_store_2d(&map_u, st + 32768 + b * 8192, 32 * b, row);
                 }
-                bulk_commit();
-                // staging read out: the next v tiles (this item's next pair, or
-                // the next item's first) may land, T1/T2 may be rewritten
-                if (pr + 1 < n_pairs || next < n_items) bulk_wait_read();
-                if (pr + 1 < n_pairs) issue_v_item(item, pr + 1);
-                else if (next < n_items) issue_v_item(next, 0);
+                bulk_commit();  // waited (reads) before T1 / T2 are next written
             }
-            v_pending = pr + 1 < n_pairs || next < n_items;
             __syncthreads();
         }
         if (!failed && p.ready) pub = item;
@@ -652,9 +651,11 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
 __global__ void __launch_bounds__(kChunkThreads, 1)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
-                  const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
-                  const __grid_constant__ CUtensorMap map_kql, ChunkArgs p) {
-    chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_u, map_kqh, map_kql, p, blockIdx.x, gridDim.x);
+                  const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                  const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
+                  ChunkArgs p) {
+    chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
+                    blockIdx.x, gridDim.x);
 }
 
 // --------------------------------------------------------------- chunk_scan
@@ -662,19 +663,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // lanes [64p, 64p+64) of the state, of U and of the outputs.  The state
 // recurrence per chunk is a chain of two tensor-core products,
 //   U = U~ - W S   (rows 0..63 of P4 = [W; Q] S),   S <- e^{G_last} S + K''^T U
-// (P7, K'' = diag(e^{G_last-G}) K, written by chunk_prep).  Every step of the
+// (P7, K'' = diag(e^{G_last-G}) K, formed as K^T U' with U' = diag(e^{G_last-G})
+// U, so that the key tile is chunk_prep's copy of its input and the decay
+// factors, all <= 1, scale the fp32 U before it is split).  Every step of the
 // chain is spread over all eight warps: thread (warp w, lane l) owns key lane
 // 32 (w%4) + l of the state and value lanes 32 (w/4) .. +31 of this CTA's
 // slice, which is exactly the part of the tensor-memory accumulators that the
 // warp may read.  Per chunk c:
-//   1. thread 0 issues P4_c = [W; Q] S into D4[c%3], then the previous chunk's
-//      output term P6_{c-1} = (M o QK^T) U_{c-1} into D6[(c-1)%3], which runs
-//      while the tensor pipe would otherwise wait for U_c
+//   1. thread 0 issues P4_c = [W; Q] S into D4[c%3]
 //   2. warps 0,1,4,5 (accumulator rows 0..63): U_c = U~ - W S -> smem;
 //      warps 2,3,6,7 (rows 64..127), meanwhile: the output of chunk c-2,
 //      o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t, gated RMSNorm (sums of squares
 //      exchanged with the peer CTA through distributed shared memory), store
-//   3. thread 0 issues P7_c = K''^T U -> Ds
+//   3. thread 0 issues P7_c = K^T U' -> Ds, then the previous chunk's output
+//      term P6_{c-1} = (M o QK^T) U_{c-1} into D6[(c-1)%3] (an MMA holds its
+//      issuing warp ~75 cycles per instruction: issued after P7 it delays
+//      neither P4 nor thread 0's own rows of U)
 //   4. all warps: S <- e^{G_last} S + Ds, re-split S into smem
 // Accumulators D4 and D6 have three slots and U two buffers, so that the
 // output can trail the chain by two chunks.  Every wait is bounded
@@ -684,12 +688,13 @@ constexpr int kDS = kD / kSplit;  // value lanes per CTA
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64
 constexpr uint32_t kScanA4H = 32768, kScanA4L = 65536;      // [W; Q] K-major 128 x 128 (hi, lo)
-constexpr uint32_t kScanKH = 98304, kScanKL = 114688;       // K'' as MN-major A (dk 128 x t 64)
+constexpr uint32_t kScanKH = 98304, kScanKL = 114688;       // K as MN-major A (dk 128 x t 64)
 constexpr uint32_t kScanBu = 131072;                        // U, MN-major 64 x 64: buffer b at
                                                             //   +b*16384 (hi), +8192 (lo)
 constexpr uint32_t kScanQk = 163840;                        // M o QK^T rows (K-major 64 x 64):
                                                             //   buffer b at +b*16384 (hi), +8192 (lo)
-constexpr uint32_t kScanEnd = 196608;
+constexpr uint32_t kScanUp = 196608;                        // U' = diag(e^{G_last-G}) U (hi, +8192 lo)
+constexpr uint32_t kScanEnd = 212992;
 // tensor-memory columns: D4 and D6 in three slots each (chunk c uses c%3)
 constexpr uint32_t kTmD4 = 0, kTmD6 = 192, kTmDs = 384;
 
@@ -733,7 +738,7 @@ __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, Sca
 __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
                                                 const CUtensorMap& map_kqh, const CUtensorMap& map_kql,
-                                                const CUtensorMap& map_kkh, const CUtensorMap& map_kkl,
+                                                const CUtensorMap& map_kwh, const CUtensorMap& map_kwl,
                                                 const ChunkArgs& p, const int h, const int n) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -838,13 +843,14 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         }
         sy.n_a4 += 1;
     };
-    auto issue_k = [&](int c) {  // decayed key rows K'', both key-lane blocks (MN-major A)
+    auto issue_k = [&](int c) {  // key rows of the chunk, both key-lane blocks (MN-major A)
         if (p.ready) fence_proxy_async_global();
+        const int krow = ((c_begin + c) * p.n_k_heads + hk) * kC;
         mbar_arrive_expect_tx(&sy.k, 4 * 8192);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            tma_load_2d(smem + kScanKH + b * 8192, &map_kkh, &sy.k, 64 * b, wrow(c));
-            tma_load_2d(smem + kScanKL + b * 8192, &map_kkl, &sy.k, 64 * b, wrow(c));
+            tma_load_2d(smem + kScanKH + b * 8192, &map_kwh, &sy.k, 64 * b, krow);
+            tma_load_2d(smem + kScanKL + b * 8192, &map_kwl, &sy.k, 64 * b, krow);
         }
         sy.n_k += 1;
     };
@@ -870,6 +876,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     const uint64_t dA4 = desc_kmajor_sw128(smem_u32(smem + kScanA4H));
     const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
     const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
+    const uint64_t dUp = desc_mnmajor_sw128(smem_u32(smem + kScanUp), 8192);
     const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
     const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
     constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
@@ -881,17 +888,23 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     const bool sigmoid_gate = p.act == 1;
 
     float ut[32];   // U~ row (U warps), prefetched one chunk ahead
+    float gu = 0.f, glu = 0.f;  // G_t of that row and G_last of its chunk
     uint4 zr[4];    // z row (output warps) of the chunk whose output is pending
+    float gz = 0.f; // G_t of that row
     auto load_ut = [&](int c) {
-        const float4* src = reinterpret_cast<const float4*>(p.u_ws + ((size_t)wrow(c) + row) * kD + v0 + cl);
+        gu = gcum(c, row);
+        glu = gcum(c, chunk_len(c) - 1);
+        const float4* src = reinterpret_cast<const float4*>(p.u_ws + (size_t)wrow(c) * kD) +
+                            ((v0 + cl) >> 2) * kC + row;  // [4-column group][row][4]
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float4 v = src[i];
+            const float4 v = src[i * kC];
             ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
         }
     };
     auto load_z = [&](int c) {
         const int t = row - 64;
+        gz = gcum(c, t);
         if (t < chunk_len(c)) {
             const uint4* zp = reinterpret_cast<const uint4*>(
                 p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0 + cl);
@@ -908,7 +921,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     auto output = [&](int c) -> bool {
         const int t = row - 64, s = c & 1, L = chunk_len(c);
         const uint32_t slot = (uint32_t)(c % 3) * 64;
-        const float eg = __expf(gcum(c, t));
+        const float eg = __expf(gz);
         bool ok = wait_or_dead(&sy.p6[c % 3], (c / 3) & 1, sy, 7);
         float o[32];
         if (ok) {
@@ -996,7 +1009,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     for (int c = 0; c < n_ch; ++c) {
         const float gam = __expf(gl_next);  // state decay over chunk c
         if (c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
-        // 1. P4_c = [W; Q] S into D4[c%3], then P6_{c-1}
+        // 1. P4_c = [W; Q] S into D4[c%3]
         if (tid == 0) {
             bool ok = wait_or_dead(&sy.a4, c & 1, sy, 4);
             if (ok) {
@@ -1011,12 +1024,12 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 mma_commit(&sy.p4);
                 last_commit = &sy.p4;
                 last_parity = c & 1;
-                if (c > 0) issue_p6(c - 1);
             }
         }
         __syncwarp();
         // 2. U_c (rows 0..63) | output of chunk c-2 (rows 64..127)
         if (is_u) {
+            const float eu = __expf(glu - gu);  // e^{G_last-G_t}, while P4_c runs
             if (wait_or_dead(&sy.p4, c & 1, sy, 5)) {
                 tc_fence_after_sync();
                 if (tid == 128 && c + 1 < n_ch) issue_a4(c + 1);  // P4_c has read the [W; Q] tile
@@ -1025,15 +1038,26 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 tmem_ld32(tmem + kTmD4 + (uint32_t)(c % 3) * 64 + lane_off + cl, ws);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ut[j] -= ws[j];
-                // buffer c%2 held U_{c-2}: its products finished before P4_c
+                // U' = e^{G_last-G_t} U_t first, for P7 (P7_{c-1} has read the
+                // last one); then U itself into buffer c%2 for P6_c, which is
+                // issued in the next chunk (buffer c%2 held U_{c-2}, whose
+                // product P6_{c-2} thread 0 issued before P4_c)
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                    float us[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) us[e] = ut[8 * ch + e] * eu;
+                    split_store(us, smem + kScanUp + o, smem + kScanUp + 8192 + o);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&sy.u);
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     const uint32_t o = (c & 1) * 16384 + row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
                     split_store(ut + 8 * ch, smem + kScanBu + o, smem + kScanBu + 8192 + o);
                 }
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                mbar_arrive(&sy.u);
                 if (c + 1 < n_ch) load_ut(c + 1);
             }
         } else {
@@ -1046,7 +1070,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             // closing barrier
             if (p.ready && tid == 64 && c + 2 < n_ch) wait_chunk(c + 2);
         }
-        // 3. P7_c = K''^T U -> Ds
+        // 3. P7_c = K''^T U = K^T U' -> Ds, then the previous chunk's output term
         if (tid == 0) {
             const bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
             if (ok) {
@@ -1054,11 +1078,13 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 const uint32_t id7 = idesc_bf16_f32(128, kDS, true, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, bu(c & 1, k),
-                         bu(c & 1, k) + kLo8, id7, k > 0 ? 1u : 0u);
+                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, dUp + k * 128,
+                         dUp + kLo8 + k * 128, id7, k > 0 ? 1u : 0u);
                 mma_commit(&sy.p7);
                 last_commit = &sy.p7;
                 last_parity = c & 1;
+                // behind P7 in the pipe: delays neither P4 nor this warp's rows of U
+                if (c > 0) issue_p6(c - 1);
             }
         }
         __syncwarp();
@@ -1076,7 +1102,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         if (__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead))) break;
         tc_fence_after_sync();
         if (tid == 32) {  // off thread 0, which goes on to P4_{c+1}
-            if (c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K''_c
+            if (c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K_c
             // QK^T_{c+1} (for P6_{c+1}, issued in chunk c+2) into the buffer P6_{c-1} has read
             if (c > 0 && c + 1 < n_ch && wait_or_dead(&sy.p6[(c - 1) % 3], ((c - 1) / 3) & 1, sy, 7))
                 issue_qk(c + 1);
@@ -1102,8 +1128,8 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
         for (int b = 0; b < 2; ++b)
             if (sy.n_qk[b] > 0) mbar_wait(&sy.qk[b], (sy.n_qk[b] - 1) & 1);
-        if (last_commit) mbar_wait(last_commit, last_parity);
     }
+    if (last_commit) mbar_wait(last_commit, last_parity);
     if (p.state_out && !sy.dead) {
         float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
@@ -1122,9 +1148,9 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 
 chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
-                  const __grid_constant__ CUtensorMap map_kkh, const __grid_constant__ CUtensorMap map_kkl,
+                  const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                   ChunkArgs p) {
-    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kkh, map_kkl, p,
+    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
                     blockIdx.x / kSplit, blockIdx.y);
 }
 
@@ -1140,14 +1166,15 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                    const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
-                   const __grid_constant__ CUtensorMap map_u, const __grid_constant__ CUtensorMap map_kqh,
-                   const __grid_constant__ CUtensorMap map_kql, const __grid_constant__ CUtensorMap map_kkh,
-                   const __grid_constant__ CUtensorMap map_kkl, ChunkArgs p, int n_prep) {
+                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
+                   ChunkArgs p, int n_prep) {
     if ((int)blockIdx.x < n_prep) {
-        chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_u, map_kqh, map_kql, p, blockIdx.x, n_prep);
+        chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
+                        blockIdx.x, n_prep);
     } else {
         const int s = ((int)blockIdx.x - n_prep) / kSplit;  // n_prep is even: clusters stay aligned
-        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kkh, map_kkl, p,
+        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
                         s % p.n_v_heads, s / p.n_v_heads);
     }
 }
@@ -1175,8 +1202,8 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.u = off; off = up(off + crow * kD * 4);
     l.qk_hi = off; off = up(off + crow * kC * 2);
     l.qk_lo = off; off = up(off + crow * kC * 2);
-    l.kk_hi = off; off = up(off + crow * kD * 2);
-    l.kk_lo = off; off = up(off + crow * kD * 2);
+    l.kw_hi = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
+    l.kw_lo = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
     l.gcum = off; off = up(off + crow * 4);
     l.ready = off; off = up(off + (size_t)chunks * n_k_heads * 4);
     l.total = off;
@@ -1240,6 +1267,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     cv.qkv_lo_out = ws + l.qkv_lo;
     cv.g_out = reinterpret_cast<float*>(ws + l.g);
     cv.beta_out = reinterpret_cast<float*>(ws + l.beta);
+    cv.zero_tail = kC;  // the padding chunk after the last token: read by partial-chunk tiles
     cudaError_t e = timed_launch("conv_prologue", st, [&] { return launch_conv_prologue(cv, true, st); });
     if (e != cudaSuccess) return e;
     if (a.n_seq == 0) return cudaSuccess;
@@ -1269,16 +1297,15 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.u_ws = reinterpret_cast<float*>(ws + l.u);
     p.qk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_hi);
     p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
-    p.kk_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.kk_hi);
-    p.kk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.kk_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl, m_u;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kkh = m_kkl = m_u = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kwh = m_kwl = m_qh;
+    const uint64_t krows = (uint64_t)l.n_chunks * hk_n * kC;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
@@ -1287,9 +1314,8 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kkh, ws + l.kk_hi, crow, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kkl, ws + l.kk_lo, crow, kD, kD, 64, 64) ||
-            !make_tma_map_f32_2d(&m_u, ws + l.u, crow, kD, kD, 64, 32))
+            !make_tma_map_bf16_2d(&m_kwh, ws + l.kw_hi, krows, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_kwl, ws + l.kw_lo, krows, kD, kD, 64, 64))
             return cudaErrorInvalidValue;
     }
 
@@ -1320,21 +1346,21 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         p.ready = reinterpret_cast<int*>(ws + l.ready);
         return timed_launch("chunk_fused", st, [&] {
             chunk_fused_kernel<<<dim3(n_prep + scan_ctas), kChunkThreads, std::max(prep_smem, scan_smem),
-                                 st>>>(m_qh, m_ql, m_wh, m_wl, m_u, m_kqh, m_kql, m_kkh, m_kkl, p, n_prep);
+                                 st>>>(m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p, n_prep);
             return cudaGetLastError();
         });
     }
     if (l.n_chunks > 0) {
         e = timed_launch("chunk_prep", st, [&] {
             chunk_prep_kernel<<<dim3(std::min(n_items, sm_count())), kChunkThreads, prep_smem, st>>>(
-                m_qh, m_ql, m_wh, m_wl, m_u, m_kqh, m_kql, p);
+                m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p);
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;
     }
     e = timed_launch("chunk_scan", st, [&] {
         chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
-            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kkh, m_kkl, p);
+            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p);
         return cudaGetLastError();
     });
     return e;

@@ -184,11 +184,17 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
         return;
     }
     const int tb = tile0 + warp * kPro128Tok;  // first token of this warp
+    const int c = unit * 128 + 4 * lane;       // first channel of this lane
+    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(p.qkv_out);
+    __nv_bfloat16* __restrict__ out_lo = static_cast<__nv_bfloat16*>(p.qkv_lo_out);
+    for (int t = max(tb, p.n_tokens); t < min(tb + kPro128Tok, p.n_tokens + p.zero_tail); ++t) {
+        *reinterpret_cast<uint2*>(out + (size_t)t * cd + c) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(out_lo + (size_t)t * cd + c) = make_uint2(0u, 0u);
+    }
     if (tb >= p.n_tokens) return;              // warp-uniform
     const bool is_q = unit < p.n_k_heads;
     const bool norm = unit < 2 * p.n_k_heads;
     const float scale = is_q ? rsqrtf(128.f) : 1.f;
-    const int c = unit * 128 + 4 * lane;  // first channel of this lane
     const int K = p.conv_k, keep = K - 1, pad = 4 - K;
     float w[4][4];
 #pragma unroll
@@ -203,8 +209,6 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
                                               : make_uint2(0u, 0u);
     }
     const __nv_bfloat16* __restrict__ cs_in = static_cast<const __nv_bfloat16*>(p.conv_state_in);
-    __nv_bfloat16* __restrict__ out = static_cast<__nv_bfloat16*>(p.qkv_out);
-    __nv_bfloat16* __restrict__ out_lo = static_cast<__nv_bfloat16*>(p.qkv_lo_out);
     int n = seq_of_token(p.cu_seqlens, p.n_seq, tb);
     int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
 #pragma unroll
@@ -298,7 +302,8 @@ __global__ void conv_state_kernel(ConvStateArgs p) {
 cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream) {
     if (p.n_tokens == 0) return cudaSuccess;
     if (bf16 && p.d_k == 128 && p.d_v == 128 && p.qkv_lo_out) {
-        dim3 grid((p.n_tokens + kPro128Tile - 1) / kPro128Tile, 2 * p.n_k_heads + p.n_v_heads + 1);
+        dim3 grid((p.n_tokens + p.zero_tail + kPro128Tile - 1) / kPro128Tile,
+                  2 * p.n_k_heads + p.n_v_heads + 1);
         conv_prologue_d128_kernel<<<grid, 256, 0, stream>>>(p);
         return cudaGetLastError();
     }

@@ -24,6 +24,7 @@ struct ConvArgs {
     void* qkv_lo_out;           // [T, CD] bf16 residual x - bf16(x), or null (bf16 only)
     float* g_out;               // [T, Hv]
     float* beta_out;            // [T, Hv]
+    int zero_tail;              // rows [T, T + zero_tail) of qkv_out / qkv_lo_out set to 0
 };
 
 struct ConvStateArgs {
@@ -80,11 +81,9 @@ struct ChunkArgs {
     float* state_out;             // or null
     __nv_bfloat16* w_hi;          // [chunks, Hv, 64, dk] W (hi, lo)
     __nv_bfloat16* w_lo;
-    float* u_ws;                  // [chunks, Hv, 64, dv] U~ (fp32)
+    float* u_ws;                  // [chunks, Hv, dv/4, 64, 4] U~ (fp32), 4-column groups
     __nv_bfloat16* qk_hi;         // [chunks, Hv, 64, 64] masked decayed Q K^T (hi, lo)
     __nv_bfloat16* qk_lo;
-    __nv_bfloat16* kk_hi;         // [chunks, Hv, 64, dk] decayed keys e^{G_last-G_t} k_t (hi, lo)
-    __nv_bfloat16* kk_lo;
     float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
     __nv_bfloat16* out;           // [T, Hv*dv]
     int* ready;                   // [chunks, Hk] item done flags (fused launch), else null
@@ -92,8 +91,8 @@ struct ChunkArgs {
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, kk_hi, kk_lo, gcum,
-        ready, total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, kw_hi, kw_lo, gcum, ready,
+        total;
     int n_chunks;
 };
 
