@@ -48,17 +48,6 @@ __device__ int g_device_error = 0;
 
 __device__ __forceinline__ void report_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
-struct ChunkPos {
-    int n, t0, L;
-};
-
-__device__ __forceinline__ ChunkPos chunk_pos(const int32_t* cu_seqlens, const int32_t* cu_chunks,
-                                              int n_seq, int c) {
-    const int n = seq_of_token(cu_chunks, n_seq, c);
-    const int t0 = cu_seqlens[n] + (c - cu_chunks[n]) * kC;
-    return {n, t0, min(kC, cu_seqlens[n + 1] - t0)};
-}
-
 __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float f) {
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -89,11 +78,12 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
 __device__ __forceinline__ bool any_failed(bool ok) { return __syncthreads_or(ok ? 0 : 1) != 0; }
 
 // ------------------------------------------------------------ chunk table
-// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C).  One CTA; it
-// also clears the n_ready item flags of the fused launch.
+// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C), and per chunk its
+// first token and length.  One CTA; it also clears the n_ready item flags of
+// the fused launch.
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu_seqlens, int n_seq,
-                                                           int32_t* cu_chunks, int* ready,
-                                                           int n_ready) {
+                                                           int32_t* cu_chunks, int2* chunk_info,
+                                                           int* ready, int n_ready) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -129,6 +119,12 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu_seq
         __syncthreads();
         if (tid == 1023) carry = before + incl;
         __syncthreads();
+    }
+    const int n_chunks = n_seq > 0 ? cu_chunks[n_seq] : 0;
+    for (int c = tid; c < n_chunks; c += 1024) {
+        const int n = seq_of_token(cu_chunks, n_seq, c);
+        const int t0 = cu_seqlens[n] + (c - cu_chunks[n]) * kC;
+        chunk_info[c] = make_int2(t0, min(kC, cu_seqlens[n + 1] - t0));
     }
 }
 
@@ -237,9 +233,8 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
     bool tma_pending = false, mma_pending = false, v_pending = false;
 
     // q rows (0..63) and k rows (64..127) of item it, both column blocks
-    auto issue_qk_tiles = [&](int it) {
-        const int ci = it / p.n_k_heads, hki = it % p.n_k_heads;
-        const int t0i = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, ci).t0;
+    auto issue_qk_tiles = [&](int it, int t0i) {  // t0i: first token of item it's chunk
+        const int hki = it % p.n_k_heads;
         mbar_arrive_expect_tx(&bar_tma, 8 * 8192);
         const int qc = hki * kD, kc = p.n_k_heads * kD + hki * kD;
 #pragma unroll
@@ -252,9 +247,8 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
     };
     // v rows of pair pr of item it: hi blocks at kPrepV + (2*slot + b) * 8192,
     // lo blocks 32 KB further
-    auto issue_v_item = [&](int it, int pr) {
-        const int ci = it / p.n_k_heads, hki = it % p.n_k_heads;
-        const int t0i = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, ci).t0;
+    auto issue_v_item = [&](int it, int t0i, int pr) {
+        const int hki = it % p.n_k_heads;
         const int nb = min(2, R - 2 * pr);
         mbar_arrive_expect_tx(&bar_v, nb * 4 * 8192);
         for (int sl = 0; sl < nb; ++sl) {
@@ -266,9 +260,35 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             }
         }
     };
-    if (tid == 0 && worker < n_items) {
-        issue_qk_tiles(worker);
-        issue_v_item(worker, 0);
+    // Chunk position (first token, length) of an item two items ahead, and the
+    // gate inputs of the next item (whose position is then in hand): neither
+    // load waits on the other.
+    auto info = [&](int it) { return it < n_items ? p.chunk_info[it / p.n_k_heads] : make_int2(0, 0); };
+    int2 ci_n = make_int2(0, 0);                   // the next item's (at the top of an item)
+    int2 ci_nn = info(worker + n_workers);          // the one after
+    float ng0 = 0.f, ng1 = 0.f, nb0 = 0.f, nb1 = 0.f;
+    auto prefetch_gates = [&](int it) {  // ci_n holds item it's position
+        if (warp < R) {
+            const int h = (it % p.n_k_heads) * R + warp;
+            const int s0 = 2 * lane, s1 = 2 * lane + 1;
+            ng0 = ng1 = nb0 = nb1 = 0.f;
+            if (s0 < ci_n.y) {
+                ng0 = p.g[(size_t)(ci_n.x + s0) * hv_n + h];
+                nb0 = p.beta[(size_t)(ci_n.x + s0) * hv_n + h];
+            }
+            if (s1 < ci_n.y) {
+                ng1 = p.g[(size_t)(ci_n.x + s1) * hv_n + h];
+                nb1 = p.beta[(size_t)(ci_n.x + s1) * hv_n + h];
+            }
+        }
+    };
+    if (worker < n_items) {
+        ci_n = info(worker);
+        prefetch_gates(worker);
+        if (tid == 0) {
+            issue_qk_tiles(worker, ci_n.x);
+            issue_v_item(worker, ci_n.x, 0);
+        }
     }
     tma_pending = v_pending = worker < n_items;
     int pub = -1;  // finished item whose flag is still to be set
@@ -276,21 +296,14 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
     for (int item = worker; item < n_items; item += n_workers) {
     const int c = item / p.n_k_heads, hk = item % p.n_k_heads;
     const int next = item + n_workers;
-    const ChunkPos cp = chunk_pos(p.cu_seqlens, p.cu_chunks, p.n_seq, c);
-    const int t0 = cp.t0, L = cp.L;
+    const int t0 = ci_n.x, L = ci_n.y;
     bool failed = false;
+    const float g0 = ng0, g1 = ng1, b0 = nb0, b1 = nb1;
+    ci_n = ci_nn;                              // the next item's position, loaded an item ago
+    ci_nn = info(next + n_workers);
+    if (next < n_items) prefetch_gates(next);  // lands while this item runs
     if (warp < R) {  // cumulative log-decay and write strength of value head hk*R + warp
-        const int h = hk * R + warp;
         const int s0 = 2 * lane, s1 = 2 * lane + 1;
-        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-        if (s0 < L) {
-            g0 = p.g[(size_t)(t0 + s0) * hv_n + h];
-            b0 = p.beta[(size_t)(t0 + s0) * hv_n + h];
-        }
-        if (s1 < L) {
-            g1 = p.g[(size_t)(t0 + s1) * hv_n + h];
-            b1 = p.beta[(size_t)(t0 + s1) * hv_n + h];
-        }
         const float local = g0 + g1;
         float incl = local;
 #pragma unroll
@@ -576,13 +589,13 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 // done): the next item's may land while this one is written out
                 if (tid == 0) {
                     bulk_wait_read();  // the K tile store has read the tile
-                    issue_qk_tiles(next);
+                    issue_qk_tiles(next, ci_n.x);
                 }
                 tma_pending = true;
             }
             if (tid == 0) {  // the products have read the v tiles: the next ones may land
-                if (pr + 1 < n_pairs) issue_v_item(item, pr + 1);
-                else if (next < n_items) issue_v_item(next, 0);
+                if (pr + 1 < n_pairs) issue_v_item(item, t0, pr + 1);
+                else if (next < n_items) issue_v_item(next, ci_n.x, 0);
             }
             v_pending = pr + 1 < n_pairs || next < n_items;
             // ---- phase D: W rows (hi, lo) staged in the free T tiles (head a in
@@ -1197,6 +1210,7 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.g = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.beta = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.cu_chunks = off; off = up(off + (size_t)(n_seq + 1) * 4);
+    l.chunk_info = off; off = up(off + (size_t)chunks * 8);
     l.w_hi = off; off = up(off + crow * kD * 2);
     l.w_lo = off; off = up(off + crow * kD * 2);
     l.u = off; off = up(off + crow * kD * 4);
@@ -1275,6 +1289,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     int32_t* cu_chunks = reinterpret_cast<int32_t*>(ws + l.cu_chunks);
     e = timed_launch("chunk_table", st, [&] {
         chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.n_seq, cu_chunks,
+                                               reinterpret_cast<int2*>(ws + l.chunk_info),
                                                reinterpret_cast<int*>(ws + l.ready),
                                                l.n_chunks * hk_n);
         return cudaGetLastError();
@@ -1285,6 +1300,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.n_seq = a.n_seq; p.n_tokens = T; p.n_chunks = l.n_chunks;
     p.n_k_heads = hk_n; p.n_v_heads = hv_n; p.act = a.act; p.rms_eps = a.rms_eps;
     p.cu_seqlens = a.cu_seqlens; p.cu_chunks = cu_chunks;
+    p.chunk_info = reinterpret_cast<const int2*>(ws + l.chunk_info);
     p.qkv_hi = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_hi);
     p.qkv_lo = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_lo);
     p.g = reinterpret_cast<const float*>(ws + l.g);

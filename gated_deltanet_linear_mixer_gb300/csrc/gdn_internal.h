@@ -71,6 +71,7 @@ struct ChunkArgs {
     float rms_eps;
     const int32_t* cu_seqlens;    // [n_seq+1]
     const int32_t* cu_chunks;     // [n_seq+1] chunk offsets (workspace)
+    const int2* chunk_info;       // [chunks] first token and length of each chunk (workspace)
     const __nv_bfloat16* qkv_hi;  // [T, CD] normalised q | k | v, hi part (workspace)
     const __nv_bfloat16* qkv_lo;  // [T, CD] lo part (workspace)
     const float* g;               // [T, Hv] log-decay (workspace)
@@ -91,8 +92,8 @@ struct ChunkArgs {
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, w_hi, w_lo, u, qk_hi, qk_lo, kw_hi, kw_lo, gcum, ready,
-        total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, chunk_info, w_hi, w_lo, u, qk_hi, qk_lo, kw_hi, kw_lo,
+        gcum, ready, total;
     int n_chunks;
 };
 
