@@ -34,6 +34,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
+# DRAM bytes (read + write) per launch of a workload's dominant kernel, from the
+# ncu captures summarised under profiles/ (absent until a capture of the current
+# kernel exists; an entry is removed whenever its kernel changes).
+TRAFFIC = {
+    # profiles/chunk_fused_prefill_T4096.md, the bench's own workload
+    ("prefill", "chunk_fused"): 313_456_384 + 213_951_232,
+    # profiles/recurrent_decode_N64.md (64 sequences; the traffic is per sequence,
+    # so x 256/64 for the bench's 256)
+    ("decode", "recurrent"): (139_112_960 + 73_842_432) * 4,
+}
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -361,12 +371,24 @@ def run_gpu(args):
         dom_name, (dom_n, dom_ms) = dom
         dom_avg_ms = dom_ms / dom_n
         kb = r.kernel_bytes(dom_name, rep.keys())
-        achieved = kb / (dom_avg_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": kb,
-                "kernel_ms": dom_avg_ms,
-                "kernel_share": dom_ms / sum(v[1] for v in rep.values())}
+        share = dom_ms / sum(v[1] for v in rep.values())
+        if dom_name == "chunk_fused":
+            # every tensor-core contraction of the chunked form runs in this one
+            # launch: a contraction, measured against the bf16 tensor peak
+            fl = r.useful_flops()
+            achieved = fl / (dom_avg_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"], "traffic": TRAFFIC.get((r.key, dom_name)),
+                    "peak_source": peaks["source"] + " (bf16 burst)",
+                    "useful_flops_per_launch": fl, "kernel_ms": dom_avg_ms, "kernel_share": share}
+        else:
+            achieved = kb / (dom_avg_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": TRAFFIC.get((r.key, dom_name)), "peak_source": peaks["source"],
+                    "algorithmic_bytes_per_launch": kb, "kernel_ms": dom_avg_ms,
+                    "kernel_share": share}
         step_bytes = r.algorithmic_bytes()
         res = {
             "value": tok_s, "unit": UNIT, "ms_per_step": t_max,

@@ -233,6 +233,27 @@ def test_invalid_arguments_raise():
                    torch.zeros((1, 17, 4), dtype=d.dtype, device="cuda"), st)
 
 
+TC_CASES = sorted(k for k in PREFILL_CASES if k.startswith("tc_"))
+
+
+@pytest.mark.parametrize("name", TC_CASES)
+def test_prefill_fused_and_two_kernel_launches_agree(name, monkeypatch):
+    """Small batches run prep and scan as one launch (scan clusters wait on
+    the prep CTAs' per-chunk flags); GDN_PREFILL_FUSED=0 forces the two-kernel
+    launch.  Both do the same arithmetic: results must be bit-identical, and the
+    two-kernel launch must meet the oracle on its own."""
+    case = PREFILL_CASES[name]()
+    monkeypatch.setenv("GDN_PREFILL_FUSED", "0")
+    two = gpu_prefill(case)
+    monkeypatch.setenv("GDN_PREFILL_FUSED", "1")
+    one = gpu_prefill(case)
+    assert torch.equal(one["out"], two["out"])
+    assert torch.equal(one["state"], two["state"])
+    ref = run_oracle(case)
+    assert rel_err(two["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(two["state"], ref["state"]) <= TOL["bf16"]
+
+
 # ---------------------------------------------------------------- full sizes
 
 def test_full_size_prefill_T4096():
