@@ -40,7 +40,7 @@ namespace gdn {
 
 using namespace tc;
 
-constexpr int kC = 64;             // chunk length
+constexpr int kC = kChunkTokens;   // chunk length
 constexpr int kD = 128;            // d_k = d_v on this path
 constexpr int kChunkThreads = 256;
 
@@ -76,57 +76,6 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
 // Uniform decision after a bounded wait: every thread learns whether any
 // thread's wait gave up.
 __device__ __forceinline__ bool any_failed(bool ok) { return __syncthreads_or(ok ? 0 : 1) != 0; }
-
-// ------------------------------------------------------------ chunk table
-// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C), and per chunk its
-// first token and length.  One CTA; it also clears the n_ready item flags of
-// the fused launch.
-__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu_seqlens, int n_seq,
-                                                           int32_t* cu_chunks, int2* chunk_info,
-                                                           int* ready, int n_ready) {
-    __shared__ int32_t warp_tot[32];
-    __shared__ int32_t carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < n_ready; i += 1024) ready[i] = 0;
-    if (tid == 0) {
-        carry = 0;
-        cu_chunks[0] = 0;
-    }
-    __syncthreads();
-    for (int base = 0; base < n_seq; base += 1024) {
-        const int i = base + tid;
-        const int v = i < n_seq ? (cu_seqlens[i + 1] - cu_seqlens[i] + kC - 1) / kC : 0;
-        int incl = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int w = warp_tot[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, w, off);
-                if (lane >= off) w += y;
-            }
-            warp_tot[lane] = w;  // inclusive over warps
-        }
-        __syncthreads();
-        const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + carry;
-        if (i < n_seq) cu_chunks[i + 1] = before + incl;
-        __syncthreads();
-        if (tid == 1023) carry = before + incl;
-        __syncthreads();
-    }
-    const int n_chunks = n_seq > 0 ? cu_chunks[n_seq] : 0;
-    for (int c = tid; c < n_chunks; c += 1024) {
-        const int n = seq_of_token(cu_chunks, n_seq, c);
-        const int t0 = cu_seqlens[n] + (c - cu_chunks[n]) * kC;
-        chunk_info[c] = make_int2(t0, min(kC, cu_seqlens[n + 1] - t0));
-    }
-}
 
 // Split arithmetic.  Every tensor-core operand is carried as a pair of bf16
 // tiles, hi = bf16(x) and lo = bf16(x - hi), which together hold ~16
@@ -1282,19 +1231,17 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     cv.g_out = reinterpret_cast<float*>(ws + l.g);
     cv.beta_out = reinterpret_cast<float*>(ws + l.beta);
     cv.zero_tail = kC;  // the padding chunk after the last token: read by partial-chunk tiles
+    int32_t* cu_chunks = reinterpret_cast<int32_t*>(ws + l.cu_chunks);
+    if (a.n_seq > 0) {  // the chunk table, built by one CTA of the prologue
+        cv.cu_chunks = cu_chunks;
+        cv.chunk_info = reinterpret_cast<int2*>(ws + l.chunk_info);
+        cv.ready = reinterpret_cast<int*>(ws + l.ready);
+        cv.n_ready = l.n_chunks * hk_n;
+    }
     cudaError_t e = timed_launch("conv_prologue", st, [&] { return launch_conv_prologue(cv, true, st); });
     if (e != cudaSuccess) return e;
     if (a.n_seq == 0) return cudaSuccess;
 
-    int32_t* cu_chunks = reinterpret_cast<int32_t*>(ws + l.cu_chunks);
-    e = timed_launch("chunk_table", st, [&] {
-        chunk_table_kernel<<<1, 1024, 0, st>>>(a.cu_seqlens, a.n_seq, cu_chunks,
-                                               reinterpret_cast<int2*>(ws + l.chunk_info),
-                                               reinterpret_cast<int*>(ws + l.ready),
-                                               l.n_chunks * hk_n);
-        return cudaGetLastError();
-    });
-    if (e != cudaSuccess) return e;
 
     ChunkArgs p{};
     p.n_seq = a.n_seq; p.n_tokens = T; p.n_chunks = l.n_chunks;

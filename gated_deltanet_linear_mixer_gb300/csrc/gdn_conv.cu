@@ -152,12 +152,59 @@ conv_prologue_kernel(ConvArgs p) {
     }
 }
 
+// cu_chunks[i] = sum over sequences j < i of ceil(len_j / C); per chunk its
+// first token and length; the item flags cleared.  One CTA of 256 threads.
+__device__ void chunk_table_cta(const ConvArgs& p) {
+    __shared__ int32_t warp_tot[8];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < p.n_ready; i += 256) p.ready[i] = 0;
+    if (tid == 0) {
+        carry = 0;
+        p.cu_chunks[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < p.n_seq; base += 256) {
+        const int i = base + tid;
+        const int v = i < p.n_seq ? (p.cu_seqlens[i + 1] - p.cu_seqlens[i] + kChunkTokens - 1) / kChunkTokens : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < 8 ? warp_tot[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            if (lane < 8) warp_tot[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int before = (warp > 0 ? warp_tot[warp - 1] : 0) + carry;
+        if (i < p.n_seq) p.cu_chunks[i + 1] = before + incl;
+        __syncthreads();
+        if (tid == 255) carry = before + incl;
+        __syncthreads();
+    }
+    const int n_chunks = p.n_seq > 0 ? p.cu_chunks[p.n_seq] : 0;
+    for (int c = tid; c < n_chunks; c += 256) {
+        const int n = seq_of_token(p.cu_chunks, p.n_seq, c);
+        const int t0 = p.cu_seqlens[n] + (c - p.cu_chunks[n]) * kChunkTokens;
+        p.chunk_info[c] = make_int2(t0, min(kChunkTokens, p.cu_seqlens[n + 1] - t0));
+    }
+}
+
 // The prologue for bf16 activations with d_k = d_v = 128 (the tensor-core
 // prefill): one warp per (128-channel unit, 8-token run), 4 channels per lane,
 // four CTAs per SM.  The warp's 11 raw rows (3 of halo) are loaded up front with 8-byte
 // coalesced loads; per token the L2 norm of a q/k head is a full-warp
 // reduction.  Writes q|k|v as a (hi, lo) bf16 pair, g and beta like
-// conv_prologue_kernel.
+// conv_prologue_kernel; the first CTA of the gate row also builds the chunk table.
 constexpr int kPro128Tok = 8;                   // tokens per warp
 constexpr int kPro128Tile = 8 * kPro128Tok;     // tokens per CTA
 
@@ -169,7 +216,8 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(p.x);
 
-    if (unit == n_units) {  // gates for this token tile
+    if (unit == n_units) {  // gates for this token tile (and, in the first, the chunk table)
+        if (blockIdx.x == 0 && p.cu_chunks) chunk_table_cta(p);
         const int hv_n = p.n_v_heads;
         const __nv_bfloat16* __restrict__ a = static_cast<const __nv_bfloat16*>(p.a);
         const __nv_bfloat16* __restrict__ b = static_cast<const __nv_bfloat16*>(p.b);

@@ -9,6 +9,9 @@
 
 namespace gdn {
 
+// Tokens per chunk of the tensor-core prefill.
+constexpr int kChunkTokens = 64;
+
 struct ConvArgs {
     int n_seq, n_tokens, n_k_heads, n_v_heads, d_k, d_v, conv_k;
     float l2_eps;
@@ -25,6 +28,13 @@ struct ConvArgs {
     float* g_out;               // [T, Hv]
     float* beta_out;            // [T, Hv]
     int zero_tail;              // rows [T, T + zero_tail) of qkv_out / qkv_lo_out set to 0
+    // Chunk table of the tensor-core prefill, built by one CTA of the d=128
+    // prologue (null otherwise): offsets per sequence, (first token, length)
+    // per chunk, and n_ready item flags cleared.
+    int32_t* cu_chunks;         // [n_seq+1]
+    int2* chunk_info;           // [chunks]
+    int* ready;
+    int n_ready;
 };
 
 struct ConvStateArgs {
