@@ -61,6 +61,16 @@ gdn_status check_dims(const gdn_dims* d, const char* fn) {
     return GDN_OK;
 }
 
+long long conv_dim(const gdn_dims* d) {
+    return 2LL * d->n_k_heads * d->d_k + (long long)d->n_v_heads * d->d_v;
+}
+
+bool ranges_overlap(const void* a, const void* b, size_t bytes) {
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
 gdn_status check_params(const gdn_params* p, bool need_norm, const char* fn) {
     if (!p) return fail(GDN_ERR_INVALID_ARG, fn, "params is NULL");
     if (!p->conv_w || !p->A_log || !p->dt_bias || (need_norm && !p->norm_w))
@@ -305,6 +315,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    bool conv_done = false;
     if (gdn::chunked_supported(dims->d_k, dims->d_v, dims->n_k_heads, dims->n_v_heads, bf16)) {
         if (reinterpret_cast<uintptr_t>(workspace) & 255u)
             return fail(GDN_ERR_WORKSPACE, fn, "workspace must be 256-byte aligned");
@@ -317,6 +328,13 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         c.norm_w = params->norm_w; c.conv_state_in = conv_state_in;
         c.state_in = initial_state; c.state_out = final_state; c.out = out;
         c.workspace = workspace;
+        // the new conv history comes from the prologue's launch unless it is
+        // updated in place (the prologue still reads the old one)
+        if (conv_state_out && !ranges_overlap(conv_state_in, conv_state_out,
+                                              (size_t)n_seq * conv_dim(dims) * (dims->conv_k - 1) * 2)) {
+            c.conv_state_out = conv_state_out;
+            conv_done = true;
+        }
         gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads, dims->n_v_heads,
                                      &c.layout);
         if ((st = cuda_status(gdn::launch_chunked_prefill(c, s), fn, "chunked prefill launch")) !=
@@ -335,7 +353,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
                           "recurrent launch")) != GDN_OK)
         return st;
     }
-    if (conv_state_out) {
+    if (conv_state_out && !conv_done) {
         gdn::ConvStateArgs c{};
         c.n_seq = n_seq; c.n_k_heads = dims->n_k_heads; c.n_v_heads = dims->n_v_heads;
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;

@@ -1226,6 +1226,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     cv.cu_seqlens = a.cu_seqlens; cv.x = a.x; cv.a = a.a; cv.b = a.b;
     cv.conv_w = a.conv_w; cv.A_log = a.A_log; cv.dt_bias = a.dt_bias;
     cv.conv_state_in = a.conv_state_in;
+    cv.conv_state_out = a.conv_state_out;
     cv.qkv_out = ws + l.qkv_hi;
     cv.qkv_lo_out = ws + l.qkv_lo;
     cv.g_out = reinterpret_cast<float*>(ws + l.g);

@@ -17,6 +17,32 @@
 namespace gdn {
 
 constexpr int kConvThreads = 128;
+
+// Channel ch of sequence n (first token bos, len tokens): its new history is
+// the last K-1 raw inputs, oldest first, shifted in from the old history when
+// the sequence is shorter than K-1 (zeros without one).
+template <typename T>
+__device__ __forceinline__ void conv_history_one(const T* __restrict__ x, const T* __restrict__ cs_in,
+                                                 T* __restrict__ cs_out, int cd, int keep, int n,
+                                                 int ch, int bos, int len) {
+    T nw[3];
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+        if (s >= keep) break;
+        const int ti = len - keep + s;
+        if (ti >= 0)
+            nw[s] = x[(size_t)(bos + ti) * cd + ch];
+        else if (cs_in)
+            nw[s] = cs_in[((size_t)n * cd + ch) * keep + keep + ti];
+        else
+            nw[s] = from_f32<T>(0.0f);
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+        if (s >= keep) break;
+        cs_out[((size_t)n * cd + ch) * keep + s] = nw[s];
+    }
+}
 constexpr int kConvTokTile = 64;
 
 template <typename T>
@@ -216,6 +242,18 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(p.x);
 
+    if (unit == n_units + 1) {  // the new conv history of every sequence (grid-stride)
+        const int keep = p.conv_k - 1;
+        const int nblk = (cd + 255) / 256;
+        for (int it = blockIdx.x; it < p.n_seq * nblk; it += gridDim.x) {
+            const int n = it / nblk, ch = (it % nblk) * 256 + tid;
+            if (ch < cd)
+                conv_history_one<__nv_bfloat16>(x, static_cast<const __nv_bfloat16*>(p.conv_state_in),
+                                                static_cast<__nv_bfloat16*>(p.conv_state_out), cd, keep,
+                                                n, ch, p.cu_seqlens[n], p.cu_seqlens[n + 1] - p.cu_seqlens[n]);
+        }
+        return;
+    }
     if (unit == n_units) {  // gates for this token tile (and, in the first, the chunk table)
         if (blockIdx.x == 0 && p.cu_chunks) chunk_table_cta(p);
         const int hv_n = p.n_v_heads;
@@ -325,33 +363,15 @@ __global__ void conv_state_kernel(ConvStateArgs p) {
         len = p.uniform_T;
     }
     if (p.lengths) len = min(max(p.lengths[n], 0), len);  // accepted prefix (commit)
-    const T* __restrict__ x = static_cast<const T*>(p.x);
-    const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
-    T* __restrict__ cs_out = static_cast<T*>(p.conv_state_out);
-    T nw[3];
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-        if (s >= keep) break;
-        const int ti = len - keep + s;
-        if (ti >= 0)
-            nw[s] = x[(size_t)(bos + ti) * cd + ch];
-        else if (cs_in)
-            nw[s] = cs_in[((size_t)n * cd + ch) * keep + keep + ti];
-        else
-            nw[s] = from_f32<T>(0.0f);
-    }
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-        if (s >= keep) break;
-        cs_out[((size_t)n * cd + ch) * keep + s] = nw[s];
-    }
+    conv_history_one<T>(static_cast<const T*>(p.x), static_cast<const T*>(p.conv_state_in),
+                        static_cast<T*>(p.conv_state_out), cd, keep, n, ch, bos, len);
 }
 
 cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream) {
     if (p.n_tokens == 0) return cudaSuccess;
     if (bf16 && p.d_k == 128 && p.d_v == 128 && p.qkv_lo_out) {
         dim3 grid((p.n_tokens + p.zero_tail + kPro128Tile - 1) / kPro128Tile,
-                  2 * p.n_k_heads + p.n_v_heads + 1);
+                  2 * p.n_k_heads + p.n_v_heads + 1 + (p.conv_state_out ? 1 : 0));
         conv_prologue_d128_kernel<<<grid, 256, 0, stream>>>(p);
         return cudaGetLastError();
     }

@@ -35,6 +35,9 @@ struct ConvArgs {
     int2* chunk_info;           // [chunks]
     int* ready;
     int n_ready;
+    // New conv history [N, CD, K-1], written by an extra CTA row of the d=128
+    // prologue; only when it does not alias conv_state_in (else null)
+    void* conv_state_out;
 };
 
 struct ConvStateArgs {
@@ -125,6 +128,7 @@ struct ChunkLaunch {
     const void *x, *z, *a, *b;
     const float *conv_w, *A_log, *dt_bias, *norm_w;
     const void* conv_state_in;
+    void* conv_state_out;  // written by the prologue when set (see ConvArgs)
     const float* state_in;
     float* state_out;
     void* out;
