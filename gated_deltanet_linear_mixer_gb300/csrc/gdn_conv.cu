@@ -283,11 +283,20 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
     const float scale = is_q ? rsqrtf(128.f) : 1.f;
     const int K = p.conv_k, keep = K - 1, pad = 4 - K;
     float w[4][4];
+    if (K == 4 && (reinterpret_cast<uintptr_t>(p.conv_w) & 15u) == 0) {  // 4 channels x 4 taps, 64 B
+        const float4* wp = reinterpret_cast<const float4*>(p.conv_w + (size_t)c * 4);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < 4; ++e) {
+            const float4 v = wp[e];
+            w[e][0] = v.x; w[e][1] = v.y; w[e][2] = v.z; w[e][3] = v.w;
+        }
+    } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) w[e][k] = k >= pad ? p.conv_w[(size_t)(c + e) * K + (k - pad)] : 0.f;
-    uint2 raw[kPro128Tok + 3];  // rows tb-3 .. tb+15
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[e][k] = k >= pad ? p.conv_w[(size_t)(c + e) * K + (k - pad)] : 0.f;
+    }
+    uint2 raw[kPro128Tok + 3];  // rows tb-3 .. tb+7
 #pragma unroll
     for (int i = 0; i < kPro128Tok + 3; ++i) {
         const int rr = tb - 3 + i;
@@ -297,6 +306,41 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
     const __nv_bfloat16* __restrict__ cs_in = static_cast<const __nv_bfloat16*>(p.conv_state_in);
     int n = seq_of_token(p.cu_seqlens, p.n_seq, tb);
     int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
+    // SiLU, the q/k L2 norm (q scaled), the (hi, lo) split and the stores of token t
+    auto finish = [&](float* acc, int t) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = siluf_(acc[e]);
+        if (norm) {
+            float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = rsqrtf(ss + p.l2_eps) * scale;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] *= inv;
+        }
+        const uint32_t h01 = pack_bf16_pair(acc[0], acc[1]), h23 = pack_bf16_pair(acc[2], acc[3]);
+        const float l0 = acc[0] - __uint_as_float(h01 << 16), l1 = acc[1] - __uint_as_float(h01 & 0xFFFF0000u);
+        const float l2 = acc[2] - __uint_as_float(h23 << 16), l3 = acc[3] - __uint_as_float(h23 & 0xFFFF0000u);
+        *reinterpret_cast<uint2*>(out + (size_t)t * cd + c) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2*>(out_lo + (size_t)t * cd + c) =
+            make_uint2(pack_bf16_pair(l0, l1), pack_bf16_pair(l2, l3));
+    };
+    if (tb - 3 >= bos && tb + kPro128Tok <= eos) {  // the run and its halo lie in one sequence
+#pragma unroll
+        for (int j = 0; j < kPro128Tok; ++j) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint2 r = raw[j + k];
+                acc[0] = fmaf(w[0][k], __uint_as_float(r.x << 16), acc[0]);
+                acc[1] = fmaf(w[1][k], __uint_as_float(r.x & 0xFFFF0000u), acc[1]);
+                acc[2] = fmaf(w[2][k], __uint_as_float(r.y << 16), acc[2]);
+                acc[3] = fmaf(w[3][k], __uint_as_float(r.y & 0xFFFF0000u), acc[3]);
+            }
+            finish(acc, tb + j);
+        }
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < kPro128Tok; ++j) {
         const int t = tb + j;
@@ -326,22 +370,7 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[e] = fmaf(w[e][k], v[e], acc[e]);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = siluf_(acc[e]);
-        if (norm) {
-            float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = rsqrtf(ss + p.l2_eps) * scale;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] *= inv;
-        }
-        const uint32_t h01 = pack_bf16_pair(acc[0], acc[1]), h23 = pack_bf16_pair(acc[2], acc[3]);
-        const float l0 = acc[0] - __uint_as_float(h01 << 16), l1 = acc[1] - __uint_as_float(h01 & 0xFFFF0000u);
-        const float l2 = acc[2] - __uint_as_float(h23 << 16), l3 = acc[3] - __uint_as_float(h23 & 0xFFFF0000u);
-        *reinterpret_cast<uint2*>(out + (size_t)t * cd + c) = make_uint2(h01, h23);
-        *reinterpret_cast<uint2*>(out_lo + (size_t)t * cd + c) =
-            make_uint2(pack_bf16_pair(l0, l1), pack_bf16_pair(l2, l3));
+        finish(acc, t);
     }
 }
 
