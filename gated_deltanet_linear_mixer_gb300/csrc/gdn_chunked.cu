@@ -172,6 +172,8 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_v, 1);
         fence_barrier_init();
+        for (const CUtensorMap* m : {&map_qh, &map_ql, &map_wh, &map_wl, &map_kqh, &map_kql, &map_kwh, &map_kwl})
+            tma_prefetch_desc(m);
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
     tc_fence_before_sync();
@@ -760,6 +762,8 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         sy.dead = 0;
         sy.n_a4 = sy.n_k = sy.n_qk[0] = sy.n_qk[1] = 0;
         fence_barrier_init();
+        for (const CUtensorMap* m : {&map_qh, &map_ql, &map_wh, &map_wl, &map_kqh, &map_kql, &map_kwh, &map_kwl})
+            tma_prefetch_desc(m);
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
     fence_proxy_async_smem();
