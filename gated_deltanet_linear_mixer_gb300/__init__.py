@@ -29,7 +29,7 @@ ACT_SILU, ACT_SIGMOID = 0, 1
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
-           "gdn_prefill_noalloc_scratch_bytes", "gdn_decode", "gdn_decode_commit",
+           "gdn_prefill_noalloc_scratch_bytes", "gdn_decode", "gdn_verify", "gdn_decode_commit",
            "gdn_timing_enable", "gdn_timing_report", "gdn_device_error", "gdn_last_error",
            "gdn_version")
 
@@ -76,9 +76,10 @@ def load(path: str | None = None):
     lib.gdn_prefill_noalloc_scratch_bytes.argtypes = []
     lib.gdn_prefill_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.gdn_decode.argtypes = [PD, PP, I32, I32, P, P, P, P, P, P, P, P, P]
+    lib.gdn_verify.argtypes = [PD, PP, I32, I32, P, P, P, P, P, P, P, P]
     lib.gdn_decode_commit.argtypes = [PD, I32, I32, P, P, P, P, P, P]
     for f in ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
-              "gdn_decode", "gdn_decode_commit"):
+              "gdn_decode", "gdn_verify", "gdn_decode_commit"):
         getattr(lib, f).restype = ctypes.c_int
     lib.gdn_timing_enable.argtypes = [I32]
     lib.gdn_timing_enable.restype = ctypes.c_int
@@ -325,6 +326,29 @@ def decode(d: Dims, params: Params, x, z, a, b, state, conv_state=None, inter_st
     return out
 
 
+def verify(d: Dims, params: Params, x, z, a, b, state, conv_state=None, out=None):
+    """gdn_verify: x [N, T, CD]; state and conv_state are only read.
+
+    Returns out [N, T, Hv*dv].  Replay the accepted prefix with ``prefill``."""
+    lib = load()
+    dev = x.device
+    n, tt = x.shape[0], x.shape[1]
+    vd = d.n_v_heads * d.d_v
+    _t(x, "x", d.dtype, (n, tt, d.conv_dim))
+    _t(z, "z", d.dtype, (n, tt, vd))
+    _t(a, "a", d.dtype, (n, tt, d.n_v_heads))
+    _t(b, "b", d.dtype, (n, tt, d.n_v_heads))
+    _t(state, "state", torch.float32, (n, d.n_v_heads, d.d_k, d.d_v))
+    _t(conv_state, "conv_state", d.dtype, (n, d.conv_dim, d.conv_k - 1))
+    out = out if out is not None else torch.empty((n, tt, vd), dtype=d.dtype, device=dev)
+    _t(out, "out", d.dtype, (n, tt, vd))
+    dd, pp = d.c(), params.c(d)
+    st = lib.gdn_verify(ctypes.byref(dd), ctypes.byref(pp), n, tt, _p(x), _p(z), _p(a), _p(b),
+                        _p(state), _p(conv_state), _p(out), _stream(dev))
+    _check("gdn_verify", st)
+    return out
+
+
 def decode_commit(d: Dims, accepted, x, inter_states, state, conv_state=None):
     """gdn_decode_commit: keep the first accepted[i] tokens of a verify call."""
     lib = load()
@@ -343,4 +367,4 @@ def decode_commit(d: Dims, accepted, x, inter_states, state, conv_state=None):
 
 __all__ = ["Dims", "Params", "GDNError", "load", "version", "timing_enable", "timing_report",
            "conv", "prefill",
-           "prefill_workspace_size", "decode", "decode_commit", "EXPORTS", "LIB_PATH"]
+           "prefill_workspace_size", "decode", "verify", "decode_commit", "EXPORTS", "LIB_PATH"]

@@ -71,6 +71,19 @@ bool ranges_overlap(const void* a, const void* b, size_t bytes) {
     return x < y + bytes && y < x + bytes;
 }
 
+// The bf16 prefill takes the chunked tensor-core path unless every sequence
+// has at most kShortPrefill tokens (a replayed verify prefix, a batch of
+// decode-sized prompts): then the token-recurrent kernel, which streams each
+// state once and has no chunk to fill, is the faster one.
+constexpr int kShortPrefill = 16;
+bool use_chunked(const gdn_dims* d, int n_seq, const int32_t* cu_host) {
+    if (!gdn::chunked_supported(d->d_k, d->d_v, d->n_k_heads, d->n_v_heads, d->dtype == GDN_DTYPE_BF16))
+        return false;
+    for (int i = 0; i < n_seq; ++i)
+        if (cu_host[i + 1] - cu_host[i] > kShortPrefill) return true;
+    return false;
+}
+
 gdn_status check_params(const gdn_params* p, bool need_norm, const char* fn) {
     if (!p) return fail(GDN_ERR_INVALID_ARG, fn, "params is NULL");
     if (!p->conv_w || !p->A_log || !p->dt_bias || (need_norm && !p->norm_w))
@@ -276,11 +289,11 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
     if (n_seq < 0) return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
     if (n_seq > 0 && !cu_seqlens_host) return fail(GDN_ERR_INVALID_ARG, fn, "cu_seqlens_host is NULL");
     *bytes = 0;
-    if (gdn::chunked_supported(dims->d_k, dims->d_v, dims->n_k_heads, dims->n_v_heads,
-                               dims->dtype == GDN_DTYPE_BF16) && n_seq > 0) {
+    if (n_seq > 0) {
         int total = 0;
         if ((st = check_cu(n_seq, cu_seqlens_host, cu_seqlens_host, &total, fn)) != GDN_OK)
             return st;
+        if (!use_chunked(dims, n_seq, cu_seqlens_host)) return GDN_OK;
         *bytes = gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads,
                                               dims->n_v_heads, nullptr);
     }
@@ -316,7 +329,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     bool conv_done = false;
-    if (gdn::chunked_supported(dims->d_k, dims->d_v, dims->n_k_heads, dims->n_v_heads, bf16)) {
+    if (use_chunked(dims, n_seq, cu_seqlens_host)) {
         if (reinterpret_cast<uintptr_t>(workspace) & 255u)
             return fail(GDN_ERR_WORKSPACE, fn, "workspace must be 256-byte aligned");
         gdn::ChunkLaunch c{};
@@ -410,6 +423,38 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
             return st;
     }
     return GDN_OK;
+}
+
+gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_seq, int32_t T,
+                      const void* x, const void* z, const void* a, const void* b,
+                      const float* state, const void* conv_state, void* out, void* stream) {
+    const char* fn = "gdn_verify";
+    gdn_status st;
+    if ((st = check_dims(dims, fn)) != GDN_OK) return st;
+    if ((st = check_params(params, true, fn)) != GDN_OK) return st;
+    if (n_seq < 0 || n_seq > (1 << 24))
+        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..2^24 (got %d)", n_seq);
+    if (T < 1 || T > 16) return fail(GDN_ERR_INVALID_ARG, fn, "T must be 1..16 (got %d)", T);
+    g_err[0] = '\0';
+    if (n_seq == 0) return GDN_OK;
+    if (!x || !z || !a || !b || !state || !out)
+        return fail(GDN_ERR_INVALID_ARG, fn, "an input or output pointer is NULL");
+    if (!aligned16(x) || !aligned16(z) || !aligned16(out) || !aligned16(state))
+        return fail(GDN_ERR_INVALID_ARG, fn, "x, z, out and the state must be 16-byte aligned");
+    const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gdn::RecurrentArgs r{};
+    r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
+    r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
+    r.cu_seqlens = nullptr; r.uniform_T = T;
+    r.x = x; r.z = z; r.a = a; r.b = b;
+    r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
+    r.norm_w = params->norm_w; r.conv_state_in = conv_state;
+    r.state_in = state;  // read once; no state, intermediate or history is written
+    r.out = out;
+    return cuda_status(timed_launch("recurrent", s, [&] {
+                           return gdn::launch_recurrent(r, dims->d_k, dims->d_v, bf16, s);
+                       }), fn, "recurrent launch");
 }
 
 gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,

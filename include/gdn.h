@@ -178,6 +178,24 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
                       void* stream);
 
 /*
+ * gdn_verify -- speculative verify for rollback by replay (qwen.rs
+ * QwenSession::rewind keeps the pre-verify state and the drafts' inputs and
+ * re-runs the accepted ones).  T draft tokens (1 <= T <= 16) of each sequence
+ * run against state [N, Hv, dk, dv] and conv_state [N, CD, K-1] (may be NULL:
+ * zero history), which are only read; out [N, T, Hv*dv] is the only write, so
+ * the state traffic is one read.  Layouts as gdn_decode.  After acceptance
+ * the caller replays each sequence's accepted prefix with gdn_prefill from the
+ * same state and history (cu_seqlens built from the accepted counts; a prefix
+ * of at most 16 tokens runs on the token-recurrent kernel), which writes the
+ * new state and history.  Against gdn_decode with inter_states plus
+ * gdn_decode_commit this moves (1 + 2) instead of (1 + T + 2) state slabs per
+ * sequence, at the price of recomputing the accepted tokens.
+ */
+gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_seq, int32_t T,
+                      const void* x, const void* z, const void* a, const void* b,
+                      const float* state, const void* conv_state, void* out, void* stream);
+
+/*
  * gdn_decode_commit -- after a verify call of gdn_decode that wrote
  * inter_states, keep the first accepted[i] of the T tokens of sequence i:
  * state[i] becomes inter_states[i, accepted[i]-1] (left as is when

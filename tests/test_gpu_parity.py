@@ -208,6 +208,50 @@ def test_decode_commit_keeps_accepted_prefix():
         assert rel_err(cs[i], ref["conv_state"][0]) == 0.0
 
 
+@pytest.mark.parametrize("d_k", [128, 64])
+def test_verify_then_replay_gives_the_committed_state(d_k):
+    """Rollback by replay: gdn_verify runs the drafts against a read-only state
+    (its outputs are gdn_decode's, and nothing else is written); replaying each
+    sequence's accepted prefix with gdn_prefill from the kept state and history
+    (the token-recurrent path: every prefix is short) gives the state that
+    gdn_decode wrote as an intermediate and the history gdn_decode_commit keeps,
+    bit for bit, and both match the oracle run on the accepted prefix."""
+    n, tt = 6, 4
+    accepted = [0, 1, 2, 3, 4, 2]
+    case = _gen("rp", mode="decode", n_seq=n, tokens_per_seq=tt, d_k=d_k, act="sigmoid",
+                state_std=0.05, conv_state_std=1.0, seed=27, want_inter=True)
+    d, _ = dims(case)
+    t = upload(case)
+    x, z, a, b = (t[k].view(n, tt, -1) for k in ("x", "z", "a", "b"))
+    st0, cs0 = t["state"].clone(), t["conv_state"].clone()
+    inter = torch.full((n, tt, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
+    out_ref = gdn.decode(d, t["params"], x, z, a, b, st0.clone(), cs0.clone(), inter)
+    st_v, cs_v = st0.clone(), cs0.clone()
+    out_v = gdn.verify(d, t["params"], x, z, a, b, st_v, conv_state=cs_v)
+    torch.cuda.synchronize()
+    assert torch.equal(out_v, out_ref)
+    assert torch.equal(st_v, st0) and torch.equal(cs_v, cs0)
+    # replay: the accepted prefixes packed as one variable-length prefill
+    cu = np.concatenate([[0], np.cumsum(accepted)]).astype(np.int32)
+    pick = lambda u: torch.cat([u[i, :j] for i, j in enumerate(accepted)])  # noqa: E731
+    st_r, cs_r = st0.clone(), torch.empty_like(cs0)
+    gdn.prefill(d, t["params"], cu, pick(x), pick(z), pick(a), pick(b), initial_state=st_r,
+                final_state=st_r, conv_state_in=cs0, conv_state_out=cs_r)
+    # the commit path on the same intermediates
+    st_c, cs_c = st0.clone(), cs0.clone()
+    gdn.decode_commit(d, torch.tensor(accepted, dtype=torch.int32, device="cuda"), x, inter,
+                      st_c, cs_c)
+    torch.cuda.synchronize()
+    assert torch.equal(cs_r, cs_c)
+    assert torch.equal(st_r, st_c)
+    for i, j in enumerate(accepted):
+        sub, _ = _subcase(case, [i])
+        sub.cu_seqlens = np.array([0, j], dtype=np.int32)
+        sub.x, sub.z, sub.a, sub.b = sub.x[:j], sub.z[:j], sub.a[:j], sub.b[:j]
+        ref = run_oracle(sub)
+        assert rel_err(st_r[i], ref["state"][0]) <= TOL["bf16"]
+
+
 def test_decode_equals_prefill_of_same_tokens():
     """T decode tokens against a state == prefill of those T tokens from that state."""
     case = _gen("dp", mode="decode", n_seq=3, tokens_per_seq=4, state_std=0.05,
