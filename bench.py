@@ -84,7 +84,9 @@ WORKLOADS = {
     "decode": 2,
     "varlen": 3,
     "spec_verify": 4,
+    "spec_replay": 4,   # the same drafts, verified read-only, accepted prefix replayed
 }
+REPLAY_ACCEPTED = 2     # tokens of every sequence's 4 drafts accepted in spec_replay
 
 
 class Runner:
@@ -115,13 +117,29 @@ class Runner:
         self.inter = None
         if key == "spec_verify":
             self.inter = torch.empty((n, c.tokens_per_seq, c.n_v_heads, c.d_k, c.d_v), device=device)
+        if key == "spec_replay":  # the accepted prefixes, packed, and their cu_seqlens
+            t, j = c.tokens_per_seq, REPLAY_ACCEPTED
+            take = lambda u: u.view(n, t, -1)[:, :j].reshape(n * j, -1).contiguous()  # noqa: E731
+            self.rx, self.rz, self.ra, self.rb = (take(u) for u in (self.x, self.z, self.a, self.b))
+            self.rcu_host = torch.arange(0, n * j + 1, j, dtype=torch.int32)
+            self.rcu_dev = self.rcu_host.to(device)
+            self.rout = torch.empty((n * j, vd), dtype=torch.bfloat16, device=device)
         ws = gdn.prefill_workspace_size(self.d, self.cu_host) if c.mode == "prefill" else 0
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
 
     # -- one step through the public API (device-resident inputs)
     def step(self):
         gdn, c = self.gdn, self.case
-        if c.mode == "prefill":
+        if self.key == "spec_replay":
+            n, t = c.n_seq, c.tokens_per_seq
+            gdn.verify(self.d, self.params, self.x.view(n, t, -1), self.z.view(n, t, -1),
+                       self.a.view(n, t, -1), self.b.view(n, t, -1), self.state, self.conv,
+                       self.out.view(n, t, -1))
+            gdn.prefill(self.d, self.params, (self.rcu_dev, self.rcu_host), self.rx, self.rz,
+                        self.ra, self.rb, initial_state=self.state, final_state=self.state,
+                        conv_state_in=self.conv, conv_state_out=self.conv, out=self.rout,
+                        workspace=self.ws)
+        elif c.mode == "prefill":
             gdn.prefill(self.d, self.params, (self.cu_dev, self.cu_host), self.x, self.z, self.a,
                         self.b, initial_state=self.state0, final_state=self.final,
                         conv_state_in=None, conv_state_out=self.conv_out, out=self.out,
@@ -148,6 +166,10 @@ class Runner:
             return act + n * (2 * _state_bytes(c) + 2 * _conv_state_bytes(c))
         if self.key == "spec_verify":  # state read once, T states written, conv state read
             return act + n * ((1 + c.tokens_per_seq) * _state_bytes(c) + _conv_state_bytes(c))
+        if self.key == "spec_replay":  # verify: state and history read; replay of the accepted
+            # prefix: its inputs read once more, state and history read and written
+            return (act + _act_bytes_per_token(c) * n * REPLAY_ACCEPTED
+                    + n * (3 * _state_bytes(c) + 3 * _conv_state_bytes(c)))
         raise KeyError(self.key)
 
     def kernel_bytes(self, name, kernels=()):
@@ -157,10 +179,13 @@ class Runner:
         K-1 history rows; the step's other kernels share the rest."""
         c = self.case
         conv = c.n_seq * _conv_state_bytes(c)
-        hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0}[self.key]
+        hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0,
+                "spec_replay": 2 * conv}[self.key]
         if name == "conv_state":
             return hist
-        return self.algorithmic_bytes() - (hist if "conv_state" in kernels else 0)
+        rest = self.algorithmic_bytes() - (hist if "conv_state" in kernels else 0)
+        # spec_replay launches the recurrent kernel twice a step (verify, replay)
+        return rest / 2 if self.key == "spec_replay" else rest
 
     def useful_flops(self, chunk=64):
         """Useful flops of the chunked form per step (prefill), else of the recurrence."""
@@ -348,7 +373,8 @@ def run_gpu(args):
     sampler = ClockSampler(index=local)
     sampler.start()
 
-    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify") if k in args.extras]
+    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify", "spec_replay")
+                          if k in args.extras]
     results = {}
     total_launches = 0
     for key in keys:
@@ -520,7 +546,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
-    ap.add_argument("--extras", default="decode,varlen,spec_verify",
+    ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay",
                     help="comma list of extra workloads in the same line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64"],
