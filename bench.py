@@ -85,7 +85,9 @@ WORKLOADS = {
     "varlen": 3,
     "spec_verify": 4,
     "spec_replay": 4,   # the same drafts, verified read-only, accepted prefix replayed
+    "layer": 1,         # the T=4096 prefill inside a whole layer: in_proj -> core -> out_proj
 }
+LAYER_HIDDEN = 2048     # model width of the layer workload (Qwen3-Next's hidden size)
 REPLAY_ACCEPTED = 2     # tokens of every sequence's 4 drafts accepted in spec_replay
 
 
@@ -124,13 +126,31 @@ class Runner:
             self.rcu_host = torch.arange(0, n * j + 1, j, dtype=torch.int32)
             self.rcu_dev = self.rcu_host.to(device)
             self.rout = torch.empty((n * j, vd), dtype=torch.bfloat16, device=device)
+        if key == "layer":  # synthetic bf16 weights ~N(0, 1/in_features), hidden states ~N(0,1)
+            rng = np.random.default_rng(5)
+            shapes = {"w_qkv": (c.conv_dim, LAYER_HIDDEN), "w_z": (vd, LAYER_HIDDEN),
+                      "w_a": (c.n_v_heads, LAYER_HIDDEN), "w_b": (c.n_v_heads, LAYER_HIDDEN),
+                      "w_out": (LAYER_HIDDEN, vd)}
+            w = {k: bf(rng.normal(0, 1 / np.sqrt(v[1]), size=v).astype(np.float32))
+                 for k, v in shapes.items()}
+            self.proj = gdn.Proj(w["w_qkv"], w["w_z"], w["w_a"], w["w_b"], w["w_out"])
+            self.h = bf(rng.normal(size=(c.n_tokens, LAYER_HIDDEN)).astype(np.float32))
+            self.layer_out = torch.empty_like(self.h)
+            self.layer_ws = torch.empty(gdn.layer_prefill_workspace_size(self.d, LAYER_HIDDEN,
+                                                                         self.cu_host),
+                                        dtype=torch.uint8, device=device)
         ws = gdn.prefill_workspace_size(self.d, self.cu_host) if c.mode == "prefill" else 0
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
 
     # -- one step through the public API (device-resident inputs)
     def step(self):
         gdn, c = self.gdn, self.case
-        if self.key == "spec_replay":
+        if self.key == "layer":
+            gdn.layer_prefill(self.d, self.params, self.proj, (self.cu_dev, self.cu_host), self.h,
+                              initial_state=self.state0, final_state=self.final,
+                              conv_state_out=self.conv_out, out=self.layer_out,
+                              workspace=self.layer_ws)
+        elif self.key == "spec_replay":
             n, t = c.n_seq, c.tokens_per_seq
             gdn.verify(self.d, self.params, self.x.view(n, t, -1), self.z.view(n, t, -1),
                        self.a.view(n, t, -1), self.b.view(n, t, -1), self.state, self.conv,
@@ -160,6 +180,10 @@ class Runner:
         n = c.n_seq
         if self.key == "prefill":      # zero initial state (not read); final state + conv state out
             return act + n * (_state_bytes(c) + _conv_state_bytes(c))
+        if self.key == "layer":        # h in, h_out, the weights once, final state + conv state out
+            vd = c.n_v_heads * c.d_v
+            w = 2 * LAYER_HIDDEN * (c.conv_dim + 2 * vd + 2 * c.n_v_heads)
+            return 4 * LAYER_HIDDEN * c.n_tokens + w + n * (_state_bytes(c) + _conv_state_bytes(c))
         if self.key == "varlen":       # initial state in, final state out, conv state out
             return act + n * (2 * _state_bytes(c) + _conv_state_bytes(c))
         if self.key == "decode":       # state and conv state read and written in place
@@ -180,33 +204,39 @@ class Runner:
         c = self.case
         conv = c.n_seq * _conv_state_bytes(c)
         hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0,
-                "spec_replay": 2 * conv}[self.key]
+                "spec_replay": 2 * conv, "layer": conv}[self.key]
         if name == "conv_state":
             return hist
         rest = self.algorithmic_bytes() - (hist if "conv_state" in kernels else 0)
         # spec_replay launches the recurrent kernel twice a step (verify, replay)
         return rest / 2 if self.key == "spec_replay" else rest
 
-    def useful_flops(self, chunk=64):
-        """Useful flops of the chunked form per step (prefill), else of the recurrence."""
+    def useful_flops(self, chunk=64, with_proj=True):
+        """Useful flops of the chunked form per step (prefill), else of the recurrence;
+        the layer workload adds its projections (in_proj: CD + Hv*dv + 2 Hv outputs,
+        out_proj: hidden outputs from Hv*dv) unless with_proj is False."""
         c = self.case
         dk, dv = c.d_k, c.d_v
         if c.mode == "prefill":
             per_tok_head = 6 * dk * dv + chunk * (3 * dk + 2 * dv) + chunk * chunk / 3
         else:
             per_tok_head = 5 * dk * dv
-        return per_tok_head * c.n_v_heads * c.n_tokens
+        flops = per_tok_head * c.n_v_heads * c.n_tokens
+        if self.key == "layer" and with_proj:
+            vd = c.n_v_heads * dv
+            flops += 2 * c.n_tokens * LAYER_HIDDEN * (c.conv_dim + 2 * vd + 2 * c.n_v_heads)
+        return flops
 
     # -- end to end: pinned host buffers, H2D of the step's inputs, the call,
     # D2H of the step's outputs.
     def setup_e2e(self):
         torch = self.torch
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
-        self.h_in = [pin(t) for t in (self.x, self.z, self.a, self.b)]
-        self.d_in = [self.x, self.z, self.a, self.b]
-        # the step's result read back by the caller: the mixer output (states
-        # stay resident on the device for the next call)
-        outs = [self.out]
+        self.d_in = [self.h] if self.key == "layer" else [self.x, self.z, self.a, self.b]
+        self.h_in = [pin(t) for t in self.d_in]
+        # the step's result read back by the caller: the mixer (or layer) output
+        # (states stay resident on the device for the next call)
+        outs = [self.layer_out] if self.key == "layer" else [self.out]
         self.d_out = outs
         self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
         self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
@@ -373,13 +403,15 @@ def run_gpu(args):
     sampler = ClockSampler(index=local)
     sampler.start()
 
-    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify", "spec_replay")
+    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify", "spec_replay", "layer")
                           if k in args.extras]
     results = {}
     total_launches = 0
     for key in keys:
         case = workloads.config(WORKLOADS[key])
         r = Runner(key, case, device)
+        r.step()  # one untimed call: one-time costs (module loading, library setup) stay out
+        torch.cuda.synchronize()
         t_start = time.time()
         gdn.timing_enable(True)
         ms = time_steps(r.step, args.steps, args.warmup, flush_buf, stream, barrier)
@@ -388,7 +420,9 @@ def run_gpu(args):
         t_stop = time.time()
         # timing_report counts warm-up launches too: scale to the timed steps
         per_step_launch = {k: v[0] / (args.steps + args.warmup) for k, v in rep.items()}
-        launches = int(round(sum(per_step_launch.values()) * args.steps))
+        # this library's kernels only (the layer's projections are cuBLAS GEMMs)
+        launches = int(round(sum(v for k, v in per_step_launch.items()
+                                 if not k.startswith("proj_")) * args.steps))
         mean_ms = statistics.mean(ms)
         t_max = max_over_ranks(mean_ms, device=device)
         tok_s = world * r.tokens / (t_max / 1e3)
@@ -401,7 +435,7 @@ def run_gpu(args):
         if dom_name == "chunk_fused":
             # every tensor-core contraction of the chunked form runs in this one
             # launch: a contraction, measured against the bf16 tensor peak
-            fl = r.useful_flops()
+            fl = r.useful_flops(with_proj=False)
             achieved = fl / (dom_avg_ms / 1e3) / 1e12
             roof = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -546,7 +580,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
-    ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay",
+    ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay,layer",
                     help="comma list of extra workloads in the same line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64"],

@@ -30,6 +30,7 @@ ACT_SILU, ACT_SIGMOID = 0, 1
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
            "gdn_prefill_noalloc_scratch_bytes", "gdn_decode", "gdn_verify", "gdn_decode_commit",
+           "gdn_layer_prefill_workspace_size", "gdn_layer_prefill",
            "gdn_timing_enable", "gdn_timing_report", "gdn_device_error", "gdn_last_error",
            "gdn_version")
 
@@ -52,6 +53,11 @@ class _Dims(ctypes.Structure):
 class _Params(ctypes.Structure):
     _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
                 ("dt_bias", ctypes.c_void_p), ("norm_w", ctypes.c_void_p)]
+
+
+class _Proj(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_z", ctypes.c_void_p), ("w_a", ctypes.c_void_p),
+                ("w_b", ctypes.c_void_p), ("w_out", ctypes.c_void_p)]
 
 
 _lib = None
@@ -78,8 +84,12 @@ def load(path: str | None = None):
     lib.gdn_decode.argtypes = [PD, PP, I32, I32, P, P, P, P, P, P, P, P, P]
     lib.gdn_verify.argtypes = [PD, PP, I32, I32, P, P, P, P, P, P, P, P]
     lib.gdn_decode_commit.argtypes = [PD, I32, I32, P, P, P, P, P, P]
+    lib.gdn_layer_prefill_workspace_size.argtypes = [PD, I32, I32, P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.gdn_layer_prefill.argtypes = [PD, PP, ctypes.POINTER(_Proj), I32, I32, P, P, P, P, P, P, P,
+                                      P, P, ctypes.c_size_t, P]
     for f in ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
-              "gdn_decode", "gdn_verify", "gdn_decode_commit"):
+              "gdn_decode", "gdn_verify", "gdn_decode_commit", "gdn_layer_prefill_workspace_size",
+              "gdn_layer_prefill"):
         getattr(lib, f).restype = ctypes.c_int
     lib.gdn_timing_enable.argtypes = [I32]
     lib.gdn_timing_enable.restype = ctypes.c_int
@@ -295,6 +305,68 @@ def prefill(d: Dims, params: Params, cu_seqlens, x, z, a, b, *, initial_state=No
     return out
 
 
+class Proj:
+    """Projection weights around the core, bf16 [out_features, in_features]."""
+
+    def __init__(self, w_qkv, w_z, w_a, w_b, w_out):
+        self.w_qkv, self.w_z, self.w_a, self.w_b, self.w_out = w_qkv, w_z, w_a, w_b, w_out
+        self.hidden = int(w_qkv.shape[1])
+
+    def c(self, d: "Dims") -> _Proj:
+        vd = d.n_v_heads * d.d_v
+        _t(self.w_qkv, "w_qkv", torch.bfloat16, (d.conv_dim, self.hidden))
+        _t(self.w_z, "w_z", torch.bfloat16, (vd, self.hidden))
+        _t(self.w_a, "w_a", torch.bfloat16, (d.n_v_heads, self.hidden))
+        _t(self.w_b, "w_b", torch.bfloat16, (d.n_v_heads, self.hidden))
+        _t(self.w_out, "w_out", torch.bfloat16, (self.hidden, vd))
+        return _Proj(*(ctypes.c_void_p(w.data_ptr()) for w in
+                       (self.w_qkv, self.w_z, self.w_a, self.w_b, self.w_out)))
+
+
+def layer_prefill_workspace_size(d: Dims, hidden: int, cu_seqlens) -> int:
+    lib = load()
+    host = torch.tensor(list(cu_seqlens), dtype=torch.int32) if not isinstance(
+        cu_seqlens, torch.Tensor) else cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    out = ctypes.c_size_t(0)
+    dd = d.c()
+    _check("gdn_layer_prefill_workspace_size",
+           lib.gdn_layer_prefill_workspace_size(ctypes.byref(dd), hidden, host.numel() - 1,
+                                                ctypes.c_void_p(host.data_ptr()), ctypes.byref(out)))
+    return int(out.value)
+
+
+def layer_prefill(d: Dims, params: Params, proj: Proj, cu_seqlens, h, *, initial_state=None,
+                  final_state=None, conv_state_in=None, conv_state_out=None, out=None,
+                  workspace=None):
+    """gdn_layer_prefill: h [T, hidden] bf16 -> returns h_out [T, hidden] bf16."""
+    lib = load()
+    dev = h.device
+    cu_d, cu_h = _cu_pair(cu_seqlens, dev)
+    n = cu_h.numel() - 1
+    t = int(cu_h[-1]) if n > 0 else 0
+    hid = proj.hidden
+    _t(h, "h", torch.bfloat16, (t, hid))
+    st_shape = (n, d.n_v_heads, d.d_k, d.d_v)
+    _t(initial_state, "initial_state", torch.float32, st_shape)
+    _t(final_state, "final_state", torch.float32, st_shape)
+    cs_shape = (n, d.conv_dim, d.conv_k - 1)
+    _t(conv_state_in, "conv_state_in", d.dtype, cs_shape)
+    _t(conv_state_out, "conv_state_out", d.dtype, cs_shape)
+    out = out if out is not None else torch.empty((t, hid), dtype=torch.bfloat16, device=dev)
+    _t(out, "out", torch.bfloat16, (t, hid))
+    need = layer_prefill_workspace_size(d, hid, cu_h)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dd, pp, pj = d.c(), params.c(d), proj.c(d)
+    st = lib.gdn_layer_prefill(ctypes.byref(dd), ctypes.byref(pp), ctypes.byref(pj), hid, n,
+                               _p(cu_d), ctypes.c_void_p(cu_h.data_ptr()), _p(h),
+                               _p(initial_state), _p(final_state), _p(conv_state_in),
+                               _p(conv_state_out), _p(out), _p(workspace), ws_bytes, _stream(dev))
+    _check("gdn_layer_prefill", st)
+    return out
+
+
 def decode(d: Dims, params: Params, x, z, a, b, state, conv_state=None, inter_states=None,
            out=None):
     """gdn_decode: x [N, T, CD] (or [N*T, CD] with T=1), state [N,Hv,dk,dv] fp32.
@@ -367,4 +439,5 @@ def decode_commit(d: Dims, accepted, x, inter_states, state, conv_state=None):
 
 __all__ = ["Dims", "Params", "GDNError", "load", "version", "timing_enable", "timing_report",
            "conv", "prefill",
-           "prefill_workspace_size", "decode", "verify", "decode_commit", "EXPORTS", "LIB_PATH"]
+           "prefill_workspace_size", "decode", "verify", "decode_commit", "Proj",
+           "layer_prefill_workspace_size", "layer_prefill", "EXPORTS", "LIB_PATH"]

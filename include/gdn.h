@@ -210,6 +210,42 @@ gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,
                              const float* inter_states, float* state, void* conv_state,
                              void* stream);
 
+/* Weights of the projections around the core (a GDN layer's in_proj_* and
+ * out_proj), bf16 device arrays in the [out_features, in_features] row-major
+ * layout of qwen.rs's linear weights, 16-byte aligned. */
+typedef struct gdn_proj {
+    const void* w_qkv; /* [CD, hidden]    in_proj_qkv -> x */
+    const void* w_z;   /* [Hv*dv, hidden] in_proj_z   -> z */
+    const void* w_a;   /* [Hv, hidden]    in_proj_a   -> a */
+    const void* w_b;   /* [Hv, hidden]    in_proj_b   -> b */
+    const void* w_out; /* [hidden, Hv*dv] out_proj */
+} gdn_proj;
+
+/*
+ * gdn_layer_prefill_workspace_size / gdn_layer_prefill -- one GDN layer's
+ * prefill: the input projections x = h W_qkv^T, z = h W_z^T, a = h W_a^T,
+ * b = h W_b^T (qwen.rs gdn_forward, its linear_multi over the hidden states),
+ * the core exactly as gdn_prefill, then h_out = y W_out^T (out_proj).  bf16
+ * only.  The projections are plain bf16 GEMMs with fp32 accumulation (cuBLAS);
+ * their results, like the core's output y, are rounded to bf16, the core's
+ * activation type.
+ *   hidden: model width, a multiple of 8.  h_in, h_out [T, hidden] bf16.
+ *   The states, cu_seqlens and their rules are those of gdn_prefill.
+ *   workspace: at least gdn_layer_prefill_workspace_size() bytes, 256-byte
+ *   aligned; it holds x, z, a, b, y, cuBLAS's workspace and the core's.
+ * The first call on a device creates that device's cuBLAS handle (cuBLAS may
+ * allocate a little device memory then; nothing allocates afterwards); calls
+ * from several host threads are serialised.
+ */
+gdn_status gdn_layer_prefill_workspace_size(const gdn_dims* dims, int32_t hidden, int32_t n_seq,
+                                            const int32_t* cu_seqlens_host, size_t* bytes);
+gdn_status gdn_layer_prefill(const gdn_dims* dims, const gdn_params* params,
+                             const gdn_proj* proj, int32_t hidden, int32_t n_seq,
+                             const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                             const void* h_in, const float* initial_state, float* final_state,
+                             const void* conv_state_in, void* conv_state_out, void* h_out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * gdn_timing_enable / gdn_timing_report -- per-kernel device timing (the
  * library's tracing hook; the pages time their GDN phases with scoped timers,

@@ -214,4 +214,33 @@ def gdn(d: Dims, cu_seqlens, x, z, a, b, conv_w, A_log, dt_bias, norm_w,
     return res
 
 
-__all__ = ["Dims", "build", "conv", "normalize", "gates", "recurrence", "gated_norm", "gdn"]
+def round_bf16(x):
+    """Nearest bf16 value (ties to even) of each element, as float64.
+
+    The value is first rounded to float32, as a GPU's fp32 accumulator holds it,
+    then to the 8-bit bf16 mantissa."""
+    u = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32)).view(np.uint32)
+    u = ((u.astype(np.uint64) + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return u.view(np.float32).astype(np.float64)
+
+
+def layer(d: Dims, cu_seqlens, h, w_qkv, w_z, w_a, w_b, w_out, conv_w, A_log, dt_bias,
+          norm_w, conv_state=None, state=None):
+    """A GDN layer's prefill around the core (qwen.rs gdn_forward: the
+    in_proj_qkv / in_proj_z / in_proj_a / in_proj_b linear_multi over the hidden
+    states, the core, then out_proj).  Weights are [out_features, in_features].
+
+    Reading: the projections' results and the core's output cross the core's
+    boundary in bf16, the activation type of the bf16 workloads, so they are
+    rounded to bf16 here as they are on the GPU; everything else is float64.
+    Returns ``gdn``'s dict plus ``h_out`` [T, hidden]."""
+    h = _f64(h)
+    x, z, a, b = (round_bf16(h @ _f64(w).T) for w in (w_qkv, w_z, w_a, w_b))
+    res = gdn(d, cu_seqlens, x, z, a, b, conv_w, A_log, dt_bias, norm_w, conv_state=conv_state,
+              state=state)
+    res["h_out"] = round_bf16(res["out"]) @ _f64(w_out).T
+    return res
+
+
+__all__ = ["Dims", "build", "conv", "normalize", "gates", "recurrence", "gated_norm", "gdn",
+           "round_bf16", "layer"]

@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import gated_deltanet_linear_mixer_gb300 as gdn
+import oracle
 from gated_deltanet_linear_mixer_gb300 import workloads
 from gdn_cases import TOL, dims, gpu_decode, gpu_prefill, rel_err, run_oracle, upload
 
@@ -296,6 +297,75 @@ def test_prefill_fused_and_two_kernel_launches_agree(name, monkeypatch):
     ref = run_oracle(case)
     assert rel_err(two["out"], ref["out"]) <= TOL["bf16"]
     assert rel_err(two["state"], ref["state"]) <= TOL["bf16"]
+
+
+def _layer_inputs(case, hidden, seed, exact=False):
+    """bf16 hidden states ~N(0,1) and projection weights ~N(0, 1/in_features).
+
+    exact: hidden states are integers in [-4, 4] and every in_proj row has 8
+    nonzero weights of +-1/16, so each projection is a multiple of 1/16 below 3
+    in magnitude: exact in bf16 and in any fp32 summation order.  The bf16
+    rounding of the projections is then no decision at all, and both sides feed
+    the core the same values (with dense weights, cuBLAS's fp32 sums and the
+    oracle's float64 ones round ~0.1% of the values to neighbouring bf16s, and
+    the core's final state is that sensitive)."""
+    rng = np.random.default_rng(seed)
+    vd, hv = case.n_v_heads * case.d_v, case.n_v_heads
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)  # noqa: E731
+    shapes = {"w_qkv": (case.conv_dim, hidden), "w_z": (vd, hidden), "w_a": (hv, hidden),
+              "w_b": (hv, hidden), "w_out": (hidden, vd)}
+    if not exact:
+        h = bf(rng.normal(size=(case.n_tokens, hidden)))
+        w = {k: bf(rng.normal(0, 1 / np.sqrt(s[1]), size=s)) for k, s in shapes.items()}
+        return h, w
+    h = bf(rng.integers(-4, 5, size=(case.n_tokens, hidden)).astype(np.float64))
+    w = {}
+    for k, (rows, cols) in shapes.items():
+        if k == "w_out":  # out_proj rounds nothing on the way: dense
+            w[k] = bf(rng.normal(0, 1 / np.sqrt(cols), size=(rows, cols)))
+            continue
+        m = np.zeros((rows, cols))
+        for r in range(rows):
+            m[r, rng.choice(cols, 8, replace=False)] = rng.choice([-1 / 16, 1 / 16], 8)
+        w[k] = bf(m)
+    return h, w
+
+
+def _layer_check(case, hidden, seed, exact=False):
+    d, od = dims(case)
+    t = upload(case)
+    h, w = _layer_inputs(case, hidden, seed, exact)
+    proj = gdn.Proj(*(w[k].cuda() for k in ("w_qkv", "w_z", "w_a", "w_b", "w_out")))
+    n = case.n_seq
+    st = torch.full((n, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
+    cs = torch.full((n, d.conv_dim, d.conv_k - 1), float("nan"), dtype=d.dtype, device="cuda")
+    got = gdn.layer_prefill(d, t["params"], proj, case.cu_seqlens, h.cuda(),
+                            initial_state=t["state"], final_state=st,
+                            conv_state_in=t["conv_state"], conv_state_out=cs)
+    torch.cuda.synchronize()
+    f = lambda u: u.float().numpy()  # noqa: E731
+    ref = oracle.layer(od, case.cu_seqlens, f(h), f(w["w_qkv"]), f(w["w_z"]), f(w["w_a"]),
+                       f(w["w_b"]), f(w["w_out"]), case.conv_w, case.A_log, case.dt_bias,
+                       case.norm_w, case.conv_state, case.state)
+    assert rel_err(got, ref["h_out"]) <= TOL["bf16"]
+    assert rel_err(st, ref["state"]) <= TOL["bf16"]
+    assert rel_err(cs, ref["conv_state"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("lengths", [[150, 70, 1], [5, 9, 16]])
+def test_layer_prefill_matches_oracle(lengths):
+    """in_proj (cuBLAS) -> core -> out_proj against the oracle's float64
+    projections; [5, 9, 16] takes the short-sequence (token-recurrent) core."""
+    case = _gen("ly", lengths=lengths, state_std=0.05, conv_state_std=1.0, seed=41)
+    _layer_check(case, hidden=256, seed=141)
+
+
+def test_layer_prefill_qwen3_next_width():
+    """The layer at the workload's head geometry (Hk=16, Hv=32, d=128) and a
+    2048-wide model, one 1024-token sequence (the fused tensor-core core), with
+    projections exact in bf16 (see _layer_inputs)."""
+    case = _gen("lw", n_k_heads=16, n_v_heads=32, lengths=[1024], seed=42)
+    _layer_check(case, hidden=2048, seed=142, exact=True)
 
 
 # ---------------------------------------------------------------- full sizes

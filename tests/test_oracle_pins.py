@@ -374,6 +374,42 @@ def test_gdn_equals_composition_of_stages():
     np.testing.assert_array_equal(r["g"], g)
 
 
+def test_layer_with_selection_projections_is_the_core():
+    """Projections that select disjoint column blocks of h (hidden = CD + Hv*dv
+    + 2 Hv) and an out_proj that puts y in the first Hv*dv columns: the layer is
+    the core on those blocks, exactly (bf16-valued inputs are left unchanged by
+    the bf16 rounding).  A transposed weight, or two projections fed to the
+    wrong core inputs, fails it."""
+    d = _dims(act="sigmoid")
+    cd, vd, hv = d.conv_dim, d.n_v_heads * d.d_v, d.n_v_heads
+    hidden = cd + vd + 2 * hv
+    case = _rng_case(d, [9, 4], seed=73)
+    rng = np.random.default_rng(74)
+    h = oracle.round_bf16(rng.normal(size=(int(case["cu"][-1]), hidden)))
+    eye = np.eye(hidden)
+    w_qkv, w_z = eye[:cd], eye[cd:cd + vd]
+    w_a, w_b = eye[cd + vd:cd + vd + hv], eye[cd + vd + hv:]
+    w_out = np.zeros((hidden, vd))
+    w_out[:vd] = np.eye(vd)
+    r = oracle.layer(d, case["cu"], h, w_qkv, w_z, w_a, w_b, w_out, case["conv_w"],
+                     case["A_log"], case["dt_bias"], case["norm_w"], case["conv_state"],
+                     case["state"])
+    x, z = h[:, :cd], h[:, cd:cd + vd]
+    a, b = h[:, cd + vd:cd + vd + hv], h[:, cd + vd + hv:]
+    ref = oracle.gdn(d, case["cu"], x, z, a, b, case["conv_w"], case["A_log"], case["dt_bias"],
+                     case["norm_w"], case["conv_state"], case["state"])
+    np.testing.assert_array_equal(r["h_out"][:, :vd], oracle.round_bf16(ref["out"]))
+    np.testing.assert_array_equal(r["h_out"][:, vd:], 0.0)
+    np.testing.assert_array_equal(r["state"], ref["state"])
+
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(75)
+    v = rng.normal(size=4096) * np.exp(rng.uniform(-20, 20, 4096))
+    want = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(v), want)
+
+
 def test_decode_steps_equal_one_prefill():
     """T one-token calls carrying (state, conv state) == one T-token call, and the
     per-token intermediate states equal the states after each single step."""
