@@ -47,7 +47,8 @@ class _Dims(ctypes.Structure):
     _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("conv_k", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+                ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float),
+                ("head_map", ctypes.c_int32), ("decay_form", ctypes.c_int32)]
 
 
 class _Params(ctypes.Structure):
@@ -122,6 +123,8 @@ class Dims:
     act: str = "silu"
     l2_eps: float = 1e-6
     rms_eps: float = 1e-6
+    head_map: str = "contiguous"   # value head h reads key head h // (Hv/Hk), or h % Hk ("tiled")
+    decay_form: str = "A_log"      # Params.A_log holds log A, or the decay coefficient ("coef")
 
     @property
     def conv_dim(self) -> int:
@@ -132,10 +135,15 @@ class Dims:
             raise ValueError("activation dtype must be torch.float32 or torch.bfloat16")
         if self.act not in ("silu", "sigmoid"):
             raise ValueError("act must be 'silu' or 'sigmoid'")
+        if self.head_map not in ("contiguous", "tiled"):
+            raise ValueError("head_map must be 'contiguous' or 'tiled'")
+        if self.decay_form not in ("A_log", "coef"):
+            raise ValueError("decay_form must be 'A_log' or 'coef'")
         return _Dims(self.n_k_heads, self.n_v_heads, self.d_k, self.d_v, self.conv_k,
                      DTYPE_BF16 if self.dtype == torch.bfloat16 else DTYPE_F32,
                      ACT_SIGMOID if self.act == "sigmoid" else ACT_SILU,
-                     self.l2_eps, self.rms_eps)
+                     self.l2_eps, self.rms_eps, 1 if self.head_map == "tiled" else 0,
+                     1 if self.decay_form == "coef" else 0)
 
 
 @dataclass

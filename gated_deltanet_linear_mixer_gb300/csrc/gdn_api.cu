@@ -53,6 +53,10 @@ gdn_status check_dims(const gdn_dims* d, const char* fn) {
         return fail(GDN_ERR_INVALID_ARG, fn, "dtype %d is not a gdn_dtype", d->dtype);
     if (d->act != GDN_ACT_SILU && d->act != GDN_ACT_SIGMOID)
         return fail(GDN_ERR_INVALID_ARG, fn, "act %d is not a gdn_act", d->act);
+    if (d->head_map != GDN_HEADS_CONTIGUOUS && d->head_map != GDN_HEADS_TILED)
+        return fail(GDN_ERR_INVALID_ARG, fn, "head_map %d is not a gdn_head_map", d->head_map);
+    if (d->decay_form != GDN_DECAY_A_LOG && d->decay_form != GDN_DECAY_COEF)
+        return fail(GDN_ERR_INVALID_ARG, fn, "decay_form %d is not a gdn_decay_form", d->decay_form);
     if (!(d->l2_eps > 0.f) || !std::isfinite(d->l2_eps) || !(d->rms_eps > 0.f) ||
         !std::isfinite(d->rms_eps))
         return fail(GDN_ERR_INVALID_ARG, fn, "eps values must be finite and > 0");
@@ -263,7 +267,7 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_se
     p.n_seq = n_seq; p.n_tokens = total;
     p.n_k_heads = dims->n_k_heads; p.n_v_heads = dims->n_v_heads;
     p.d_k = dims->d_k; p.d_v = dims->d_v; p.conv_k = dims->conv_k; p.l2_eps = dims->l2_eps;
-    p.cu_seqlens = cu_seqlens; p.x = x; p.a = a; p.b = b;
+    p.cu_seqlens = cu_seqlens; p.x = x; p.a = a; p.b = b; p.decay_form = dims->decay_form;
     p.conv_w = params->conv_w; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
     p.conv_state_in = conv_state_in; p.qkv_out = qkv_out; p.g_out = g_out; p.beta_out = beta_out;
     if ((st = cuda_status(timed_launch("conv_prologue", s, [&] { return gdn::launch_conv_prologue(p, bf16, s); }), fn, "conv prologue launch")) != GDN_OK)
@@ -335,6 +339,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         gdn::ChunkLaunch c{};
         c.n_seq = n_seq; c.n_tokens = total; c.n_k_heads = dims->n_k_heads;
         c.n_v_heads = dims->n_v_heads; c.conv_k = dims->conv_k; c.act = dims->act;
+        c.head_map = dims->head_map; c.decay_form = dims->decay_form;
         c.l2_eps = dims->l2_eps; c.rms_eps = dims->rms_eps; c.cu_seqlens = cu_seqlens;
         c.x = x; c.z = z; c.a = a; c.b = b;
         c.conv_w = params->conv_w; c.A_log = params->A_log; c.dt_bias = params->dt_bias;
@@ -357,6 +362,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     gdn::RecurrentArgs r{};
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
+    r.head_map = dims->head_map; r.decay_form = dims->decay_form;
     r.cu_seqlens = cu_seqlens; r.uniform_T = 0;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
@@ -401,6 +407,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     gdn::RecurrentArgs r{};
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
+    r.head_map = dims->head_map; r.decay_form = dims->decay_form;
     r.cu_seqlens = nullptr; r.uniform_T = T;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
@@ -446,6 +453,7 @@ gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_
     gdn::RecurrentArgs r{};
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
+    r.head_map = dims->head_map; r.decay_form = dims->decay_form;
     r.cu_seqlens = nullptr; r.uniform_T = T;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;

@@ -203,7 +203,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         const int nb = min(2, R - 2 * pr);
         mbar_arrive_expect_tx(&bar_v, nb * 4 * 8192);
         for (int sl = 0; sl < nb; ++sl) {
-            const int vc = 2 * p.n_k_heads * kD + (hki * R + 2 * pr + sl) * kD;
+            const int vc = 2 * p.n_k_heads * kD + value_head(hki, 2 * pr + sl, R, p.n_k_heads, p.head_map) * kD;
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 tma_load_2d(smem + kPrepV + (2 * sl + b) * 8192, &map_qh, &bar_v, vc + 64 * b, t0i);
@@ -220,7 +220,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
     float ng0 = 0.f, ng1 = 0.f, nb0 = 0.f, nb1 = 0.f;
     auto prefetch_gates = [&](int it) {  // ci_n holds item it's position
         if (warp < R) {
-            const int h = (it % p.n_k_heads) * R + warp;
+            const int h = value_head(it % p.n_k_heads, warp, R, p.n_k_heads, p.head_map);
             const int s0 = 2 * lane, s1 = 2 * lane + 1;
             ng0 = ng1 = nb0 = nb1 = 0.f;
             if (s0 < ci_n.y) {
@@ -353,7 +353,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 float v[64];
                 tmem_ld64(tmem + kTpGram + ((32u * q) << 16), v);
                 if (hh < nb) {
-                    const int r = 2 * pr + hh, h = hk * R + r;
+                    const int r = 2 * pr + hh, h = value_head(hk, r, R, p.n_k_heads, p.head_map);
                     const float* Gr = sG + r * kC;
                     const float Gt = Gr[t];
                     if (q < 2) {  // masked decayed Q K^T row t -> staging tile (hi, lo)
@@ -383,7 +383,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             __syncthreads();
             if (tid == 64) {  // M o QK^T tiles -> workspace (thread 64 idles in the diagonal solve)
                 for (int hh = 0; hh < nb; ++hh) {
-                    const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
+                    const int row = (c * hv_n + value_head(hk, 2 * pr + hh, R, p.n_k_heads, p.head_map)) * kC;
                     tma_store_2d(&map_kqh, smem + kPrepT2 + hh * 16384, 0, row);
                     tma_store_2d(&map_kql, smem + kPrepT2 + hh * 16384 + 8192, 0, row);
                 }
@@ -566,7 +566,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
                 tmem_ld64(tmem + (hh ? kTpUb : kTpUa) + ((32u * q) << 16) + 64 * half, v);
                 if (hh < nb) {
-                    const int h = hk * R + 2 * pr + hh;
+                    const int h = value_head(hk, 2 * pr + hh, R, p.n_k_heads, p.head_map);
                     float4* dst = reinterpret_cast<float4*>(p.u_ws + (size_t)(c * hv_n + h) * kC * kD) +
                                   (16 * half) * kC + t;
 #pragma unroll
@@ -581,7 +581,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             tc_fence_after_sync();
             if (tid == 0) {
                 for (int hh = 0; hh < nb; ++hh) {
-                    const int row = (c * hv_n + hk * R + 2 * pr + hh) * kC;
+                    const int row = (c * hv_n + value_head(hk, 2 * pr + hh, R, p.n_k_heads, p.head_map)) * kC;
                     const uint8_t* st = smem + (hh ? kPrepT2 : kPrepT1);
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
@@ -721,7 +721,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int v0 = static_cast<int>(rank) * kDS;  // first value lane of this CTA
     const int hv_n = p.n_v_heads;
-    const int R = hv_n / p.n_k_heads, hk = h / R;
+    const int R = hv_n / p.n_k_heads, hk = key_head(h, R, p.n_k_heads, p.head_map);
     const int bos = p.cu_seqlens[n], eos = p.cu_seqlens[n + 1];
     const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
@@ -1228,6 +1228,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     cv.n_seq = a.n_seq; cv.n_tokens = T; cv.n_k_heads = hk_n; cv.n_v_heads = hv_n;
     cv.d_k = kD; cv.d_v = kD; cv.conv_k = a.conv_k; cv.l2_eps = a.l2_eps;
     cv.cu_seqlens = a.cu_seqlens; cv.x = a.x; cv.a = a.a; cv.b = a.b;
+    cv.decay_form = a.decay_form;
     cv.conv_w = a.conv_w; cv.A_log = a.A_log; cv.dt_bias = a.dt_bias;
     cv.conv_state_in = a.conv_state_in;
     cv.conv_state_out = a.conv_state_out;
@@ -1251,6 +1252,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     ChunkArgs p{};
     p.n_seq = a.n_seq; p.n_tokens = T; p.n_chunks = l.n_chunks;
     p.n_k_heads = hk_n; p.n_v_heads = hv_n; p.act = a.act; p.rms_eps = a.rms_eps;
+    p.head_map = a.head_map;
     p.cu_seqlens = a.cu_seqlens; p.cu_chunks = cu_chunks;
     p.chunk_info = reinterpret_cast<const int2*>(ws + l.chunk_info);
     p.qkv_hi = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_hi);

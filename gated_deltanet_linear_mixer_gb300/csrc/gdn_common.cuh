@@ -84,8 +84,17 @@ __device__ __forceinline__ float gatef_(float z, int act) {
     return act == 1 ? sigmoidf_(z) : siluf_(z);
 }
 // log-decay g = -exp(A_log) * softplus(a + dt_bias)
-__device__ __forceinline__ float log_decay(float a, float A_log, float dt_bias) {
-    return -expf(A_log) * softplusf_(a + dt_bias);
+// Log-decay g of one token and value head; A is log A (form 0) or the decay
+// coefficient itself (form 1, the GGUF ssm_a).
+__device__ __forceinline__ float log_decay(float a, float A, float dt_bias, int form) {
+    return (form ? A : -expf(A)) * softplusf_(a + dt_bias);
+}
+
+// Key head of value head h (tiled: h % Hk; contiguous: h / R), and the r-th
+// value head of key head hk (R = Hv / Hk value heads per key head).
+__device__ __forceinline__ int key_head(int h, int R, int Hk, int tiled) { return tiled ? h % Hk : h / R; }
+__device__ __forceinline__ int value_head(int hk, int r, int R, int Hk, int tiled) {
+    return tiled ? hk + Hk * r : hk * R + r;
 }
 
 // Two floats rounded to bf16 (nearest even) and packed, first in the low half.

@@ -65,7 +65,7 @@ conv_prologue_kernel(ConvArgs p) {
             const int h = i % hv_n;
             if (t >= p.n_tokens) break;
             const size_t idx = (size_t)t * hv_n + h;
-            p.g_out[idx] = log_decay(to_f32(a[idx]), p.A_log[h], p.dt_bias[h]);
+            p.g_out[idx] = log_decay(to_f32(a[idx]), p.A_log[h], p.dt_bias[h], p.decay_form);
             p.beta_out[idx] = sigmoidf_(to_f32(b[idx]));
         }
         return;
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
             const int h = i % hv_n;
             if (t >= p.n_tokens) break;
             const size_t idx = (size_t)t * hv_n + h;
-            p.g_out[idx] = log_decay(__bfloat162float(a[idx]), p.A_log[h], p.dt_bias[h]);
+            p.g_out[idx] = log_decay(__bfloat162float(a[idx]), p.A_log[h], p.dt_bias[h], p.decay_form);
             p.beta_out[idx] = sigmoidf_(__bfloat162float(b[idx]));
         }
         return;

@@ -14,6 +14,7 @@ constexpr int kChunkTokens = 64;
 
 struct ConvArgs {
     int n_seq, n_tokens, n_k_heads, n_v_heads, d_k, d_v, conv_k;
+    int decay_form;             // gdn_decay_form
     float l2_eps;
     const int32_t* cu_seqlens;  // [n_seq+1]
     const void* x;              // [T, CD]
@@ -52,6 +53,7 @@ struct ConvStateArgs {
 
 struct RecurrentArgs {
     int n_seq, n_k_heads, n_v_heads, conv_k, act;
+    int head_map, decay_form;   // gdn_head_map, gdn_decay_form
     float l2_eps, rms_eps;
     const int32_t* cu_seqlens;  // [n_seq+1], or null with uniform_T tokens per sequence
     int uniform_T;
@@ -81,6 +83,7 @@ struct CommitArgs {
 // tensor cores are kept as bf16 (hi, lo) pairs: hi = bf16(x), lo = bf16(x - hi).
 struct ChunkArgs {
     int n_seq, n_tokens, n_chunks, n_k_heads, n_v_heads, act;
+    int head_map;                 // gdn_head_map
     float rms_eps;
     const int32_t* cu_seqlens;    // [n_seq+1]
     const int32_t* cu_chunks;     // [n_seq+1] chunk offsets (workspace)
@@ -123,6 +126,7 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
 
 struct ChunkLaunch {
     int n_seq, n_tokens, n_k_heads, n_v_heads, conv_k, act;
+    int head_map, decay_form;
     float l2_eps, rms_eps;
     const int32_t* cu_seqlens;
     const void *x, *z, *a, *b;

@@ -43,7 +43,7 @@ recurrent_kernel(RecurrentArgs p) {
     const int hv = blockIdx.x;
     const int n = blockIdx.y;
     const int hv_n = p.n_v_heads;
-    const int hk = hv / (hv_n / p.n_k_heads);
+    const int hk = key_head(hv, hv_n / p.n_k_heads, p.n_k_heads, p.head_map);
     const int cd = 2 * p.n_k_heads * DK + hv_n * DV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c4 = tid % L, rg = tid / L;
@@ -102,7 +102,7 @@ recurrent_kernel(RecurrentArgs p) {
         }
         if (tid < nb) {
             const size_t gi = (size_t)(bos + t0 + tid) * hv_n + hv;
-            gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv]));
+            gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv], p.decay_form));
             bet[tid] = sigmoidf_(to_f32(bv[gi]));
         }
         __syncthreads();

@@ -60,6 +60,17 @@ typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
  * the qwen4_exp config (output_gate_sigmoid) use sigmoid. */
 typedef enum gdn_act { GDN_ACT_SILU = 0, GDN_ACT_SIGMOID = 1 } gdn_act;
 
+/* Which key head a value head reads (qwen.rs DeltaRule::run): h / (Hv/Hk),
+ * contiguous groups (cpu.rs deltanet, the safetensors checkpoints), or h % Hk,
+ * tiled (the GGUF checkpoints' layout). */
+typedef enum gdn_head_map { GDN_HEADS_CONTIGUOUS = 0, GDN_HEADS_TILED = 1 } gdn_head_map;
+
+/* What gdn_params.A_log holds (qwen.rs loader, decay_coef): log A, the
+ * checkpoint's A_log, so that g = -exp(A_log) softplus(a + dt_bias); or the
+ * decay coefficient itself (GGUF ssm_a, which stores -exp(A_log)), so that
+ * g = A_log[h] softplus(a + dt_bias). */
+typedef enum gdn_decay_form { GDN_DECAY_A_LOG = 0, GDN_DECAY_COEF = 1 } gdn_decay_form;
+
 /* Geometry (names of qwen4_exp.rs GdnCfg / qwen.rs QwenConfig).
  * Supported: d_k, d_v in {32, 64, 128}; 2 <= conv_k <= 4;
  * n_v_heads a multiple of n_k_heads; eps > 0. */
@@ -73,6 +84,8 @@ typedef struct gdn_dims {
     int32_t act;       /* gdn_act of the output gate */
     float l2_eps;      /* q/k L2-norm eps (1e-6 on the pages) */
     float rms_eps;     /* gated RMSNorm eps (1e-6 / rms_norm_eps) */
+    int32_t head_map;  /* gdn_head_map; 0 (contiguous) when zero-initialised */
+    int32_t decay_form; /* gdn_decay_form; 0 (A_log) when zero-initialised */
 } gdn_dims;
 
 /* Per-layer parameters, fp32 device pointers (qwen.rs loader: conv1d.weight

@@ -46,7 +46,8 @@ class _Dims(ctypes.Structure):
     _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("conv_k", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("l2_eps", ctypes.c_double), ("rms_eps", ctypes.c_double)]
+                ("l2_eps", ctypes.c_double), ("rms_eps", ctypes.c_double),
+                ("tiled", ctypes.c_int32), ("decay_coef", ctypes.c_int32)]
 
 
 def _load():
@@ -80,6 +81,8 @@ class Dims:
     act: str = "silu"          # output gate: "silu" or "sigmoid"
     l2_eps: float = 1e-6
     rms_eps: float = 1e-6
+    head_map: str = "contiguous"  # key head of value head h: h // (Hv/Hk), or h % Hk ("tiled")
+    decay_form: str = "A_log"     # A_log holds log A, or the decay coefficient itself ("coef")
 
     @property
     def conv_dim(self) -> int:
@@ -88,8 +91,11 @@ class Dims:
     def _c(self) -> _Dims:
         if self.act not in ("silu", "sigmoid"):
             raise ValueError(f"act must be 'silu' or 'sigmoid', got {self.act!r}")
+        if self.head_map not in ("contiguous", "tiled") or self.decay_form not in ("A_log", "coef"):
+            raise ValueError("head_map must be 'contiguous' or 'tiled', decay_form 'A_log' or 'coef'")
         return _Dims(self.n_k_heads, self.n_v_heads, self.d_k, self.d_v, self.conv_k,
-                     1 if self.act == "sigmoid" else 0, self.l2_eps, self.rms_eps)
+                     1 if self.act == "sigmoid" else 0, self.l2_eps, self.rms_eps,
+                     1 if self.head_map == "tiled" else 0, 1 if self.decay_form == "coef" else 0)
 
 
 def _f64(a):

@@ -46,6 +46,8 @@ typedef struct {
     int32_t act;        /* output gate: 0 = SiLU, 1 = sigmoid */
     double l2_eps;      /* 1e-6 on both pages */
     double rms_eps;     /* 1e-6 on cpu.rs; rms_norm_eps on qwen.rs */
+    int32_t tiled;      /* key head of value head hv: hv % Hk if 1, hv / (Hv/Hk) if 0 */
+    int32_t decay_coef; /* A_log[] holds the decay coefficient itself if 1 */
 } oracle_dims;
 
 static int conv_dim(const oracle_dims* d) {
@@ -157,9 +159,10 @@ void oracle_normalize(const oracle_dims* d, int n_tok, const double* c,
 
 /*
  * Step a4: write strength beta = sigmoid(b) and log-decay
- * g = -exp(A_log) * softplus(a + dt_bias), per token and value head.
+ * g = decay_coef * softplus(a + dt_bias), per token and value head.
  * [qwen.rs] DeltaRule::run (beta, ga, softplus, decay) with the loader's
- * decay_coef = -exp(A_log); [cpu.rs] deltanet (beta, g, decay = g.exp()).
+ * decay_coef = -exp(A_log), or the GGUF ssm_a read as decay_coef directly
+ * (d->decay_coef); [cpu.rs] deltanet (beta, g, decay = g.exp()).
  */
 void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double* b,
                   const double* A_log, const double* dt_bias, double* g, double* beta) {
@@ -168,7 +171,8 @@ void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double
         for (int h = 0; h < hv_n; ++h) {
             const size_t i = (size_t)t * hv_n + h;
             beta[i] = sigmoid(b[i]);
-            g[i] = -exp(A_log[h]) * softplus(a[i] + dt_bias[h]);
+            const double coef = d->decay_coef ? A_log[h] : -exp(A_log[h]);
+            g[i] = coef * softplus(a[i] + dt_bias[h]);
         }
     }
 }
@@ -176,7 +180,8 @@ void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double
 /*
  * Step a5: the gated delta rule in its recurrent form, token by token.
  * [cpu.rs] deltanet and [qwen.rs] DeltaRule::run, per value head hv with key
- * head hk = hv / (Hv/Hk) (contiguous groups):
+ * head hk = hv / (Hv/Hk) (contiguous groups), or hk = hv % Hk when d->tiled
+ * (qwen.rs DeltaRule::run's `tiled`):
  *   S <- exp(g) * S                (decay first)
  *   kv = S^T k                     (read of the decayed state)
  *   delta = beta * (v - kv)
@@ -198,7 +203,7 @@ void oracle_recurrence(const oracle_dims* d, int n_seq, const int32_t* cu_seqlen
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int n = 0; n < n_seq; ++n) {
         for (int hv = 0; hv < hv_n; ++hv) {
-            const int hk = hv / group;
+            const int hk = d->tiled ? hv % hk_n : hv / group;
             const int bos = cu_seqlens[n];
             const int len = cu_seqlens[n + 1] - bos;
             double* s = (double*)malloc(sizeof(double) * slab);

@@ -47,9 +47,15 @@ def rel_err(got, ref) -> float:
 
 
 def dims(case):
+    """Library and oracle geometry of a case; a case may carry head_map and
+    decay_form (the ABI options), else the defaults."""
     tdt = torch.bfloat16 if case.dtype == "bf16" else torch.float32
-    d = gdn.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, tdt, case.act)
-    od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act)
+    opt = dict(head_map=getattr(case, "head_map", "contiguous"),
+               decay_form=getattr(case, "decay_form", "A_log"))
+    d = gdn.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, tdt, case.act,
+                 **opt)
+    od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act,
+                     **opt)
     return d, od
 
 

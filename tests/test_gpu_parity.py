@@ -278,6 +278,41 @@ def test_invalid_arguments_raise():
                    torch.zeros((1, 17, 4), dtype=d.dtype, device="cuda"), st)
 
 
+def _with_options(case, head_map="contiguous", decay_form="A_log"):
+    """The ABI options of the pages' GGUF checkpoints on a generated case: the
+    tiled value-to-key map, and the decay coefficient given instead of A_log
+    (rounded to fp32 first, so that both sides read the same values)."""
+    case.head_map, case.decay_form = head_map, decay_form
+    if decay_form == "coef":
+        case.A_log = (-np.exp(case.A_log)).astype(np.float32).astype(np.float64)
+    return case
+
+
+@pytest.mark.parametrize("name,decay_form", [("tc_gqa_R4", "A_log"), ("tc_gqa_R8", "coef"),
+                                             ("ragged_bf16_d128_states", "coef"),
+                                             ("bf16_dk32_dv64_K2_gqa4", "A_log"),
+                                             ("ragged_f32_dk64_dv128_sigmoid", "coef")])
+def test_prefill_tiled_head_map_and_decay_coef_match_oracle(name, decay_form):
+    """Tensor-core (d=128 bf16) and token-recurrent paths with the tiled map."""
+    case = _with_options(PREFILL_CASES[name](), "tiled", decay_form)
+    ref = run_oracle(case)
+    got = gpu_prefill(case)
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+
+
+def test_decode_tiled_head_map_and_decay_coef_match_oracle():
+    case = _with_options(_gen("dt", mode="decode", n_seq=5, tokens_per_seq=4, n_k_heads=2,
+                              n_v_heads=6, act="sigmoid", state_std=0.05, conv_state_std=1.0,
+                              seed=28, want_inter=True), "tiled", "coef")
+    ref = run_oracle(case, want_inter=True)
+    got = gpu_decode(case, inter=True)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    n, tt = case.n_seq, case.tokens_per_seq
+    assert rel_err(got["inter"], ref["inter"].reshape(n, tt, *ref["inter"].shape[1:])) <= TOL["bf16"]
+
+
 TC_CASES = sorted(k for k in PREFILL_CASES if k.startswith("tc_"))
 
 

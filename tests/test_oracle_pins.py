@@ -410,6 +410,64 @@ def test_round_bf16_matches_torch():
     np.testing.assert_array_equal(oracle.round_bf16(v), want)
 
 
+def test_tiled_head_map_is_the_contiguous_one_with_value_heads_permuted():
+    """Value head h reading key head h % Hk (tiled) is, bit for bit, the
+    contiguous map (key head j // R) run on the same heads renumbered j = hk R + r
+    for h = hk + Hk r: every per-value-head input (v channels and their conv
+    weights and history, z, a, b, A_log, dt_bias, state) moved with its head."""
+    d_t = oracle.Dims(2, 6, 8, 8, 4, "sigmoid", head_map="tiled")
+    d_c = oracle.Dims(2, 6, 8, 8, 4, "sigmoid")
+    hk_n, hv_n, dv = 2, 6, 8
+    rr = hv_n // hk_n
+    case = _rng_case(d_c, [11, 5], seed=76)
+    perm = np.empty(hv_n, dtype=int)  # contiguous slot j holds tiled head perm[j]
+    for hk in range(hk_n):
+        for r in range(rr):
+            perm[hk * rr + r] = hk + hk_n * r
+    kd = 2 * hk_n * 8
+
+    def per_head(u, axis, width):
+        shp = list(u.shape)
+        v = u.reshape(shp[:axis] + [hv_n, width] + shp[axis + 1:])
+        return np.take(v, perm, axis=axis).reshape(shp)
+
+    def move(c):
+        m = dict(c)
+        m["x"] = np.concatenate([c["x"][:, :kd], per_head(c["x"][:, kd:], 1, dv)], axis=1)
+        m["conv_w"] = np.concatenate([c["conv_w"][:kd], per_head(c["conv_w"][kd:], 0, dv)])
+        m["conv_state"] = np.concatenate([c["conv_state"][:, :kd],
+                                          per_head(c["conv_state"][:, kd:], 1, dv)], axis=1)
+        m["z"] = per_head(c["z"], 1, dv)
+        m["a"], m["b"] = c["a"][:, perm], c["b"][:, perm]
+        m["A_log"], m["dt_bias"] = c["A_log"][perm], c["dt_bias"][perm]
+        m["state"] = c["state"][:, perm]
+        return m
+
+    def run(d, c):
+        return oracle.gdn(d, c["cu"], c["x"], c["z"], c["a"], c["b"], c["conv_w"], c["A_log"],
+                          c["dt_bias"], c["norm_w"], c["conv_state"], c["state"])
+    rt, rc = run(d_t, case), run(d_c, move(case))
+    np.testing.assert_array_equal(per_head(rt["out"], 1, dv), rc["out"])
+    np.testing.assert_array_equal(rt["state"][:, perm], rc["state"])
+
+
+def test_decay_coefficient_form_equals_A_log_form():
+    """Giving the decay coefficient A = -exp(A_log) itself (the GGUF ssm_a)
+    gives the same gates and outputs as giving A_log."""
+    d = _dims()
+    d_coef = oracle.Dims(d.n_k_heads, d.n_v_heads, d.d_k, d.d_v, d.conv_k, d.act, decay_form="coef")
+    case = _rng_case(d, [7, 9], seed=77)
+    coef = -np.exp(case["A_log"])
+    g1, _ = oracle.gates(d, case["a"], case["b"], case["A_log"], case["dt_bias"])
+    g2, _ = oracle.gates(d_coef, case["a"], case["b"], coef, case["dt_bias"])
+    np.testing.assert_allclose(g2, g1, rtol=1e-14, atol=0)
+    r1 = oracle.gdn(d, case["cu"], case["x"], case["z"], case["a"], case["b"], case["conv_w"],
+                    case["A_log"], case["dt_bias"], case["norm_w"], case["conv_state"], case["state"])
+    r2 = oracle.gdn(d_coef, case["cu"], case["x"], case["z"], case["a"], case["b"], case["conv_w"],
+                    coef, case["dt_bias"], case["norm_w"], case["conv_state"], case["state"])
+    np.testing.assert_allclose(r2["out"], r1["out"], rtol=1e-12, atol=1e-14)
+
+
 def test_decode_steps_equal_one_prefill():
     """T one-token calls carrying (state, conv state) == one T-token call, and the
     per-token intermediate states equal the states after each single step."""
