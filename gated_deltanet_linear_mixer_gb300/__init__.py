@@ -48,7 +48,8 @@ class _Dims(ctypes.Structure):
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("conv_k", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("head_map", ctypes.c_int32), ("decay_form", ctypes.c_int32)]
+                ("head_map", ctypes.c_int32), ("decay_form", ctypes.c_int32),
+                ("decay_per_channel", ctypes.c_int32)]
 
 
 class _Params(ctypes.Structure):
@@ -125,10 +126,16 @@ class Dims:
     rms_eps: float = 1e-6
     head_map: str = "contiguous"   # value head h reads key head h // (Hv/Hk), or h % Hk ("tiled")
     decay_form: str = "A_log"      # Params.A_log holds log A, or the decay coefficient ("coef")
+    per_channel_decay: bool = False  # one decay per key channel: a [T, Hv*dk], dt_bias [Hv*dk]
 
     @property
     def conv_dim(self) -> int:
         return 2 * self.n_k_heads * self.d_k + self.n_v_heads * self.d_v
+
+    @property
+    def gate_width(self) -> int:
+        """Columns of the decay-gate input a (and entries of dt_bias)."""
+        return self.n_v_heads * (self.d_k if self.per_channel_decay else 1)
 
     def c(self) -> _Dims:
         if self.dtype not in (torch.float32, torch.bfloat16):
@@ -143,7 +150,7 @@ class Dims:
                      DTYPE_BF16 if self.dtype == torch.bfloat16 else DTYPE_F32,
                      ACT_SIGMOID if self.act == "sigmoid" else ACT_SILU,
                      self.l2_eps, self.rms_eps, 1 if self.head_map == "tiled" else 0,
-                     1 if self.decay_form == "coef" else 0)
+                     1 if self.decay_form == "coef" else 0, 1 if self.per_channel_decay else 0)
 
 
 @dataclass
@@ -157,7 +164,7 @@ class Params:
     def c(self, d: Dims) -> _Params:
         _t(self.conv_w, "conv_w", torch.float32, (d.conv_dim, d.conv_k))
         _t(self.A_log, "A_log", torch.float32, (d.n_v_heads,))
-        _t(self.dt_bias, "dt_bias", torch.float32, (d.n_v_heads,))
+        _t(self.dt_bias, "dt_bias", torch.float32, (d.gate_width,))
         _t(self.norm_w, "norm_w", torch.float32, (d.d_v,))
         return _Params(self.conv_w.data_ptr(), self.A_log.data_ptr(), self.dt_bias.data_ptr(),
                        self.norm_w.data_ptr())
@@ -247,7 +254,7 @@ def conv(d: Dims, params: Params, cu_seqlens, x, a, b, conv_state_in=None, conv_
     n = cu_h.numel() - 1
     t = int(cu_h[-1]) if n > 0 else 0
     _t(x, "x", d.dtype, (t, d.conv_dim))
-    _t(a, "a", d.dtype, (t, d.n_v_heads))
+    _t(a, "a", d.dtype, (t, d.gate_width))
     _t(b, "b", d.dtype, (t, d.n_v_heads))
     cs_shape = (n, d.conv_dim, d.conv_k - 1)
     _t(conv_state_in, "conv_state_in", d.dtype, cs_shape)
@@ -290,7 +297,7 @@ def prefill(d: Dims, params: Params, cu_seqlens, x, z, a, b, *, initial_state=No
     vd = d.n_v_heads * d.d_v
     _t(x, "x", d.dtype, (t, d.conv_dim))
     _t(z, "z", d.dtype, (t, vd))
-    _t(a, "a", d.dtype, (t, d.n_v_heads))
+    _t(a, "a", d.dtype, (t, d.gate_width))
     _t(b, "b", d.dtype, (t, d.n_v_heads))
     st_shape = (n, d.n_v_heads, d.d_k, d.d_v)
     _t(initial_state, "initial_state", torch.float32, st_shape)
@@ -389,10 +396,10 @@ def decode(d: Dims, params: Params, x, z, a, b, state, conv_state=None, inter_st
     vd = d.n_v_heads * d.d_v
     _t(x, "x", d.dtype, (n, tt, d.conv_dim))
     z = z.reshape(n, tt, vd) if z.dim() == 2 else z
-    a = a.reshape(n, tt, d.n_v_heads) if a.dim() == 2 else a
+    a = a.reshape(n, tt, d.gate_width) if a.dim() == 2 else a
     b = b.reshape(n, tt, d.n_v_heads) if b.dim() == 2 else b
     _t(z, "z", d.dtype, (n, tt, vd))
-    _t(a, "a", d.dtype, (n, tt, d.n_v_heads))
+    _t(a, "a", d.dtype, (n, tt, d.gate_width))
     _t(b, "b", d.dtype, (n, tt, d.n_v_heads))
     _t(state, "state", torch.float32, (n, d.n_v_heads, d.d_k, d.d_v))
     _t(conv_state, "conv_state", d.dtype, (n, d.conv_dim, d.conv_k - 1))
@@ -416,7 +423,7 @@ def verify(d: Dims, params: Params, x, z, a, b, state, conv_state=None, out=None
     vd = d.n_v_heads * d.d_v
     _t(x, "x", d.dtype, (n, tt, d.conv_dim))
     _t(z, "z", d.dtype, (n, tt, vd))
-    _t(a, "a", d.dtype, (n, tt, d.n_v_heads))
+    _t(a, "a", d.dtype, (n, tt, d.gate_width))
     _t(b, "b", d.dtype, (n, tt, d.n_v_heads))
     _t(state, "state", torch.float32, (n, d.n_v_heads, d.d_k, d.d_v))
     _t(conv_state, "conv_state", d.dtype, (n, d.conv_dim, d.conv_k - 1))

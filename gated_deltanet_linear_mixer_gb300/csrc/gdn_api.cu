@@ -57,6 +57,8 @@ gdn_status check_dims(const gdn_dims* d, const char* fn) {
         return fail(GDN_ERR_INVALID_ARG, fn, "head_map %d is not a gdn_head_map", d->head_map);
     if (d->decay_form != GDN_DECAY_A_LOG && d->decay_form != GDN_DECAY_COEF)
         return fail(GDN_ERR_INVALID_ARG, fn, "decay_form %d is not a gdn_decay_form", d->decay_form);
+    if (d->decay_per_channel != 0 && d->decay_per_channel != 1)
+        return fail(GDN_ERR_INVALID_ARG, fn, "decay_per_channel must be 0 or 1");
     if (!(d->l2_eps > 0.f) || !std::isfinite(d->l2_eps) || !(d->rms_eps > 0.f) ||
         !std::isfinite(d->rms_eps))
         return fail(GDN_ERR_INVALID_ARG, fn, "eps values must be finite and > 0");
@@ -81,7 +83,8 @@ bool ranges_overlap(const void* a, const void* b, size_t bytes) {
 // state once and has no chunk to fill, is the faster one.
 constexpr int kShortPrefill = 16;
 bool use_chunked(const gdn_dims* d, int n_seq, const int32_t* cu_host) {
-    if (!gdn::chunked_supported(d->d_k, d->d_v, d->n_k_heads, d->n_v_heads, d->dtype == GDN_DTYPE_BF16))
+    if (!gdn::chunked_supported(d->d_k, d->d_v, d->n_k_heads, d->n_v_heads, d->dtype == GDN_DTYPE_BF16) ||
+        d->decay_per_channel)
         return false;
     for (int i = 0; i < n_seq; ++i)
         if (cu_host[i + 1] - cu_host[i] > kShortPrefill) return true;
@@ -268,6 +271,7 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_se
     p.n_k_heads = dims->n_k_heads; p.n_v_heads = dims->n_v_heads;
     p.d_k = dims->d_k; p.d_v = dims->d_v; p.conv_k = dims->conv_k; p.l2_eps = dims->l2_eps;
     p.cu_seqlens = cu_seqlens; p.x = x; p.a = a; p.b = b; p.decay_form = dims->decay_form;
+    p.per_channel = dims->decay_per_channel;
     p.conv_w = params->conv_w; p.A_log = params->A_log; p.dt_bias = params->dt_bias;
     p.conv_state_in = conv_state_in; p.qkv_out = qkv_out; p.g_out = g_out; p.beta_out = beta_out;
     if ((st = cuda_status(timed_launch("conv_prologue", s, [&] { return gdn::launch_conv_prologue(p, bf16, s); }), fn, "conv prologue launch")) != GDN_OK)
@@ -363,6 +367,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
     r.head_map = dims->head_map; r.decay_form = dims->decay_form;
+    r.per_channel = dims->decay_per_channel;
     r.cu_seqlens = cu_seqlens; r.uniform_T = 0;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
@@ -408,6 +413,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
     r.head_map = dims->head_map; r.decay_form = dims->decay_form;
+    r.per_channel = dims->decay_per_channel;
     r.cu_seqlens = nullptr; r.uniform_T = T;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;
@@ -454,6 +460,7 @@ gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_
     r.n_seq = n_seq; r.n_k_heads = dims->n_k_heads; r.n_v_heads = dims->n_v_heads;
     r.conv_k = dims->conv_k; r.act = dims->act; r.l2_eps = dims->l2_eps; r.rms_eps = dims->rms_eps;
     r.head_map = dims->head_map; r.decay_form = dims->decay_form;
+    r.per_channel = dims->decay_per_channel;
     r.cu_seqlens = nullptr; r.uniform_T = T;
     r.x = x; r.z = z; r.a = a; r.b = b;
     r.conv_w = params->conv_w; r.A_log = params->A_log; r.dt_bias = params->dt_bias;

@@ -60,13 +60,15 @@ conv_prologue_kernel(ConvArgs p) {
         const int hv_n = p.n_v_heads;
         const T* __restrict__ a = static_cast<const T*>(p.a);
         const T* __restrict__ b = static_cast<const T*>(p.b);
-        for (int i = threadIdx.x; i < kConvTokTile * hv_n; i += kConvThreads) {
-            const int t = tile0 + i / hv_n;
-            const int h = i % hv_n;
+        const int nc = p.per_channel ? p.d_k : 1;  // decays per value head
+        for (int i = threadIdx.x; i < kConvTokTile * hv_n * nc; i += kConvThreads) {
+            const int t = tile0 + i / (hv_n * nc);
+            const int h = (i / nc) % hv_n, j = i % nc;
             if (t >= p.n_tokens) break;
             const size_t idx = (size_t)t * hv_n + h;
-            p.g_out[idx] = log_decay(to_f32(a[idx]), p.A_log[h], p.dt_bias[h], p.decay_form);
-            p.beta_out[idx] = sigmoidf_(to_f32(b[idx]));
+            p.g_out[idx * nc + j] = log_decay(to_f32(a[idx * nc + j]), p.A_log[h],
+                                              p.dt_bias[(size_t)h * nc + j], p.decay_form);
+            if (j == 0) p.beta_out[idx] = sigmoidf_(to_f32(b[idx]));
         }
         return;
     }

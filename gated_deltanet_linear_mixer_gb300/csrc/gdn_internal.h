@@ -15,6 +15,7 @@ constexpr int kChunkTokens = 64;
 struct ConvArgs {
     int n_seq, n_tokens, n_k_heads, n_v_heads, d_k, d_v, conv_k;
     int decay_form;             // gdn_decay_form
+    int per_channel;            // one decay per key channel: a [T, Hv*dk], g_out [T, Hv*dk]
     float l2_eps;
     const int32_t* cu_seqlens;  // [n_seq+1]
     const void* x;              // [T, CD]
@@ -54,6 +55,7 @@ struct ConvStateArgs {
 struct RecurrentArgs {
     int n_seq, n_k_heads, n_v_heads, conv_k, act;
     int head_map, decay_form;   // gdn_head_map, gdn_decay_form
+    int per_channel;            // one decay per key channel (a [T, Hv*dk], dt_bias [Hv*dk])
     float l2_eps, rms_eps;
     const int32_t* cu_seqlens;  // [n_seq+1], or null with uniform_T tokens per sequence
     int uniform_T;

@@ -92,6 +92,8 @@ extern "C" gdn_status gdn_layer_prefill(const gdn_dims* dims, const gdn_params* 
     if (st != GDN_OK) return st;
     if (dims->dtype != GDN_DTYPE_BF16)
         return gdn::set_error(GDN_ERR_UNSUPPORTED, fn, "the layer runs on bf16 activations only");
+    if (dims->decay_per_channel)
+        return gdn::set_error(GDN_ERR_UNSUPPORTED, fn, "per-channel decays are not built into the layer");
     if (!proj || !proj->w_qkv || !proj->w_z || !proj->w_a || !proj->w_b || !proj->w_out)
         return gdn::set_error(GDN_ERR_INVALID_ARG, fn, "a projection weight is NULL");
     if (!aligned16(proj->w_qkv) || !aligned16(proj->w_z) || !aligned16(proj->w_a) ||

@@ -36,6 +36,7 @@ recurrent_kernel(RecurrentArgs p) {
 
     __shared__ float cbuf[kRecTokBlock][CH];
     __shared__ float gam[kRecTokBlock], bet[kRecTokBlock], kqs[kRecTokBlock];
+    __shared__ float gamc[kRecTokBlock][DK];  // per key channel (p.per_channel)
     __shared__ float red[NW][2][DV];
     __shared__ __align__(16) float dlt[DV];  // read back as float4
     __shared__ float ysum[DV / 32];
@@ -102,8 +103,18 @@ recurrent_kernel(RecurrentArgs p) {
         }
         if (tid < nb) {
             const size_t gi = (size_t)(bos + t0 + tid) * hv_n + hv;
-            gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv], p.decay_form));
+            if (!p.per_channel)
+                gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv], p.decay_form));
             bet[tid] = sigmoidf_(to_f32(bv[gi]));
+        }
+        if (p.per_channel) {  // S <- diag(e^{g_t}) S: one decay per key channel (state row)
+            for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
+                const int tau = idx / DK, r = idx % DK;
+                const size_t gi = ((size_t)(bos + t0 + tau) * hv_n + hv) * DK + r;
+                gamc[tau][r] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[(size_t)hv * DK + r],
+                                              p.decay_form));
+            }
+            if (tid < nb) gam[tid] = 1.f;  // the decay sits on the rows instead
         }
         __syncthreads();
         // ---- L2-normalise q and k of each token (one warp per token), k.q
@@ -133,12 +144,15 @@ recurrent_kernel(RecurrentArgs p) {
         // ---- the delta rule, token by token
         for (int tau = 0; tau < nb; ++tau) {
             const int t = bos + t0 + tau;
-            const float gm = gam[tau], bt = bet[tau];
+            const float gm = gam[tau], bt = bet[tau], gm_h = gm;
             float kv[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const int r = rg + RG * i;
-                const float kr = cbuf[tau][DK + r], qr = cbuf[tau][r];
+                // with per-channel decays, S^T k and S^T q of the decayed state
+                // fold row r's decay into k_r and q_r
+                const float fr = p.per_channel ? gamc[tau][r] : 1.f;
+                const float kr = cbuf[tau][DK + r] * fr, qr = cbuf[tau][r] * fr;
                 kv[0] = fmaf(s[i].x, kr, kv[0]); sq[0] = fmaf(s[i].x, qr, sq[0]);
                 kv[1] = fmaf(s[i].y, kr, kv[1]); sq[1] = fmaf(s[i].y, qr, sq[1]);
                 kv[2] = fmaf(s[i].z, kr, kv[2]); sq[2] = fmaf(s[i].z, qr, sq[2]);
@@ -188,6 +202,7 @@ recurrent_kernel(RecurrentArgs p) {
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const float kr = cbuf[tau][DK + rg + RG * i];
+                const float gm = p.per_channel ? gamc[tau][rg + RG * i] : gm_h;
                 s[i].x = fmaf(gm, s[i].x, kr * dv4.x);
                 s[i].y = fmaf(gm, s[i].y, kr * dv4.y);
                 s[i].z = fmaf(gm, s[i].z, kr * dv4.z);

@@ -86,6 +86,13 @@ typedef struct gdn_dims {
     float rms_eps;     /* gated RMSNorm eps (1e-6 / rms_norm_eps) */
     int32_t head_map;  /* gdn_head_map; 0 (contiguous) when zero-initialised */
     int32_t decay_form; /* gdn_decay_form; 0 (A_log) when zero-initialised */
+    /* 1: one decay per key channel (the per-channel decayed delta rule of the
+     * pages' Kimi Delta Attention mixer, qwen.rs Mixer::Kda): S <- diag(e^g) S
+     * with g [T, Hv, dk] = coef[h] softplus(a[t, h, i] + dt_bias[h, i]); the
+     * gate input a is then [T, Hv*dk] and dt_bias [Hv*dk] (b stays [T, Hv]).
+     * Runs on the token-recurrent kernel; gdn_layer_prefill refuses it.
+     * 0 (one decay per value head) when zero-initialised. */
+    int32_t decay_per_channel;
 } gdn_dims;
 
 /* Per-layer parameters, fp32 device pointers (qwen.rs loader: conv1d.weight

@@ -47,7 +47,8 @@ class _Dims(ctypes.Structure):
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("conv_k", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("l2_eps", ctypes.c_double), ("rms_eps", ctypes.c_double),
-                ("tiled", ctypes.c_int32), ("decay_coef", ctypes.c_int32)]
+                ("tiled", ctypes.c_int32), ("decay_coef", ctypes.c_int32),
+                ("per_channel", ctypes.c_int32)]
 
 
 def _load():
@@ -83,6 +84,7 @@ class Dims:
     rms_eps: float = 1e-6
     head_map: str = "contiguous"  # key head of value head h: h // (Hv/Hk), or h % Hk ("tiled")
     decay_form: str = "A_log"     # A_log holds log A, or the decay coefficient itself ("coef")
+    per_channel_decay: bool = False  # one decay per key channel: a [T, Hv, dk], dt_bias [Hv, dk]
 
     @property
     def conv_dim(self) -> int:
@@ -95,7 +97,8 @@ class Dims:
             raise ValueError("head_map must be 'contiguous' or 'tiled', decay_form 'A_log' or 'coef'")
         return _Dims(self.n_k_heads, self.n_v_heads, self.d_k, self.d_v, self.conv_k,
                      1 if self.act == "sigmoid" else 0, self.l2_eps, self.rms_eps,
-                     1 if self.head_map == "tiled" else 0, 1 if self.decay_form == "coef" else 0)
+                     1 if self.head_map == "tiled" else 0, 1 if self.decay_form == "coef" else 0,
+                     1 if self.per_channel_decay else 0)
 
 
 def _f64(a):
@@ -141,11 +144,12 @@ def normalize(d: Dims, c):
 
 
 def gates(d: Dims, a, b, A_log, dt_bias):
-    """Step a4. Returns (g, beta), each [T, Hv]."""
+    """Step a4. Returns (g, beta), each [T, Hv]; g is [T, Hv, dk] with a decay
+    per key channel (then a is [T, Hv*dk] and dt_bias [Hv*dk])."""
     lib = _load()
     a, b, A_log, dt_bias = _f64(a), _f64(b), _f64(A_log), _f64(dt_bias)
     t = a.shape[0]
-    g = np.empty((t, d.n_v_heads))
+    g = np.empty((t, d.n_v_heads, d.d_k) if d.per_channel_decay else (t, d.n_v_heads))
     beta = np.empty((t, d.n_v_heads))
     dd = d._c()
     lib.oracle_gates(ctypes.byref(dd), t, _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g),
@@ -206,7 +210,7 @@ def gdn(d: Dims, cu_seqlens, x, z, a, b, conv_w, A_log, dt_bias, norm_w,
         res["q_hat"] = np.empty((t, d.n_k_heads, d.d_k))
         res["k_hat"] = np.empty((t, d.n_k_heads, d.d_k))
         res["v"] = np.empty((t, d.n_v_heads, d.d_v))
-        res["g"] = np.empty((t, d.n_v_heads))
+        res["g"] = np.empty((t, d.n_v_heads, d.d_k) if d.per_channel_decay else (t, d.n_v_heads))
         res["beta"] = np.empty((t, d.n_v_heads))
     dd = d._c()
     rc = lib.oracle_gdn(ctypes.byref(dd), n, _ptr(cu), _ptr(x), _ptr(z), _ptr(a), _ptr(b),

@@ -48,6 +48,7 @@ typedef struct {
     double rms_eps;     /* 1e-6 on cpu.rs; rms_norm_eps on qwen.rs */
     int32_t tiled;      /* key head of value head hv: hv % Hk if 1, hv / (Hv/Hk) if 0 */
     int32_t decay_coef; /* A_log[] holds the decay coefficient itself if 1 */
+    int32_t per_channel; /* 1: a decay per key channel (a [T,Hv,dk], dt_bias [Hv,dk]) */
 } oracle_dims;
 
 static int conv_dim(const oracle_dims* d) {
@@ -167,12 +168,14 @@ void oracle_normalize(const oracle_dims* d, int n_tok, const double* c,
 void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double* b,
                   const double* A_log, const double* dt_bias, double* g, double* beta) {
     const int hv_n = d->n_v_heads;
+    const int nc = d->per_channel ? d->d_k : 1; /* decays per value head */
     for (int t = 0; t < n_tok; ++t) {
         for (int h = 0; h < hv_n; ++h) {
             const size_t i = (size_t)t * hv_n + h;
             beta[i] = sigmoid(b[i]);
             const double coef = d->decay_coef ? A_log[h] : -exp(A_log[h]);
-            g[i] = coef * softplus(a[i] + dt_bias[h]);
+            for (int j = 0; j < nc; ++j)
+                g[i * nc + j] = coef * softplus(a[i * nc + j] + dt_bias[(size_t)h * nc + j]);
         }
     }
 }
@@ -218,11 +221,13 @@ void oracle_recurrence(const oracle_dims* d, int n_seq, const int32_t* cu_seqlen
                 const double* qh = q_hat + (t * hk_n + hk) * dk;
                 const double* kh = k_hat + (t * hk_n + hk) * dk;
                 const double* vh = v + (t * hv_n + hv) * dv;
-                const double decay = exp(g[t * hv_n + hv]);
+                /* one decay per value head, or one per key channel (row ik) */
+                const double* gt = g + (t * hv_n + hv) * (d->per_channel ? dk : 1);
                 const double bt = beta[t * hv_n + hv];
                 for (int iv = 0; iv < dv; ++iv) kv_mem[iv] = 0.0;
                 for (int ik = 0; ik < dk; ++ik) {
                     double* row = s + (size_t)ik * dv;
+                    const double decay = exp(gt[d->per_channel ? ik : 0]);
                     for (int iv = 0; iv < dv; ++iv) {
                         row[iv] *= decay;
                         kv_mem[iv] += row[iv] * kh[ik];
@@ -294,11 +299,12 @@ int oracle_gdn(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
     const size_t key_n = n_tok * d->n_k_heads * d->d_k;
     const size_t val_n = n_tok * d->n_v_heads * d->d_v;
     const size_t gate_n = n_tok * d->n_v_heads;
+    const size_t decay_n = gate_n * (d->per_channel ? d->d_k : 1);
     double* c = (double*)malloc(sizeof(double) * (n_tok * cd + 1));
     double* qh = q_hat_out ? q_hat_out : (double*)malloc(sizeof(double) * (key_n + 1));
     double* kh = k_hat_out ? k_hat_out : (double*)malloc(sizeof(double) * (key_n + 1));
     double* vv = v_out ? v_out : (double*)malloc(sizeof(double) * (val_n + 1));
-    double* gg = g_out ? g_out : (double*)malloc(sizeof(double) * (gate_n + 1));
+    double* gg = g_out ? g_out : (double*)malloc(sizeof(double) * (decay_n + 1));
     double* bb = beta_out ? beta_out : (double*)malloc(sizeof(double) * (gate_n + 1));
     double* o = (double*)malloc(sizeof(double) * (val_n + 1));
     int rc = 0;

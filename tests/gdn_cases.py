@@ -51,7 +51,8 @@ def dims(case):
     decay_form (the ABI options), else the defaults."""
     tdt = torch.bfloat16 if case.dtype == "bf16" else torch.float32
     opt = dict(head_map=getattr(case, "head_map", "contiguous"),
-               decay_form=getattr(case, "decay_form", "A_log"))
+               decay_form=getattr(case, "decay_form", "A_log"),
+               per_channel_decay=getattr(case, "per_channel_decay", False))
     d = gdn.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, tdt, case.act,
                  **opt)
     od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act,

@@ -313,6 +313,39 @@ def test_decode_tiled_head_map_and_decay_coef_match_oracle():
     assert rel_err(got["inter"], ref["inter"].reshape(n, tt, *ref["inter"].shape[1:])) <= TOL["bf16"]
 
 
+def _per_channel(case, seed):
+    """The case with one decay per key channel: gate inputs a [T, Hv*dk] ~N(0,1)
+    (bf16-rounded for bf16 cases) and dt_bias [Hv*dk] ~N(0, 0.1)."""
+    rng = np.random.default_rng(seed)
+    a = rng.normal(size=(case.a.shape[0], case.n_v_heads * case.d_k))
+    case.a = workloads.round_bf16(a.astype(np.float32)).astype(np.float64) if case.dtype == "bf16" else a
+    case.dt_bias = rng.normal(0, 0.1, case.n_v_heads * case.d_k)
+    case.per_channel_decay = True
+    return case
+
+
+@pytest.mark.parametrize("name", ["ragged_bf16_d128_states", "bf16_slow_decay_long",
+                                  "f32_slow_decay", "tc_gqa_R8"])
+def test_prefill_per_channel_decay_matches_oracle(name):
+    """One decay per key channel (token-recurrent kernel, also for d=128 bf16)."""
+    case = _per_channel(PREFILL_CASES[name](), seed=91)
+    ref = run_oracle(case)
+    got = gpu_prefill(case)
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+
+
+def test_decode_per_channel_decay_matches_oracle():
+    case = _per_channel(_gen("dp", mode="decode", n_seq=4, tokens_per_seq=4, act="sigmoid",
+                             state_std=0.05, conv_state_std=1.0, seed=29, want_inter=True), seed=92)
+    ref = run_oracle(case, want_inter=True)
+    got = gpu_decode(case, inter=True)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    n, tt = case.n_seq, case.tokens_per_seq
+    assert rel_err(got["inter"], ref["inter"].reshape(n, tt, *ref["inter"].shape[1:])) <= TOL["bf16"]
+
+
 TC_CASES = sorted(k for k in PREFILL_CASES if k.startswith("tc_"))
 
 

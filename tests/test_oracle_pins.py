@@ -468,6 +468,44 @@ def test_decay_coefficient_form_equals_A_log_form():
     np.testing.assert_allclose(r2["out"], r1["out"], rtol=1e-12, atol=1e-14)
 
 
+def test_per_channel_decay_with_equal_channels_is_the_scalar_rule():
+    """One decay per key channel, all channels of a value head given the same
+    gate input and bias: exactly the one-decay-per-head rule."""
+    d = _dims()
+    d_pc = oracle.Dims(d.n_k_heads, d.n_v_heads, d.d_k, d.d_v, d.conv_k, d.act,
+                       per_channel_decay=True)
+    case = _rng_case(d, [8, 5], seed=78)
+    a_pc = np.repeat(case["a"], d.d_k, axis=1)
+    dtb_pc = np.repeat(case["dt_bias"], d.d_k)
+    run = lambda dd, a, dtb: oracle.gdn(dd, case["cu"], case["x"], case["z"], a, case["b"],  # noqa: E731
+                                         case["conv_w"], case["A_log"], dtb, case["norm_w"],
+                                         case["conv_state"], case["state"])
+    r1, r2 = run(d, case["a"], case["dt_bias"]), run(d_pc, a_pc, dtb_pc)
+    np.testing.assert_array_equal(r2["out"], r1["out"])
+    np.testing.assert_array_equal(r2["state"], r1["state"])
+
+
+def test_per_channel_decay_without_writes_decays_each_state_row():
+    """beta = 0: the state only decays, row i (key channel i) by exp(sum_t g[t, h, i]),
+    and the readout is the decayed state read by q (closed form)."""
+    d = oracle.Dims(1, 2, 8, 4, 4, "silu", per_channel_decay=True)
+    rng = np.random.default_rng(79)
+    t = 6
+    q = rng.normal(size=(t, 1, 8))
+    k = rng.normal(size=(t, 1, 8))
+    v = rng.normal(size=(t, 2, 4))
+    g = -rng.uniform(0, 1, size=(t, 2, 8))
+    s0 = rng.normal(size=(1, 2, 8, 4))
+    o, s1, _ = oracle.recurrence(d, [0, t], q, k, v, g, np.zeros((t, 2)), s0)
+    cum = np.cumsum(g, axis=0)  # [t, h, i]
+    want_s = s0[0] * np.exp(cum[-1])[:, :, None]
+    np.testing.assert_allclose(s1[0], want_s, rtol=1e-13, atol=1e-15)
+    for tt in range(t):
+        st = s0[0] * np.exp(cum[tt])[:, :, None]  # [h, i, dv]
+        want_o = np.einsum("hij,i->hj", st, q[tt, 0])
+        np.testing.assert_allclose(o[tt], want_o, rtol=1e-12, atol=1e-14)
+
+
 def test_decode_steps_equal_one_prefill():
     """T one-token calls carrying (state, conv state) == one T-token call, and the
     per-token intermediate states equal the states after each single step."""
