@@ -1116,8 +1116,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                   ChunkArgs p) {
+    // sequences with the most chunks start first: the last wave is shorter
     chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
-                    blockIdx.x / kSplit, blockIdx.y);
+                    blockIdx.x / kSplit, p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y);
 }
 
 // ------------------------------------------------------------- chunk_fused
@@ -1164,6 +1165,7 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.beta = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.cu_chunks = off; off = up(off + (size_t)(n_seq + 1) * 4);
     l.chunk_info = off; off = up(off + (size_t)chunks * 8);
+    l.seq_order = off; off = up(off + (size_t)n_seq * 4);
     l.w_hi = off; off = up(off + crow * kD * 2);
     l.w_lo = off; off = up(off + crow * kD * 2);
     l.u = off; off = up(off + crow * kD * 4);
@@ -1243,6 +1245,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         cv.chunk_info = reinterpret_cast<int2*>(ws + l.chunk_info);
         cv.ready = reinterpret_cast<int*>(ws + l.ready);
         cv.n_ready = l.n_chunks * hk_n;
+        // a longest-first launch order for the two-kernel scan (quadratic in
+        // the sequence count, so only for batches of up to 1024 sequences)
+        if (a.n_seq > 1 && a.n_seq <= 1024) cv.seq_order = reinterpret_cast<int32_t*>(ws + l.seq_order);
     }
     cudaError_t e = timed_launch("conv_prologue", st, [&] { return launch_conv_prologue(cv, true, st); });
     if (e != cudaSuccess) return e;
@@ -1255,6 +1260,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.head_map = a.head_map;
     p.cu_seqlens = a.cu_seqlens; p.cu_chunks = cu_chunks;
     p.chunk_info = reinterpret_cast<const int2*>(ws + l.chunk_info);
+    p.seq_order = cv.seq_order;
     p.qkv_hi = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_hi);
     p.qkv_lo = reinterpret_cast<const __nv_bfloat16*>(ws + l.qkv_lo);
     p.g = reinterpret_cast<const float*>(ws + l.g);

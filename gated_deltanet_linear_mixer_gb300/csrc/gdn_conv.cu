@@ -220,6 +220,17 @@ __device__ void chunk_table_cta(const ConvArgs& p) {
         __syncthreads();
     }
     const int n_chunks = p.n_seq > 0 ? p.cu_chunks[p.n_seq] : 0;
+    if (p.seq_order) {  // rank of sequence i: longer ones first, ties in index order
+        for (int i = tid; i < p.n_seq; i += 256) {
+            const int ci = p.cu_chunks[i + 1] - p.cu_chunks[i];
+            int rank = 0;
+            for (int j = 0; j < p.n_seq; ++j) {
+                const int cj = p.cu_chunks[j + 1] - p.cu_chunks[j];
+                rank += cj > ci || (cj == ci && j < i);
+            }
+            p.seq_order[rank] = i;
+        }
+    }
     for (int c = tid; c < n_chunks; c += 256) {
         const int n = seq_of_token(p.cu_chunks, p.n_seq, c);
         const int t0 = p.cu_seqlens[n] + (c - p.cu_chunks[n]) * kChunkTokens;

@@ -37,6 +37,7 @@ struct ConvArgs {
     int2* chunk_info;           // [chunks]
     int* ready;
     int n_ready;
+    int32_t* seq_order;         // [n_seq] sequences by chunk count, longest first, or null
     // New conv history [N, CD, K-1], written by an extra CTA row of the d=128
     // prologue; only when it does not alias conv_state_in (else null)
     void* conv_state_out;
@@ -90,6 +91,7 @@ struct ChunkArgs {
     const int32_t* cu_seqlens;    // [n_seq+1]
     const int32_t* cu_chunks;     // [n_seq+1] chunk offsets (workspace)
     const int2* chunk_info;       // [chunks] first token and length of each chunk (workspace)
+    const int32_t* seq_order;     // [n_seq] scan launch order (longest first), or null
     const __nv_bfloat16* qkv_hi;  // [T, CD] normalised q | k | v, hi part (workspace)
     const __nv_bfloat16* qkv_lo;  // [T, CD] lo part (workspace)
     const float* g;               // [T, Hv] log-decay (workspace)
@@ -110,8 +112,8 @@ struct ChunkArgs {
 
 // Byte offsets of the chunked path's workspace regions.
 struct ChunkLayout {
-    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, chunk_info, w_hi, w_lo, u, qk_hi, qk_lo, kw_hi, kw_lo,
-        gcum, ready, total;
+    size_t qkv_hi, qkv_lo, g, beta, cu_chunks, chunk_info, seq_order, w_hi, w_lo, u, qk_hi, qk_lo,
+        kw_hi, kw_lo, gcum, ready, total;
     int n_chunks;
 };
 
