@@ -134,3 +134,88 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(RuntimeError, match="not found"):
         gdn.load(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(head_map=2), "head_map"),
+    (dict(decay_form=-1), "decay_form"),
+    (dict(decay_per_channel=2), "decay_per_channel"),
+])
+def test_bad_options_are_rejected(lib, kw, msg):
+    assert _prefill(lib, _dims(**kw)) == 1
+    assert msg in lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("T", [0, 17])
+def test_verify_token_count_is_checked(lib, T):
+    d = _dims()
+    st = lib.gdn_verify(ctypes.byref(d), ctypes.byref(PARAMS), 4, T, FAKE, FAKE, FAKE, FAKE,
+                        FAKE, None, FAKE, None)
+    assert st == 1 and "T must be" in lib.gdn_last_error().decode()
+
+
+def test_verify_pointer_checks(lib):
+    d = _dims()
+    assert lib.gdn_verify(ctypes.byref(d), ctypes.byref(PARAMS), 0, 4, None, None, None, None,
+                          None, None, None, None) == 0
+    assert lib.gdn_verify(ctypes.byref(d), ctypes.byref(PARAMS), 2, 4, FAKE, FAKE, FAKE, FAKE,
+                          None, None, FAKE, None) == 1
+    assert "NULL" in lib.gdn_last_error().decode()
+    assert lib.gdn_verify(ctypes.byref(d), ctypes.byref(PARAMS), 2, 4, FAKE, FAKE, FAKE, FAKE,
+                          ctypes.c_void_p(0x10008), None, FAKE, None) == 1
+    assert "aligned" in lib.gdn_last_error().decode()
+
+
+def _proj(addr=0x10000):
+    p = ctypes.c_void_p(addr)
+    return gdn._Proj(p, p, p, p, p)
+
+
+def _layer(lib, d, proj, hidden=64, n_seq=1, cu_host=(0, 4), ws=None, ws_bytes=0):
+    cu = (ctypes.c_int32 * len(cu_host))(*cu_host)
+    return lib.gdn_layer_prefill(ctypes.byref(d), ctypes.byref(PARAMS),
+                                 ctypes.byref(proj) if proj is not None else None, hidden, n_seq,
+                                 FAKE, ctypes.cast(cu, ctypes.c_void_p), FAKE, None, None, None,
+                                 None, FAKE, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("hidden", [0, 7, 12, -8])
+def test_layer_hidden_is_checked(lib, hidden):
+    d = _dims()
+    cu = (ctypes.c_int32 * 2)(0, 4)
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_layer_prefill_workspace_size(ctypes.byref(d), hidden, 1,
+                                                ctypes.cast(cu, ctypes.c_void_p),
+                                                ctypes.byref(n)) == 1
+    assert "hidden" in lib.gdn_last_error().decode()
+
+
+def test_layer_workspace_covers_the_core(lib):
+    d = _dims()
+    cu = (ctypes.c_int32 * 3)(0, 4096, 5000)
+    core, layer = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), 2, ctypes.cast(cu, ctypes.c_void_p),
+                                          ctypes.byref(core)) == 0
+    assert lib.gdn_layer_prefill_workspace_size(ctypes.byref(d), 2048, 2,
+                                                ctypes.cast(cu, ctypes.c_void_p),
+                                                ctypes.byref(layer)) == 0
+    # x, z, a, b and y (bf16) plus the core's own workspace, all inside the layer's
+    cd = 2 * 16 * 128 + 32 * 128
+    act = 5000 * (cd + 2 * 32 * 128 + 2 * 32) * 2
+    assert layer.value >= core.value + act and layer.value % 256 == 0
+
+
+def test_layer_refusals(lib):
+    assert _layer(lib, _dims(dtype=0), _proj()) == 2
+    assert "bf16" in lib.gdn_last_error().decode()
+    assert _layer(lib, _dims(decay_per_channel=1), _proj()) == 2
+    assert "per-channel" in lib.gdn_last_error().decode()
+    assert _layer(lib, _dims(), None) == 1
+    assert "projection" in lib.gdn_last_error().decode()
+    assert _layer(lib, _dims(), _proj(0x10004)) == 1
+    assert "aligned" in lib.gdn_last_error().decode()
+    # no sequences: nothing to do, and no cuBLAS handle is created
+    assert _layer(lib, _dims(), _proj(), n_seq=0, cu_host=(0,)) == 0
+    # too small a workspace is refused before any launch
+    assert _layer(lib, _dims(), _proj(), ws=FAKE, ws_bytes=256) == 4
+    assert "workspace" in lib.gdn_last_error().decode()
