@@ -15,7 +15,9 @@ publish no GPU implementation of this core), on a bounded sample per step.
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and a
 device synchronize; a 256 MiB buffer (2x L2) is written between timed steps
-and each step is bracketed by CUDA events on the launching stream.
+and each step is bracketed by CUDA events on the launching stream.  The
+per-kernel durations come from a second pass of the same K steps with
+libgdn's per-launch events switched on, which the step time leaves out.
 """
 from __future__ import annotations
 
@@ -310,6 +312,10 @@ class ClockSampler:
 
 # -------------------------------------------------------------------- timing
 
+KERNEL_TIMING = ("per-launch CUDA events on the launch stream, over a second timed pass of the "
+                 "same K steps (the step time is taken without them)")
+
+
 def _flush(buf):
     buf.add_(1)
 
@@ -321,6 +327,9 @@ def time_steps(fn, steps, warmup, flush_buf, stream, barrier):
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
+    # one extra flush queued ahead: the first timed step's launches are
+    # enqueued while the GPU is still busy, as those of every later step are
+    _flush(flush_buf)
     evs = []
     for _ in range(steps):
         _flush(flush_buf)
@@ -413,8 +422,13 @@ def run_gpu(args):
         r.step()  # one untimed call: one-time costs (module loading, library setup) stay out
         torch.cuda.synchronize()
         t_start = time.time()
-        gdn.timing_enable(True)
+        # the step time, without per-launch instrumentation (the library's
+        # timing events between launches cost a few microseconds each)
         ms = time_steps(r.step, args.steps, args.warmup, flush_buf, stream, barrier)
+        # the same K steps again with a CUDA event pair around every launch,
+        # recorded on its stream: per-kernel durations for the roofline
+        gdn.timing_enable(True)
+        time_steps(r.step, args.steps, args.warmup, flush_buf, stream, barrier)
         rep = gdn.timing_report()
         gdn.timing_enable(False)
         t_stop = time.time()
@@ -441,14 +455,15 @@ def run_gpu(args):
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["bf16_tflops"], "traffic": TRAFFIC.get((r.key, dom_name)),
                     "peak_source": peaks["source"] + " (bf16 burst)",
-                    "useful_flops_per_launch": fl, "kernel_ms": dom_avg_ms, "kernel_share": share}
+                    "useful_flops_per_launch": fl, "kernel_ms": dom_avg_ms, "kernel_share": share,
+                    "kernel_timing": KERNEL_TIMING}
         else:
             achieved = kb / (dom_avg_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                     "traffic": TRAFFIC.get((r.key, dom_name)), "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": kb, "kernel_ms": dom_avg_ms,
-                    "kernel_share": share}
+                    "kernel_share": share, "kernel_timing": KERNEL_TIMING}
         step_bytes = r.algorithmic_bytes()
         res = {
             "value": tok_s, "unit": UNIT, "ms_per_step": t_max,
@@ -577,7 +592,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay,layer",

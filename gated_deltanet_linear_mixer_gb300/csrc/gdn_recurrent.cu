@@ -24,7 +24,9 @@ namespace gdn {
 constexpr int kRecThreads = 256;
 constexpr int kRecTokBlock = 8;  // tokens whose prologue is computed together
 
-template <int DK, int DV, typename T>
+// PC: one decay per key channel (p.per_channel), a separate instance so that
+// the scalar-decay kernel carries none of its work.
+template <int DK, int DV, typename T, bool PC>
 __global__ void __launch_bounds__(kRecThreads, 2)
 recurrent_kernel(RecurrentArgs p) {
     constexpr int L = DV / 4;            // lanes per state row
@@ -36,7 +38,7 @@ recurrent_kernel(RecurrentArgs p) {
 
     __shared__ float cbuf[kRecTokBlock][CH];
     __shared__ float gam[kRecTokBlock], bet[kRecTokBlock], kqs[kRecTokBlock];
-    __shared__ float gamc[kRecTokBlock][DK];  // per key channel (p.per_channel)
+    __shared__ float gamc[PC ? kRecTokBlock : 1][PC ? DK : 1];  // per key channel
     __shared__ float red[NW][2][DV];
     __shared__ __align__(16) float dlt[DV];  // read back as float4
     __shared__ float ysum[DV / 32];
@@ -103,11 +105,11 @@ recurrent_kernel(RecurrentArgs p) {
         }
         if (tid < nb) {
             const size_t gi = (size_t)(bos + t0 + tid) * hv_n + hv;
-            if (!p.per_channel)
+            if (!PC)
                 gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv], p.decay_form));
             bet[tid] = sigmoidf_(to_f32(bv[gi]));
         }
-        if (p.per_channel) {  // S <- diag(e^{g_t}) S: one decay per key channel (state row)
+        if (PC) {  // S <- diag(e^{g_t}) S: one decay per key channel (state row)
             for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
                 const int tau = idx / DK, r = idx % DK;
                 const size_t gi = ((size_t)(bos + t0 + tau) * hv_n + hv) * DK + r;
@@ -151,7 +153,7 @@ recurrent_kernel(RecurrentArgs p) {
                 const int r = rg + RG * i;
                 // with per-channel decays, S^T k and S^T q of the decayed state
                 // fold row r's decay into k_r and q_r
-                const float fr = p.per_channel ? gamc[tau][r] : 1.f;
+                const float fr = PC ? gamc[tau][r] : 1.f;
                 const float kr = cbuf[tau][DK + r] * fr, qr = cbuf[tau][r] * fr;
                 kv[0] = fmaf(s[i].x, kr, kv[0]); sq[0] = fmaf(s[i].x, qr, sq[0]);
                 kv[1] = fmaf(s[i].y, kr, kv[1]); sq[1] = fmaf(s[i].y, qr, sq[1]);
@@ -202,7 +204,7 @@ recurrent_kernel(RecurrentArgs p) {
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const float kr = cbuf[tau][DK + rg + RG * i];
-                const float gm = p.per_channel ? gamc[tau][rg + RG * i] : gm_h;
+                const float gm = PC ? gamc[tau][rg + RG * i] : gm_h;
                 s[i].x = fmaf(gm, s[i].x, kr * dv4.x);
                 s[i].y = fmaf(gm, s[i].y, kr * dv4.y);
                 s[i].z = fmaf(gm, s[i].z, kr * dv4.z);
@@ -229,7 +231,10 @@ static cudaError_t launch_recurrent_t(const RecurrentArgs& p, int dk, int dv, cu
     dim3 grid(p.n_v_heads, p.n_seq);
 #define GDN_REC_CASE(A, B)                                                        \
     if (dk == A && dv == B) {                                                     \
-        recurrent_kernel<A, B, T><<<grid, kRecThreads, 0, st>>>(p);               \
+        if (p.per_channel)                                                        \
+            recurrent_kernel<A, B, T, true><<<grid, kRecThreads, 0, st>>>(p);     \
+        else                                                                      \
+            recurrent_kernel<A, B, T, false><<<grid, kRecThreads, 0, st>>>(p);    \
         return cudaGetLastError();                                                \
     }
     GDN_REC_CASE(32, 32) GDN_REC_CASE(32, 64) GDN_REC_CASE(32, 128)
