@@ -41,10 +41,10 @@ METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
 # kernel exists; an entry is removed whenever its kernel changes).
 TRAFFIC = {
     # profiles/chunk_fused_prefill_T4096.md, the bench's own workload
-    ("prefill", "chunk_fused"): 312_234_240 + 212_412_672,
+    ("prefill", "chunk_fused"): 315_110_656 + 212_748_800,
     # profiles/recurrent_decode_N64.md (64 sequences; the traffic is per sequence,
     # so x 256/64 for the bench's 256)
-    ("decode", "recurrent"): (139_114_496 + 73_932_544) * 4,
+    ("decode", "recurrent"): (139_106_560 + 73_355_264) * 4,
 }
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
@@ -230,26 +230,56 @@ class Runner:
         return flops
 
     # -- end to end: pinned host buffers, H2D of the step's inputs, the call,
-    # D2H of the step's outputs.
+    # D2H of the step's outputs, pipelined as a serving loop runs them: the
+    # inputs of step i+1 are copied in and the output of step i-1 is read back
+    # on two copy streams while step i computes (two device buffer sets).
     def setup_e2e(self):
         torch = self.torch
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
-        self.d_in = [self.h] if self.key == "layer" else [self.x, self.z, self.a, self.b]
-        self.h_in = [pin(t) for t in self.d_in]
+        self.in_names = ["h"] if self.key == "layer" else ["x", "z", "a", "b"]
         # the step's result read back by the caller: the mixer (or layer) output
         # (states stay resident on the device for the next call)
-        outs = [self.layer_out] if self.key == "layer" else [self.out]
-        self.d_out = outs
-        self.h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+        self.out_names = ["layer_out"] if self.key == "layer" else ["out"]
+        self.sets = []
+        for k in range(2):
+            d_in = {n: getattr(self, n) if k == 0 else getattr(self, n).clone() for n in self.in_names}
+            d_out = {n: getattr(self, n) if k == 0 else torch.empty_like(getattr(self, n))
+                     for n in self.out_names}
+            h_in = {n: pin(t) for n, t in d_in.items()}
+            h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in d_out.items()}
+            self.sets.append((d_in, d_out, h_in, h_out))
+        self.h2d = sum(t.numel() * t.element_size() for t in self.sets[0][2].values())
+        self.d2h = sum(t.numel() * t.element_size() for t in self.sets[0][3].values())
+        self.s_in, self.s_out = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+        self.ev_in, self.ev_done, self.ev_read = ev(), ev(), ev()
+        self.e2e_i = 0
 
-    def e2e_step(self):
-        for h, d in zip(self.h_in, self.d_in):
-            d.copy_(h, non_blocking=True)
+    def e2e_step(self, stream, flush=None):
+        """One pipelined step on buffer set i % 2; `stream` is the compute stream."""
+        torch, k = self.torch, self.e2e_i % 2
+        d_in, d_out, h_in, h_out = self.sets[k]
+        if self.e2e_i >= 2:
+            self.s_in.wait_event(self.ev_done[k])   # step i-2 has read this input set
+        with torch.cuda.stream(self.s_in):
+            for n in self.in_names:
+                d_in[n].copy_(h_in[n], non_blocking=True)
+        self.ev_in[k].record(self.s_in)
+        stream.wait_event(self.ev_in[k])
+        if self.e2e_i >= 2:
+            stream.wait_event(self.ev_read[k])      # step i-2's output has been read back
+        if flush is not None:
+            _flush(flush)
+        for n in self.in_names + self.out_names:
+            setattr(self, n, (d_in | d_out)[n])
         self.step()
-        for d, h in zip(self.d_out, self.h_out):
-            h.copy_(d, non_blocking=True)
+        self.ev_done[k].record(stream)
+        self.s_out.wait_event(self.ev_done[k])
+        with torch.cuda.stream(self.s_out):
+            for n in self.out_names:
+                h_out[n].copy_(d_out[n], non_blocking=True)
+        self.ev_read[k].record(self.s_out)
+        self.e2e_i += 1
 
 
 # ------------------------------------------------------------------- clocks
@@ -343,6 +373,31 @@ def time_steps(fn, steps, warmup, flush_buf, stream, barrier):
     barrier()
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in evs]
+
+
+def time_e2e(r, steps, warmup, stream, barrier):
+    """Mean ms per step of K pipelined end-to-end steps: from an event before the
+    first input copy to one after the last output has been read back.  No L2
+    flush between steps (it would sit inside the timed span): every workload's
+    step touches more than L2 holds (its states or its workspace), and inputs
+    just copied in are where a serving loop finds them."""
+    import torch
+    for _ in range(warmup):
+        r.e2e_step(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    r.s_in.wait_stream(stream)   # the first copy starts after the start event
+    for _ in range(steps):
+        r.e2e_step(stream)
+    stream.wait_stream(r.s_out)  # the end event follows the last read-back
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
 
 
 def cpu_baseline(key, case, max_seconds=10.0):
@@ -489,11 +544,13 @@ def run_gpu(args):
                 "frac": fl / (t_max / 1e3) / 1e12 / peaks["bf16_tflops"]}
         # end to end through the public API with host buffers
         r.setup_e2e()
-        e2e_ms = time_steps(r.e2e_step, max(2, args.steps // 2), 1, flush_buf, stream, barrier)
-        e2e_mean = max_over_ranks(statistics.mean(e2e_ms), device=device)
+        e2e_mean = max_over_ranks(time_e2e(r, args.steps, args.warmup, stream, barrier), device=device)
         res["e2e"] = {"value": world * r.tokens / (e2e_mean / 1e3), "unit": UNIT,
                       "h2d_bytes_per_step": r.h2d, "d2h_bytes_per_step": r.d2h,
-                      "ms_per_step": e2e_mean}
+                      "ms_per_step": e2e_mean,
+                      "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams "
+                                    "while step i computes",
+                      "l2": "no flush between steps: each step touches more than L2 holds"}
         if rank == 0 and not args.no_cpu_baseline and key in ("prefill", "decode"):
             res["cpu_baseline"] = cpu_baseline(key, case)
         results[key] = res
