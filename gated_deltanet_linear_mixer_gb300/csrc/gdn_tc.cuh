@@ -62,32 +62,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// try_wait that may suspend the thread for up to `hint_ns` while the phase is
-// incomplete (it resumes as soon as the phase completes), so that waiting
-// warps leave the issue slots to the working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t* bar, uint32_t parity,
-                                                            uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // `timeout_ns` and returns false (the caller records an error and unwinds),
@@ -114,24 +88,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-// Prefetch of one tile of a 2-D tensor map into L2 (no shared memory, no
-// completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-// 1-D bulk copy global -> shared of `bytes` (multiple of 16; both addresses
-// 16-byte aligned), completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
-                                          uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 // 2-D tiled bulk tensor store shared -> global of one box, tracked by the
@@ -228,12 +184,6 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t addr, uint32_t m
     return d;
 }
 
-// Byte offset of element (k, mn) in an MN-major SW128 tile (see above).
-__device__ __forceinline__ uint32_t mn_offset(uint32_t k, uint32_t mn, uint32_t mn_block_bytes) {
-    return (mn >> 6) * mn_block_bytes + (k >> 3) * 1024u + (k & 7u) * 128u +
-           ((((mn & 63u) >> 3) ^ (k & 7u)) << 4) + (mn & 7u) * 2u;
-}
-
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, shape
 // M x N; each operand K-major unless its *_mn flag is set.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
@@ -320,11 +270,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
     int v;
@@ -380,18 +325,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // AND-reduction form: every participant learns whether all passed `ok`.
 __device__ __forceinline__ void group_sync(uint32_t id, uint32_t count) {
     asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool group_all(bool ok, uint32_t id, uint32_t count) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(ok ? 1u : 0u), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 
 // Pack two floats into a bf16x2 word (round to nearest even), low half first.
