@@ -102,7 +102,9 @@ gdn_status check_params(const gdn_params* p, bool need_norm, const char* fn) {
 gdn_status check_cu(int32_t n_seq, const int32_t* cu_dev, const int32_t* cu_host, int* total,
                     const char* fn) {
     if (n_seq < 0) return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be >= 0 (got %d)", n_seq);
-    if (n_seq > (1 << 24)) return fail(GDN_ERR_UNSUPPORTED, fn, "n_seq %d is too large", n_seq);
+    if (n_seq > GDN_MAX_SEQUENCES)
+        return fail(GDN_ERR_UNSUPPORTED, fn, "n_seq %d is above GDN_MAX_SEQUENCES (%d)", n_seq,
+                    GDN_MAX_SEQUENCES);
     *total = 0;
     if (n_seq == 0) return GDN_OK;
     if (!cu_dev || !cu_host) return fail(GDN_ERR_INVALID_ARG, fn, "cu_seqlens pointer is NULL");
@@ -396,8 +398,9 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     gdn_status st;
     if ((st = check_dims(dims, fn)) != GDN_OK) return st;
     if ((st = check_params(params, true, fn)) != GDN_OK) return st;
-    if (n_seq < 0 || n_seq > (1 << 24))
-        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..2^24 (got %d)", n_seq);
+    if (n_seq < 0 || n_seq > GDN_MAX_SEQUENCES)
+        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..GDN_MAX_SEQUENCES (%d) (got %d)",
+                    GDN_MAX_SEQUENCES, n_seq);
     if (T < 1 || T > 16) return fail(GDN_ERR_INVALID_ARG, fn, "T must be 1..16 (got %d)", T);
     g_err[0] = '\0';
     if (n_seq == 0) return GDN_OK;
@@ -445,8 +448,9 @@ gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_
     gdn_status st;
     if ((st = check_dims(dims, fn)) != GDN_OK) return st;
     if ((st = check_params(params, true, fn)) != GDN_OK) return st;
-    if (n_seq < 0 || n_seq > (1 << 24))
-        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..2^24 (got %d)", n_seq);
+    if (n_seq < 0 || n_seq > GDN_MAX_SEQUENCES)
+        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..GDN_MAX_SEQUENCES (%d) (got %d)",
+                    GDN_MAX_SEQUENCES, n_seq);
     if (T < 1 || T > 16) return fail(GDN_ERR_INVALID_ARG, fn, "T must be 1..16 (got %d)", T);
     g_err[0] = '\0';
     if (n_seq == 0) return GDN_OK;
@@ -478,8 +482,9 @@ gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,
     const char* fn = "gdn_decode_commit";
     gdn_status st;
     if ((st = check_dims(dims, fn)) != GDN_OK) return st;
-    if (n_seq < 0 || n_seq > (1 << 24))
-        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..2^24 (got %d)", n_seq);
+    if (n_seq < 0 || n_seq > GDN_MAX_SEQUENCES)
+        return fail(GDN_ERR_INVALID_ARG, fn, "n_seq must be 0..GDN_MAX_SEQUENCES (%d) (got %d)",
+                    GDN_MAX_SEQUENCES, n_seq);
     if (T < 1 || T > 16) return fail(GDN_ERR_INVALID_ARG, fn, "T must be 1..16 (got %d)", T);
     g_err[0] = '\0';
     if (n_seq == 0) return GDN_OK;

@@ -35,12 +35,17 @@
  *   (or, for GDN_ERR_CUDA, a launch failed), and gdn_last_error() returns a
  *   message naming the call and the reason.  No call aborts the process.
  * - Buffers must be 16-byte aligned (x, z, out, states, qkv_out).
+ * - A call takes at most GDN_MAX_SEQUENCES sequences (kernels index them on
+ *   the second grid dimension); larger batches are refused before any launch.
  */
 #ifndef GDN_H
 #define GDN_H
 
 #include <stddef.h>
 #include <stdint.h>
+
+/* Most sequences one call takes (the CUDA grid's second dimension). */
+#define GDN_MAX_SEQUENCES 65535
 
 #ifdef __cplusplus
 extern "C" {

@@ -219,3 +219,26 @@ def test_layer_refusals(lib):
     # too small a workspace is refused before any launch
     assert _layer(lib, _dims(), _proj(), ws=FAKE, ws_bytes=256) == 4
     assert "workspace" in lib.gdn_last_error().decode()
+
+
+def test_sequence_count_limit(lib):
+    """More than GDN_MAX_SEQUENCES sequences is refused on the host."""
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    limit = int(re.search(r"#define GDN_MAX_SEQUENCES (\d+)", text).group(1))
+    d = _dims()
+    for fn in ("gdn_decode", "gdn_verify"):
+        if fn == "gdn_decode":
+            args = [ctypes.byref(d), ctypes.byref(PARAMS), limit + 1, 1, FAKE, FAKE, FAKE, FAKE,
+                    FAKE, None, None, FAKE, None]
+        else:
+            args = [ctypes.byref(d), ctypes.byref(PARAMS), limit + 1, 1, FAKE, FAKE, FAKE, FAKE,
+                    FAKE, None, FAKE, None]
+        assert getattr(lib, fn)(*args) == 1
+        assert "GDN_MAX_SEQUENCES" in lib.gdn_last_error().decode()
+    assert lib.gdn_decode_commit(ctypes.byref(d), limit + 1, 1, FAKE, FAKE, FAKE, FAKE, None,
+                                 None) == 1
+    cu = (ctypes.c_int32 * (limit + 2))(*range(limit + 2))
+    n = ctypes.c_size_t(0)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d), limit + 1,
+                                          ctypes.cast(cu, ctypes.c_void_p), ctypes.byref(n)) == 2
+    assert "GDN_MAX_SEQUENCES" in lib.gdn_last_error().decode()
