@@ -45,6 +45,9 @@ TRAFFIC = {
     # profiles/recurrent_decode_N64.md (64 sequences; the traffic is per sequence,
     # so x 256/64 for the bench's 256)
     ("decode", "recurrent"): (139_106_560 + 73_355_264) * 4,
+    # profiles/chunk_prep_varlen_N16_T8990.md (149 chunks; the traffic grows with
+    # the chunk count, so x 1,015 / 149 for the bench's variable-length batch)
+    ("varlen", "chunk_prep"): (298_879_232 + 409_328_384) * 1015 // 149,
 }
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
@@ -636,13 +639,20 @@ def run_profile(args):
                                   dtype="bf16", act="sigmoid", seed=2, state_std=0.05,
                                   conv_state_std=1.0)
         key = "decode"
+    elif key == "varlen_small":  # 16 sequences of 128..1024 tokens: the two-kernel launch, ~1 GB
+        case = workloads.generate("varlen_small_N16_U128_1024_Hk16_Hv32_d128_bf16", n_k_heads=16,
+                                  n_v_heads=32, d_k=128, d_v=128, conv_k=4,
+                                  random_lengths=(16, 128, 1024), dtype="bf16", act="silu", seed=3,
+                                  state_std=0.05)
+        key = "varlen"
     else:
         case = workloads.config(WORKLOADS[key])
     r = Runner(key, case, torch.device("cuda", 0))
     for _ in range(2):
         r.step()
     torch.cuda.synchronize()
-    print(json.dumps({"profile": args.profile, "workload": case.name,
+    print(json.dumps({"profile": args.profile, "workload": case.name, "n_seq": case.n_seq,
+                      "tokens": int(case.cu_seqlens[-1]) if case.cu_seqlens is not None else None,
                       "device_error": gdn.device_error()}))
 
 
@@ -655,7 +665,7 @@ def main():
     ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay,layer",
                     help="comma list of extra workloads in the same line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64"],
+    ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64", "varlen_small"],
                     help="run one warm-up and one call of a workload, untimed (for ncu)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
