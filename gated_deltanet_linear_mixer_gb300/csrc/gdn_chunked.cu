@@ -1298,15 +1298,21 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 4 * kC * 4;
     const size_t scan_smem = 1024 + kScanEnd;
     const size_t prep_smem_max = 1024 + kPrepVec + 8 * 4 * kC * 4;
-    static bool attrs_set = false;
-    if (!attrs_set) {
-        cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(prep_smem_max));
-        cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(scan_smem));
-        cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(std::max(prep_smem_max, scan_smem)));
-        attrs_set = true;
+    // the kernels' shared-memory opt-in is a per-device setting
+    static bool attrs_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attrs_set[dev]) {
+        cudaError_t ae = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(prep_smem_max));
+        if (ae == cudaSuccess)
+            ae = cudaFuncSetAttribute(chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(scan_smem));
+        if (ae == cudaSuccess)
+            ae = cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(std::max(prep_smem_max, scan_smem)));
+        if (ae != cudaSuccess) return ae;
+        attrs_set[dev] = true;
     }
     const int n_items = l.n_chunks * hk_n;
     // One fused launch when the scan's clusters leave at least 32 CTA slots
