@@ -5,6 +5,7 @@ error metric max|gpu - ref| / rms(ref) and the tolerances 1e-4 (fp32
 activations) and 2e-2 (bf16 activations, fp32 state).
 """
 import copy
+import os
 
 import numpy as np
 import pytest
@@ -452,6 +453,29 @@ def test_full_size_prefill_T4096_slow_decay():
     got = gpu_prefill(case)
     assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+
+
+def test_long_single_sequence_fused_launch():
+    """One 32,768-token sequence (512 chunks, long-memory gates so that the state
+    carries across every chunk) through the fused launch, whose scan waits on
+    prep's per-chunk flags 512 times; matches the oracle and the two-kernel
+    launch bit for bit."""
+    case = _gen("long", n_k_heads=2, n_v_heads=4, lengths=[32768], state_std=0.05, seed=61,
+                slow_decay=True)
+    t = upload(case)
+    got = gpu_prefill(case, t)
+    ref = run_oracle(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"].float(), ref["conv_state"]) == 0.0
+    os.environ["GDN_PREFILL_FUSED"] = "0"
+    try:
+        two = gpu_prefill(case, t)
+    finally:
+        del os.environ["GDN_PREFILL_FUSED"]
+    assert torch.equal(got["out"], two["out"]) and torch.equal(got["state"], two["state"])
+    code = gdn.device_error()
+    assert code == 0
 
 
 @pytest.mark.parametrize("slow", [False, True])
