@@ -455,6 +455,32 @@ def test_full_size_prefill_T4096_slow_decay():
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("kind", ["bf16_tensor_core", "f32_recurrent", "bf16_decode"])
+def test_saturated_gates(kind):
+    """Gate inputs at the ends of their range, all exact in bf16: a + dt_bias past
+    softplus's identity threshold (20) and far below 0 (no decay at all), beta
+    saturated at 0 and 1, mixed token by token, so that the chunked form sees
+    in-chunk decays from 1 down to e^-480 (underflow) and the recurrence
+    alternates between a full write, no write and a wiped state."""
+    if kind == "bf16_decode":
+        case = _gen("sat_d", mode="decode", n_seq=3, tokens_per_seq=4, act="sigmoid",
+                    state_std=0.05, conv_state_std=1.0, seed=71)
+    else:
+        case = _gen("sat", dtype="bf16" if kind == "bf16_tensor_core" else "f32",
+                    lengths=[300, 65, 17], state_std=0.05, seed=72)
+    rng = np.random.default_rng(73)
+    case.a = rng.choice([-30.0, -8.0, 0.0, 8.0, 25.0, 30.0], size=case.a.shape).astype(case.a.dtype)
+    case.b = rng.choice([-30.0, -5.0, 0.0, 5.0, 30.0], size=case.b.shape).astype(case.b.dtype)
+    ref = run_oracle(case)
+    if kind == "bf16_decode":
+        got = gpu_decode(case)
+    else:
+        got = gpu_prefill(case)
+    tol = TOL["f32"] if kind == "f32_recurrent" else TOL["bf16"]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+
+
 def test_long_single_sequence_fused_launch():
     """One 32,768-token sequence (512 chunks, long-memory gates so that the state
     carries across every chunk) through the fused launch, whose scan waits on
