@@ -481,6 +481,22 @@ def test_saturated_gates(kind):
     assert rel_err(got["state"], ref["state"]) <= tol
 
 
+def test_decode_at_the_sequence_limit():
+    """A decode step of exactly GDN_MAX_SEQUENCES sequences (the largest grid the
+    kernels are launched with), small heads so that the state stays small."""
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                             "include", "gdn.h")).read()
+    limit = int(text.split("#define GDN_MAX_SEQUENCES")[1].split()[0])
+    case = _gen("maxseq", mode="decode", n_seq=limit, tokens_per_seq=1, n_k_heads=1, n_v_heads=1,
+                d_k=32, d_v=32, dtype="f32", act="sigmoid", state_std=0.05, conv_state_std=1.0,
+                seed=81)
+    ref = run_oracle(case)
+    got = gpu_decode(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["f32"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["f32"]
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
 def test_long_single_sequence_fused_launch():
     """One 32,768-token sequence (512 chunks, long-memory gates so that the state
     carries across every chunk) through the fused launch, whose scan waits on
