@@ -28,6 +28,7 @@
 // operand is K-major (the one A that would be MN-major, the scaled keys of the
 // state increment, is transposed by threads).
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -1182,12 +1183,13 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
 }
 
 // CTAs of chunk_fused_kernel that can be resident at once (2 x its active
-// clusters), per device; 0 when the query fails.
+// clusters), per device; 0 when the query fails.  (The per-device caches here
+// are atomics: host threads may make their first call on a device at once.)
 static int fused_capacity(size_t smem) {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!cached[dev]) {
+    if (!cached[dev].load()) {
         cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
         cudaLaunchConfig_t cfg{};
@@ -1199,22 +1201,23 @@ static int fused_capacity(size_t smem) {
             cudaGetLastError();
             nc = 0;
         }
-        cached[dev] = nc > 0 ? 2 * nc : -1;
+        cached[dev].store(nc > 0 ? 2 * nc : -1);
     }
-    return cached[dev] > 0 ? cached[dev] : 0;
+    const int cap = cached[dev].load();
+    return cap > 0 ? cap : 0;
 }
 
 // SMs of the current device (the persistent prep kernel runs one CTA per SM).
 static int sm_count() {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev].load()) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached[dev] = n;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev].store(n);
     }
-    return cached[dev];
+    return cached[dev].load();
 }
 
 cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
@@ -1299,10 +1302,10 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     const size_t scan_smem = 1024 + kScanEnd;
     const size_t prep_smem_max = 1024 + kPrepVec + 8 * 4 * kC * 4;
     // the kernels' shared-memory opt-in is a per-device setting
-    static bool attrs_set[64] = {};
+    static std::atomic<bool> attrs_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attrs_set[dev]) {
+    if (!attrs_set[dev].load()) {
         cudaError_t ae = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               static_cast<int>(prep_smem_max));
         if (ae == cudaSuccess)
@@ -1312,7 +1315,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             ae = cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(std::max(prep_smem_max, scan_smem)));
         if (ae != cudaSuccess) return ae;
-        attrs_set[dev] = true;
+        attrs_set[dev].store(true);
     }
     const int n_items = l.n_chunks * hk_n;
     // One fused launch when the scan's clusters leave at least 32 CTA slots
