@@ -258,7 +258,7 @@ class Runner:
         self.ev_in, self.ev_done, self.ev_read = ev(), ev(), ev()
         self.e2e_i = 0
 
-    def e2e_step(self, stream, flush=None):
+    def e2e_step(self, stream):
         """One pipelined step on buffer set i % 2; `stream` is the compute stream."""
         torch, k = self.torch, self.e2e_i % 2
         d_in, d_out, h_in, h_out = self.sets[k]
@@ -271,8 +271,6 @@ class Runner:
         stream.wait_event(self.ev_in[k])
         if self.e2e_i >= 2:
             stream.wait_event(self.ev_read[k])      # step i-2's output has been read back
-        if flush is not None:
-            _flush(flush)
         for n in self.in_names + self.out_names:
             setattr(self, n, (d_in | d_out)[n])
         self.step()
