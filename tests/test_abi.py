@@ -242,3 +242,33 @@ def test_sequence_count_limit(lib):
     assert lib.gdn_prefill_workspace_size(ctypes.byref(d), limit + 1,
                                           ctypes.cast(cu, ctypes.c_void_p), ctypes.byref(n)) == 2
     assert "GDN_MAX_SEQUENCES" in lib.gdn_last_error().decode()
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/gdn.h compiles as strict C99, and a C program that takes the
+    address of every declared entry point links against libgdn.so."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    names = sorted(_declared())
+    src = tmp_path / "use_gdn.c"
+    src.write_text('#include "gdn.h"\n#include <stdio.h>\n'
+                   "typedef void (*fp)(void);\n"
+                   "int main(void) {\n"
+                   "    fp table[] = {\n" +
+                   "".join(f"        (fp){n},\n" for n in names) +
+                   "    };\n"
+                   '    printf("%d %s\\n", (int)(sizeof table / sizeof table[0]), gdn_version());\n'
+                   "    return 0;\n}\n")
+    exe = tmp_path / "use_gdn"
+    libdir = os.path.dirname(gdn.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                        str(exe), "-L", libdir, "-lgdn", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split()[0] == str(len(names))
