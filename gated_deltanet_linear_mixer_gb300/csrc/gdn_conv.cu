@@ -425,9 +425,75 @@ cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stre
     return cudaGetLastError();
 }
 
+// The same for K = 4 (three history slots), 16 bytes of channels a thread: its
+// history block (3 x 16 bytes, slot-minor) is read and written whole, and each
+// new input row is one 16-byte load.  A thread reads and writes only its own
+// block, so the update may be in place.
+template <typename T>
+__global__ void conv_state_vec_kernel(ConvStateArgs p) {
+    constexpr int VEC = 16 / (int)sizeof(T);  // channels a thread
+    constexpr int KEEP = 3;
+    const int n = blockIdx.y;
+    const int cd = 2 * p.n_k_heads * p.d_k + p.n_v_heads * p.d_v;
+    const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * VEC;
+    if (c0 >= cd) return;
+    int bos, len;
+    if (p.cu_seqlens) {
+        bos = p.cu_seqlens[n];
+        len = p.cu_seqlens[n + 1] - bos;
+    } else {
+        bos = n * p.uniform_T;
+        len = p.uniform_T;
+    }
+    if (p.lengths) len = min(max(p.lengths[n], 0), len);  // accepted prefix (commit)
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const size_t blk = ((size_t)n * cd + c0) * KEEP;  // element offset of the block
+    union Block { uint4 u[KEEP]; T v[KEEP * VEC]; };
+    Block old, nw;
+    if (len < KEEP) {  // some slots come from the old history (zeros without one)
+        if (p.conv_state_in) {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.conv_state_in) + blk);
+#pragma unroll
+            for (int i = 0; i < KEEP; ++i) old.u[i] = src[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < KEEP; ++i) old.u[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < KEEP; ++s) {
+        const int ti = len - KEEP + s;  // token of slot s, relative to the sequence start
+        if (ti >= 0) {
+            union { uint4 u; T v[VEC]; } row;
+            row.u = *reinterpret_cast<const uint4*>(x + (size_t)(bos + ti) * cd + c0);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) nw.v[e * KEEP + s] = row.v[e];
+        } else {  // old slot j = KEEP + ti (0..2), picked with constant indices
+            const int j = KEEP + ti;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                nw.v[e * KEEP + s] = j == 0 ? old.v[e * KEEP] : (j == 1 ? old.v[e * KEEP + 1] : old.v[e * KEEP + 2]);
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.conv_state_out) + blk);
+#pragma unroll
+    for (int i = 0; i < KEEP; ++i) dst[i] = nw.u[i];
+}
+
 cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t stream) {
     if (p.n_seq == 0 || p.conv_k < 2) return cudaSuccess;
     const int cd = 2 * p.n_k_heads * p.d_k + p.n_v_heads * p.d_v;
+    const int vec = bf16 ? 8 : 4;
+    auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (p.conv_k == 4 && cd % vec == 0 && al16(p.x) && al16(p.conv_state_out) &&
+        (!p.conv_state_in || al16(p.conv_state_in))) {
+        dim3 grid((cd / vec + 255) / 256, p.n_seq);
+        if (bf16)
+            conv_state_vec_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+        else
+            conv_state_vec_kernel<float><<<grid, 256, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     dim3 grid((cd + 255) / 256, p.n_seq);
     if (bf16)
         conv_state_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
