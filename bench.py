@@ -11,7 +11,9 @@ CUDA events recorded by libgdn on the launching stream, and an end-to-end
 figure through the public API with pinned host buffers.
 
 ``--impl reference`` times the CPU oracle instead (the only baseline: the pages
-publish no GPU implementation of this core), on a bounded sample per step.
+publish no GPU implementation of this core): the float build of its C source,
+one whole prefill workload per step.  The same build, on the same workloads, is
+each GPU line's ``cpu_baseline``.
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and a
 device synchronize; a 256 MiB buffer (2x L2) is written between timed steps
@@ -36,18 +38,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
-# DRAM bytes (read + write) per launch of a workload's dominant kernel, from the
-# ncu captures summarised under profiles/ (absent until a capture of the current
-# kernel exists; an entry is removed whenever its kernel changes).
+# DRAM bytes (read + write) per launch of a workload's dominant kernel, from an
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the kernel as it
+# is now: (bytes, where they come from).  A capture of a smaller case is scaled
+# by the units it processes, and the source says so.  An entry is removed when
+# its kernel changes, until it is captured again.
 TRAFFIC = {
-    # profiles/chunk_fused_prefill_T4096.md, the bench's own workload
-    ("prefill", "chunk_fused"): 315_110_656 + 212_748_800,
-    # profiles/recurrent_decode_N64.md (64 sequences; the traffic is per sequence,
-    # so x 256/64 for the bench's 256)
-    ("decode", "recurrent"): (139_106_560 + 73_355_264) * 4,
-    # profiles/chunk_prep_varlen_N16_T8990.md (149 chunks; the traffic grows with
-    # the chunk count, so x 1,015 / 149 for the bench's variable-length batch)
-    ("varlen", "chunk_prep"): (298_879_232 + 409_328_384) * 1015 // 149,
+    # 64-sequence decode step; the traffic is per sequence: x 256/64
+    ("decode", "recurrent"): ((139_106_560 + 73_355_264) * 4,
+                              "ncu capture of the 64-sequence decode step, scaled x 256/64"),
 }
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
@@ -401,41 +400,42 @@ def time_e2e(r, steps, warmup, stream, barrier):
     return a.elapsed_time(b) / steps
 
 
-def cpu_baseline(key, case, max_seconds=10.0):
-    """Time the CPU oracle as it stands on a bounded sample of the workload."""
+def cpu_baseline(key, case, runs=3):
+    """The oracle's float build (the same C source as the parity oracle, built with
+    float arithmetic, OpenMP over tokens and over (sequence, value head)) timed on
+    the whole workload: the median of `runs` runs on all host cores."""
     import oracle
     od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act)
-    cu = case.cu_seqlens
-    if case.mode == "prefill":
-        # leading tokens of the first sequence, with its initial state
-        take = min(int(cu[1] - cu[0]), 256)
-        sl = slice(0, take)
-        args = ([0, take], case.x[sl], case.z[sl], case.a[sl], case.b[sl])
-        st = None if case.state is None else case.state[:1]
-        cs = None if case.conv_state is None else case.conv_state[:1]
-        sample = f"first {take} tokens of sequence 0 (all {case.n_v_heads} heads)"
-        tokens = take
-    else:
-        nseq = min(case.n_seq, 16)
-        t = case.tokens_per_seq
-        rows = slice(0, nseq * t)
-        args = (cu[:nseq + 1], case.x[rows], case.z[rows], case.a[rows], case.b[rows])
-        st = case.state[:nseq]
-        cs = None if case.conv_state is None else case.conv_state[:nseq]
-        sample = f"{nseq} of {case.n_seq} sequences x {t} tokens"
-        tokens = nseq * t
     times = []
-    t_end = time.time() + max_seconds
-    while len(times) < 3 and (not times or time.time() < t_end):
+    for _ in range(runs):
         t0 = time.perf_counter()
-        oracle.gdn(od, args[0], *args[1:], case.conv_w, case.A_log, case.dt_bias, case.norm_w,
-                   cs, st, want_inter=(key == "spec_verify"))
+        oracle.gdn_f32(od, case.cu_seqlens, case.x, case.z, case.a, case.b, case.conv_w,
+                       case.A_log, case.dt_bias, case.norm_w, case.conv_state, case.state)
         times.append(time.perf_counter() - t0)
     med = statistics.median(times)
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": tokens / med, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": sample + f", f64 C oracle with OpenMP over (sequence, value head), "
-                               f"median of {len(times)} runs"}
+    sample = (f"the whole workload ({case.n_seq} sequences, {case.n_tokens} tokens, all "
+              f"{case.n_v_heads} heads): the oracle's C source built with float arithmetic, "
+              f"OpenMP over tokens and over (sequence, value head), median of {runs} runs")
+    return {"value": case.n_tokens / med, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds_per_run": med}
+
+
+def h2d_ceiling(nbytes, device, reps=10):
+    """GB/s of a plain pinned host-to-device copy of `nbytes` (the ceiling of the
+    end-to-end figure when the step's input copy bounds it)."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9
 
 
 def run_gpu(args):
@@ -509,7 +509,9 @@ def run_gpu(args):
             achieved = fl / (dom_avg_ms / 1e3) / 1e12
             roof = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"], "traffic": TRAFFIC.get((r.key, dom_name)),
+                    "frac": achieved / peaks["bf16_tflops"],
+                    "traffic": TRAFFIC.get((r.key, dom_name), (None, None))[0],
+                    "traffic_source": TRAFFIC.get((r.key, dom_name), (None, None))[1],
                     "peak_source": peaks["source"] + " (bf16 burst)",
                     "useful_flops_per_launch": fl, "kernel_ms": dom_avg_ms, "kernel_share": share,
                     "kernel_timing": KERNEL_TIMING}
@@ -517,7 +519,9 @@ def run_gpu(args):
             achieved = kb / (dom_avg_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": TRAFFIC.get((r.key, dom_name)), "peak_source": peaks["source"],
+                    "traffic": TRAFFIC.get((r.key, dom_name), (None, None))[0],
+                    "traffic_source": TRAFFIC.get((r.key, dom_name), (None, None))[1],
+                    "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": kb, "kernel_ms": dom_avg_ms,
                     "kernel_share": share, "kernel_timing": KERNEL_TIMING}
         step_bytes = r.algorithmic_bytes()
@@ -552,6 +556,10 @@ def run_gpu(args):
                       "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams "
                                     "while step i computes",
                       "l2": "no flush between steps: each step touches more than L2 holds"}
+        if r.h2d >= (16 << 20):  # where the input copy can bound the step: its ceiling beside it
+            gbs = h2d_ceiling(r.h2d, device)
+            res["e2e"]["h2d_ceiling_gbs"] = gbs
+            res["e2e"]["h2d_bound_tokens_s"] = world * r.tokens / (r.h2d / (gbs * 1e9))
         if rank == 0 and not args.no_cpu_baseline and key in ("prefill", "decode"):
             res["cpu_baseline"] = cpu_baseline(key, case)
         results[key] = res
@@ -579,6 +587,13 @@ def run_gpu(args):
     }
     for k in keys[1:]:
         line[k] = results[k]
+    # compact per-workload figures, last in the line (a reader that keeps only
+    # the line's tail still has them)
+    line["summary"] = {k: {"tokens_s": round(v["value"]), "ms": round(v["ms_per_step"], 4),
+                           "kernel": v["roofline"]["kernel"], "bound": v["roofline"]["bound"],
+                           "frac": round(v["roofline"]["frac"], 4),
+                           "e2e_tokens_s": round(v["e2e"]["value"])}
+                       for k, v in results.items()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -586,7 +601,8 @@ def run_gpu(args):
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm, on the prefill workload's config."""
+    """The CPU oracle (its float build, as cpu_baseline times it) as the reference
+    arm, on the prefill workload's config; each step is one whole-workload run."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -594,10 +610,8 @@ def run_reference(args):
     import oracle
     case = workloads.config(1)
     od = oracle.Dims(case.n_k_heads, case.n_v_heads, case.d_k, case.d_v, case.conv_k, case.act)
-    take = 128
-    sl = slice(0, take)
-    run = lambda: oracle.gdn(od, [0, take], case.x[sl], case.z[sl], case.a[sl], case.b[sl],  # noqa: E731
-                             case.conv_w, case.A_log, case.dt_bias, case.norm_w)
+    run = lambda: oracle.gdn_f32(od, case.cu_seqlens, case.x, case.z, case.a, case.b,  # noqa: E731
+                                 case.conv_w, case.A_log, case.dt_bias, case.norm_w)
     for _ in range(args.warmup):
         run()
     times = []
@@ -607,12 +621,13 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     mean_s = statistics.mean(times)
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    v = take / mean_s
-    sample = (f"first {take} of the {case.n_tokens} tokens per step (all {case.n_v_heads} heads), "
-              "f64 C oracle with OpenMP over (sequence, value head)")
+    v = case.n_tokens / mean_s
+    sample = (f"the whole workload per step ({case.n_tokens} tokens, all {case.n_v_heads} heads): "
+              "the oracle's C source built with float arithmetic, OpenMP over tokens and over "
+              "(sequence, value head)")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": case.name, "n_seq": case.n_seq, "tokens": case.n_tokens,
                        "Hk": case.n_k_heads, "Hv": case.n_v_heads, "d_k": case.d_k,

@@ -23,7 +23,9 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_OK = 0
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
-                3: "GDN_ERR_CUDA", 4: "GDN_ERR_WORKSPACE"}
+                3: "GDN_ERR_CUDA", 4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_TIMEOUT",
+                6: "GDN_ERR_INJECTED"}
+GDN_ERR_TIMEOUT, GDN_ERR_INJECTED = 5, 6
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_SILU, ACT_SIGMOID = 0, 1
 
@@ -31,8 +33,8 @@ ACT_SILU, ACT_SIGMOID = 0, 1
 EXPORTS = ("gdn_conv", "gdn_prefill_workspace_size", "gdn_prefill", "gdn_prefill_noalloc",
            "gdn_prefill_noalloc_scratch_bytes", "gdn_decode", "gdn_verify", "gdn_decode_commit",
            "gdn_layer_prefill_workspace_size", "gdn_layer_prefill",
-           "gdn_timing_enable", "gdn_timing_report", "gdn_device_error", "gdn_last_error",
-           "gdn_version")
+           "gdn_timing_enable", "gdn_timing_report", "gdn_device_error", "gdn_sync_status",
+           "gdn_last_error", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -99,6 +101,8 @@ def load(path: str | None = None):
     lib.gdn_timing_report.restype = ctypes.c_size_t
     lib.gdn_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), I32]
     lib.gdn_device_error.restype = ctypes.c_int
+    lib.gdn_sync_status.argtypes = [P]
+    lib.gdn_sync_status.restype = ctypes.c_int
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_last_error.argtypes = []
     lib.gdn_version.restype = ctypes.c_char_p
@@ -243,6 +247,13 @@ def device_error(reset: bool = True) -> int:
     code = ctypes.c_int32(0)
     _check("gdn_device_error", load().gdn_device_error(ctypes.byref(code), 1 if reset else 0))
     return int(code.value)
+
+
+def sync_status(device=None) -> None:
+    """gdn_sync_status on the current stream: waits for it, then raises GDNError
+    (status GDN_ERR_TIMEOUT) if a bounded device wait gave up since the last
+    check; the word is cleared either way."""
+    _check("gdn_sync_status", load().gdn_sync_status(_stream(device)))
 
 
 def conv(d: Dims, params: Params, cu_seqlens, x, a, b, conv_state_in=None, conv_state_out=None,
@@ -453,6 +464,7 @@ def decode_commit(d: Dims, accepted, x, inter_states, state, conv_state=None):
 
 
 __all__ = ["Dims", "Params", "GDNError", "load", "version", "timing_enable", "timing_report",
+           "device_error", "sync_status",
            "conv", "prefill",
            "prefill_workspace_size", "decode", "verify", "decode_commit", "Proj",
            "layer_prefill_workspace_size", "layer_prefill", "EXPORTS", "LIB_PATH"]

@@ -3,6 +3,7 @@
 // caller's stream.  No entry point allocates device memory.
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -33,6 +34,32 @@ gdn_status cuda_status(cudaError_t e, const char* fn, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Whether the comma-separated list in the environment variable GDN_FAULT names
+// `site` (or "all").  Read on every call, so a test can set and clear it.
+bool fault_listed(const char* site) {
+    const char* v = std::getenv("GDN_FAULT");
+    if (!v || !*v) return false;
+    const size_t n = std::strlen(site);
+    for (const char* p = v; *p;) {
+        const char* e = p;
+        while (*e && *e != ',') ++e;
+        const size_t len = static_cast<size_t>(e - p);
+        if ((len == n && std::strncmp(p, site, n) == 0) || (len == 3 && std::strncmp(p, "all", 3) == 0))
+            return true;
+        p = *e ? e + 1 : e;
+    }
+    return false;
+}
+
+// Host-side fault injection: a call whose site GDN_FAULT lists fails with
+// GDN_ERR_INJECTED after validating its arguments and before it enqueues any
+// work, so that a caller's failure path can be exercised without a GPU fault.
+gdn_status injected(const char* site, const char* fn) {
+    if (!fault_listed(site)) return GDN_OK;
+    return fail(GDN_ERR_INJECTED, fn, "fault injected at site '%s' (GDN_FAULT); nothing was enqueued",
+                site);
+}
 
 bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
@@ -173,6 +200,8 @@ void drain_pending_locked() {
 
 namespace gdn {
 
+gdn_status inject_fault(const char* site, const char* fn) { return injected(site, fn); }
+
 gdn_status set_error(gdn_status st, const char* fn, const char* fmt, ...) {
     int n = std::snprintf(g_err, sizeof(g_err), "%s: ", fn);
     if (n < 0) n = 0;
@@ -244,6 +273,23 @@ gdn_status gdn_device_error(int32_t* code, int32_t reset) {
     return st;
 }
 
+gdn_status gdn_sync_status(void* stream) {
+    const char* fn = "gdn_sync_status";
+    gdn_status st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), fn,
+                                "synchronizing the stream");
+    if (st != GDN_OK) return st;
+    int code = 0;
+    if ((st = cuda_status(gdn::read_device_error(&code, true), fn, "reading the error word")) != GDN_OK)
+        return st;
+    if (code)
+        return fail(GDN_ERR_TIMEOUT, fn,
+                    "a bounded device wait of the tensor-core prefill gave up (wait code %d%s); the "
+                    "outputs and states written by the calls since the last check are invalid",
+                    code, code == 11 ? ": a scan waited for a chunk's prep rows" : "");
+    g_err[0] = '\0';
+    return GDN_OK;
+}
+
 const char* gdn_last_error(void) { return g_err; }
 
 const char* gdn_version(void) { return "gdn-gb300 0.1 (sm_103a)"; }
@@ -265,6 +311,7 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_params* params, int32_t n_se
         return fail(GDN_ERR_INVALID_ARG, fn, "an input or output pointer is NULL");
     if ((x && !aligned16(x)) || (qkv_out && !aligned16(qkv_out)))
         return fail(GDN_ERR_INVALID_ARG, fn, "x and qkv_out must be 16-byte aligned");
+    if ((st = injected("conv", fn)) != GDN_OK) return st;
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -334,6 +381,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         return fail(GDN_ERR_WORKSPACE, fn, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
     g_err[0] = '\0';
+    if ((st = injected("prefill", fn)) != GDN_OK) return st;
     if (n_seq == 0) return GDN_OK;
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -352,6 +400,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         c.norm_w = params->norm_w; c.conv_state_in = conv_state_in;
         c.state_in = initial_state; c.state_out = final_state; c.out = out;
         c.workspace = workspace;
+        c.stall = fault_listed("stall_scan") ? 1 : 0;
         // the new conv history comes from the prologue's launch unless it is
         // updated in place (the prologue still reads the old one)
         if (conv_state_out && !ranges_overlap(conv_state_in, conv_state_out,
@@ -409,6 +458,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
     if (!aligned16(x) || !aligned16(z) || !aligned16(out) || !aligned16(state) ||
         (inter_states && !aligned16(inter_states)))
         return fail(GDN_ERR_INVALID_ARG, fn, "x, z, out and the states must be 16-byte aligned");
+    if ((st = injected("decode", fn)) != GDN_OK) return st;
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -458,6 +508,7 @@ gdn_status gdn_verify(const gdn_dims* dims, const gdn_params* params, int32_t n_
         return fail(GDN_ERR_INVALID_ARG, fn, "an input or output pointer is NULL");
     if (!aligned16(x) || !aligned16(z) || !aligned16(out) || !aligned16(state))
         return fail(GDN_ERR_INVALID_ARG, fn, "x, z, out and the state must be 16-byte aligned");
+    if ((st = injected("verify", fn)) != GDN_OK) return st;
     const bool bf16 = dims->dtype == GDN_DTYPE_BF16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gdn::RecurrentArgs r{};
@@ -492,6 +543,7 @@ gdn_status gdn_decode_commit(const gdn_dims* dims, int32_t n_seq, int32_t T,
         return fail(GDN_ERR_INVALID_ARG, fn, "a required pointer is NULL");
     if (!aligned16(inter_states) || !aligned16(state))
         return fail(GDN_ERR_INVALID_ARG, fn, "the states must be 16-byte aligned");
+    if ((st = injected("commit", fn)) != GDN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gdn::CommitArgs c{};
     c.n_seq = n_seq; c.n_v_heads = dims->n_v_heads; c.d_k = dims->d_k; c.d_v = dims->d_v;

@@ -76,7 +76,25 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
 
 // Uniform decision after a bounded wait: every thread learns whether any
 // thread's wait gave up.
-__device__ __forceinline__ bool any_failed(bool ok) { return __syncthreads_or(ok ? 0 : 1) != 0; }
+// Barriers of the prep role: named barrier 1 over its eight warps (256
+// threads), so that a launch may carry more warps than prep uses.
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Every prep thread learns whether any of them passed v != 0.
+__device__ __forceinline__ bool prep_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+// Uniform decision after a bounded wait: every prep thread learns whether any
+// thread's wait gave up.
+__device__ __forceinline__ bool prep_failed(bool ok) { return prep_any(!ok); }
 
 // Split arithmetic.  Every tensor-core operand is carried as a pair of bf16
 // tiles, hi = bf16(x) and lo = bf16(x - hi), which together hold ~16
@@ -86,14 +104,15 @@ __device__ __forceinline__ bool any_failed(bool ok) { return __syncthreads_or(ok
 // (2^-9 relative) would put the largest outputs' error far above 2e-2 of the
 // output RMS.
 __device__ __forceinline__ void split_store(const float* f, uint8_t* hi, uint8_t* lo) {
-    float h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        h[e] = __bfloat162float(__float2bfloat16_rn(f[e]));
-        l[e] = f[e] - h[e];
+    for (int i = 0; i < 4; ++i) {  // hi rounded once per pair; lo = the exact remainder, rounded
+        h[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+        l[i] = pack_bf16x2(f[2 * i] - __uint_as_float(h[i] << 16),
+                           f[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u));
     }
-    *reinterpret_cast<uint4*>(hi) = pack_bf16x8(h);
-    *reinterpret_cast<uint4*>(lo) = pack_bf16x8(l);
+    *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 __device__ __forceinline__ void load_pair(const uint8_t* hi, const uint8_t* lo, float* f) {
     float l[8];
@@ -178,7 +197,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
     tc_fence_before_sync();
-    __syncthreads();
+    prep_sync();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
     uint32_t mma_phase = 0, tma_phase = 0, v_phase = 0;
@@ -274,7 +293,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         sCs2[warp * kC + s1] = b1;
     }
     do {
-        if (any_failed(mbar_wait(&bar_tma, tma_phase))) {  // this item's q, k tiles
+        if (prep_failed(mbar_wait(&bar_tma, tma_phase))) {  // this item's q, k tiles
             if (tid == 0) report_error(1);
             failed = true;
             break;
@@ -292,7 +311,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        __syncthreads();
+        prep_sync();
         tc_fence_after_sync();
         if (tid == 0) {  // Gram: rows 0..63 = Q K^T, rows 64..127 = K K^T
 #pragma unroll
@@ -313,7 +332,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             bulk_commit();
         }
         mma_pending = true;
-        if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
+        if (prep_failed(mbar_wait(&bar_mma, mma_phase))) {
             if (tid == 0) report_error(2);
             failed = true;
             break;
@@ -328,7 +347,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
 
         for (int pr = 0; pr < n_pairs; ++pr) {
             const int nb = min(2, R - 2 * pr);
-            if (any_failed(mbar_wait(&bar_v, v_phase))) {  // this pair's v tiles
+            if (prep_failed(mbar_wait(&bar_v, v_phase))) {  // this pair's v tiles
                 if (tid == 0) report_error(7);
                 failed = true;
                 break;
@@ -345,7 +364,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
             }
             if (tid == 0) bulk_wait_read();  // the last W stores have read T1 / T2
-            __syncthreads();
+            prep_sync();
             // ---- phase A: M o QK^T rows (warps 0,1 / 4,5) and A^T (warps 2,3 / 6,7)
             {
                 const int hh = warp >> 2;             // head of the pair this warp serves
@@ -381,7 +400,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
             }
             fence_proxy_async_smem();
-            __syncthreads();
+            prep_sync();
             if (tid == 64) {  // M o QK^T tiles -> workspace (thread 64 idles in the diagonal solve)
                 for (int hh = 0; hh < nb; ++hh) {
                     const int row = (c * hv_n + value_head(hk, 2 * pr + hh, R, p.n_k_heads, p.head_map)) * kC;
@@ -408,7 +427,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
 #pragma unroll
                     for (int r = 0; r < 16; ++r) prep_tf(smem, hh, 16 * i + r)[16 * i + j] = x[r];
                 }
-                __syncthreads();
+                prep_sync();
                 // block row i: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, j < i; a task
                 // is one row r of block j and four adjacent columns 4*c4 ..
                 for (int i = 1; i < 4; ++i) {
@@ -441,7 +460,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                             *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
                         }
                     }
-                    __syncthreads();
+                    prep_sync();
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         const int qq = e + 128 * m;
@@ -464,7 +483,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                             y[m] = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                         }
                     }
-                    __syncthreads();
+                    prep_sync();
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         const int qq = e + 128 * m;
@@ -473,11 +492,11 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                             *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
                         }
                     }
-                    __syncthreads();
+                    prep_sync();
                 }
             }
             if (tid == 64) bulk_wait_all();  // the QK^T tiles have landed (T2 is rewritten next)
-            __syncthreads();
+            prep_sync();
             // ---- T' = T diag(beta e^G), T'' = T diag(beta): split into the A tiles
             for (int it = tid; it < 2 * kC * 8; it += kChunkThreads) {
                 const int hh = it >> 9, t = (it >> 3) & 63, ch = it & 7;
@@ -503,7 +522,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            __syncthreads();
+            prep_sync();
             tc_fence_after_sync();
             // ---- phase C: W = [T'_a; T'_b] K ; U~_x = [T''_a; T''_b] V_x
             if (tid == 0) {
@@ -528,7 +547,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 mma_commit(&bar_mma);
             }
             mma_pending = true;
-            if (any_failed(mbar_wait(&bar_mma, mma_phase))) {
+            if (prep_failed(mbar_wait(&bar_mma, mma_phase))) {
                 if (tid == 0) report_error(3);
                 failed = true;
                 break;
@@ -578,7 +597,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            __syncthreads();
+            prep_sync();
             tc_fence_after_sync();
             if (tid == 0) {
                 for (int hh = 0; hh < nb; ++hh) {
@@ -592,7 +611,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
                 bulk_commit();  // waited (reads) before T1 / T2 are next written
             }
-            __syncthreads();
+            prep_sync();
         }
         if (!failed && p.ready) pub = item;
     } while (false);
@@ -604,11 +623,11 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         if (tma_pending) mbar_wait(&bar_tma, tma_phase);
         if (v_pending) mbar_wait(&bar_v, v_phase);
     }
-    if (__syncthreads_or(mma_pending) && tid == 0) mbar_wait(&bar_mma, mma_phase);
+    if (prep_any(mma_pending) && tid == 0) mbar_wait(&bar_mma, mma_phase);
     if (tid == 0) bulk_wait_all();
     if (tid == 0 && pub >= 0) publish_item(p.ready + pub);
     tc_fence_before_sync();
-    __syncthreads();
+    prep_sync();
     tc_fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
@@ -630,28 +649,36 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 //   U = U~ - W S   (rows 0..63 of P4 = [W; Q] S),   S <- e^{G_last} S + K''^T U
 // (P7, K'' = diag(e^{G_last-G}) K, formed as K^T U' with U' = diag(e^{G_last-G})
 // U, so that the key tile is chunk_prep's copy of its input and the decay
-// factors, all <= 1, scale the fp32 U before it is split).  Every step of the
-// chain is spread over all eight warps: thread (warp w, lane l) owns key lane
-// 32 (w%4) + l of the state and value lanes 32 (w/4) .. +31 of this CTA's
-// slice, which is exactly the part of the tensor-memory accumulators that the
-// warp may read.  Per chunk c:
-//   1. thread 0 issues P4_c = [W; Q] S into D4[c%3]
-//   2. warps 0,1,4,5 (accumulator rows 0..63): U_c = U~ - W S -> smem;
-//      warps 2,3,6,7 (rows 64..127), meanwhile: the output of chunk c-2,
-//      o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t, gated RMSNorm (sums of squares
-//      exchanged with the peer CTA through distributed shared memory), store
-//   3. thread 0 issues P7_c = K^T U' -> Ds, then the previous chunk's output
-//      term P6_{c-1} = (M o QK^T) U_{c-1} into D6[(c-1)%3] (an MMA holds its
-//      issuing warp ~75 cycles per instruction: issued after P7 it delays
-//      neither P4 nor thread 0's own rows of U)
-//   4. all warps: S <- e^{G_last} S + Ds, re-split S into smem
-// Accumulators D4 and D6 have three slots and U two buffers, so that the
-// output can trail the chain by two chunks.  Every wait is bounded
-// (wait_or_dead).
+// factors, all <= 1, scale the fp32 U before it is split).
+//
+// Warp roles (12 warps launched at 168 registers a thread; a register split
+// gives the eight compute warps 192 and the control warpgroup 120, which adds
+// up to the launch's 384 x 168):
+//   warps 0..7  compute.  Thread (warp w, lane l) owns key lane 32 (w%4) + l
+//               of the state and value lanes 32 (w/4) .. +31 of this CTA's
+//               slice, which is exactly the part of the tensor-memory
+//               accumulators that the warp may read.  Warps 0,1,4,5
+//               (accumulator rows 0..63) form U_c; warps 2,3,6,7 (rows
+//               64..127) write the output of chunk c-1,
+//               o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t with the gated RMSNorm
+//               (sums of squares exchanged with the peer CTA through
+//               distributed shared memory); all eight update the state.
+//   warp 8      one lane issues every MMA: P4_c, then (once U_c is in shared
+//               memory) P7_c and the output term P6_c = (M o QK^T)_c U_c.
+//   warp 9      one lane issues every TMA load, each as soon as the MMA that
+//               read the buffer's previous contents is done (and, in the
+//               fused launch, the chunk's prep rows are published).
+// Split products: P4 and P7 (the chain) take the hi and lo halves of their B
+// operand side by side as one N=128 product, A_hi [B_hi | B_lo], plus
+// A_lo B_hi into the first half; the result is the sum of the accumulator's
+// two halves.  P6 (off the chain) is hi.hi + hi.lo + lo.hi into one N=64
+// accumulator.  Every wait is bounded (wait_or_dead).
 constexpr int kSplit = 2;
-constexpr int kDS = kD / kSplit;  // value lanes per CTA
+constexpr int kDS = kD / kSplit;      // value lanes per CTA
+constexpr int kScanThreads = 384;     // 8 compute warps + a control warpgroup
+constexpr int kComputeThreads = 256;
 // shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64
+constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64 (lo = 2nd N block)
 constexpr uint32_t kScanA4H = 32768, kScanA4L = 65536;      // [W; Q] K-major 128 x 128 (hi, lo)
 constexpr uint32_t kScanKH = 98304, kScanKL = 114688;       // K as MN-major A (dk 128 x t 64)
 constexpr uint32_t kScanBu = 131072;                        // U, MN-major 64 x 64: buffer b at
@@ -660,15 +687,21 @@ constexpr uint32_t kScanQk = 163840;                        // M o QK^T rows (K-
                                                             //   buffer b at +b*16384 (hi), +8192 (lo)
 constexpr uint32_t kScanUp = 196608;                        // U' = diag(e^{G_last-G}) U (hi, +8192 lo)
 constexpr uint32_t kScanEnd = 212992;
-// tensor-memory columns: D4 and D6 in three slots each (chunk c uses c%3)
-constexpr uint32_t kTmD4 = 0, kTmD6 = 192, kTmDs = 384;
+// tensor-memory columns: P4 in two 128-column slots (chunk c uses c%2), P7 in
+// 128 columns, P6 in two 64-column slots
+constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 384;
 
 struct ScanSync {
-    // p6 per accumulator slot: the output warps wait for it chunks later, and
-    // a slot's barrier is re-armed only once that slot's output has been read
-    uint64_t a4, k, qk[2], p4, p7, p6[3], u, x[2], xf[2];
+    uint64_t a4, k, qk[2];     // TMA loads landed
+    uint64_t s_lo, s_hi;       // S_c rows 0..63 / 64..127 split into shared memory (128 threads each)
+    uint64_t p4, p7, p6[2];    // MMA groups done (tcgen05.commit)
+    uint64_t u, u2;            // U'_c, then U_c, in shared memory (128 U threads)
+    uint64_t d4free[2];        // output warps have read slot c%2 of P4 and P6 (128 threads)
+    uint64_t x[2], xf[2];      // peer's sums of squares arrived / slot free
     int dead;
-    int n_a4, n_k, n_qk[2];  // TMA loads issued per barrier
+    int n_a4, n_k, n_qk[2];    // TMA loads issued per barrier (producer)
+    int n_commits;             // MMA groups committed (issuer)
+    uint32_t last_commit;      // barrier index and parity of the issuer's last commit
 };
 
 // Bounded wait that also gives up as soon as another thread of this CTA (or,
@@ -715,10 +748,6 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q = warp & 3, half = warp >> 2;
-    const int row = 32 * q + lane;       // accumulator lane: key lane / token row
-    const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice
-    const uint32_t lane_off = (32u * q) << 16;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int v0 = static_cast<int>(rank) * kDS;  // first value lane of this CTA
     const int hv_n = p.n_v_heads;
@@ -727,47 +756,29 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     const int c_begin = p.cu_chunks[n], n_ch = p.cu_chunks[n + 1] - c_begin;
     const size_t slab = ((size_t)n * hv_n + h) * kD * kD;
     const int qcol = hk * kD;
-    const bool is_u = q < 2;  // warps 0,1,4,5: accumulator rows 0..63
 
-    float S[32];  // S[row][v0 + cl .. +31]
-    if (p.state_in) {
-        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + v0 + cl);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = src[i];
-            S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) S[i] = 0.f;
-    }
-    auto store_s = [&] {
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
-            split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
-        }
-    };
-    store_s();
     if (tid < kDS) sNw[tid] = p.norm_w[v0 + tid];
     if (tid == 0) {
         mbar_init(&sy.a4, 1);
         mbar_init(&sy.k, 1); mbar_init(&sy.qk[0], 1); mbar_init(&sy.qk[1], 1);
+        mbar_init(&sy.s_lo, 128); mbar_init(&sy.s_hi, 128);
         mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1);
-        for (int i = 0; i < 3; ++i) mbar_init(&sy.p6[i], 1);
-        mbar_init(&sy.u, 128);
+        mbar_init(&sy.p6[0], 1); mbar_init(&sy.p6[1], 1);
+        mbar_init(&sy.u, 128); mbar_init(&sy.u2, 128);
+        mbar_init(&sy.d4free[0], 128); mbar_init(&sy.d4free[1], 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sy.x[i], 1);
             mbar_init(&sy.xf[i], 64);
         }
         sy.dead = 0;
         sy.n_a4 = sy.n_k = sy.n_qk[0] = sy.n_qk[1] = 0;
+        sy.n_commits = 0;
+        sy.last_commit = 0;
         fence_barrier_init();
         for (const CUtensorMap* m : {&map_qh, &map_ql, &map_wh, &map_wl, &map_kqh, &map_kql, &map_kwh, &map_kwl})
             tma_prefetch_desc(m);
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
-    fence_proxy_async_smem();
     tc_fence_before_sync();
     cluster_arrive();  // the peer's barriers are initialised before any remote arrive
     cluster_wait();
@@ -780,10 +791,12 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
     auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
     // Fused launch: chunk c's workspace rows come from prep CTAs running
-    // alongside; wait (bounded) for its item flag.  TMA loads of published
-    // rows follow a global proxy fence (in the issue_* helpers).
+    // alongside; the calling thread waits (bounded) for its item flag with a
+    // gpu-scope acquire before it reads them.  TMA loads of published rows
+    // follow a global proxy fence (in the issue_* helpers).
     auto wait_chunk = [&](int c) -> bool {
-        const int* f = p.ready + (size_t)(c_begin + c) * p.n_k_heads + hk;
+        if (!p.ready || c >= n_ch) return true;
+        const int* f = p.stall_flag ? p.stall_flag : p.ready + (size_t)(c_begin + c) * p.n_k_heads + hk;
         if (ld_acquire_gpu(f)) return true;
         const uint64_t t0 = globaltimer_ns();
         const long long c0 = clock64();
@@ -791,224 +804,314 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             __nanosleep(100);
             if (ld_acquire_gpu(f)) return true;
             if (*reinterpret_cast<volatile int*>(&sy.dead)) return false;
-            if (globaltimer_ns() - t0 > 2000000000ull || clock64() - c0 > (1ll << 32)) {
+            if (globaltimer_ns() - t0 > p.wait_ns || clock64() - c0 > (1ll << 32)) {
                 atomicExch(&sy.dead, 1);
                 report_error(11);
                 return false;
             }
         }
     };
-    auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
-        if (p.ready) fence_proxy_async_global();
-        mbar_arrive_expect_tx(&sy.a4, 8 * 8192);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tma_load_2d(smem + kScanA4H + b * 16384, &map_wh, &sy.a4, 64 * b, wrow(c));
-            tma_load_2d(smem + kScanA4L + b * 16384, &map_wl, &sy.a4, 64 * b, wrow(c));
-            tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_qh, &sy.a4, qcol + 64 * b, tok0(c));
-            tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_ql, &sy.a4, qcol + 64 * b, tok0(c));
-        }
-        sy.n_a4 += 1;
-    };
-    auto issue_k = [&](int c) {  // key rows of the chunk, both key-lane blocks (MN-major A)
-        if (p.ready) fence_proxy_async_global();
-        const int krow = ((c_begin + c) * p.n_k_heads + hk) * kC;
-        mbar_arrive_expect_tx(&sy.k, 4 * 8192);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            tma_load_2d(smem + kScanKH + b * 8192, &map_kwh, &sy.k, 64 * b, krow);
-            tma_load_2d(smem + kScanKL + b * 8192, &map_kwl, &sy.k, 64 * b, krow);
-        }
-        sy.n_k += 1;
-    };
-    auto issue_qk = [&](int c) {  // masked decayed Q K^T rows, into buffer c%2
-        const int b = c & 1;
-        if (p.ready) fence_proxy_async_global();
-        mbar_arrive_expect_tx(&sy.qk[b], 2 * 8192);
-        tma_load_2d(smem + kScanQk + b * 16384, &map_kqh, &sy.qk[b], 0, wrow(c));
-        tma_load_2d(smem + kScanQk + b * 16384 + 8192, &map_kql, &sy.qk[b], 0, wrow(c));
-        sy.n_qk[b] += 1;
-    };
-    if (tid == 0 && n_ch > 0 && (!p.ready || (wait_chunk(0) && (n_ch < 2 || wait_chunk(1))))) {
-        issue_a4(0);
-        issue_k(0);
-        issue_qk(0);
-        if (n_ch > 1) issue_qk(1);
-    }
-    if (p.ready) __syncthreads();  // chunks 0 and 1 are readable by every thread
 
-    // Shared-memory descriptors, computed once: a descriptor for address a + o
-    // is the one for a plus o >> 4 (the 14-bit start field cannot carry over,
-    // every address here is below 256 KB).
-    const uint64_t dA4 = desc_kmajor_sw128(smem_u32(smem + kScanA4H));
-    const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
-    const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
-    const uint64_t dUp = desc_mnmajor_sw128(smem_u32(smem + kScanUp), 8192);
-    const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
-    const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
-    constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
-    auto bu = [&](int b, int k) { return dBu + (uint64_t)b * kLo16 + k * 128; };  // U buffer b
-
-    // thread 0 issues every MMA; its last commit covers all of them
-    uint64_t* last_commit = nullptr;
-    uint32_t last_parity = 0;
-    const bool sigmoid_gate = p.act == 1;
-
-    float ut[32];   // U~ row (U warps), prefetched one chunk ahead
-    float gu = 0.f, glu = 0.f;  // G_t of that row and G_last of its chunk
-    uint4 zr[4];    // z row (output warps) of the chunk whose output is pending
-    float gz = 0.f; // G_t of that row
-    auto load_ut = [&](int c) {
-        gu = gcum(c, row);
-        glu = gcum(c, chunk_len(c) - 1);
-        const float4* src = reinterpret_cast<const float4*>(p.u_ws + (size_t)wrow(c) * kD) +
-                            ((v0 + cl) >> 2) * kC + row;  // [4-column group][row][4]
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = src[i * kC];
-            ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
-        }
-    };
-    auto load_z = [&](int c) {
-        const int t = row - 64;
-        gz = gcum(c, t);
-        if (t < chunk_len(c)) {
-            const uint4* zp = reinterpret_cast<const uint4*>(
-                p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0 + cl);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) zr[i] = zp[i];
-        }
-    };
-    if (n_ch > 0) {
-        if (is_u) load_ut(0);
-        else load_z(0);
-    }
-
-    // Output of chunk c (output warps, accumulator rows 64..127): needs P6_c done.
-    auto output = [&](int c) -> bool {
-        const int t = row - 64, s = c & 1, L = chunk_len(c);
-        const uint32_t slot = (uint32_t)(c % 3) * 64;
-        const float eg = __expf(gz);
-        bool ok = wait_or_dead(&sy.p6[c % 3], (c / 3) & 1, sy, 7);
-        float o[32];
-        if (ok) {
-            tc_fence_after_sync();
-            float b[32];
-            tmem_ld32(tmem + kTmD4 + slot + lane_off + cl, o);
-            tmem_ld32(tmem + kTmD6 + slot + lane_off + cl, b);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = fmaf(eg, o[j], b[j]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0.f;
-        }
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
-        sSq[half][t] = ss;
-        group_sync(1, 128);  // the output warps' halves of each row are in sSq
-        const float tot = sSq[0][t] + sSq[1][t];
-        if (ok && half == 0) {
-            // the peer's slot s is free once it has read chunk c-2 from it
-            ok = c < 2 || wait_or_dead(&sy.xf[s], ((c - 2) >> 1) & 1, sy, 10, true, peer_dead);
-            if (ok) {
-                if (t == 0) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
-                st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), tot,
-                             map_to_rank(smem_u32(&sy.x[s]), peer));
-            }
-        }
-        // while the peer's sums travel: o * norm_w * act(z)
-        if (sigmoid_gate) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float zz[8];
-                unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * sigmoidf_(zz[e]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float zz[8];
-                unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * siluf_(zz[e]);
-            }
-        }
-        ok = ok && wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
-        const float peer_tot = sx[s][t];
-        group_sync(1, 128);  // both halves have read sx[s] for this chunk
-        if (ok && half == 0) mbar_arrive_remote_relaxed(map_to_rank(smem_u32(&sy.xf[s]), peer), peer_tot);
-        if (ok && t < L) {  // gated RMSNorm of token t over all d_v lanes
-            const float rr = rsqrtf((tot + peer_tot) * (1.f / kD) + p.rms_eps);
-            uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
-                                                 (size_t)h * kD + v0 + cl);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
-                op[i] = pack_bf16x8(y);
-            }
-        }
-        tc_fence_before_sync();
-        return ok;
-    };
-
-    // log of the state decay over a chunk, loaded one chunk ahead
-    float gl_next = n_ch > 0 ? gcum(0, chunk_len(0) - 1) : 0.f;
-    // P6_c = (M o QK^T)_c U_c -> D6[c%3] (thread 0).  A rows 0..63 of this M=128
-    // operand are whatever precedes the QK^T rows in shared memory: they only
-    // reach accumulator rows 0..63 of D6, which nothing reads.
-    auto issue_p6 = [&](int c) {
-        if (!wait_or_dead(&sy.qk[c & 1], (c >> 1) & 1, sy, 8)) return;
-        tc_fence_after_sync();
-        const uint32_t id6 = idesc_bf16_f32(128, kDS, false, true);
-        const uint64_t dq = dQk + (uint64_t)(c & 1) * kLo16;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            mma3(tmem + kTmD6 + (uint32_t)(c % 3) * 64, dq + k * 2, dq + kLo8 + k * 2, bu(c & 1, k),
-                 bu(c & 1, k) + kLo8, id6, k > 0 ? 1u : 0u);
-        mma_commit(&sy.p6[c % 3]);
-        last_commit = &sy.p6[c % 3];
-        last_parity = (c / 3) & 1;
-    };
-    for (int c = 0; c < n_ch; ++c) {
-        const float gam = __expf(gl_next);  // state decay over chunk c
-        if (c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
-        // 1. P4_c = [W; Q] S into D4[c%3]
-        if (tid == 0) {
-            bool ok = wait_or_dead(&sy.a4, c & 1, sy, 4);
-            if (ok) {
+    if (warp >= 8) {
+        // ------------------------------------------------ control warpgroup
+        regs_dec<120>();
+        if (warp == 8 && lane == 0 && n_ch > 0) {
+            // MMA issuer.  Shared-memory descriptors, computed once: a
+            // descriptor for address a + o is the one for a plus o >> 4 (the
+            // 14-bit start field cannot carry over, every address here is below
+            // 256 KB).
+            const uint64_t dA4 = desc_kmajor_sw128(smem_u32(smem + kScanA4H));
+            const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
+            const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
+            const uint64_t dUp = desc_mnmajor_sw128(smem_u32(smem + kScanUp), 8192);
+            const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
+            const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
+            constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
+            const uint32_t id128 = idesc_bf16_f32(128, 2 * kDS, false, true);
+            const uint32_t id64 = idesc_bf16_f32(128, kDS, false, true);
+            const uint32_t id7_128 = idesc_bf16_f32(128, 2 * kDS, true, true);
+            const uint32_t id7_64 = idesc_bf16_f32(128, kDS, true, true);
+            uint32_t last = 0;  // (barrier index << 1) | parity of the last commit
+            int commits = 0;
+            for (int c = 0; c < n_ch; ++c) {
+                // P4_c = [W; Q] S_c into slot c%2: A_hi [S_hi | S_lo] + A_lo S_hi,
+                // the key lanes 0..63 as soon as the warps owning those state rows
+                // have stored them, then 64..127
+                if (!wait_or_dead(&sy.a4, c & 1, sy, 4) || !wait_or_dead(&sy.s_lo, c & 1, sy, 4))
+                    break;
+                // slot c%2 last held chunk c-2, whose output must have been read
+                // from it (the state rows 0..63 do not imply that)
+                if (c >= 2 && !wait_or_dead(&sy.d4free[c & 1], ((c - 2) >> 1) & 1, sy, 4)) break;
                 tc_fence_after_sync();
-                const uint32_t id = idesc_bf16_f32(128, kDS, false, true);
+                const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128;
+                bool hi_ok = true;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
+                    if (k == 4) {
+                        if (!(hi_ok = wait_or_dead(&sy.s_hi, c & 1, sy, 4))) break;
+                        tc_fence_after_sync();
+                    }
                     const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma3(tmem + kTmD4 + (uint32_t)(c % 3) * 64, dA4 + ao, dA4 + kLoA4 + ao,
-                         dBs + k * 128, dBs + kLo16 + k * 128, id, k > 0 ? 1u : 0u);
+                    mma_bf16(d4, dA4 + ao, dBs + k * 128, id128, k > 0 ? 1u : 0u);
+                    mma_bf16(d4, dA4 + kLoA4 + ao, dBs + k * 128, id64, 1u);
+                }
+                if (!hi_ok) {  // the MMAs already issued still complete before the unwind
+                    mma_commit(&sy.p4);
+                    last = (0u << 1) | (c & 1); ++commits;
+                    break;
                 }
                 mma_commit(&sy.p4);
-                last_commit = &sy.p4;
-                last_parity = c & 1;
+                last = (0u << 1) | (c & 1); ++commits;
+                // P7_c = K^T U'_c: K^T_hi [U'_hi | U'_lo] + K^T_lo U'_hi
+                if (!wait_or_dead(&sy.u, c & 1, sy, 6) || !wait_or_dead(&sy.k, c & 1, sy, 5)) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mma_bf16(tmem + kTmDs, dK + k * 128, dUp + k * 128, id7_128, k > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kTmDs, dK + kLo16 + k * 128, dUp + k * 128, id7_64, 1u);
+                }
+                mma_commit(&sy.p7);
+                last = (1u << 1) | (c & 1); ++commits;
+                // P6_c = (M o QK^T)_c U_c into slot c%2.  A rows 0..63 of this
+                // M=128 operand are whatever precedes the QK^T rows in shared
+                // memory: they only reach accumulator rows 0..63, which nothing
+                // reads.
+                if (!wait_or_dead(&sy.u2, c & 1, sy, 6) || !wait_or_dead(&sy.qk[c & 1], (c >> 1) & 1, sy, 8))
+                    break;
+                tc_fence_after_sync();
+                const uint64_t dq = dQk + (uint64_t)(c & 1) * kLo16;
+                const uint64_t bu = dBu + (uint64_t)(c & 1) * kLo16;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma3(tmem + kTmD6 + (uint32_t)(c & 1) * 64, dq + k * 2, dq + kLo8 + k * 2,
+                         bu + k * 128, bu + kLo8 + k * 128, id64, k > 0 ? 1u : 0u);
+                mma_commit(&sy.p6[c & 1]);
+                last = ((2u + (c & 1)) << 1) | ((c >> 1) & 1); ++commits;
+            }
+            sy.n_commits = commits;
+            sy.last_commit = last;
+        } else if (warp == 9 && lane == 0 && n_ch > 0) {
+            // TMA producer
+            auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
+                if (p.ready) fence_proxy_async_global();
+                mbar_arrive_expect_tx(&sy.a4, 8 * 8192);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_2d(smem + kScanA4H + b * 16384, &map_wh, &sy.a4, 64 * b, wrow(c));
+                    tma_load_2d(smem + kScanA4L + b * 16384, &map_wl, &sy.a4, 64 * b, wrow(c));
+                    tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_qh, &sy.a4, qcol + 64 * b, tok0(c));
+                    tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_ql, &sy.a4, qcol + 64 * b, tok0(c));
+                }
+                sy.n_a4 += 1;
+            };
+            auto issue_k = [&](int c) {  // key rows of the chunk, both key-lane blocks (MN-major A)
+                if (p.ready) fence_proxy_async_global();
+                const int krow = ((c_begin + c) * p.n_k_heads + hk) * kC;
+                mbar_arrive_expect_tx(&sy.k, 4 * 8192);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_2d(smem + kScanKH + b * 8192, &map_kwh, &sy.k, 64 * b, krow);
+                    tma_load_2d(smem + kScanKL + b * 8192, &map_kwl, &sy.k, 64 * b, krow);
+                }
+                sy.n_k += 1;
+            };
+            auto issue_qk = [&](int c) {  // masked decayed Q K^T rows, into buffer c%2
+                const int b = c & 1;
+                if (p.ready) fence_proxy_async_global();
+                mbar_arrive_expect_tx(&sy.qk[b], 2 * 8192);
+                tma_load_2d(smem + kScanQk + b * 16384, &map_kqh, &sy.qk[b], 0, wrow(c));
+                tma_load_2d(smem + kScanQk + b * 16384 + 8192, &map_kql, &sy.qk[b], 0, wrow(c));
+                sy.n_qk[b] += 1;
+            };
+            bool ok = wait_chunk(0) && wait_chunk(1);
+            if (ok) {
+                issue_a4(0);
+                issue_k(0);
+                issue_qk(0);
+                if (n_ch > 1) issue_qk(1);
+            }
+            for (int c = 0; ok && c + 1 < n_ch; ++c) {
+                // [W; Q]_{c+1} once P4_c has read [W; Q]_c
+                if (!(ok = wait_or_dead(&sy.p4, c & 1, sy, 5))) break;
+                issue_a4(c + 1);
+                // K_{c+1} once P7_c has read K_c
+                if (!(ok = wait_or_dead(&sy.p7, c & 1, sy, 5))) break;
+                issue_k(c + 1);
+                // QK^T_{c+2} into the buffer P6_c has read
+                if (c + 2 < n_ch) {
+                    if (!(ok = wait_chunk(c + 2) && wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7)))
+                        break;
+                    issue_qk(c + 2);
+                }
             }
         }
         __syncwarp();
-        // 2. U_c (rows 0..63) | output of chunk c-2 (rows 64..127)
-        if (is_u) {
-            const float eu = __expf(glu - gu);  // e^{G_last-G_t}, while P4_c runs
-            if (wait_or_dead(&sy.p4, c & 1, sy, 5)) {
-                tc_fence_after_sync();
-                if (tid == 128 && c + 1 < n_ch) issue_a4(c + 1);  // P4_c has read the [W; Q] tile
-                __syncwarp();
-                float ws[32];
-                tmem_ld32(tmem + kTmD4 + (uint32_t)(c % 3) * 64 + lane_off + cl, ws);
+    } else {
+        // ------------------------------------------------------ compute warps
+        regs_inc<192>();
+        const int q = warp & 3, half = warp >> 2;
+        const int row = 32 * q + lane;       // accumulator lane: key lane / token row
+        const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice
+        const uint32_t lane_off = (32u * q) << 16;
+        const bool is_u = q < 2;  // warps 0,1,4,5: accumulator rows 0..63
+        const bool sigmoid_gate = p.act == 1;
+
+        float S[32];  // S[row][v0 + cl .. +31]
+        if (p.state_in) {
+            const float4* src = reinterpret_cast<const float4*>(p.state_in + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) ut[j] -= ws[j];
-                // U' = e^{G_last-G_t} U_t first, for P7 (P7_{c-1} has read the
-                // last one); then U itself into buffer c%2 for P6_c, which is
-                // issued in the next chunk (buffer c%2 held U_{c-2}, whose
-                // product P6_{c-2} thread 0 issued before P4_c)
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = src[i];
+                S[4 * i] = v.x; S[4 * i + 1] = v.y; S[4 * i + 2] = v.z; S[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) S[i] = 0.f;
+        }
+        auto store_s = [&] {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                split_store(S + 8 * ch, smem + kScanBsH + o, smem + kScanBsL + o);
+            }
+        };
+        uint64_t* s_mine = is_u ? &sy.s_lo : &sy.s_hi;  // the barrier of this thread's state rows
+        store_s();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        mbar_arrive(s_mine);
+
+        float ut[32];   // U~ row (U warps), prefetched one chunk ahead
+        float gu = 0.f, glu = 0.f;  // G_t of that row and G_last of its chunk
+        uint4 zr[4];    // z row (output warps) of the chunk whose output is pending
+        float gz = 0.f; // G_t of that row
+        auto load_ut = [&](int c) {
+            gu = gcum(c, row);
+            glu = gcum(c, chunk_len(c) - 1);
+            const float4* src = reinterpret_cast<const float4*>(p.u_ws + (size_t)wrow(c) * kD) +
+                                ((v0 + cl) >> 2) * kC + row;  // [4-column group][row][4]
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = src[i * kC];
+                ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
+            }
+        };
+        auto load_z = [&](int c) {
+            const int t = row - 64;
+            gz = gcum(c, t);
+            if (t < chunk_len(c)) {
+                const uint4* zp = reinterpret_cast<const uint4*>(
+                    p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0 + cl);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) zr[i] = zp[i];
+            }
+        };
+        bool alive = n_ch == 0 || wait_chunk(0);
+        if (alive && n_ch > 0) {
+            if (is_u) load_ut(0);
+            else load_z(0);
+        }
+
+        // Output of chunk c (output warps, accumulator rows 64..127): needs P6_c.
+        // Every output warp makes the same calls (the named barriers inside
+        // must match); after a failure (alive_in false) no wait is made.
+        auto output = [&](int c, bool alive_in) -> bool {
+            const int t = row - 64, s = c & 1, L = chunk_len(c);
+            const float eg = __expf(gz);
+            bool ok = __all_sync(0xffffffffu, alive_in && wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7));
+            float o[32];
+            if (ok) {
+                tc_fence_after_sync();
+                float a[32], b[32];
+                const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
+                tmem_ld32x3(d4, d4 + 64, tmem + kTmD6 + (uint32_t)(c & 1) * 64 + lane_off + cl, a, b, o);
+                tc_fence_before_sync();
+                mbar_arrive(&sy.d4free[c & 1]);  // P4_{c+2} and P6_{c+2} may now reuse the slot
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = fmaf(eg, a[j] + b[j], o[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = 0.f;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
+            sSq[half][t] = ss;
+            group_sync(1, 128);  // the output warps' halves of each row are in sSq
+            const float tot = sSq[0][t] + sSq[1][t];
+            if (ok && half == 0) {
+                // the peer's slot s is free once it has read chunk c-2 from it
+                ok = c < 2 || wait_or_dead(&sy.xf[s], ((c - 2) >> 1) & 1, sy, 10, true, peer_dead);
+                if (ok) {
+                    if (t == 0) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
+                    st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), tot,
+                                 map_to_rank(smem_u32(&sy.x[s]), peer));
+                }
+            }
+            // while the peer's sums travel: o * norm_w * act(z)
+            if (sigmoid_gate) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float zz[8];
+                    unpack_bf16x8(zr[i], zz);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * sigmoidf_(zz[e]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float zz[8];
+                    unpack_bf16x8(zr[i], zz);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * siluf_(zz[e]);
+                }
+            }
+            ok = ok && wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
+            const float peer_tot = sx[s][t];
+            group_sync(1, 128);  // both halves have read sx[s] for this chunk
+            if (ok && half == 0) mbar_arrive_remote_relaxed(map_to_rank(smem_u32(&sy.xf[s]), peer), peer_tot);
+            if (ok && t < L) {  // gated RMSNorm of token t over all d_v lanes
+                const float rr = rsqrtf((tot + peer_tot) * (1.f / kD) + p.rms_eps);
+                uint4* op = reinterpret_cast<uint4*>(p.out + (size_t)(tok0(c) + t) * hv_n * kD +
+                                                     (size_t)h * kD + v0 + cl);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
+                    op[i] = pack_bf16x8(y);
+                }
+            }
+            return ok;
+        };
+
+        // log of the state decay over a chunk, loaded one chunk ahead
+        float gl_next = (alive && n_ch > 0) ? gcum(0, chunk_len(0) - 1) : 0.f;
+        // U warps leave the loop on a failure; output warps go through every
+        // iteration (with no waits) so that their named barriers stay matched.
+        for (int c = 0; c < n_ch; ++c) {
+            if (!alive && is_u) break;
+            const float gam = __expf(gl_next);  // state decay over chunk c
+            // chunk c+1 is read from here on (its decay, U~ rows, z gate)
+            if (alive) alive = wait_chunk(c + 1);
+            if (alive && c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
+            if (is_u) {
+                // U_c = U~ - W S_c (rows 0..63 of P4_c), U'_c = e^{G_last-G_t} U_c
+                const float eu = __expf(glu - gu);  // while P4_c runs
+                // warp-uniform: the tensor-memory loads below are warp-collective
+                if (!(alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p4, c & 1, sy, 5)))) break;
+                tc_fence_after_sync();
+                {
+                    float a[32], b[32];
+                    const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
+                    tmem_ld32x2(d4, d4 + 64, a, b);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ut[j] -= a[j] + b[j];
+                }
+                // U' for P7_c (P7_{c-1} has read the last one), then U for P6_c
+                // into buffer c%2 (P6_{c-2} has read U_{c-2}): both readers are
+                // done once P4_c is, which the issuer committed after them.  Only
+                // U' is on the chain.
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
@@ -1022,96 +1125,70 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 mbar_arrive(&sy.u);
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t o = (c & 1) * 16384 + row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
-                    split_store(ut + 8 * ch, smem + kScanBu + o, smem + kScanBu + 8192 + o);
+                    const uint32_t ob = (c & 1) * 16384 + row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                    split_store(ut + 8 * ch, smem + kScanBu + ob, smem + kScanBu + 8192 + ob);
                 }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                mbar_arrive(&sy.u2);
                 if (c + 1 < n_ch) load_ut(c + 1);
+            } else if (c > 0) {
+                // the output of chunk c-1 while the chain computes U_c
+                alive = output(c - 1, alive) && alive;
+                if (alive) load_z(c);
             }
-        } else {
-            if (c > 1) {
-                output(c - 2);
-                load_z(c - 1);
-            }
-            // chunk c+2 is first read in chunk c+1 (its cumulative decay, its
-            // [W; Q] and U~ rows): its flag is awaited before this chunk's
-            // closing barrier
-            if (p.ready && tid == 64 && c + 2 < n_ch) wait_chunk(c + 2);
-        }
-        // 3. P7_c = K''^T U = K^T U' -> Ds, then the previous chunk's output term
-        if (tid == 0) {
-            const bool ok = wait_or_dead(&sy.u, c & 1, sy, 6) && wait_or_dead(&sy.k, c & 1, sy, 5);
-            if (ok) {
+            // S_{c+1} = e^{G_last} S_c + K''^T U_c ; refresh the split copy
+            alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p7, c & 1, sy, 6));
+            if (alive) {
                 tc_fence_after_sync();
-                const uint32_t id7 = idesc_bf16_f32(128, kDS, true, true);
+                float a[32], b[32];
+                const uint32_t ds = tmem + kTmDs + lane_off + cl;
+                tmem_ld32x2(ds, ds + 64, a, b);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, dUp + k * 128,
-                         dUp + kLo8 + k * 128, id7, k > 0 ? 1u : 0u);
-                mma_commit(&sy.p7);
-                last_commit = &sy.p7;
-                last_parity = c & 1;
-                // behind P7 in the pipe: delays neither P4 nor this warp's rows of U
-                if (c > 0) issue_p6(c - 1);
+                for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], a[j] + b[j]);
+                if (c + 1 < n_ch) {
+                    store_s();
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    mbar_arrive(s_mine);
+                }
             }
         }
-        __syncwarp();
-        // 4. S <- e^{G_last} S + K''^T U ; refresh the split copy
-        if (wait_or_dead(&sy.p7, c & 1, sy, 6)) {
-            tc_fence_after_sync();
-            float ds[32];
-            tmem_ld32(tmem + kTmDs + lane_off + cl, ds);
+        if (n_ch > 0 && !is_u) alive = output(n_ch - 1, alive) && alive;
+        if (alive && p.state_out) {
+            float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], ds[j]);
-            store_s();
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead))) break;
-        tc_fence_after_sync();
-        if (tid == 32) {  // off thread 0, which goes on to P4_{c+1}
-            if (c + 1 < n_ch) issue_k(c + 1);  // P7_c has read K_c
-            // QK^T_{c+1} (for P6_{c+1}, issued in chunk c+2) into the buffer P6_{c-1} has read
-            if (c > 0 && c + 1 < n_ch && wait_or_dead(&sy.p6[(c - 1) % 3], ((c - 1) / 3) & 1, sy, 7))
-                issue_qk(c + 1);
-        }
-    }
-    const bool alive = !__syncthreads_or(*reinterpret_cast<volatile int*>(&sy.dead));
-    if (alive && n_ch > 0) {
-        if (tid == 0) issue_p6(n_ch - 1);  // the last chunk's output term
-        __syncwarp();
-        if (!is_u) {  // the two outputs still pending
-            if (n_ch > 1) {
-                output(n_ch - 2);
-                load_z(n_ch - 1);
-            }
-            output(n_ch - 1);
-        }
+        if (!alive) atomicExch(&sy.dead, 1);
     }
 
     // Unwind: no copy or MMA of this CTA may still be in flight when it leaves.
+    tc_fence_before_sync();
     __syncthreads();
+    tc_fence_after_sync();
     if (tid == 0) {
         if (sy.n_a4 > 0) mbar_wait(&sy.a4, (sy.n_a4 - 1) & 1);
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
         for (int b = 0; b < 2; ++b)
             if (sy.n_qk[b] > 0) mbar_wait(&sy.qk[b], (sy.n_qk[b] - 1) & 1);
-    }
-    if (last_commit) mbar_wait(last_commit, last_parity);
-    if (p.state_out && !sy.dead) {
-        float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + v0 + cl);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+        if (sy.n_commits > 0) {
+            const uint32_t idx = sy.last_commit >> 1, par = sy.last_commit & 1;
+            uint64_t* bar = idx == 0 ? &sy.p4 : idx == 1 ? &sy.p7 : &sy.p6[idx - 2];
+            mbar_wait(bar, par);
+        }
     }
     // No CTA may leave while its peer can still reach its shared memory.
     tc_fence_before_sync();
+    __syncthreads();
     cluster_arrive();
     cluster_wait();
     tc_fence_after_sync();
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kScanThreads, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
@@ -1130,14 +1207,20 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // (sequence, value head), and read a chunk's rows only after its flag is set,
 // so the scan of chunk c overlaps the prep of the chunks after it.  Prep CTAs
 // never wait for scan CTAs: the launch completes whichever of its CTAs are
-// resident at a time.
-__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kChunkThreads, 1)
+// resident at a time.  A prep CTA's control warpgroup hands its registers to
+// the eight prep warps and leaves.
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kScanThreads, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                    const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                    const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                    const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                    ChunkArgs p, int n_prep) {
     if ((int)blockIdx.x < n_prep) {
+        if (threadIdx.x >= kComputeThreads) {
+            regs_dec<120>();
+            return;
+        }
+        regs_inc<192>();
         chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
                         blockIdx.x, n_prep);
     } else {
@@ -1175,7 +1258,7 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     l.kw_hi = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
     l.kw_lo = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
     l.gcum = off; off = up(off + crow * 4);
-    l.ready = off; off = up(off + (size_t)chunks * n_k_heads * 4);
+    l.ready = off; off = up(off + ((size_t)chunks * n_k_heads + 1) * 4);  // + one never set (test hook)
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
     if (lay) *lay = l;
@@ -1194,7 +1277,7 @@ static int fused_capacity(size_t smem) {
                              static_cast<int>(smem));
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(2 * kSplit);
-        cfg.blockDim = dim3(kChunkThreads);
+        cfg.blockDim = dim3(kScanThreads);
         cfg.dynamicSmemBytes = smem;
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, chunk_fused_kernel, &cfg) != cudaSuccess) {
@@ -1247,7 +1330,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         cv.cu_chunks = cu_chunks;
         cv.chunk_info = reinterpret_cast<int2*>(ws + l.chunk_info);
         cv.ready = reinterpret_cast<int*>(ws + l.ready);
-        cv.n_ready = l.n_chunks * hk_n;
+        cv.n_ready = l.n_chunks * hk_n + 1;
         // a longest-first launch order for the two-kernel scan (quadratic in
         // the sequence count, so only for batches of up to 1024 sequences)
         if (a.n_seq > 1 && a.n_seq <= 1024) cv.seq_order = reinterpret_cast<int32_t*>(ws + l.seq_order);
@@ -1278,6 +1361,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     p.qk_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.qk_lo);
     p.gcum_ws = reinterpret_cast<float*>(ws + l.gcum);
     p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.wait_ns = 2000000000ull;
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
@@ -1329,8 +1413,12 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     }
     if (n_prep > 0) {
         p.ready = reinterpret_cast<int*>(ws + l.ready);
+        if (a.stall) {  // the flag after the items' ones: cleared by the prologue, never set
+            p.stall_flag = p.ready + n_items;
+            p.wait_ns = 1000000ull;
+        }
         return timed_launch("chunk_fused", st, [&] {
-            chunk_fused_kernel<<<dim3(n_prep + scan_ctas), kChunkThreads, std::max(prep_smem, scan_smem),
+            chunk_fused_kernel<<<dim3(n_prep + scan_ctas), kScanThreads, std::max(prep_smem, scan_smem),
                                  st>>>(m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p, n_prep);
             return cudaGetLastError();
         });
@@ -1344,7 +1432,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     e = timed_launch("chunk_scan", st, [&] {
-        chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kChunkThreads, scan_smem, st>>>(
+        chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kScanThreads, scan_smem, st>>>(
             m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p);
         return cudaGetLastError();
     });

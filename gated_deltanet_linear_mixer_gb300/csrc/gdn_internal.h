@@ -108,6 +108,10 @@ struct ChunkArgs {
     float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
     __nv_bfloat16* out;           // [T, Hv*dv]
     int* ready;                   // [chunks, Hk] item done flags (fused launch), else null
+    // Test hook (fused launch): when set, the scan waits on this flag, which
+    // nothing sets, for at most wait_ns, so that its bounded wait runs out.
+    const int* stall_flag;
+    unsigned long long wait_ns;   // limit of the scan's wait for a chunk's prep rows
 };
 
 // Byte offsets of the chunked path's workspace regions.
@@ -142,6 +146,7 @@ struct ChunkLaunch {
     void* out;
     void* workspace;
     ChunkLayout layout;
+    int stall;             // test hook: the fused scan waits on a flag nothing sets
 };
 
 // Workspace size (and layout) of the chunked path for this sequence layout.

@@ -15,6 +15,8 @@
 namespace gdn {
 // Records the thread's error message (defined with the other entry points).
 gdn_status set_error(gdn_status st, const char* fn, const char* fmt, ...);
+// GDN_ERR_INJECTED when the environment variable GDN_FAULT lists `site`.
+gdn_status inject_fault(const char* site, const char* fn);
 }  // namespace gdn
 
 namespace {
@@ -106,6 +108,7 @@ extern "C" gdn_status gdn_layer_prefill(const gdn_dims* dims, const gdn_params* 
         return gdn::set_error(GDN_ERR_WORKSPACE, fn,
                               "a 256-byte aligned workspace of %zu bytes is needed (%zu given)", need,
                               workspace ? workspace_bytes : (size_t)0);
+    if ((st = gdn::inject_fault("layer", fn)) != GDN_OK) return st;
     const int T = cu_seqlens_host[n_seq];
     size_t core_bytes = 0;
     gdn_prefill_workspace_size(dims, n_seq, cu_seqlens_host, &core_bytes);

@@ -4,8 +4,11 @@
 // workspace, or a serving loop that has fixed its memory before the first
 // request.  Such a caller cannot size and pass the scratch memory that
 // gdn_prefill asks for, so this entry point brings its own: one file-scope
-// device array, created when the library is loaded and held by every GPU that
-// loads it until the process exits.
+// device array.  It becomes resident on a device when this module is loaded
+// there; under CUDA's default lazy module loading that is the first
+// gdn_prefill_noalloc call on the device (its cudaGetSymbolAddress), which is
+// why that call belongs in the caller's set-up.  It then stays resident until
+// the process exits.
 //
 // Nothing here allocates: no cudaMalloc, cudaFree or allocating library
 // routine.  The array's device address is looked up once per device with
@@ -41,7 +44,9 @@ std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up on the
-// first call for that device.
+// first call for that device and kept (like the library's other per-device
+// state, it assumes the device's primary context lives as long as the process;
+// a cudaDeviceReset voids it).
 gdn_status scratch_address(void** ptr, const char* fn) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);

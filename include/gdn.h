@@ -37,6 +37,16 @@
  * - Buffers must be 16-byte aligned (x, z, out, states, qkv_out).
  * - A call takes at most GDN_MAX_SEQUENCES sequences (kernels index them on
  *   the second grid dimension); larger batches are refused before any launch.
+ * - Failure injection (testing a caller's failure path, as cortiq-engine
+ *   0.8.76 pipeline.rs does with its test-only nll_test_fail_at): the environment variable GDN_FAULT
+ *   is a comma-separated list of sites -- conv, prefill, decode, verify,
+ *   commit, layer, or all.  A call whose site is listed validates its
+ *   arguments, then returns GDN_ERR_INJECTED without enqueuing anything, so
+ *   every caller buffer is left as it was.  The site stall_scan is a device
+ *   test hook: a bf16 prefill that takes the fused tensor-core launch makes
+ *   its scan wait (for at most 1 ms) on a chunk flag that nothing sets, so
+ *   that the bounded wait runs out; the call returns GDN_OK and the next
+ *   gdn_sync_status reports GDN_ERR_TIMEOUT.  GDN_FAULT is read on every call.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -56,7 +66,9 @@ typedef enum gdn_status {
     GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size or cu_seqlens, misalignment */
     GDN_ERR_UNSUPPORTED = 2, /* geometry the kernels are not built for */
     GDN_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    GDN_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+    GDN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+    GDN_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (gdn_sync_status) */
+    GDN_ERR_INJECTED = 6     /* a fault injected through GDN_FAULT (testing) */
 } gdn_status;
 
 typedef enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
@@ -162,13 +174,18 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
  * The pages have no counterpart: their CPU loop needs no scratch memory.
  *   Arguments are those of gdn_prefill without the workspace; the scratch is
  *   a built-in device array of gdn_prefill_noalloc_scratch_bytes() bytes
- *   (64 MiB) that every GPU loading the library holds until the process exits.
+ *   (64 MiB).  It becomes resident on a device when the library's module is
+ *   loaded there -- under CUDA's default lazy module loading, during the first
+ *   gdn_prefill_noalloc call on that device -- and stays until the process
+ *   exits, so a caller whose memory is fixed up front makes that first call in
+ *   its set-up.
  *   A sequence layout needing more (gdn_prefill_workspace_size) is refused
  *   with GDN_ERR_WORKSPACE and nothing is enqueued; at Hk=16, Hv=32,
  *   d_k=d_v=128 the limit is a few hundred tokens per call.
  *   No call allocates: the first call on a device looks up the array's
  *   device address (cudaGetSymbolAddress) with that device current, so make
- *   that first call before any stream capture begins.
+ *   that first call before any stream capture begins.  The address is kept
+ *   per device for the life of the process; a cudaDeviceReset voids it.
  *   Every call on a device shares the one array: calls that can overlap on
  *   the GPU (on different streams, or from different threads without an
  *   ordering between them) race and give wrong results.  Calls ordered on one
@@ -294,6 +311,16 @@ size_t gdn_timing_report(char* buf, size_t buf_len);
  * *code (0 = no error) and clears it when reset != 0.
  */
 gdn_status gdn_device_error(int32_t* code, int32_t reset);
+
+/*
+ * gdn_sync_status -- waits for `stream` (cudaStream_t as void*), then reads and
+ * clears the device error word: GDN_ERR_TIMEOUT if a bounded device wait gave
+ * up since the last check (the outputs and states of the calls since then are
+ * invalid and must be recomputed; the CUDA context stays usable), GDN_ERR_CUDA
+ * if the stream reports a CUDA error, else GDN_OK.  A serving loop calls it
+ * where it would synchronize anyway, and fails the affected requests closed.
+ */
+gdn_status gdn_sync_status(void* stream);
 
 /* Message for the last failed call on this thread ("" if none). */
 const char* gdn_last_error(void);

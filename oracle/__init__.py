@@ -28,17 +28,22 @@ _lock = threading.Lock()
 _lib = None
 
 
+_LIB_F32_PATH = os.path.join(_HERE, "libgdn_oracle_f32.so")
+
+
 def build(force: bool = False) -> str:
-    """Compile ``gdn_oracle.c`` into ``libgdn_oracle.so`` next to it (gcc, OpenMP)."""
+    """Compile ``gdn_oracle.c`` into ``libgdn_oracle.so`` next to it (gcc, OpenMP,
+    double precision), and the same source with ``-DORACLE_REAL=float`` into
+    ``libgdn_oracle_f32.so`` (the CPU baseline the benchmark times)."""
     with _lock:
-        stale = (not os.path.exists(_LIB_PATH)) or (
-            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
-        if force or stale:
-            tmp = _LIB_PATH + f".tmp{os.getpid()}"
-            cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-                   "-o", tmp, _SRC, "-lm"]
-            subprocess.run(cmd, check=True)
-            os.replace(tmp, _LIB_PATH)
+        for path, extra in ((_LIB_PATH, []), (_LIB_F32_PATH, ["-DORACLE_REAL=float"])):
+            stale = (not os.path.exists(path)) or (os.path.getmtime(path) < os.path.getmtime(_SRC))
+            if force or stale:
+                tmp = path + f".tmp{os.getpid()}"
+                cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", *extra,
+                       "-o", tmp, _SRC, "-lm"]
+                subprocess.run(cmd, check=True)
+                os.replace(tmp, path)
     return _LIB_PATH
 
 
@@ -224,6 +229,40 @@ def gdn(d: Dims, cu_seqlens, x, z, a, b, conv_w, A_log, dt_bias, norm_w,
     return res
 
 
+_lib_f32 = None
+
+
+def gdn_f32(d: Dims, cu_seqlens, x, z, a, b, conv_w, A_log, dt_bias, norm_w,
+            conv_state=None, state=None):
+    """The whole core (a1..a6) from the float build of the same source, for
+    timing only (the CPU baseline): inputs are cast to float32, and the result
+    is ``out`` [T, Hv*dv] (float32).  Parity always uses the double build."""
+    global _lib_f32
+    if _lib_f32 is None:
+        build()
+        lib = ctypes.CDLL(_LIB_F32_PATH)
+        lib.oracle_gdn.argtypes = [ctypes.POINTER(_Dims), ctypes.c_int] + [ctypes.c_void_p] * 20
+        lib.oracle_gdn.restype = ctypes.c_int
+        _lib_f32 = lib
+    cu = _cu(cu_seqlens)
+    n = cu.size - 1
+    t = int(cu[-1])
+    f = lambda v: None if v is None else np.ascontiguousarray(np.asarray(v, dtype=np.float32))  # noqa: E731
+    x, z, a, b, conv_w, A_log, dt_bias, norm_w = map(f, (x, z, a, b, conv_w, A_log, dt_bias, norm_w))
+    cs_in, s_in = f(conv_state), f(state)
+    out = np.empty((t, d.n_v_heads * d.d_v), dtype=np.float32)
+    cs_out = np.empty((n, d.conv_dim, d.conv_k - 1), dtype=np.float32)
+    s_out = np.empty((n, d.n_v_heads, d.d_k, d.d_v), dtype=np.float32)
+    dd = d._c()
+    rc = _lib_f32.oracle_gdn(ctypes.byref(dd), n, _ptr(cu), _ptr(x), _ptr(z), _ptr(a), _ptr(b),
+                             _ptr(conv_w), _ptr(A_log), _ptr(dt_bias), _ptr(norm_w), _ptr(cs_in),
+                             _ptr(cs_out), _ptr(s_in), _ptr(s_out), None, _ptr(out),
+                             None, None, None, None, None)
+    if rc != 0:
+        raise MemoryError("oracle_gdn (float build) could not allocate its scratch")
+    return out
+
+
 def round_bf16(x):
     """Nearest bf16 value (ties to even) of each element, as float64.
 
@@ -252,5 +291,5 @@ def layer(d: Dims, cu_seqlens, h, w_qkv, w_z, w_a, w_b, w_out, conv_w, A_log, dt
     return res
 
 
-__all__ = ["Dims", "build", "conv", "normalize", "gates", "recurrence", "gated_norm", "gdn",
+__all__ = ["Dims", "build", "conv", "normalize", "gates", "recurrence", "gated_norm", "gdn", "gdn_f32",
            "round_bf16", "layer"]

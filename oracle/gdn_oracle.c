@@ -31,11 +31,20 @@
  *
  * parity: every function here is pinned by tests/test_oracle_pins.py.
  */
-#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <tgmath.h>
+
+/* The arithmetic type.  The parity build is double (the default); the CPU
+ * baseline that the benchmark times is the same code built with
+ * -DORACLE_REAL=float (tgmath.h picks exp/sqrt/log1p of that type).  The eps
+ * fields of oracle_dims stay double in both builds. */
+#ifndef ORACLE_REAL
+#define ORACLE_REAL double
+#endif
+typedef ORACLE_REAL real;
 
 typedef struct {
     int32_t n_k_heads;  /* Hk: linear_num_key_heads   */
@@ -55,12 +64,12 @@ static int conv_dim(const oracle_dims* d) {
     return 2 * d->n_k_heads * d->d_k + d->n_v_heads * d->d_v;
 }
 
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
-static double silu(double x) { return x * sigmoid(x); }
+static real sigmoid(real x) { return 1.0 / (1.0 + exp(-x)); }
+static real silu(real x) { return x * sigmoid(x); }
 
 /* [qwen.rs] DeltaRule::run: softplus is the identity above 20, else
  * ln(1 + e^x).  log1p is the same function with less rounding. */
-static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
+static real softplus(real x) { return x > 20.0 ? x : log1p(exp(x)); }
 
 /*
  * Step a1 + a2: causal depthwise conv with SiLU, and the conv-state update.
@@ -75,20 +84,21 @@ static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
  * NULL, and may alias conv_state_in.
  */
 void oracle_conv(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
-                 const double* x, const double* conv_w,
-                 const double* conv_state_in, double* c, double* conv_state_out) {
+                 const real* x, const real* conv_w,
+                 const real* conv_state_in, real* c, real* conv_state_out) {
     const int cd = conv_dim(d);
     const int kc = d->conv_k;
     const int keep = kc - 1;
     for (int n = 0; n < n_seq; ++n) {
         const int bos = cu_seqlens[n];
         const int len = cu_seqlens[n + 1] - bos;
+#pragma omp parallel for schedule(static)
         for (int i = 0; i < len; ++i) {
             for (int ch = 0; ch < cd; ++ch) {
-                double s = 0.0;
+                real s = 0.0;
                 for (int j = 0; j < kc; ++j) {
                     const int src = i - (kc - 1) + j;
-                    double v;
+                    real v;
                     if (src >= 0) {
                         v = x[(size_t)(bos + src) * cd + ch];
                     } else if (conv_state_in) {
@@ -107,7 +117,7 @@ void oracle_conv(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
         const int bos = cu_seqlens[n];
         const int len = cu_seqlens[n + 1] - bos;
         for (int ch = 0; ch < cd; ++ch) {
-            double nw[8];
+            real nw[8];
             for (int slot = 0; slot < keep; ++slot) {
                 const int ti = len - keep + slot;
                 if (ti >= 0) {
@@ -131,30 +141,31 @@ void oracle_conv(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
  * "only q receives 1/sqrt(dk)".  v is passed through unchanged.
  * Outputs: q_hat, k_hat [T, Hk, dk]; v [T, Hv, dv].
  */
-void oracle_normalize(const oracle_dims* d, int n_tok, const double* c,
-                      double* q_hat, double* k_hat, double* v) {
+void oracle_normalize(const oracle_dims* d, int n_tok, const real* c,
+                      real* q_hat, real* k_hat, real* v) {
     const int cd = conv_dim(d);
     const int hk_n = d->n_k_heads, dk = d->d_k;
     const int key_dim = hk_n * dk, value_dim = d->n_v_heads * d->d_v;
-    const double qscale = 1.0 / sqrt((double)dk);
+    const real qscale = 1.0 / sqrt((real)dk);
+#pragma omp parallel for schedule(static)
     for (int t = 0; t < n_tok; ++t) {
-        const double* row = c + (size_t)t * cd;
+        const real* row = c + (size_t)t * cd;
         for (int h = 0; h < hk_n; ++h) {
-            const double* qv = row + h * dk;
-            const double* kv = row + key_dim + h * dk;
-            double qss = 0.0, kss = 0.0;
+            const real* qv = row + h * dk;
+            const real* kv = row + key_dim + h * dk;
+            real qss = 0.0, kss = 0.0;
             for (int i = 0; i < dk; ++i) {
                 qss += qv[i] * qv[i];
                 kss += kv[i] * kv[i];
             }
-            const double qn_inv = 1.0 / sqrt(qss + d->l2_eps);
-            const double kn_inv = 1.0 / sqrt(kss + d->l2_eps);
+            const real qn_inv = 1.0 / sqrt(qss + d->l2_eps);
+            const real kn_inv = 1.0 / sqrt(kss + d->l2_eps);
             for (int i = 0; i < dk; ++i) {
                 q_hat[((size_t)t * hk_n + h) * dk + i] = qv[i] * qn_inv * qscale;
                 k_hat[((size_t)t * hk_n + h) * dk + i] = kv[i] * kn_inv;
             }
         }
-        memcpy(v + (size_t)t * value_dim, row + 2 * key_dim, sizeof(double) * value_dim);
+        memcpy(v + (size_t)t * value_dim, row + 2 * key_dim, sizeof(real) * value_dim);
     }
 }
 
@@ -165,15 +176,16 @@ void oracle_normalize(const oracle_dims* d, int n_tok, const double* c,
  * decay_coef = -exp(A_log), or the GGUF ssm_a read as decay_coef directly
  * (d->decay_coef); [cpu.rs] deltanet (beta, g, decay = g.exp()).
  */
-void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double* b,
-                  const double* A_log, const double* dt_bias, double* g, double* beta) {
+void oracle_gates(const oracle_dims* d, int n_tok, const real* a, const real* b,
+                  const real* A_log, const real* dt_bias, real* g, real* beta) {
     const int hv_n = d->n_v_heads;
     const int nc = d->per_channel ? d->d_k : 1; /* decays per value head */
+#pragma omp parallel for schedule(static)
     for (int t = 0; t < n_tok; ++t) {
         for (int h = 0; h < hv_n; ++h) {
             const size_t i = (size_t)t * hv_n + h;
             beta[i] = sigmoid(b[i]);
-            const double coef = d->decay_coef ? A_log[h] : -exp(A_log[h]);
+            const real coef = d->decay_coef ? A_log[h] : -exp(A_log[h]);
             for (int j = 0; j < nc; ++j)
                 g[i * nc + j] = coef * softplus(a[i * nc + j] + dt_bias[(size_t)h * nc + j]);
         }
@@ -197,9 +209,9 @@ void oracle_gates(const oracle_dims* d, int n_tok, const double* a, const double
  * thread pool); this loop runs them on OpenMP threads in the same way.
  */
 void oracle_recurrence(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
-                       const double* q_hat, const double* k_hat, const double* v,
-                       const double* g, const double* beta,
-                       const double* state_in, double* state_out, double* inter, double* o) {
+                       const real* q_hat, const real* k_hat, const real* v,
+                       const real* g, const real* beta,
+                       const real* state_in, real* state_out, real* inter, real* o) {
     const int hk_n = d->n_k_heads, hv_n = d->n_v_heads, dk = d->d_k, dv = d->d_v;
     const int group = hv_n / hk_n;
     const size_t slab = (size_t)dk * dv;
@@ -209,44 +221,44 @@ void oracle_recurrence(const oracle_dims* d, int n_seq, const int32_t* cu_seqlen
             const int hk = d->tiled ? hv % hk_n : hv / group;
             const int bos = cu_seqlens[n];
             const int len = cu_seqlens[n + 1] - bos;
-            double* s = (double*)malloc(sizeof(double) * slab);
-            double* kv_mem = (double*)malloc(sizeof(double) * dv);
-            double* delta = (double*)malloc(sizeof(double) * dv);
+            real* s = (real*)malloc(sizeof(real) * slab);
+            real* kv_mem = (real*)malloc(sizeof(real) * dv);
+            real* delta = (real*)malloc(sizeof(real) * dv);
             if (state_in)
-                memcpy(s, state_in + ((size_t)n * hv_n + hv) * slab, sizeof(double) * slab);
+                memcpy(s, state_in + ((size_t)n * hv_n + hv) * slab, sizeof(real) * slab);
             else
-                memset(s, 0, sizeof(double) * slab);
+                memset(s, 0, sizeof(real) * slab);
             for (int i = 0; i < len; ++i) {
                 const size_t t = (size_t)bos + i;
-                const double* qh = q_hat + (t * hk_n + hk) * dk;
-                const double* kh = k_hat + (t * hk_n + hk) * dk;
-                const double* vh = v + (t * hv_n + hv) * dv;
+                const real* qh = q_hat + (t * hk_n + hk) * dk;
+                const real* kh = k_hat + (t * hk_n + hk) * dk;
+                const real* vh = v + (t * hv_n + hv) * dv;
                 /* one decay per value head, or one per key channel (row ik) */
-                const double* gt = g + (t * hv_n + hv) * (d->per_channel ? dk : 1);
-                const double bt = beta[t * hv_n + hv];
+                const real* gt = g + (t * hv_n + hv) * (d->per_channel ? dk : 1);
+                const real bt = beta[t * hv_n + hv];
                 for (int iv = 0; iv < dv; ++iv) kv_mem[iv] = 0.0;
                 for (int ik = 0; ik < dk; ++ik) {
-                    double* row = s + (size_t)ik * dv;
-                    const double decay = exp(gt[d->per_channel ? ik : 0]);
+                    real* row = s + (size_t)ik * dv;
+                    const real decay = exp(gt[d->per_channel ? ik : 0]);
                     for (int iv = 0; iv < dv; ++iv) {
                         row[iv] *= decay;
                         kv_mem[iv] += row[iv] * kh[ik];
                     }
                 }
                 for (int iv = 0; iv < dv; ++iv) delta[iv] = (vh[iv] - kv_mem[iv]) * bt;
-                double* oh = o + (t * hv_n + hv) * dv;
+                real* oh = o + (t * hv_n + hv) * dv;
                 for (int iv = 0; iv < dv; ++iv) oh[iv] = 0.0;
                 for (int ik = 0; ik < dk; ++ik) {
-                    double* row = s + (size_t)ik * dv;
+                    real* row = s + (size_t)ik * dv;
                     for (int iv = 0; iv < dv; ++iv) {
                         row[iv] += kh[ik] * delta[iv];
                         oh[iv] += row[iv] * qh[ik];
                     }
                 }
-                if (inter) memcpy(inter + (t * hv_n + hv) * slab, s, sizeof(double) * slab);
+                if (inter) memcpy(inter + (t * hv_n + hv) * slab, s, sizeof(real) * slab);
             }
             if (state_out)
-                memcpy(state_out + ((size_t)n * hv_n + hv) * slab, s, sizeof(double) * slab);
+                memcpy(state_out + ((size_t)n * hv_n + hv) * slab, s, sizeof(real) * slab);
             free(s);
             free(kv_mem);
             free(delta);
@@ -261,18 +273,19 @@ void oracle_recurrence(const oracle_dims* d, int n_seq, const int32_t* cu_seqlen
  * head" (SiLU gate); [cpu.rs] deltanet (rms_norm then sigmoid gate when
  * output_gate_type is "sigmoid").  act: 0 = SiLU, 1 = sigmoid.
  */
-void oracle_gated_norm(const oracle_dims* d, int n_tok, const double* o, const double* z,
-                       const double* norm_w, double* y) {
+void oracle_gated_norm(const oracle_dims* d, int n_tok, const real* o, const real* z,
+                       const real* norm_w, real* y) {
     const int hv_n = d->n_v_heads, dv = d->d_v;
+#pragma omp parallel for schedule(static)
     for (int t = 0; t < n_tok; ++t) {
         for (int h = 0; h < hv_n; ++h) {
             const size_t base = ((size_t)t * hv_n + h) * dv;
-            double ss = 0.0;
+            real ss = 0.0;
             for (int j = 0; j < dv; ++j) ss += o[base + j] * o[base + j];
-            const double r = 1.0 / sqrt(ss / dv + d->rms_eps);
+            const real r = 1.0 / sqrt(ss / dv + d->rms_eps);
             for (int j = 0; j < dv; ++j) {
-                const double zz = z[base + j];
-                const double gate = d->act == 1 ? sigmoid(zz) : silu(zz);
+                const real zz = z[base + j];
+                const real gate = d->act == 1 ? sigmoid(zz) : silu(zz);
                 y[base + j] = o[base + j] * r * norm_w[j] * gate;
             }
         }
@@ -287,26 +300,26 @@ void oracle_gated_norm(const oracle_dims* d, int n_tok, const double* o, const d
  * Returns 0, or -1 when scratch could not be allocated.
  */
 int oracle_gdn(const oracle_dims* d, int n_seq, const int32_t* cu_seqlens,
-               const double* x, const double* z, const double* a, const double* b,
-               const double* conv_w, const double* A_log, const double* dt_bias,
-               const double* norm_w,
-               const double* conv_state_in, double* conv_state_out,
-               const double* state_in, double* state_out, double* inter, double* out,
-               double* q_hat_out, double* k_hat_out, double* v_out,
-               double* g_out, double* beta_out) {
+               const real* x, const real* z, const real* a, const real* b,
+               const real* conv_w, const real* A_log, const real* dt_bias,
+               const real* norm_w,
+               const real* conv_state_in, real* conv_state_out,
+               const real* state_in, real* state_out, real* inter, real* out,
+               real* q_hat_out, real* k_hat_out, real* v_out,
+               real* g_out, real* beta_out) {
     const int cd = conv_dim(d);
     const size_t n_tok = (size_t)cu_seqlens[n_seq];
     const size_t key_n = n_tok * d->n_k_heads * d->d_k;
     const size_t val_n = n_tok * d->n_v_heads * d->d_v;
     const size_t gate_n = n_tok * d->n_v_heads;
     const size_t decay_n = gate_n * (d->per_channel ? d->d_k : 1);
-    double* c = (double*)malloc(sizeof(double) * (n_tok * cd + 1));
-    double* qh = q_hat_out ? q_hat_out : (double*)malloc(sizeof(double) * (key_n + 1));
-    double* kh = k_hat_out ? k_hat_out : (double*)malloc(sizeof(double) * (key_n + 1));
-    double* vv = v_out ? v_out : (double*)malloc(sizeof(double) * (val_n + 1));
-    double* gg = g_out ? g_out : (double*)malloc(sizeof(double) * (decay_n + 1));
-    double* bb = beta_out ? beta_out : (double*)malloc(sizeof(double) * (gate_n + 1));
-    double* o = (double*)malloc(sizeof(double) * (val_n + 1));
+    real* c = (real*)malloc(sizeof(real) * (n_tok * cd + 1));
+    real* qh = q_hat_out ? q_hat_out : (real*)malloc(sizeof(real) * (key_n + 1));
+    real* kh = k_hat_out ? k_hat_out : (real*)malloc(sizeof(real) * (key_n + 1));
+    real* vv = v_out ? v_out : (real*)malloc(sizeof(real) * (val_n + 1));
+    real* gg = g_out ? g_out : (real*)malloc(sizeof(real) * (decay_n + 1));
+    real* bb = beta_out ? beta_out : (real*)malloc(sizeof(real) * (gate_n + 1));
+    real* o = (real*)malloc(sizeof(real) * (val_n + 1));
     int rc = 0;
     if (!c || !qh || !kh || !vv || !gg || !bb || !o) {
         rc = -1;

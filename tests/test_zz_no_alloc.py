@@ -85,6 +85,43 @@ def test_noalloc_prefill_matches_the_workspace_entry_point_on_two_calls():
     assert gdn.device_error(reset=True) == 0
 
 
+def test_noalloc_call_allocates_no_device_memory():
+    """After a first call (set-up: it makes the built-in array resident and looks
+    up its address), a call with another sequence layout changes neither the
+    device's free memory nor PyTorch's allocations: the call itself allocates
+    nothing.  Every buffer it is handed is allocated before the measurement."""
+    case_a, case_b = _case(44, [90, 30]), _case(45, [129, 3, 64])
+    ta, tb = upload(case_a), upload(case_b)
+    status, _, _, _ = _noalloc(case_a, ta)  # set-up call
+    assert status == gdn.GDN_OK, gdn.load().gdn_last_error().decode()
+    lib = gdn.load()
+    d, _ = dims(case_b)
+    n, dev = case_b.n_seq, tb["x"].device
+    cu_h = torch.from_numpy(case_b.cu_seqlens.astype(np.int32).copy())
+    st_out = torch.empty((n, d.n_v_heads, d.d_k, d.d_v), device=dev)
+    cs_out = torch.empty((n, d.conv_dim, d.conv_k - 1), dtype=d.dtype, device=dev)
+    out = torch.empty((case_b.n_tokens, d.n_v_heads * d.d_v), dtype=d.dtype, device=dev)
+    dd, pp = d.c(), tb["params"].c(d)
+    p = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(2):
+        status = lib.gdn_prefill_noalloc(
+            ctypes.byref(dd), ctypes.byref(pp), n, p(tb["cu"]), ctypes.c_void_p(cu_h.data_ptr()),
+            p(tb["x"]), p(tb["z"]), p(tb["a"]), p(tb["b"]), p(tb["conv_state"]), p(cs_out),
+            p(tb["state"]), p(st_out), p(out), stream)
+        assert status == gdn.GDN_OK, lib.gdn_last_error().decode()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0
+    ref_out, ref_st, _ = _regular(case_b, tb)
+    assert rel_err(out, ref_out.float().cpu().numpy()) < TOL["bf16"]
+    assert rel_err(st_out, ref_st.cpu().numpy()) < TOL["bf16"]
+
+
 def test_noalloc_refuses_a_layout_beyond_its_scratch():
     lib = gdn.load()
     limit = int(lib.gdn_prefill_noalloc_scratch_bytes())
