@@ -154,6 +154,78 @@ __device__ __forceinline__ float* prep_tf(uint8_t* smem, int hh, int row) {
     return reinterpret_cast<float*>(smem + kPrepAg + (hh * 2 + (row >> 5)) * 16384 + (row & 31) * 256);
 }
 
+// The solve's fp32 64 x 64 tiles (A, T) are row-major with their 16-byte
+// chunks XOR-swizzled by the row: chunk c of row r sits at chunk c ^ (r & 15).
+// Row vectors and the column reads of mma fragments are both free of bank
+// conflicts.  Offset (in floats) of column col within row r:
+__device__ __forceinline__ int swz_col(int r, int col) {
+    return (((col >> 2) ^ (r & 15)) << 2) + (col & 3);
+}
+
+// Warp-level bf16 tensor-core product (m16n8k16, fp32 accumulation) for the
+// 16 x 16 blocks of the triangular solve.  Operands are split like the
+// tcgen05 ones (hi = bf16(x), lo = bf16(x - hi)) and every product is
+// hi.hi + hi.lo + lo.hi.  Fragment layouts (lane = 4 g + q):
+//   A 16 x 16: a0 (g, 2q..2q+1), a1 (g+8, 2q..), a2 (g, 2q+8..), a3 (g+8, 2q+8..)
+//   B 16 x 8:  b0 (k = 2q..2q+1, n = g), b1 (k = 2q+8..2q+9, n = g)
+//   C 16 x 8:  c0, c1 (g, 2q..2q+1), c2, c3 (g+8, 2q..2q+1)
+// so the two C tiles of a 16 x 16 result are, element for element, the A
+// fragment of a following product.
+struct SplitA { uint32_t h[4], l[4]; };
+struct SplitB { uint32_t h[2], l[2]; };
+
+__device__ __forceinline__ void split2(float x, float y, uint32_t& h, uint32_t& l) {
+    h = pack_bf16x2(x, y);
+    l = pack_bf16x2(x - __uint_as_float(h << 16), y - __uint_as_float(h & 0xFFFF0000u));
+}
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// A fragment of block (bi, bj) of a swizzled tile given by its row pointers.
+template <class Rows>
+__device__ __forceinline__ SplitA solve_load_a(Rows rows, int bi, int bj, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    SplitA a;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = 16 * bi + g + 8 * (k & 1), c = 16 * bj + 2 * q + 8 * (k >> 1);
+        const float2 v = *reinterpret_cast<const float2*>(rows(r) + swz_col(r, c));
+        split2(v.x, v.y, a.h[k], a.l[k]);
+    }
+    return a;
+}
+// D (16 x 16, two C tiles) = A B (+ D), B = block (bk, bn) of a swizzled tile.
+template <class Rows>
+__device__ __forceinline__ void solve_mma(float (*d)[4], const SplitA& a, Rows rows, int bk, int bn,
+                                          int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * bn + 8 * nt + g;
+        SplitB b;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = 16 * bk + 2 * q + 8 * k;
+            split2(rows(r)[swz_col(r, c)], rows(r + 1)[swz_col(r + 1, c)], b.h[k], b.l[k]);
+        }
+        mma16816(d[nt], a.h, b.h[0], b.h[1]);
+        mma16816(d[nt], a.h, b.l[0], b.l[1]);
+        mma16816(d[nt], a.l, b.h[0], b.h[1]);
+    }
+}
+__device__ __forceinline__ SplitA solve_c_to_a(const float (*d)[4]) {
+    SplitA a;
+    split2(d[0][0], d[0][1], a.h[0], a.l[0]);
+    split2(d[0][2], d[0][3], a.h[1], a.l[1]);
+    split2(d[1][0], d[1][1], a.h[2], a.l[2]);
+    split2(d[1][2], d[1][3], a.h[3], a.l[3]);
+    return a;
+}
+
 // An item is published (p.ready non-null) once all of its workspace writes
 // have landed: the TMA stores completed, then a gpu-scope release that also
 // covers the other threads' stores (they precede it through the CTA barrier).
@@ -390,12 +462,20 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                             split_store(f, st + o, st + 8192 + o);
                         }
                         (void)h;
-                    } else {  // A^T[s][t] = beta_t e^{G_t-G_s} k_t.k_s for s < t
-                        float* sAt = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384);
+                    } else {  // A[t][s] = beta_t e^{G_t-G_s} k_t.k_s for s < t, row t, swizzled
+                        float* sA = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384) + t * kC;
                         const float bt = sBeta[r * kC + t];
 #pragma unroll
-                        for (int s = 0; s < kC; ++s)
-                            sAt[s * kC + t] = s < t ? bt * __expf(Gt - Gr[s]) * v[s] : 0.f;
+                        for (int c4 = 0; c4 < 16; ++c4) {
+                            float f[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int s = 4 * c4 + e;
+                                f[e] = s < t ? bt * __expf(Gt - Gr[s]) * v[s] : 0.f;
+                            }
+                            *reinterpret_cast<float4*>(sA + ((c4 ^ (t & 15)) << 2)) =
+                                make_float4(f[0], f[1], f[2], f[3]);
+                        }
                     }
                 }
             }
@@ -409,90 +489,79 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
                 bulk_commit();
             }
-            // ---- phase B: T = (I + A)^-1 per head, 16 x 16 blocks, fp32
+            // ---- phase B: T = (I + A)^-1 per head, by 16 x 16 blocks (4 warps a head)
+            // diagonal blocks T_ii = (I + A_ii)^-1 by forward substitution in fp32,
+            // one warp each; then with Y_ij = T_ii A_ij (i > j),
+            //   T_ij = -sum_{k=j}^{i-1} Y_ik T_kj
+            // one block distance i - j per step, on the warp tensor cores
             {
-                const int hh = tid >> 7, e = tid & 127;
-                const float* sAt = reinterpret_cast<const float*>(smem + kPrepT1 + hh * 16384);
-                auto A = [&](int row, int col) { return sAt[col * kC + row]; };
-                if (e < 64) {  // diagonal blocks: column j of (I + A_ii)^-1
-                    const int i = e >> 4, j = e & 15;
-                    float x[16];
+                const int hh = warp >> 2, w = warp & 3;
+                if (hh < nb) {
+                    float* sAf = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384);
+                    auto rowsA = [&](int r) { return sAf + r * kC; };
+                    auto rowsT = [&](int r) { return prep_tf(smem, hh, r); };
+                    const uint32_t bar = 2 + hh;  // named barrier of this head's four warps
+                    {   // T_ww, column j per lane (lanes 16..31 repeat lanes 0..15)
+                        const int i = w, j = lane & 15;
+                        float x[16];
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        float acc = r == j ? 1.f : 0.f;
+                        for (int r = 0; r < 16; ++r) {
+                            // row r of A_ii as 16-byte chunks (those left of the diagonal)
+                            const int row = 16 * i + r;
+                            float a16[16];
 #pragma unroll
-                        for (int s = 0; s < r; ++s) acc = fmaf(-A(16 * i + r, 16 * i + s), x[s], acc);
-                        x[r] = acc;
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) prep_tf(smem, hh, 16 * i + r)[16 * i + j] = x[r];
-                }
-                prep_sync();
-                // block row i: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, j < i; a task
-                // is one row r of block j and four adjacent columns 4*c4 ..
-                for (int i = 1; i < 4; ++i) {
-                    float4 y[2];
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int qq = e + 128 * m;
-                        if (qq < 64 * i) {
-                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
-                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int k = j; k < i; ++k) {
-                                const float* ar = sAt + (16 * k) * kC + 16 * i + r;
-                                const float* tb = prep_tf(smem, hh, 16 * k) + 16 * j + 4 * c4;
-#pragma unroll
-                                for (int u = 0; u < 16; ++u) {
-                                    const float a = ar[u * kC];
-                                    const float4 tv = *reinterpret_cast<const float4*>(tb + u * 64);
-                                    acc.x = fmaf(a, tv.x, acc.x); acc.y = fmaf(a, tv.y, acc.y);
-                                    acc.z = fmaf(a, tv.z, acc.z); acc.w = fmaf(a, tv.w, acc.w);
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                if (4 * c4 < r) {
+                                    const float4 v4 = *reinterpret_cast<const float4*>(
+                                        rowsA(row) + (((4 * i + c4) ^ (row & 15)) << 2));
+                                    a16[4 * c4] = v4.x; a16[4 * c4 + 1] = v4.y;
+                                    a16[4 * c4 + 2] = v4.z; a16[4 * c4 + 3] = v4.w;
                                 }
                             }
-                            y[m] = acc;
+                            float acc = r == j ? 1.f : 0.f;
+#pragma unroll
+                            for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-a16[s2], x[s2], acc);
+                            x[r] = acc;
+                            asm volatile("" ::: "memory");  // one row's loads at a time
+                        }
+                        if (lane < 16) {
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) rowsT(16 * i + r)[swz_col(16 * i + r, 16 * i + j)] = x[r];
                         }
                     }
+                    group_sync(bar, 128);
+                    SplitA y[3];  // Y_wk, k < w
+                    if (w > 0) {
+                        const SplitA tw = solve_load_a(rowsT, w, w, lane);
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int qq = e + 128 * m;
-                        if (qq < 64 * i) {
-                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
-                            *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
-                        }
-                    }
-                    prep_sync();
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int qq = e + 128 * m;
-                        if (qq < 64 * i) {
-                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
-                            const float* tr = prep_tf(smem, hh, 16 * i + r) + 16 * i;
-                            const float* pb = prep_tf(smem, hh, 16 * i) + 16 * j + 4 * c4;
-                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int s4 = 0; s4 < 4; ++s4) {
-                                const float4 tv = *reinterpret_cast<const float4*>(tr + 4 * s4);
-                                const float ts[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const float4 pv = *reinterpret_cast<const float4*>(pb + (4 * s4 + q) * 64);
-                                    acc.x = fmaf(ts[q], pv.x, acc.x); acc.y = fmaf(ts[q], pv.y, acc.y);
-                                    acc.z = fmaf(ts[q], pv.z, acc.z); acc.w = fmaf(ts[q], pv.w, acc.w);
-                                }
+                        for (int k = 0; k < 3; ++k) {
+                            if (k < w) {
+                                float d[2][4] = {};
+                                solve_mma(d, tw, rowsA, w, k, lane);
+                                y[k] = solve_c_to_a(d);
                             }
-                            y[m] = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                         }
                     }
-                    prep_sync();
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int qq = e + 128 * m;
-                        if (qq < 64 * i) {
-                            const int j = qq >> 6, r = (qq >> 2) & 15, c4 = qq & 3;
-                            *reinterpret_cast<float4*>(prep_tf(smem, hh, 16 * i + r) + 16 * j + 4 * c4) = y[m];
+                    for (int dist = 1; dist < 4; ++dist) {
+                        if (dist > 1) group_sync(bar, 128);  // T blocks of distance < dist are stored
+                        if (w >= dist) {
+                            const int j = w - dist;
+                            float d[2][4] = {};
+#pragma unroll
+                            for (int k = 0; k < 3; ++k)
+                                if (k >= j && k < w) solve_mma(d, y[k], rowsT, k, j, lane);
+                            const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                const int r0 = 16 * w + g, c = 16 * j + 8 * nt + 2 * q;
+                                *reinterpret_cast<float2*>(rowsT(r0) + swz_col(r0, c)) =
+                                    make_float2(-d[nt][0], -d[nt][1]);
+                                *reinterpret_cast<float2*>(rowsT(r0 + 8) + swz_col(r0 + 8, c)) =
+                                    make_float2(-d[nt][2], -d[nt][3]);
+                            }
                         }
                     }
-                    prep_sync();
                 }
             }
             if (tid == 64) bulk_wait_all();  // the QK^T tiles have landed (T2 is rewritten next)
@@ -504,12 +573,15 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 // blocks above the diagonal are zero (never written by the solve)
                 if (hh < nb && (ch >> 1) <= (t >> 4)) {
                     const int r = 2 * pr + hh;
-                    const float* tr = prep_tf(smem, hh, t) + 8 * ch;
+                    const float* tr = prep_tf(smem, hh, t);
+                    const float4 ta = *reinterpret_cast<const float4*>(tr + swz_col(t, 8 * ch));
+                    const float4 tb = *reinterpret_cast<const float4*>(tr + swz_col(t, 8 * ch + 4));
+                    const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int s = 8 * ch + e;
-                        f1[e] = tr[e] * sCs1[r * kC + s];
-                        f2[e] = tr[e] * sCs2[r * kC + s];
+                        f1[e] = tv[e] * sCs1[r * kC + s];
+                        f2[e] = tv[e] * sCs2[r * kC + s];
                     }
                 } else {
 #pragma unroll
@@ -652,8 +724,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // factors, all <= 1, scale the fp32 U before it is split).
 //
 // Warp roles (12 warps launched at 168 registers a thread; a register split
-// gives the eight compute warps 192 and the control warpgroup 120, which adds
-// up to the launch's 384 x 168):
+// gives the eight compute warps 200 and the control warpgroup 96: 256 x 200 +
+// 128 x 96 = 63,488, within the launch's 384 x 168 = 64,512):
 //   warps 0..7  compute.  Thread (warp w, lane l) owns key lane 32 (w%4) + l
 //               of the state and value lanes 32 (w/4) .. +31 of this CTA's
 //               slice, which is exactly the part of the tensor-memory
@@ -662,12 +734,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 //               64..127) write the output of chunk c-1,
 //               o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t with the gated RMSNorm
 //               (sums of squares exchanged with the peer CTA through
-//               distributed shared memory); all eight update the state.
-//   warp 8      one lane issues every MMA: P4_c, then (once U_c is in shared
-//               memory) P7_c and the output term P6_c = (M o QK^T)_c U_c.
-//   warp 9      one lane issues every TMA load, each as soon as the MMA that
-//               read the buffer's previous contents is done (and, in the
-//               fused launch, the chunk's prep rows are published).
+//               distributed shared memory), reading their accumulators before
+//               their share of the state update and finishing after it; all
+//               eight update the state.
+//   warp 8      one lane issues the chain's MMAs: P4_c, then, once U'_c is in
+//               shared memory, P7_c.
+//   warp 9      one lane issues every TMA and bulk copy, each as soon as the
+//               readers of the buffer's previous contents are done (and, in the
+//               fused launch, the chunk's prep rows are published), and the
+//               output term P6_c = (M o QK^T)_c U_c once P7_c is done, so that
+//               it runs in the pipe while the state is updated.
+//   warps 10,11 the gate norm_w act(z) of each chunk, from its z rows, into
+//               shared memory for the output warps.
 // Split products: P4 and P7 (the chain) take the hi and lo halves of their B
 // operand side by side as one N=128 product, A_hi [B_hi | B_lo], plus
 // A_lo B_hi into the first half; the result is the sum of the accumulator's
@@ -681,27 +759,33 @@ constexpr int kComputeThreads = 256;
 constexpr uint32_t kScanBsH = 0, kScanBsL = 16384;          // S, MN-major 128 x 64 (lo = 2nd N block)
 constexpr uint32_t kScanA4H = 32768, kScanA4L = 65536;      // [W; Q] K-major 128 x 128 (hi, lo)
 constexpr uint32_t kScanKH = 98304, kScanKL = 114688;       // K as MN-major A (dk 128 x t 64)
-constexpr uint32_t kScanBu = 131072;                        // U, MN-major 64 x 64: buffer b at
-                                                            //   +b*16384 (hi), +8192 (lo)
-constexpr uint32_t kScanQk = 163840;                        // M o QK^T rows (K-major 64 x 64):
-                                                            //   buffer b at +b*16384 (hi), +8192 (lo)
-constexpr uint32_t kScanUp = 196608;                        // U' = diag(e^{G_last-G}) U (hi, +8192 lo)
-constexpr uint32_t kScanEnd = 212992;
+constexpr uint32_t kScanBu = 131072;                        // U, MN-major 64 x 64 (hi, +8192 lo)
+constexpr uint32_t kScanQk = 147456;                        // M o QK^T rows, K-major 64 x 64 (hi, +8192 lo)
+constexpr uint32_t kScanUp = 163840;                        // U' = diag(e^{G_last-G}) U (hi, +8192 lo)
+constexpr uint32_t kScanGate = 180224;                      // norm_w act(z), fp32 64 x 64 (rows 256 B,
+                                                            //   16-byte chunks swizzled by the row)
+constexpr uint32_t kScanUt = 196608;                        // U~ of the chunk, fp32 [16 groups][64][4]
+constexpr uint32_t kScanZ = 212992;                         // z rows, bf16 64 x 64 (TMA, 128-byte swizzle)
+constexpr uint32_t kScanGc = 221184;                        // in-chunk cumulative log-decay, 2 x 64 fp32
+constexpr uint32_t kScanEnd = 221696;
 // tensor-memory columns: P4 in two 128-column slots (chunk c uses c%2), P7 in
 // 128 columns, P6 in two 64-column slots
 constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 384;
 
 struct ScanSync {
-    uint64_t a4, k, qk[2];     // TMA loads landed
+    uint64_t a4, k, qk;        // TMA loads landed
     uint64_t s_lo, s_hi;       // S_c rows 0..63 / 64..127 split into shared memory (128 threads each)
     uint64_t p4, p7, p6[2];    // MMA groups done (tcgen05.commit)
     uint64_t u, u2;            // U'_c, then U_c, in shared memory (128 U threads)
     uint64_t d4free[2];        // output warps have read slot c%2 of P4 and P6 (128 threads)
+    uint64_t gate;             // the gate warps have written the gate (64 threads)
+    uint64_t ug, zf;           // U~ and G of a chunk, its z rows, landed (bulk copies)
     uint64_t x[2], xf[2];      // peer's sums of squares arrived / slot free
     int dead;
-    int n_a4, n_k, n_qk[2];    // TMA loads issued per barrier (producer)
+    int n_a4, n_k, n_qk, n_ug, n_zf;  // copies issued per barrier (producer)
     int n_commits;             // MMA groups committed (issuer)
     uint32_t last_commit;      // barrier index and parity of the issuer's last commit
+    int n_p6;                  // P6 groups committed (producer)
 };
 
 // Bounded wait that also gives up as soon as another thread of this CTA (or,
@@ -737,7 +821,8 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
                                                 const CUtensorMap& map_kqh, const CUtensorMap& map_kql,
                                                 const CUtensorMap& map_kwh, const CUtensorMap& map_kwl,
-                                                const ChunkArgs& p, const int h, const int n) {
+                                                const CUtensorMap& map_z, const ChunkArgs& p, const int h,
+                                                const int n) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -760,22 +845,25 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     if (tid < kDS) sNw[tid] = p.norm_w[v0 + tid];
     if (tid == 0) {
         mbar_init(&sy.a4, 1);
-        mbar_init(&sy.k, 1); mbar_init(&sy.qk[0], 1); mbar_init(&sy.qk[1], 1);
+        mbar_init(&sy.k, 1); mbar_init(&sy.qk, 1);
         mbar_init(&sy.s_lo, 128); mbar_init(&sy.s_hi, 128);
         mbar_init(&sy.p4, 1); mbar_init(&sy.p7, 1);
         mbar_init(&sy.p6[0], 1); mbar_init(&sy.p6[1], 1);
         mbar_init(&sy.u, 128); mbar_init(&sy.u2, 128);
         mbar_init(&sy.d4free[0], 128); mbar_init(&sy.d4free[1], 128);
+        mbar_init(&sy.gate, 64);
+        mbar_init(&sy.ug, 1); mbar_init(&sy.zf, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sy.x[i], 1);
             mbar_init(&sy.xf[i], 64);
         }
         sy.dead = 0;
-        sy.n_a4 = sy.n_k = sy.n_qk[0] = sy.n_qk[1] = 0;
+        sy.n_a4 = sy.n_k = sy.n_qk = sy.n_ug = sy.n_zf = 0;
         sy.n_commits = 0;
+        sy.n_p6 = 0;
         sy.last_commit = 0;
         fence_barrier_init();
-        for (const CUtensorMap* m : {&map_qh, &map_ql, &map_wh, &map_wl, &map_kqh, &map_kql, &map_kwh, &map_kwl})
+        for (const CUtensorMap* m : {&map_qh, &map_ql, &map_wh, &map_wl, &map_kqh, &map_kql, &map_kwh, &map_kwl, &map_z})
             tma_prefetch_desc(m);
     }
     if (warp == 0) tmem_alloc(&tmem_slot, 512);
@@ -789,7 +877,6 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     auto wrow = [&](int c) { return ((c_begin + c) * hv_n + h) * kC; };
     auto tok0 = [&](int c) { return bos + c * kC; };
     auto chunk_len = [&](int c) { return min(kC, eos - tok0(c)); };
-    auto gcum = [&](int c, int t) { return p.gcum_ws[(size_t)wrow(c) + t]; };
     // Fused launch: chunk c's workspace rows come from prep CTAs running
     // alongside; the calling thread waits (bounded) for its item flag with a
     // gpu-scope acquire before it reads them.  TMA loads of published rows
@@ -814,7 +901,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
 
     if (warp >= 8) {
         // ------------------------------------------------ control warpgroup
-        regs_dec<120>();
+        regs_dec<96>();
         if (warp == 8 && lane == 0 && n_ch > 0) {
             // MMA issuer.  Shared-memory descriptors, computed once: a
             // descriptor for address a + o is the one for a plus o >> 4 (the
@@ -824,9 +911,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             const uint64_t dBs = desc_mnmajor_sw128(smem_u32(smem + kScanBsH), 16384);
             const uint64_t dK = desc_mnmajor_sw128(smem_u32(smem + kScanKH), 8192);
             const uint64_t dUp = desc_mnmajor_sw128(smem_u32(smem + kScanUp), 8192);
-            const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
-            const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
-            constexpr uint64_t kLo16 = 16384 >> 4, kLo8 = 8192 >> 4, kLoA4 = 32768 >> 4;
+            constexpr uint64_t kLo16 = 16384 >> 4, kLoA4 = 32768 >> 4;
             const uint32_t id128 = idesc_bf16_f32(128, 2 * kDS, false, true);
             const uint32_t id64 = idesc_bf16_f32(128, kDS, false, true);
             const uint32_t id7_128 = idesc_bf16_f32(128, 2 * kDS, true, true);
@@ -872,24 +957,39 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 }
                 mma_commit(&sy.p7);
                 last = (1u << 1) | (c & 1); ++commits;
-                // P6_c = (M o QK^T)_c U_c into slot c%2.  A rows 0..63 of this
-                // M=128 operand are whatever precedes the QK^T rows in shared
-                // memory: they only reach accumulator rows 0..63, which nothing
-                // reads.
-                if (!wait_or_dead(&sy.u2, c & 1, sy, 6) || !wait_or_dead(&sy.qk[c & 1], (c >> 1) & 1, sy, 8))
-                    break;
-                tc_fence_after_sync();
-                const uint64_t dq = dQk + (uint64_t)(c & 1) * kLo16;
-                const uint64_t bu = dBu + (uint64_t)(c & 1) * kLo16;
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma3(tmem + kTmD6 + (uint32_t)(c & 1) * 64, dq + k * 2, dq + kLo8 + k * 2,
-                         bu + k * 128, bu + kLo8 + k * 128, id64, k > 0 ? 1u : 0u);
-                mma_commit(&sy.p6[c & 1]);
-                last = ((2u + (c & 1)) << 1) | ((c >> 1) & 1); ++commits;
             }
             sy.n_commits = commits;
             sy.last_commit = last;
+        } else if (warp >= 10 && n_ch > 0) {
+            // gate warps: norm_w act(z) of token row t = 32 (warp - 10) + lane of
+            // each chunk, from its z rows, once the output warps have read the
+            // previous chunk's gate
+            const int t = 32 * (warp - 10) + lane;
+            const bool sigmoid_gate = p.act == 1;
+            float* gb = reinterpret_cast<float*>(smem + kScanGate) + t * kC;
+            const uint8_t* zrow = smem + kScanZ + t * 128;
+            for (int c = 0; c < n_ch; ++c) {
+                if (!wait_or_dead(&sy.zf, c & 1, sy, 12) ||
+                    (c > 0 && !wait_or_dead(&sy.d4free[(c - 1) & 1], ((c - 1) >> 1) & 1, sy, 9)))
+                    break;
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {  // 16-byte chunk i of the z row: value lanes 8i .. 8i+7
+                    float zz[8], gv[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(zrow + ((i ^ (t & 7)) << 4)), zz);
+                    if (sigmoid_gate) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gv[e] = sNw[8 * i + e] * sigmoidf_(zz[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gv[e] = sNw[8 * i + e] * siluf_(zz[e]);
+                    }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+                        *reinterpret_cast<float4*>(gb + (((2 * i + h2) ^ (t & 15)) << 2)) =
+                            make_float4(gv[4 * h2], gv[4 * h2 + 1], gv[4 * h2 + 2], gv[4 * h2 + 3]);
+                }
+                mbar_arrive(&sy.gate);  // also releases the z buffer
+            }
         } else if (warp == 9 && lane == 0 && n_ch > 0) {
             // TMA producer
             auto issue_a4 = [&](int c) {  // W rows (0..63) and q rows (64..127), both column blocks
@@ -915,46 +1015,90 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 }
                 sy.n_k += 1;
             };
-            auto issue_qk = [&](int c) {  // masked decayed Q K^T rows, into buffer c%2
-                const int b = c & 1;
+            auto issue_qk = [&](int c) {  // masked decayed Q K^T rows
                 if (p.ready) fence_proxy_async_global();
-                mbar_arrive_expect_tx(&sy.qk[b], 2 * 8192);
-                tma_load_2d(smem + kScanQk + b * 16384, &map_kqh, &sy.qk[b], 0, wrow(c));
-                tma_load_2d(smem + kScanQk + b * 16384 + 8192, &map_kql, &sy.qk[b], 0, wrow(c));
-                sy.n_qk[b] += 1;
+                mbar_arrive_expect_tx(&sy.qk, 2 * 8192);
+                tma_load_2d(smem + kScanQk, &map_kqh, &sy.qk, 0, wrow(c));
+                tma_load_2d(smem + kScanQk + 8192, &map_kql, &sy.qk, 0, wrow(c));
+                sy.n_qk += 1;
             };
-            bool ok = wait_chunk(0) && wait_chunk(1);
+            // the chunk's U~ rows (this CTA's 64 value lanes: 16 contiguous
+            // 4-column groups) and its cumulative log-decay, into G buffer c%2
+            auto issue_ug = [&](int c) {
+                if (p.ready) fence_proxy_async_global();
+                mbar_arrive_expect_tx(&sy.ug, 16384 + kC * 4);
+                bulk_load_1d(smem + kScanUt, p.u_ws + (size_t)wrow(c) * kD + (size_t)(v0 >> 2) * kC * 4,
+                             16384, &sy.ug);
+                bulk_load_1d(smem + kScanGc + (c & 1) * kC * 4, p.gcum_ws + wrow(c), kC * 4, &sy.ug);
+                sy.n_ug += 1;
+            };
+            auto issue_z = [&](int c) {  // the chunk's z rows, this CTA's value lanes
+                mbar_arrive_expect_tx(&sy.zf, 8192);
+                tma_load_2d(smem + kScanZ, &map_z, &sy.zf, h * kD + v0, tok0(c));
+                sy.n_zf += 1;
+            };
+            // P6_c = (M o QK^T)_c U_c into slot c%2, once U_c is in shared memory and
+            // P7_c is done (P6 then runs while the state is updated).  A rows
+            // 0..63 of this M=128 operand are whatever precedes the QK^T rows in
+            // shared memory: they only reach accumulator rows 0..63, which
+            // nothing reads.
+            const uint64_t dBu = desc_mnmajor_sw128(smem_u32(smem + kScanBu), 8192);
+            const uint64_t dQk = desc_kmajor_sw128(smem_u32(smem + kScanQk) - 8192);
+            constexpr uint64_t kLo8 = 8192 >> 4;
+            const uint32_t id64 = idesc_bf16_f32(128, kDS, false, true);
+            auto issue_p6 = [&](int c) -> bool {
+                if (!wait_or_dead(&sy.u2, c & 1, sy, 6) || !wait_or_dead(&sy.qk, c & 1, sy, 8)) return false;
+                tc_fence_after_sync();
+#pragma unroll 1  // few registers: the control warps run at 96 (off the chain)
+                for (int k = 0; k < 4; ++k)
+                    mma3(tmem + kTmD6 + (uint32_t)(c & 1) * 64, dQk + k * 2, dQk + kLo8 + k * 2,
+                         dBu + k * 128, dBu + kLo8 + k * 128, id64, k > 0 ? 1u : 0u);
+                mma_commit(&sy.p6[c & 1]);
+                sy.n_p6 += 1;
+                return true;
+            };
+            bool ok = wait_chunk(0);
             if (ok) {
+                issue_ug(0);
+                issue_z(0);
                 issue_a4(0);
                 issue_k(0);
                 issue_qk(0);
-                if (n_ch > 1) issue_qk(1);
             }
             for (int c = 0; ok && c + 1 < n_ch; ++c) {
+                if (!(ok = wait_chunk(c + 1))) break;
                 // [W; Q]_{c+1} once P4_c has read [W; Q]_c
                 if (!(ok = wait_or_dead(&sy.p4, c & 1, sy, 5))) break;
                 issue_a4(c + 1);
+                // U~_{c+1} once the U warps have read U~_c, G_{c+1} into the buffer
+                // the output warps read chunk c-1's from before arriving on d4free
+                if (!(ok = wait_or_dead(&sy.u, c & 1, sy, 6) &&
+                           (c == 0 || wait_or_dead(&sy.d4free[(c - 1) & 1], ((c - 1) >> 1) & 1, sy, 7))))
+                    break;
+                issue_ug(c + 1);
                 // K_{c+1} once P7_c has read K_c
                 if (!(ok = wait_or_dead(&sy.p7, c & 1, sy, 5))) break;
                 issue_k(c + 1);
-                // QK^T_{c+2} into the buffer P6_c has read
-                if (c + 2 < n_ch) {
-                    if (!(ok = wait_chunk(c + 2) && wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7)))
-                        break;
-                    issue_qk(c + 2);
-                }
+                if (!(ok = issue_p6(c))) break;
+                // z_{c+1} once the gate warps have turned z_c into the gate
+                if (!(ok = wait_or_dead(&sy.gate, c & 1, sy, 9))) break;
+                issue_z(c + 1);
+                // QK^T_{c+1} once P6_c has read QK^T_c
+                if (!(ok = wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7))) break;
+                issue_qk(c + 1);
             }
+            // the last chunk's output term, after its P7
+            if (ok && wait_or_dead(&sy.p7, (n_ch - 1) & 1, sy, 5)) issue_p6(n_ch - 1);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------ compute warps
-        regs_inc<192>();
+        regs_inc<200>();
         const int q = warp & 3, half = warp >> 2;
         const int row = 32 * q + lane;       // accumulator lane: key lane / token row
         const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice
         const uint32_t lane_off = (32u * q) << 16;
         const bool is_u = q < 2;  // warps 0,1,4,5: accumulator rows 0..63
-        const bool sigmoid_gate = p.act == 1;
 
         float S[32];  // S[row][v0 + cl .. +31]
         if (p.state_in) {
@@ -981,62 +1125,50 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         tc_fence_before_sync();
         mbar_arrive(s_mine);
 
-        float ut[32];   // U~ row (U warps), prefetched one chunk ahead
-        float gu = 0.f, glu = 0.f;  // G_t of that row and G_last of its chunk
-        uint4 zr[4];    // z row (output warps) of the chunk whose output is pending
-        float gz = 0.f; // G_t of that row
-        auto load_ut = [&](int c) {
-            gu = gcum(c, row);
-            glu = gcum(c, chunk_len(c) - 1);
-            const float4* src = reinterpret_cast<const float4*>(p.u_ws + (size_t)wrow(c) * kD) +
-                                ((v0 + cl) >> 2) * kC + row;  // [4-column group][row][4]
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = src[i * kC];
-                ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
-            }
-        };
-        auto load_z = [&](int c) {
-            const int t = row - 64;
-            gz = gcum(c, t);
-            if (t < chunk_len(c)) {
-                const uint4* zp = reinterpret_cast<const uint4*>(
-                    p.z + (size_t)(tok0(c) + t) * hv_n * kD + (size_t)h * kD + v0 + cl);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) zr[i] = zp[i];
-            }
-        };
-        bool alive = n_ch == 0 || wait_chunk(0);
-        if (alive && n_ch > 0) {
-            if (is_u) load_ut(0);
-            else load_z(0);
-        }
+        const float* sGc = reinterpret_cast<const float*>(smem + kScanGc);  // [2][64]
+        bool alive = true;
 
-        // Output of chunk c (output warps, accumulator rows 64..127): needs P6_c.
-        // Every output warp makes the same calls (the named barriers inside
-        // must match); after a failure (alive_in false) no wait is made.
-        auto output = [&](int c, bool alive_in) -> bool {
-            const int t = row - 64, s = c & 1, L = chunk_len(c);
-            const float eg = __expf(gz);
-            bool ok = __all_sync(0xffffffffu, alive_in && wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7));
-            float o[32];
-            if (ok) {
-                tc_fence_after_sync();
-                float a[32], b[32];
-                const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
-                tmem_ld32x3(d4, d4 + 64, tmem + kTmD6 + (uint32_t)(c & 1) * 64 + lane_off + cl, a, b, o);
-                tc_fence_before_sync();
-                mbar_arrive(&sy.d4free[c & 1]);  // P4_{c+2} and P6_{c+2} may now reuse the slot
+        // Output of chunk c (output warps, accumulator rows 64..127), in two
+        // parts around the state update that follows it: first the reads of
+        // P4's Q S rows, P6 and the gate (after which those buffers may be
+        // reused), o = e^{G_t} (Q S)_t + ((M o QK^T) U)_t, its sum of squares
+        // and the gated values; then the RMSNorm (sums of squares exchanged
+        // with the peer CTA) and the stores.  Every output warp makes the same
+        // calls (the named barriers inside must match); after a failure no
+        // wait is made.
+        float og[32];  // o * norm_w * act(z) of the pending output
+        float oss = 0.f;  // sum of o^2 over this thread's 32 value lanes
+        float gt_pend = 0.f;  // G_t of this thread's token row in the chunk whose output is pending
+        auto output_read = [&](int c, bool alive_in) -> bool {
+            const int t = row - 64;
+            bool ok = __all_sync(0xffffffffu, alive_in && wait_or_dead(&sy.p6[c & 1], (c >> 1) & 1, sy, 7) &&
+                                                  wait_or_dead(&sy.gate, c & 1, sy, 9));
+            if (!ok) return false;
+            tc_fence_after_sync();
+            float a[32], b[32];
+            const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
+            tmem_ld32x3(d4, d4 + 64, tmem + kTmD6 + (uint32_t)(c & 1) * 64 + lane_off + cl, a, b, og);
+            const float eg = __expf(gt_pend);
+            oss = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = fmaf(eg, a[j] + b[j], o[j]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = 0.f;
+            for (int j = 0; j < 32; ++j) {
+                og[j] = fmaf(eg, a[j] + b[j], og[j]);
+                oss = fmaf(og[j], og[j], oss);
             }
-            float ss = 0.f;
+            const float* gb = reinterpret_cast<const float*>(smem + kScanGate) + t * kC;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) ss = fmaf(o[j], o[j], ss);
-            sSq[half][t] = ss;
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 v = *reinterpret_cast<const float4*>(gb + ((((cl >> 2) + c4) ^ (t & 15)) << 2));
+                og[4 * c4] *= v.x; og[4 * c4 + 1] *= v.y; og[4 * c4 + 2] *= v.z; og[4 * c4 + 3] *= v.w;
+            }
+            tc_fence_before_sync();
+            // the slots of P4_{c+2} and P6_{c+2}, the gate of chunk c+1 and G buffer c%2 may be reused
+            mbar_arrive(&sy.d4free[c & 1]);
+            return true;
+        };
+        auto output_finish = [&](int c, bool ok) -> bool {
+            const int t = row - 64, s = c & 1, L = chunk_len(c);
+            sSq[half][t] = ok ? oss : 0.f;
             group_sync(1, 128);  // the output warps' halves of each row are in sSq
             const float tot = sSq[0][t] + sSq[1][t];
             if (ok && half == 0) {
@@ -1046,24 +1178,6 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                     if (t == 0) mbar_arrive_expect_tx(&sy.x[s], kC * 4);  // arm: the peer's 64 sums
                     st_async_f32(map_to_rank(smem_u32(&sx[s][t]), peer), tot,
                                  map_to_rank(smem_u32(&sy.x[s]), peer));
-                }
-            }
-            // while the peer's sums travel: o * norm_w * act(z)
-            if (sigmoid_gate) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float zz[8];
-                    unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * sigmoidf_(zz[e]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float zz[8];
-                    unpack_bf16x8(zr[i], zz);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[8 * i + e] *= sNw[cl + 8 * i + e] * siluf_(zz[e]);
                 }
             }
             ok = ok && wait_or_dead(&sy.x[s], (c >> 1) & 1, sy, 10, false, peer_dead);
@@ -1078,26 +1192,39 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 for (int i = 0; i < 4; ++i) {
                     float y[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = o[8 * i + e] * rr;
+                    for (int e = 0; e < 8; ++e) y[e] = og[8 * i + e] * rr;
                     op[i] = pack_bf16x8(y);
                 }
             }
             return ok;
         };
 
-        // log of the state decay over a chunk, loaded one chunk ahead
-        float gl_next = (alive && n_ch > 0) ? gcum(0, chunk_len(0) - 1) : 0.f;
-        // U warps leave the loop on a failure; output warps go through every
-        // iteration (with no waits) so that their named barriers stay matched.
+        // The compute warps read no global memory inside the loop: the chunk
+        // data come into shared memory by the producer's copies, and global
+        // loads in flight would hold up every mbarrier arrive (a release)
+        // until they land.  U warps leave the loop on a failure; output warps
+        // go through every iteration (with no waits) so that their named
+        // barriers stay matched.
         for (int c = 0; c < n_ch; ++c) {
             if (!alive && is_u) break;
-            const float gam = __expf(gl_next);  // state decay over chunk c
-            // chunk c+1 is read from here on (its decay, U~ rows, z gate)
-            if (alive) alive = wait_chunk(c + 1);
-            if (alive && c + 1 < n_ch) gl_next = gcum(c + 1, chunk_len(c + 1) - 1);
+            // U~ and G of chunk c (the output warps read G of chunk c here, before
+            // their arrive for chunk c-1 lets the producer reuse this buffer)
+            alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.ug, c & 1, sy, 12));
+            const float* gc = sGc + (c & 1) * kC;
+            const float gam = alive ? __expf(gc[chunk_len(c) - 1]) : 0.f;  // state decay over chunk c
+            float gt_next = 0.f;
+            if (!is_u && alive) gt_next = gc[row - 64];
+            bool out_ok = false;
             if (is_u) {
                 // U_c = U~ - W S_c (rows 0..63 of P4_c), U'_c = e^{G_last-G_t} U_c
-                const float eu = __expf(glu - gu);  // while P4_c runs
+                const float eu = __expf(gc[chunk_len(c) - 1] - gc[row]);
+                float ut[32];
+                const float4* us4 = reinterpret_cast<const float4*>(smem + kScanUt) + ((cl >> 2) * kC + row);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = us4[i * kC];
+                    ut[4 * i] = v.x; ut[4 * i + 1] = v.y; ut[4 * i + 2] = v.z; ut[4 * i + 3] = v.w;
+                }
                 // warp-uniform: the tensor-memory loads below are warp-collective
                 if (!(alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p4, c & 1, sy, 5)))) break;
                 tc_fence_after_sync();
@@ -1109,9 +1236,9 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                     for (int j = 0; j < 32; ++j) ut[j] -= a[j] + b[j];
                 }
                 // U' for P7_c (P7_{c-1} has read the last one), then U for P6_c
-                // into buffer c%2 (P6_{c-2} has read U_{c-2}): both readers are
-                // done once P4_c is, which the issuer committed after them.  Only
-                // U' is on the chain.
+                // (P6_{c-1} has read U_{c-1}): both readers are done once P4_c
+                // is, which the issuer committed after them.  Only U' is on the
+                // chain.  The arrive on u also releases the U~ buffer.
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     const uint32_t o = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
@@ -1123,20 +1250,23 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&sy.u);
+                // U_c replaces U_{c-1} once P6_{c-1} has read it
+                if (c > 0 && !(alive = __all_sync(0xffffffffu, wait_or_dead(&sy.p6[(c - 1) & 1],
+                                                                            ((c - 1) >> 1) & 1, sy, 7))))
+                    break;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t ob = (c & 1) * 16384 + row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
+                    const uint32_t ob = row * 128 + (((4 * half + ch) ^ (row & 7)) << 4);
                     split_store(ut + 8 * ch, smem + kScanBu + ob, smem + kScanBu + 8192 + ob);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 mbar_arrive(&sy.u2);
-                if (c + 1 < n_ch) load_ut(c + 1);
             } else if (c > 0) {
-                // the output of chunk c-1 while the chain computes U_c
-                alive = output(c - 1, alive) && alive;
-                if (alive) load_z(c);
+                // the output of chunk c-1, read before this chunk's state update
+                out_ok = output_read(c - 1, alive);
             }
+            gt_pend = gt_next;
             // S_{c+1} = e^{G_last} S_c + K''^T U_c ; refresh the split copy
             alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p7, c & 1, sy, 6));
             if (alive) {
@@ -1153,8 +1283,12 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                     mbar_arrive(s_mine);
                 }
             }
+            if (!is_u && c > 0) alive = output_finish(c - 1, out_ok && alive) && alive;
         }
-        if (n_ch > 0 && !is_u) alive = output(n_ch - 1, alive) && alive;
+        if (n_ch > 0 && !is_u) {
+            const bool ok = output_read(n_ch - 1, alive);
+            alive = output_finish(n_ch - 1, ok && alive) && alive;
+        }
         if (alive && p.state_out) {
             float4* dst = reinterpret_cast<float4*>(p.state_out + slab + (size_t)row * kD + v0 + cl);
 #pragma unroll
@@ -1171,11 +1305,13 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     if (tid == 0) {
         if (sy.n_a4 > 0) mbar_wait(&sy.a4, (sy.n_a4 - 1) & 1);
         if (sy.n_k > 0) mbar_wait(&sy.k, (sy.n_k - 1) & 1);
-        for (int b = 0; b < 2; ++b)
-            if (sy.n_qk[b] > 0) mbar_wait(&sy.qk[b], (sy.n_qk[b] - 1) & 1);
+        if (sy.n_qk > 0) mbar_wait(&sy.qk, (sy.n_qk - 1) & 1);
+        if (sy.n_ug > 0) mbar_wait(&sy.ug, (sy.n_ug - 1) & 1);
+        if (sy.n_zf > 0) mbar_wait(&sy.zf, (sy.n_zf - 1) & 1);
+        if (sy.n_p6 > 0) mbar_wait(&sy.p6[(sy.n_p6 - 1) & 1], ((sy.n_p6 - 1) >> 1) & 1);
         if (sy.n_commits > 0) {
             const uint32_t idx = sy.last_commit >> 1, par = sy.last_commit & 1;
-            uint64_t* bar = idx == 0 ? &sy.p4 : idx == 1 ? &sy.p7 : &sy.p6[idx - 2];
+            uint64_t* bar = idx == 0 ? &sy.p4 : &sy.p7;
             mbar_wait(bar, par);
         }
     }
@@ -1193,9 +1329,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                   const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
-                  ChunkArgs p) {
+                  const __grid_constant__ CUtensorMap map_z, ChunkArgs p) {
     // sequences with the most chunks start first: the last wave is shorter
-    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
+    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                     blockIdx.x / kSplit, p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y);
 }
 
@@ -1208,24 +1344,25 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 // so the scan of chunk c overlaps the prep of the chunks after it.  Prep CTAs
 // never wait for scan CTAs: the launch completes whichever of its CTAs are
 // resident at a time.  A prep CTA's control warpgroup hands its registers to
-// the eight prep warps and leaves.
+// the eight prep warps (232 each) and leaves.
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kScanThreads, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
                    const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
                    const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                    const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
-                   ChunkArgs p, int n_prep) {
+                   const __grid_constant__ CUtensorMap map_z, ChunkArgs p, int n_prep) {
     if ((int)blockIdx.x < n_prep) {
+        // the control warpgroup leaves: 256 x 232 + 128 x 40 = 384 x 168
         if (threadIdx.x >= kComputeThreads) {
-            regs_dec<120>();
+            regs_dec<40>();
             return;
         }
-        regs_inc<192>();
+        regs_inc<232>();
         chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
                         blockIdx.x, n_prep);
     } else {
         const int s = ((int)blockIdx.x - n_prep) / kSplit;  // n_prep is even: clusters stay aligned
-        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
+        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                         s % p.n_v_heads, s / p.n_v_heads);
     }
 }
@@ -1365,9 +1502,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
 
     // Tensor maps; with no chunk at all (only empty sequences) no kernel
     // dereferences them and they stay zero.
-    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl;
+    CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z;
     std::memset(&m_qh, 0, sizeof(m_qh));
-    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kwh = m_kwl = m_qh;
+    m_ql = m_wh = m_wl = m_kqh = m_kql = m_kwh = m_kwl = m_z = m_qh;
     const uint64_t krows = (uint64_t)l.n_chunks * hk_n * kC;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
     if (l.n_chunks > 0) {
@@ -1378,7 +1515,8 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kwh, ws + l.kw_hi, krows, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_kwl, ws + l.kw_lo, krows, kD, kD, 64, 64))
+            !make_tma_map_bf16_2d(&m_kwl, ws + l.kw_lo, krows, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_z, a.z, (uint64_t)T, (uint64_t)hv_n * kD, (uint64_t)hv_n * kD, 64, 64))
             return cudaErrorInvalidValue;
     }
 
@@ -1419,7 +1557,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         }
         return timed_launch("chunk_fused", st, [&] {
             chunk_fused_kernel<<<dim3(n_prep + scan_ctas), kScanThreads, std::max(prep_smem, scan_smem),
-                                 st>>>(m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p, n_prep);
+                                 st>>>(m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p, n_prep);
             return cudaGetLastError();
         });
     }
@@ -1433,7 +1571,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     }
     e = timed_launch("chunk_scan", st, [&] {
         chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kScanThreads, scan_smem, st>>>(
-            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, p);
+            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p);
         return cudaGetLastError();
     });
     return e;
