@@ -490,9 +490,7 @@ def run_gpu(args):
         t_stop = time.time()
         # timing_report counts warm-up launches too: scale to the timed steps
         per_step_launch = {k: v[0] / (args.steps + args.warmup) for k, v in rep.items()}
-        # this library's kernels only (the layer's projections are cuBLAS GEMMs)
-        launches = int(round(sum(v for k, v in per_step_launch.items()
-                                 if not k.startswith("proj_")) * args.steps))
+        launches = int(round(sum(per_step_launch.values()) * args.steps))
         mean_ms = statistics.mean(ms)
         t_max = max_over_ranks(mean_ms, device=device)
         tok_s = world * r.tokens / (t_max / 1e3)

@@ -1583,6 +1583,9 @@ cudaError_t read_device_error(int* code, bool reset) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
     }
+    int gemm = 0;  // the projection GEMM's word (codes 20..23)
+    if (e == cudaSuccess) e = read_gemm_error(&gemm, reset);
+    if (e == cudaSuccess && *code == 0) *code = gemm;
     return e;
 }
 

@@ -160,6 +160,23 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t stream);
 // Sticky device-side error word set by a kernel whose bounded wait gave up.
 cudaError_t read_device_error(int* code, bool reset);
 
+// Projection GEMM on tcgen05: C_s = A W_s^T for up to four weights W_s that
+// share A (all bf16 row-major; W_s is [n, k], C_s is [m, n] with row stride
+// ldc), one launch.  A, W_s and C_s 16-byte aligned; k a multiple of 8.
+struct GemmSegment {
+    const void* w;
+    void* c;
+    int n, ldc;
+};
+struct GemmLaunch {
+    const void* a;
+    int m, k, n_seg;
+    GemmSegment seg[4];
+};
+cudaError_t launch_gemm_bf16(const GemmLaunch& g, cudaStream_t stream);
+// The projection GEMM's device error word (a bounded wait that gave up).
+cudaError_t read_gemm_error(int* code, bool reset);
+
 cudaError_t launch_conv_prologue(const ConvArgs& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurrentArgs& p, int d_k, int d_v, bool bf16,

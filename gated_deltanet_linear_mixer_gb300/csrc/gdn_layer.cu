@@ -2,12 +2,10 @@
 // (gdn_prefill) and the output projection.  qwen.rs gdn_forward runs
 // in_proj_qkv, in_proj_z, in_proj_b and in_proj_a as one linear_multi over the
 // hidden states, then the core, then out_proj over the gated-norm output.
-// The projections are plain bf16 GEMMs with fp32 accumulation, run by cuBLAS;
-// everything between them runs in this library's kernels.
-#include <cublas_v2.h>
+// Here the four input projections are one launch of this library's tcgen05
+// GEMM (each written in the layout the core reads: x [T, CD], z [T, Hv*dv],
+// a, b [T, Hv]), and out_proj a second launch over the core's output y.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "gdn.h"
 #include "gdn_internal.h"
@@ -21,12 +19,10 @@ gdn_status inject_fault(const char* site, const char* fn);
 
 namespace {
 
-constexpr size_t kBlasWorkspace = size_t(32) << 20;  // handed to cuBLAS from the caller's workspace
-
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct LayerLayout {
-    size_t x, z, a, b, y, blas, core, total;
+    size_t x, z, a, b, y, core, total;
 };
 
 LayerLayout layer_layout(const gdn_dims* d, size_t T, size_t core_bytes) {
@@ -39,28 +35,12 @@ LayerLayout layer_layout(const gdn_dims* d, size_t T, size_t core_bytes) {
     l.a = off; off = up256(off + T * hv * 2);
     l.b = off; off = up256(off + T * hv * 2);
     l.y = off; off = up256(off + T * vd * 2);
-    l.blas = off; off = up256(off + kBlasWorkspace);
     l.core = off; off = up256(off + core_bytes);
     l.total = off;
     return l;
 }
 
-// One cuBLAS handle per device, created on the first layer call there; the
-// calls that use it are serialised (a handle has one stream and workspace).
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// C [M, N] = A [M, K] W [N, K]^T, all bf16 row-major, fp32 accumulation.
-// Column-major view: C^T = W A^T, i.e. op(W) = T on a [K, N] column-major W.
-cublasStatus_t gemm_bf16_nt(cublasHandle_t h, int M, int N, int K, const void* A, const void* W,
-                            void* C) {
-    const float one = 1.f, zero = 0.f;
-    return cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, N, M, K, &one, W, CUDA_R_16BF, K, A,
-                        CUDA_R_16BF, K, &zero, C, CUDA_R_16BF, N, CUBLAS_COMPUTE_32F,
-                        CUBLAS_GEMM_DEFAULT);
-}
 
 }  // namespace
 
@@ -118,38 +98,26 @@ extern "C" gdn_status gdn_layer_prefill(const gdn_dims* dims, const gdn_params* 
     const int vd = dims->n_v_heads * dims->d_v, hv = dims->n_v_heads;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return gdn::set_error(GDN_ERR_CUDA, fn, "no usable current device");
-    std::lock_guard<std::mutex> lk(g_blas_mu);
-    if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) {
-        g_blas[dev] = nullptr;
-        return gdn::set_error(GDN_ERR_CUDA, fn, "cublasCreate failed");
-    }
-    cublasHandle_t h = g_blas[dev];
-    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS ||
-        cublasSetWorkspace(h, ws + l.blas, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS)
-        return gdn::set_error(GDN_ERR_CUDA, fn, "cublasSetStream / cublasSetWorkspace failed");
-    cublasStatus_t bs = CUBLAS_STATUS_SUCCESS;
-    auto gemm = [&](const char* name, int N, int K, const void* A, const void* W, void* C) {
-        gdn::timed_launch(name, s, [&] {
-            bs = gemm_bf16_nt(h, T, N, K, A, W, C);
-            return bs == CUBLAS_STATUS_SUCCESS ? cudaSuccess : cudaErrorUnknown;
-        });
-        return bs == CUBLAS_STATUS_SUCCESS;
-    };
-    if (!gemm("proj_qkv", cd, hidden, h_in, proj->w_qkv, ws + l.x) ||
-        !gemm("proj_z", vd, hidden, h_in, proj->w_z, ws + l.z) ||
-        !gemm("proj_a", hv, hidden, h_in, proj->w_a, ws + l.a) ||
-        !gemm("proj_b", hv, hidden, h_in, proj->w_b, ws + l.b))
-        return gdn::set_error(GDN_ERR_CUDA, fn, "input projection GEMM failed (cuBLAS status %d)",
-                              (int)bs);
+    // the input projections, one launch: x = h W_qkv^T, z = h W_z^T, a = h W_a^T, b = h W_b^T
+    gdn::GemmLaunch in{};
+    in.a = h_in; in.m = T; in.k = hidden; in.n_seg = 4;
+    in.seg[0] = {proj->w_qkv, ws + l.x, cd, cd};
+    in.seg[1] = {proj->w_z, ws + l.z, vd, vd};
+    in.seg[2] = {proj->w_a, ws + l.a, hv, hv};
+    in.seg[3] = {proj->w_b, ws + l.b, hv, hv};
+    cudaError_t e = gdn::timed_launch("proj_in", s, [&] { return gdn::launch_gemm_bf16(in, s); });
+    if (e != cudaSuccess)
+        return gdn::set_error(GDN_ERR_CUDA, fn, "input projection launch failed: %s", cudaGetErrorString(e));
     st = gdn_prefill(dims, params, n_seq, cu_seqlens, cu_seqlens_host, ws + l.x, ws + l.z, ws + l.a,
                      ws + l.b, conv_state_in, conv_state_out, initial_state, final_state, ws + l.y,
                      ws + l.core, core_bytes, stream);
     if (st != GDN_OK) return st;
-    if (!gemm("proj_out", hidden, vd, ws + l.y, proj->w_out, h_out))
-        return gdn::set_error(GDN_ERR_CUDA, fn, "output projection GEMM failed (cuBLAS status %d)",
-                              (int)bs);
+    // out_proj over the core's output y
+    gdn::GemmLaunch out{};
+    out.a = ws + l.y; out.m = T; out.k = vd; out.n_seg = 1;
+    out.seg[0] = {proj->w_out, h_out, hidden, hidden};
+    e = gdn::timed_launch("proj_out", s, [&] { return gdn::launch_gemm_bf16(out, s); });
+    if (e != cudaSuccess)
+        return gdn::set_error(GDN_ERR_CUDA, fn, "output projection launch failed: %s", cudaGetErrorString(e));
     return GDN_OK;
 }

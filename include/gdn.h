@@ -268,16 +268,15 @@ typedef struct gdn_proj {
  * prefill: the input projections x = h W_qkv^T, z = h W_z^T, a = h W_a^T,
  * b = h W_b^T (qwen.rs gdn_forward, its linear_multi over the hidden states),
  * the core exactly as gdn_prefill, then h_out = y W_out^T (out_proj).  bf16
- * only.  The projections are plain bf16 GEMMs with fp32 accumulation (cuBLAS);
- * their results, like the core's output y, are rounded to bf16, the core's
+ * only.  The projections run on this library's tcgen05 GEMM (bf16 operands,
+ * fp32 accumulation): the four input projections in one launch that writes x,
+ * z, a and b in the layouts the core reads, out_proj in a second.  Their
+ * results, like the core's output y, are rounded to bf16, the core's
  * activation type.
  *   hidden: model width, a multiple of 8.  h_in, h_out [T, hidden] bf16.
  *   The states, cu_seqlens and their rules are those of gdn_prefill.
  *   workspace: at least gdn_layer_prefill_workspace_size() bytes, 256-byte
- *   aligned; it holds x, z, a, b, y, cuBLAS's workspace and the core's.
- * The first call on a device creates that device's cuBLAS handle (cuBLAS may
- * allocate a little device memory then; nothing allocates afterwards); calls
- * from several host threads are serialised.
+ *   aligned; it holds x, z, a, b, y and the core's workspace.
  */
 gdn_status gdn_layer_prefill_workspace_size(const gdn_dims* dims, int32_t hidden, int32_t n_seq,
                                             const int32_t* cu_seqlens_host, size_t* bytes);

@@ -214,7 +214,7 @@ def test_layer_refusals(lib):
     assert "projection" in lib.gdn_last_error().decode()
     assert _layer(lib, _dims(), _proj(0x10004)) == 1
     assert "aligned" in lib.gdn_last_error().decode()
-    # no sequences: nothing to do, and no cuBLAS handle is created
+    # no sequences: nothing to do
     assert _layer(lib, _dims(), _proj(), n_seq=0, cu_host=(0,)) == 0
     # too small a workspace is refused before any launch
     assert _layer(lib, _dims(), _proj(), ws=FAKE, ws_bytes=256) == 4

@@ -375,7 +375,7 @@ def _layer_inputs(case, hidden, seed, exact=False):
     nonzero weights of +-1/16, so each projection is a multiple of 1/16 below 3
     in magnitude: exact in bf16 and in any fp32 summation order.  The bf16
     rounding of the projections is then no decision at all, and both sides feed
-    the core the same values (with dense weights, cuBLAS's fp32 sums and the
+    the core the same values (with dense weights, the GEMM's fp32 sums and the
     oracle's float64 ones round ~0.1% of the values to neighbouring bf16s, and
     the core's final state is that sensitive)."""
     rng = np.random.default_rng(seed)
@@ -423,7 +423,7 @@ def _layer_check(case, hidden, seed, exact=False):
 
 @pytest.mark.parametrize("lengths", [[150, 70, 1], [5, 9, 16]])
 def test_layer_prefill_matches_oracle(lengths):
-    """in_proj (cuBLAS) -> core -> out_proj against the oracle's float64
+    """in_proj (the tcgen05 GEMM) -> core -> out_proj against the oracle's float64
     projections; [5, 9, 16] takes the short-sequence (token-recurrent) core."""
     case = _gen("ly", lengths=lengths, state_std=0.05, conv_state_std=1.0, seed=41)
     _layer_check(case, hidden=256, seed=141)
