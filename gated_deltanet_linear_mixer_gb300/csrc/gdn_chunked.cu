@@ -1583,9 +1583,10 @@ cudaError_t read_device_error(int* code, bool reset) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
     }
-    int gemm = 0;  // the projection GEMM's word (codes 20..23)
+    int gemm = 0, rec = 0;  // the projection GEMM's word (codes 20..23), the recurrent kernel's (30)
     if (e == cudaSuccess) e = read_gemm_error(&gemm, reset);
-    if (e == cudaSuccess && *code == 0) *code = gemm;
+    if (e == cudaSuccess) e = read_rec_error(&rec, reset);
+    if (e == cudaSuccess && *code == 0) *code = gemm ? gemm : rec;
     return e;
 }
 

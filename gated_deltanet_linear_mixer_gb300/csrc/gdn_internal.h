@@ -182,5 +182,7 @@ cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t st
 cudaError_t launch_recurrent(const RecurrentArgs& p, int d_k, int d_v, bool bf16,
                              cudaStream_t stream);
 cudaError_t launch_commit_state(const CommitArgs& p, cudaStream_t stream);
+// The token-recurrent kernel's device error word (30: a state copy wait gave up).
+cudaError_t read_rec_error(int* code, bool reset);
 
 }  // namespace gdn

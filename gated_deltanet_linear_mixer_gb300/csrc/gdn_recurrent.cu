@@ -6,9 +6,16 @@
 // decayed state, rank-one write, readout), with the conv/normalise/gate
 // prologue and the gated-RMSNorm epilogue fused in.
 //
-// Design (memory-bound): one CTA of 256 threads per (sequence, value head).
-// The d_k x d_v fp32 state slab is streamed from HBM once, held in registers
-// for all the tokens of the call, and written back once.  Thread layout: a
+// Design (memory-bound): persistent CTAs of 256 threads, two per SM, each
+// walking (sequence, value head) items.  The d_k x d_v fp32 state slab of an
+// item is streamed from HBM once, held in registers for all the tokens of the
+// call, and written back once; while an item computes, the next item's slab
+// is already on its way into shared memory (one bulk async copy), so every
+// SM keeps two slabs of loads in flight between its items.  The inputs of an
+// item's first token block (its q|k|v rows, conv history and weights, z rows)
+// come into shared memory by per-thread async copies issued together with the
+// gate loads at the start of the item, so that they cost one round trip to
+// memory instead of one per dependent load.  Thread layout: a
 // state row (d_v floats) is covered by d_v/4 lanes with one float4 each, so
 // every load/store instruction of a warp moves whole 128..512-byte rows; the
 // CTA's row groups split the d_k rows.  The two per-token column reductions
@@ -16,13 +23,39 @@
 // a warp, then shared memory across warps.  The readout uses
 // o = e^g S^T q + (k.q) delta, which equals S'^T q for the written state S'
 // (S' = e^g S + k delta^T), so the state is read once per token.
+#include <algorithm>
+#include <atomic>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 
 constexpr int kRecThreads = 256;
 constexpr int kRecTokBlock = 8;  // tokens whose prologue is computed together
+constexpr int kRecCtasPerSm = 2;
+
+// This file's device error word: 30 = a CTA's wait for its state copy gave up.
+__device__ int g_rec_error = 0;
+
+// 16-byte asynchronous copy global -> shared (cp.async, tracked per thread).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Dynamic shared-memory layout of recurrent_kernel (byte offsets; every
+// region 16-byte aligned).
+template <int DK, int DV, typename T> struct RecStage {
+    static constexpr int CH = 2 * DK + DV;
+    static constexpr uint32_t kX = DK * DV * 4;
+    static constexpr uint32_t kCs = kX + kRecTokBlock * CH * sizeof(T);
+    static constexpr uint32_t kW = kCs + ((CH * 3 * sizeof(T) + 15) / 16) * 16;
+    static constexpr uint32_t kZ = kW + CH * 4 * 4;
+    static constexpr uint32_t kBytes = kZ + kRecTokBlock * DV * sizeof(T);
+};
 
 // PC: one decay per key channel (p.per_channel), a separate instance so that
 // the scalar-decay kernel carries none of its work.
@@ -42,15 +75,45 @@ recurrent_kernel(RecurrentArgs p) {
     __shared__ float red[NW][2][DV];
     __shared__ __align__(16) float dlt[DV];  // read back as float4
     __shared__ float ysum[DV / 32];
+    __shared__ __align__(8) uint64_t bar_s;  // the state copy of the CTA's next item
+    // dynamic shared memory: that copy [DK][DV], then the raw inputs of an
+    // item's first token block (async copies): q | k | v rows, conv history
+    // [channel][K-1], conv weights [channel][K], z rows
+    extern __shared__ __align__(128) float s_next[];
+    using Stage = RecStage<DK, DV, T>;
+    uint8_t* dyn = reinterpret_cast<uint8_t*>(s_next);
+    T (*st_x)[CH] = reinterpret_cast<T (*)[CH]>(dyn + Stage::kX);
+    T* st_cs = reinterpret_cast<T*>(dyn + Stage::kCs);
+    float* st_w = reinterpret_cast<float*>(dyn + Stage::kW);
+    T (*st_z)[DV] = reinterpret_cast<T (*)[DV]>(dyn + Stage::kZ);
 
-    const int hv = blockIdx.x;
-    const int n = blockIdx.y;
     const int hv_n = p.n_v_heads;
-    const int hk = key_head(hv, hv_n / p.n_k_heads, p.n_k_heads, p.head_map);
     const int cd = 2 * p.n_k_heads * DK + hv_n * DV;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c4 = tid % L, rg = tid / L;
     const int K = p.conv_k, keep = K - 1;
+    const int n_items = p.n_seq * hv_n;  // item = n * Hv + hv: also its state slab's index
+    constexpr uint32_t kSlabBytes = DK * DV * 4;
+
+    if (tid == 0) {
+        tc::mbar_init(&bar_s, 1);
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    auto issue_state = [&](int item) {  // one thread: the slab in 16 KB pieces
+        tc::mbar_arrive_expect_tx(&bar_s, kSlabBytes);
+        for (uint32_t off = 0; off < kSlabBytes; off += 16384)
+            tc::bulk_load_1d(reinterpret_cast<uint8_t*>(s_next) + off,
+                             p.state_in + (size_t)item * DK * DV + off / 4, min(16384u, kSlabBytes - off),
+                             &bar_s);
+    };
+    uint32_t s_phase = 0;
+    bool s_pending = p.state_in && (int)blockIdx.x < n_items;
+    if (s_pending && tid == 0) issue_state(blockIdx.x);
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int n = item / hv_n, hv = item - n * hv_n;
+    const int hk = key_head(hv, hv_n / p.n_k_heads, p.n_k_heads, p.head_map);
 
     int bos, len;
     if (p.cu_seqlens) {
@@ -68,13 +131,81 @@ recurrent_kernel(RecurrentArgs p) {
     const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
     T* __restrict__ out = static_cast<T*>(p.out);
 
-    // Issue the state loads first; they stay in flight during the prologue.
-    const size_t slab = ((size_t)n * hv_n + hv) * DK * DV;
+    // Async copies of the first token block's inputs (every range is a
+    // multiple of 16 bytes at a 16-byte aligned offset of its array, given
+    // 16-byte aligned bases, which `staged` checks), and its gate inputs.
+    const int nb0 = min(kRecTokBlock, len);
+    const bool staged = len > 0 && ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.z) |
+                                     reinterpret_cast<uintptr_t>(p.conv_w) |
+                                     reinterpret_cast<uintptr_t>(cs_in)) & 15) == 0;
+    float a_pre = 0.f, b_pre = 0.f;
+    if (staged) {
+        constexpr int QC = DK * (int)sizeof(T) / 16, XC = CH * (int)sizeof(T) / 16;
+        const int chq = hk * DK, chk = p.n_k_heads * DK + hk * DK, chv = 2 * p.n_k_heads * DK + hv * DV;
+        // chunk c of a q|k|v list with per_q chunks per key range: first channel, chunk within
+        auto range_of = [&](int c, int per_q, int& ch, int& off) {
+            const int r = c < per_q ? 0 : c < 2 * per_q ? 1 : 2;
+            ch = r == 0 ? chq : r == 1 ? chk : chv;
+            off = c - r * per_q;
+        };
+        for (int i = tid; i < nb0 * XC; i += kRecThreads) {
+            const int tau = i / XC, c = i - tau * XC;
+            int ch, off;
+            range_of(c, QC, ch, off);
+            cp_async16(reinterpret_cast<uint4*>(&st_x[tau][0]) + c,
+                       reinterpret_cast<const uint4*>(x + (size_t)(bos + tau) * cd + ch) + off);
+        }
+        if (cs_in) {
+            const int per_q = QC * keep, tot = (2 * DK + DV) * (int)sizeof(T) * keep / 16;
+            for (int c = tid; c < tot; c += kRecThreads) {
+                int ch, off;
+                range_of(c, per_q, ch, off);
+                cp_async16(reinterpret_cast<uint4*>(st_cs) + c,
+                           reinterpret_cast<const uint4*>(cs_in + ((size_t)n * cd + ch) * keep) + off);
+            }
+        }
+        {
+            const int per_q = DK * K / 4, tot = CH * K / 4;
+            for (int c = tid; c < tot; c += kRecThreads) {
+                int ch, off;
+                range_of(c, per_q, ch, off);
+                cp_async16(reinterpret_cast<uint4*>(st_w) + c,
+                           reinterpret_cast<const uint4*>(p.conv_w + (size_t)ch * K) + off);
+            }
+        }
+        constexpr int ZC = DV * (int)sizeof(T) / 16;
+        for (int i = tid; i < nb0 * ZC; i += kRecThreads) {
+            const int tau = i / ZC, c = i - tau * ZC;
+            cp_async16(reinterpret_cast<uint4*>(&st_z[tau][0]) + c,
+                       reinterpret_cast<const uint4*>(z + ((size_t)(bos + tau) * hv_n + hv) * DV) + c);
+        }
+        cp_async_commit();
+        if (tid < nb0) {
+            const size_t gi = (size_t)(bos + tid) * hv_n + hv;
+            if (!PC) a_pre = to_f32(av[gi]);
+            b_pre = to_f32(bv[gi]);
+        }
+    }
+
+    // The state: from the copy that was in flight since the previous item;
+    // once every thread has taken its rows, the next item's copy is issued.
+    const size_t slab = (size_t)item * DK * DV;
     float4 s[RPT];
     if (p.state_in) {
-        const float4* src = reinterpret_cast<const float4*>(p.state_in + slab);
+        if (!__syncthreads_and(tc::mbar_wait(&bar_s, s_phase))) {
+            if (tid == 0) atomicCAS(&g_rec_error, 0, 30);
+            break;
+        }
+        s_phase ^= 1;
+        s_pending = false;
+        const float4* src = reinterpret_cast<const float4*>(s_next);
 #pragma unroll
         for (int i = 0; i < RPT; ++i) s[i] = src[(rg + RG * i) * L + c4];
+        __syncthreads();
+        if (item + (int)gridDim.x < n_items) {
+            if (tid == 0) issue_state(item + gridDim.x);
+            s_pending = true;
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < RPT; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -82,7 +213,23 @@ recurrent_kernel(RecurrentArgs p) {
 
     for (int t0 = 0; t0 < len; t0 += kRecTokBlock) {
         const int nb = min(kRecTokBlock, len - t0);
+        const bool from_stage = staged && t0 == 0;
         // ---- prologue: conv + SiLU for nb tokens x (q | k | v) channels
+        if (from_stage) {
+            cp_async_wait_all();
+            __syncthreads();
+            for (int idx = tid; idx < nb * CH; idx += kRecThreads) {
+                const int tau = idx / CH, lc = idx % CH;
+                float acc = 0.f;
+                for (int j = 0; j < K; ++j) {
+                    const int tt = tau - keep + j;  // token of the item (this block starts it)
+                    const float v = tt >= 0 ? to_f32(st_x[tt][lc])
+                                    : cs_in ? to_f32(st_cs[lc * keep + keep + tt]) : 0.f;
+                    acc = fmaf(st_w[lc * K + j], v, acc);
+                }
+                cbuf[tau][lc] = siluf_(acc);
+            }
+        } else
         for (int idx = tid; idx < nb * CH; idx += kRecThreads) {
             const int tau = idx / CH, lc = idx % CH;
             const int ch = lc < DK ? hk * DK + lc
@@ -106,8 +253,9 @@ recurrent_kernel(RecurrentArgs p) {
         if (tid < nb) {
             const size_t gi = (size_t)(bos + t0 + tid) * hv_n + hv;
             if (!PC)
-                gam[tid] = expf(log_decay(to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv], p.decay_form));
-            bet[tid] = sigmoidf_(to_f32(bv[gi]));
+                gam[tid] = expf(log_decay(from_stage ? a_pre : to_f32(av[gi]), p.A_log[hv], p.dt_bias[hv],
+                                          p.decay_form));
+            bet[tid] = sigmoidf_(from_stage ? b_pre : to_f32(bv[gi]));
         }
         if (PC) {  // S <- diag(e^{g_t}) S: one decay per key channel (state row)
             for (int idx = tid; idx < nb * DK; idx += kRecThreads) {
@@ -197,7 +345,8 @@ recurrent_kernel(RecurrentArgs p) {
                 for (int w = 0; w < DV / 32; ++w) tot += ysum[w];
                 const float rr = rsqrtf(tot / (float)DV + p.rms_eps);
                 const size_t oi = (size_t)t * hv_n * DV + (size_t)hv * DV + tid;
-                const float y = o * rr * p.norm_w[tid] * gatef_(to_f32(z[oi]), p.act);
+                const float zv = from_stage ? to_f32(st_z[tau][tid]) : to_f32(z[oi]);
+                const float y = o * rr * p.norm_w[tid] * gatef_(zv, p.act);
                 out[oi] = from_f32<T>(y);
             }
             const float4 dv4 = *reinterpret_cast<const float4*>(&dlt[c4 * 4]);
@@ -224,19 +373,54 @@ recurrent_kernel(RecurrentArgs p) {
 #pragma unroll
         for (int i = 0; i < RPT; ++i) dst[(rg + RG * i) * L + c4] = s[i];
     }
+    }  // items
+
+    // no copy may be in flight when the CTA leaves (only after a give-up)
+    if (s_pending && tid == 0 && !tc::mbar_wait(&bar_s, s_phase)) atomicCAS(&g_rec_error, 0, 30);
+}
+
+// SMs of the current device, cached per device.
+static int rec_sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev].load()) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev].store(n);
+    }
+    return cached[dev].load();
+}
+
+template <int DK, int DV, typename T, bool PC>
+static cudaError_t launch_rec_inst(const RecurrentArgs& p, cudaStream_t st) {
+    constexpr int kSmem = RecStage<DK, DV, T>::kBytes;  // the next item's state slab, the input staging
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load()) {
+        cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<DK, DV, T, PC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        // the whole unified L1 as shared memory: two CTAs per SM must fit
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(recurrent_kernel<DK, DV, T, PC>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        attr_set[dev].store(true);
+    }
+    const int items = p.n_seq * p.n_v_heads;
+    const int grid = std::min(items, kRecCtasPerSm * rec_sm_count());
+    recurrent_kernel<DK, DV, T, PC><<<grid, kRecThreads, kSmem, st>>>(p);
+    return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_recurrent_t(const RecurrentArgs& p, int dk, int dv, cudaStream_t st) {
-    dim3 grid(p.n_v_heads, p.n_seq);
-#define GDN_REC_CASE(A, B)                                                        \
-    if (dk == A && dv == B) {                                                     \
-        if (p.per_channel)                                                        \
-            recurrent_kernel<A, B, T, true><<<grid, kRecThreads, 0, st>>>(p);     \
-        else                                                                      \
-            recurrent_kernel<A, B, T, false><<<grid, kRecThreads, 0, st>>>(p);    \
-        return cudaGetLastError();                                                \
-    }
+    // the bulk state copies read 16-byte aligned slabs
+    if (p.state_in && reinterpret_cast<uintptr_t>(p.state_in) % 16) return cudaErrorInvalidValue;
+#define GDN_REC_CASE(A, B)                                                                         \
+    if (dk == A && dv == B)                                                                        \
+        return p.per_channel ? launch_rec_inst<A, B, T, true>(p, st) : launch_rec_inst<A, B, T, false>(p, st);
     GDN_REC_CASE(32, 32) GDN_REC_CASE(32, 64) GDN_REC_CASE(32, 128)
     GDN_REC_CASE(64, 32) GDN_REC_CASE(64, 64) GDN_REC_CASE(64, 128)
     GDN_REC_CASE(128, 32) GDN_REC_CASE(128, 64) GDN_REC_CASE(128, 128)
@@ -260,6 +444,15 @@ __global__ void __launch_bounds__(256) commit_state_kernel(CommitArgs p) {
         p.inter + (((size_t)n * p.T + (j - 1)) * p.n_v_heads + hv) * slab);
     float4* dst = reinterpret_cast<float4*>(p.state + ((size_t)n * p.n_v_heads + hv) * slab);
     for (size_t i = threadIdx.x; i < slab / 4; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t read_rec_error(int* code, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_rec_error, sizeof(int));
+    if (e == cudaSuccess && reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_rec_error, &zero, sizeof(int));
+    }
+    return e;
 }
 
 cudaError_t launch_commit_state(const CommitArgs& p, cudaStream_t st) {
