@@ -44,9 +44,16 @@ METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
 # by the units it processes, and the source says so.  An entry is removed when
 # its kernel changes, until it is captured again.
 TRAFFIC = {
+    ("prefill", "chunk_fused"): (216_812_288 + 193_505_536, "ncu capture of this workload's launch"),
+    ("layer", "chunk_fused"): (216_812_288 + 193_505_536,
+                               "ncu capture of the same launch in the T=4096 prefill workload"),
     # 64-sequence decode step; the traffic is per sequence: x 256/64
-    ("decode", "recurrent"): ((139_106_560 + 73_355_264) * 4,
+    ("decode", "recurrent"): ((139_134_208 + 73_977_088) * 4,
                               "ncu capture of the 64-sequence decode step, scaled x 256/64"),
+    ("spec_verify", "recurrent"): (144_244_992 + 477_105_664, "ncu capture of this workload's launch"),
+    # 16 sequences of 128..1024 tokens (149 chunks); the traffic is per chunk: x 1015/149
+    ("varlen", "chunk_scan"): (round((659_001_856 + 96_884_992) * 1015 / 149),
+                               "ncu capture of a 149-chunk varlen case, scaled x 1015/149 chunks"),
 }
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
