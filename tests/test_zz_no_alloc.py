@@ -4,8 +4,9 @@ Callers such as an engine plugin handed only its inputs and outputs, or a
 serving loop whose device memory is fixed before it starts, cannot allocate
 the workspace gdn_prefill asks for; gdn_prefill_noalloc runs the same prefill
 on a built-in device array instead.  These tests call it through the C ABI
-directly and check it against gdn_prefill on the same inputs, on two calls in
-a row (the second call finds the first call's contents in the shared array).
+directly and check it against gdn_prefill on the same inputs and against the
+oracle, on two calls in a row (the second call finds the first call's contents
+in the shared array).
 
 The file is named so that pytest collects it last.
 """
@@ -17,7 +18,7 @@ import torch
 
 import gated_deltanet_linear_mixer_gb300 as gdn
 from gated_deltanet_linear_mixer_gb300 import workloads
-from gdn_cases import TOL, dims, rel_err, upload
+from gdn_cases import TOL, dims, rel_err, run_oracle, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -70,8 +71,8 @@ def _regular(case, t):
 
 def test_noalloc_prefill_matches_the_workspace_entry_point_on_two_calls():
     """Two calls in a row with different inputs and sequence layouts; each must
-    match gdn_prefill (same kernels, caller-owned workspace) within the suite's
-    bf16 tolerance, and the conv history exactly."""
+    match gdn_prefill (same kernels, caller-owned workspace) and the oracle within
+    the suite's bf16 tolerance, and the conv history exactly."""
     gdn.device_error(reset=True)
     for seed, lengths in ((41, [200, 64, 131]), (42, [77, 1, 256])):
         case = _case(seed, lengths)
@@ -82,6 +83,10 @@ def test_noalloc_prefill_matches_the_workspace_entry_point_on_two_calls():
         assert rel_err(out, ref_out.float().cpu().numpy()) < TOL["bf16"]
         assert rel_err(st, ref_st.cpu().numpy()) < TOL["bf16"]
         assert torch.equal(cs, ref_cs)
+        oracle_ref = run_oracle(case)
+        assert rel_err(out, oracle_ref["out"]) <= TOL["bf16"]
+        assert rel_err(st, oracle_ref["state"]) <= TOL["bf16"]
+        assert rel_err(cs.float(), oracle_ref["conv_state"]) == 0.0
     assert gdn.device_error(reset=True) == 0
 
 
