@@ -685,7 +685,16 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
             }
             prep_sync();
         }
-        if (!failed && p.ready) pub = item;
+        if (!failed && p.ready) {
+            if (item == worker) {
+                // a CTA's first item is published as soon as its stores have
+                // landed: the first chunk rows gate the scan's start, while later
+                // rows are ready long before the scan reaches them
+                if (tid == 0) publish_item(p.ready + item);
+            } else {
+                pub = item;  // published after the next item's Gram, when its stores are long done
+            }
+        }
     } while (false);
     if (failed) break;
     }
