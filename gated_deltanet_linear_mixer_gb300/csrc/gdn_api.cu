@@ -283,7 +283,7 @@ gdn_status gdn_sync_status(void* stream) {
         return st;
     if (code)
         return fail(GDN_ERR_TIMEOUT, fn,
-                    "a bounded device wait of the tensor-core prefill gave up (wait code %d%s); the "
+                    "a bounded device wait gave up (wait code %d%s); the "
                     "outputs and states written by the calls since the last check are invalid",
                     code, code == 11 ? ": a scan waited for a chunk's prep rows" : "");
     g_err[0] = '\0';
