@@ -630,7 +630,10 @@ def run_reference(args):
     sample = (f"the whole workload per step ({case.n_tokens} tokens, all {case.n_v_heads} heads): "
               "the oracle's C source built with float arithmetic, OpenMP over tokens and over "
               "(sequence, value head)")
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+    # n_gpus is the launch's N, as in the device arm's line; the oracle itself runs
+    # on rank 0's host cores and uses no GPU
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "runs_on": "host cores of rank 0 (no GPU)",
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
