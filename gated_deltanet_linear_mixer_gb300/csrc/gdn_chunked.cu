@@ -22,6 +22,9 @@
 //               per chunk three MMA groups ([W; e^G Q] S, then (M o QK^T) U and
 //               (e^{G_last-G} K)^T U), the state update and the fused gated
 //               RMSNorm epilogue.
+//   chunk_fused both phases in one launch (prep CTAs publish each item's
+//               flag; scan clusters wait on it), for batches whose scan alone
+//               would leave most SMs idle; the two-kernel form serves the rest.
 // Every operand tile is either loaded by TMA with the 128-byte swizzle or
 // written by threads in the same layout.  B operands whose contraction runs
 // along a tile's rows (S, U, [K|V] rows) use the MN-major descriptor; every A

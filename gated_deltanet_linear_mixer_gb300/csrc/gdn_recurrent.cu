@@ -25,6 +25,7 @@
 // (S' = e^g S + k delta^T), so the state is read once per token.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -379,6 +380,402 @@ recurrent_kernel(RecurrentArgs p) {
     if (s_pending && tid == 0 && !tc::mbar_wait(&bar_s, s_phase)) atomicCAS(&g_rec_error, 0, 30);
 }
 
+// ------------------------------------------------------------ read-only verify
+// A verify call that keeps no state (no state_out, no intermediates; at most
+// kRecSub tokens per sequence, scalar decay) needs the state only to read it.
+// Its tokens then share one pass over the state: with S the state before the
+// first token, G_j the decay through token j and D_ij the decay over the
+// tokens after i through j,
+//   kv_j = G_j S^T k_j + sum_{i<j} D_ij (k_i.k_j) delta_i,
+//   delta_j = beta_j (v_j - kv_j),
+//   o_j = G_j S^T q_j + sum_{i<=j} D_ij (k_i.q_j) delta_i,
+// which is the token-by-token rule (S_j = e^{g_j} S_{j-1} + k_j delta_j^T,
+// o_j = S_j^T q_j) unrolled over the call's tokens.  The state is never
+// written, so no thread updates it.
+constexpr int kRecSub = 4;  // tokens per sequence the read-only kernel takes
+
+// Dynamic shared memory of verify_ro_kernel (byte offsets, 16-byte aligned):
+// the next item's state slab; the item's input staging (q|k|v rows, conv
+// history, conv weights), reused for the per-warp column sums once the conv
+// has read it; the z rows.
+template <int DK, int DV, typename T> struct RoStage {
+    static constexpr int CH = 2 * DK + DV;
+    static constexpr uint32_t kX = DK * DV * 4;
+    static constexpr uint32_t kCs = kX + kRecSub * CH * sizeof(T);
+    static constexpr uint32_t kW = kCs + ((CH * 3 * sizeof(T) + 15) / 16) * 16;
+    static constexpr uint32_t kStageEnd = kW + CH * 4 * 4;
+    static constexpr uint32_t kRedEnd = kX + (kRecThreads / 32) * kRecSub * DV * 2 * 4;
+    static constexpr uint32_t kZ = kStageEnd > kRedEnd ? kStageEnd : kRedEnd;
+    static constexpr uint32_t kBytes = kZ + kRecSub * DV * sizeof(T);
+};
+
+// N consecutive floats of a shared-memory row (16-byte vectors when N is a
+// multiple of 4, the caller's offset then being one too).
+template <int N>
+__device__ __forceinline__ void ro_rows(float (&v)[N], const float* src) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src + i);
+            v[i] = f.x;
+            v[i + 1] = f.y;
+            v[i + 2] = f.z;
+            v[i + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = src[i];
+    }
+}
+
+// The one pass over this thread's state rows: S^T k_j and S^T q_j (raw conv
+// outputs) for the M tokens, reduced over the warp's row groups and stored
+// per warp, key and query sums of a column side by side:
+// red[((warp * kRecSub + j) * DV + column) * 2 + {0: key, 1: query}].
+template <int M, int DK, int DV, int RPT, int L, int CH>
+__device__ __forceinline__ void ro_colsums(const float4 (&s)[RPT], const float (*cbuf)[CH], int rg, int lane,
+                                           int warp, int c4, float* red) {
+    constexpr int G = RPT % 4 == 0 ? 4 : 1;  // rows per shared-memory load
+    float acc[M][2][4];
+#pragma unroll
+    for (int j = 0; j < M; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][0][e] = acc[j][1][e] = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < RPT; i0 += G) {
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            float kr[G], qr[G];
+            ro_rows<G>(kr, &cbuf[j][DK + RPT * rg + i0]);
+            ro_rows<G>(qr, &cbuf[j][RPT * rg + i0]);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float4 sv = s[i0 + g];
+                acc[j][0][0] = fmaf(sv.x, kr[g], acc[j][0][0]);
+                acc[j][1][0] = fmaf(sv.x, qr[g], acc[j][1][0]);
+                acc[j][0][1] = fmaf(sv.y, kr[g], acc[j][0][1]);
+                acc[j][1][1] = fmaf(sv.y, qr[g], acc[j][1][1]);
+                acc[j][0][2] = fmaf(sv.z, kr[g], acc[j][0][2]);
+                acc[j][1][2] = fmaf(sv.z, qr[g], acc[j][1][2]);
+                acc[j][0][3] = fmaf(sv.w, kr[g], acc[j][0][3]);
+                acc[j][1][3] = fmaf(sv.w, qr[g], acc[j][1][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = L; off < 32; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < M; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[j][0][e] += __shfl_xor_sync(0xffffffffu, acc[j][0][e], off);
+                acc[j][1][e] += __shfl_xor_sync(0xffffffffu, acc[j][1][e], off);
+            }
+    if (lane < L) {
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            float4* dst = reinterpret_cast<float4*>(&red[((warp * kRecSub + j) * DV + c4 * 4) * 2]);
+            dst[0] = make_float4(acc[j][0][0], acc[j][1][0], acc[j][0][1], acc[j][1][1]);
+            dst[1] = make_float4(acc[j][0][2], acc[j][1][2], acc[j][0][3], acc[j][1][3]);
+        }
+    }
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kRecThreads, 2)
+verify_ro_kernel(RecurrentArgs p) {
+    constexpr int L = DV / 4;            // lanes per state row
+    constexpr int RG = kRecThreads / L;  // row groups
+    constexpr int RPT = DK / RG;         // rows per thread (consecutive)
+    constexpr int CH = 2 * DK + DV;      // channels this head reads: q | k | v
+    constexpr int NW = kRecThreads / 32;
+    static_assert(DK % RG == 0 && RPT >= 1 && 2 * DV <= kRecThreads, "unsupported head dims");
+
+    __shared__ __align__(16) float cbuf[kRecSub][CH];  // conv outputs q | k | v (raw)
+    __shared__ float gam[kRecSub], bet[kRecSub];
+    // the inverse norms of q and k, the decay from the first token through
+    // this one, and the normalised, decayed key.key and key.query products with
+    // the earlier tokens (the last cfq entry: with the token's own key)
+    __shared__ float nq[kRecSub], nk[kRecSub], gcum[kRecSub];
+    __shared__ float cfk[kRecSub][kRecSub], cfq[kRecSub][kRecSub];
+    __shared__ float ysum[kRecSub][NW];
+    __shared__ __align__(8) uint64_t bar_s;  // the state copy of the CTA's next item
+    extern __shared__ __align__(128) float s_next[];
+    using Stage = RoStage<DK, DV, T>;
+    uint8_t* dyn = reinterpret_cast<uint8_t*>(s_next);
+    T (*st_x)[CH] = reinterpret_cast<T (*)[CH]>(dyn + Stage::kX);
+    T* st_cs = reinterpret_cast<T*>(dyn + Stage::kCs);
+    float* st_w = reinterpret_cast<float*>(dyn + Stage::kW);
+    float* red = reinterpret_cast<float*>(dyn + Stage::kX);  // after the conv: the column sums
+    T (*st_z)[DV] = reinterpret_cast<T (*)[DV]>(dyn + Stage::kZ);
+
+    const int hv_n = p.n_v_heads, m = p.uniform_T;
+    const int cd = 2 * p.n_k_heads * DK + hv_n * DV;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c4 = tid % L, rg = tid / L;
+    const int K = p.conv_k, keep = K - 1;
+    const int n_items = p.n_seq * hv_n;
+    constexpr uint32_t kSlabBytes = DK * DV * 4;
+
+    if (tid == 0) {
+        tc::mbar_init(&bar_s, 1);
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    auto issue_state = [&](int item) {  // one thread: the slab in 16 KB pieces
+        tc::mbar_arrive_expect_tx(&bar_s, kSlabBytes);
+        for (uint32_t off = 0; off < kSlabBytes; off += 16384)
+            tc::bulk_load_1d(reinterpret_cast<uint8_t*>(s_next) + off,
+                             p.state_in + (size_t)item * DK * DV + off / 4, min(16384u, kSlabBytes - off),
+                             &bar_s);
+    };
+    uint32_t s_phase = 0;
+    bool s_pending = (int)blockIdx.x < n_items;
+    if (s_pending && tid == 0) issue_state(blockIdx.x);
+
+    const T* __restrict__ x = static_cast<const T*>(p.x);
+    const T* __restrict__ z = static_cast<const T*>(p.z);
+    const T* __restrict__ av = static_cast<const T*>(p.a);
+    const T* __restrict__ bv = static_cast<const T*>(p.b);
+    const T* __restrict__ cs_in = static_cast<const T*>(p.conv_state_in);
+    T* __restrict__ out = static_cast<T*>(p.out);
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int n = item / hv_n, hv = item - n * hv_n;
+        const int hk = key_head(hv, hv_n / p.n_k_heads, p.n_k_heads, p.head_map);
+        const int bos = n * m;
+
+        // the item's inputs by per-thread async copies (16-byte aligned bases,
+        // checked by the host), and its gate inputs
+        {
+            constexpr int QC = DK * (int)sizeof(T) / 16, XC = CH * (int)sizeof(T) / 16;
+            const int chq = hk * DK, chk = p.n_k_heads * DK + hk * DK, chv = 2 * p.n_k_heads * DK + hv * DV;
+            auto range_of = [&](int c, int per_q, int& ch, int& off) {
+                const int r = c < per_q ? 0 : c < 2 * per_q ? 1 : 2;
+                ch = r == 0 ? chq : r == 1 ? chk : chv;
+                off = c - r * per_q;
+            };
+            for (int i = tid; i < m * XC; i += kRecThreads) {
+                const int tau = i / XC, c = i - tau * XC;
+                int ch, off;
+                range_of(c, QC, ch, off);
+                cp_async16(reinterpret_cast<uint4*>(&st_x[tau][0]) + c,
+                           reinterpret_cast<const uint4*>(x + (size_t)(bos + tau) * cd + ch) + off);
+            }
+            if (cs_in) {
+                const int per_q = QC * keep, tot = CH * (int)sizeof(T) * keep / 16;
+                for (int c = tid; c < tot; c += kRecThreads) {
+                    int ch, off;
+                    range_of(c, per_q, ch, off);
+                    cp_async16(reinterpret_cast<uint4*>(st_cs) + c,
+                               reinterpret_cast<const uint4*>(cs_in + ((size_t)n * cd + ch) * keep) + off);
+                }
+            }
+            {
+                const int per_q = DK * K / 4, tot = CH * K / 4;
+                for (int c = tid; c < tot; c += kRecThreads) {
+                    int ch, off;
+                    range_of(c, per_q, ch, off);
+                    cp_async16(reinterpret_cast<uint4*>(st_w) + c,
+                               reinterpret_cast<const uint4*>(p.conv_w + (size_t)ch * K) + off);
+                }
+            }
+            constexpr int ZC = DV * (int)sizeof(T) / 16;
+            for (int i = tid; i < m * ZC; i += kRecThreads) {
+                const int tau = i / ZC, c = i - tau * ZC;
+                cp_async16(reinterpret_cast<uint4*>(&st_z[tau][0]) + c,
+                           reinterpret_cast<const uint4*>(z + ((size_t)(bos + tau) * hv_n + hv) * DV) + c);
+            }
+            cp_async_commit();
+        }
+        float a_pre = 0.f, b_pre = 0.f;
+        if (tid < m) {
+            const size_t gi = (size_t)(bos + tid) * hv_n + hv;
+            a_pre = to_f32(av[gi]);
+            b_pre = to_f32(bv[gi]);
+        }
+
+        // the state, from the copy in flight since the previous item; the next
+        // item's copy goes out once every thread has taken its rows
+        float4 s[RPT];
+        if (!__syncthreads_and(tc::mbar_wait(&bar_s, s_phase))) {
+            if (tid == 0) atomicCAS(&g_rec_error, 0, 30);
+            cp_async_wait_all();
+            break;
+        }
+        s_phase ^= 1;
+        s_pending = false;
+        {
+            const float4* src = reinterpret_cast<const float4*>(s_next);
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) s[i] = src[(RPT * rg + i) * L + c4];
+        }
+        __syncthreads();
+        if (item + (int)gridDim.x < n_items) {
+            if (tid == 0) issue_state(item + gridDim.x);
+            s_pending = true;
+        }
+
+        // ---- conv + SiLU of the m tokens x (q | k | v) channels
+        cp_async_wait_all();
+        __syncthreads();
+        if (K == 4) {
+            // one channel a thread, sliding over the tokens: each input value
+            // and the channel's weights are read once
+            for (int lc = tid; lc < CH; lc += kRecThreads) {
+                const float4 w4 = *reinterpret_cast<const float4*>(&st_w[lc * 4]);
+                float h0 = 0.f, h1 = 0.f, h2 = 0.f;  // tokens -3, -2, -1
+                if (cs_in) {
+                    h0 = to_f32(st_cs[lc * 3]);
+                    h1 = to_f32(st_cs[lc * 3 + 1]);
+                    h2 = to_f32(st_cs[lc * 3 + 2]);
+                }
+                for (int tau = 0; tau < m; ++tau) {
+                    const float xv = to_f32(st_x[tau][lc]);
+                    float acc = fmaf(w4.x, h0, 0.f);
+                    acc = fmaf(w4.y, h1, acc);
+                    acc = fmaf(w4.z, h2, acc);
+                    acc = fmaf(w4.w, xv, acc);
+                    cbuf[tau][lc] = siluf_(acc);
+                    h0 = h1;
+                    h1 = h2;
+                    h2 = xv;
+                }
+            }
+        } else {
+            for (int idx = tid; idx < m * CH; idx += kRecThreads) {
+                const int tau = idx / CH, lc = idx % CH;
+                float acc = 0.f;
+                for (int j = 0; j < K; ++j) {
+                    const int tt = tau - keep + j;
+                    const float v = tt >= 0 ? to_f32(st_x[tt][lc])
+                                    : cs_in ? to_f32(st_cs[lc * keep + keep + tt]) : 0.f;
+                    acc = fmaf(st_w[lc * K + j], v, acc);
+                }
+                cbuf[tau][lc] = siluf_(acc);
+            }
+        }
+        if (tid < m) {
+            gam[tid] = expf(log_decay(a_pre, p.A_log[hv], p.dt_bias[hv], p.decay_form));
+            bet[tid] = sigmoidf_(b_pre);
+        }
+        __syncthreads();
+
+        // ---- per token (one warp each), from the raw conv outputs: the inverse
+        // norms of q and k and, with each earlier token i, the products
+        // k_i.k_i, k_i.k and k_i.q, turned into the coefficients of the solve
+        if (warp < m) {
+            constexpr int NV = 3 + 3 * (kRecSub - 1);
+            const int tau = warp;
+            float v[NV];
+#pragma unroll
+            for (int j = 0; j < NV; ++j) v[j] = 0.f;
+            for (int r = lane; r < DK; r += 32) {
+                const float q = cbuf[tau][r], k = cbuf[tau][DK + r];
+                v[0] = fmaf(q, q, v[0]);
+                v[1] = fmaf(k, k, v[1]);
+                v[2] = fmaf(k, q, v[2]);
+#pragma unroll
+                for (int j = 0; j < kRecSub - 1; ++j)
+                    if (j < tau) {
+                        const float ki = cbuf[j][DK + r];
+                        v[3 + 3 * j] = fmaf(ki, ki, v[3 + 3 * j]);
+                        v[4 + 3 * j] = fmaf(ki, k, v[4 + 3 * j]);
+                        v[5 + 3 * j] = fmaf(ki, q, v[5 + 3 * j]);
+                    }
+            }
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+                if (j < 3 + 3 * tau) v[j] = group_sum<32>(v[j]);
+            if (lane == 0) {
+                const float qi = rsqrtf(v[0] + p.l2_eps) * rsqrtf((float)DK);
+                const float ki = rsqrtf(v[1] + p.l2_eps);
+                nq[tau] = qi;
+                nk[tau] = ki;
+                cfq[tau][tau] = v[2] * ki * qi;
+                float gc = gam[0];
+                for (int u = 1; u <= tau; ++u) gc *= gam[u];
+                gcum[tau] = gc;
+                float dec = 1.f;  // decay over the tokens after j, through this one
+#pragma unroll
+                for (int j = kRecSub - 2; j >= 0; --j)
+                    if (j < tau) {
+                        dec *= gam[j + 1];
+                        const float kj = rsqrtf(v[3 + 3 * j] + p.l2_eps);
+                        cfk[tau][j] = dec * (v[4 + 3 * j] * kj * ki);
+                        cfq[tau][j] = dec * (v[5 + 3 * j] * kj * qi);
+                    }
+            }
+        }
+        // ---- the one pass over the state (the conv has read the staging, which
+        // the column sums now overwrite)
+        switch (m) {
+            case 1: ro_colsums<1, DK, DV, RPT, L, CH>(s, cbuf, rg, lane, warp, c4, red); break;
+            case 2: ro_colsums<2, DK, DV, RPT, L, CH>(s, cbuf, rg, lane, warp, c4, red); break;
+            case 3: ro_colsums<3, DK, DV, RPT, L, CH>(s, cbuf, rg, lane, warp, c4, red); break;
+            default: ro_colsums<4, DK, DV, RPT, L, CH>(s, cbuf, rg, lane, warp, c4, red); break;
+        }
+        __syncthreads();
+
+        // ---- the solve, two lanes a column: the even lane sums the key side
+        // and forms delta_j, the odd lane the query side and o_j
+        float o[kRecSub];
+        if (tid < 2 * DV) {
+            const int c = tid >> 1, h = tid & 1;
+            float part[kRecSub], dl[kRecSub];
+#pragma unroll
+            for (int j = 0; j < kRecSub; ++j)
+                if (j < m) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) acc += red[((w * kRecSub + j) * DV + c) * 2 + h];
+                    part[j] = acc;
+                }
+#pragma unroll
+            for (int j = 0; j < kRecSub; ++j)
+                if (j < m) {
+                    float kv = gcum[j] * (part[j] * nk[j]);
+#pragma unroll
+                    for (int i = 0; i < j; ++i) kv = fmaf(cfk[j][i], dl[i], kv);
+                    const float d = bet[j] * (cbuf[j][2 * DK + c] - kv);
+                    dl[j] = __shfl_sync(0xffffffffu, d, lane & ~1);
+                    float oo = gcum[j] * (part[j] * nq[j]);
+#pragma unroll
+                    for (int i = 0; i <= j; ++i) oo = fmaf(cfq[j][i], dl[i], oo);
+                    o[j] = oo;
+                    const float o2 = group_sum<32>(h ? oo * oo : 0.f);
+                    if (lane == 0) ysum[j][warp] = o2;
+                }
+        }
+        __syncthreads();
+
+        // ---- gated RMSNorm and the outputs: lane h of a column writes the
+        // tokens j with j % 2 == h
+        if (tid < 2 * DV) {
+            const int c = tid >> 1, h = tid & 1;
+            const float rn = p.norm_w[c];
+#pragma unroll
+            for (int j = 0; j < kRecSub; ++j)
+                if (j < m) {
+                    const float oj = __shfl_sync(0xffffffffu, o[j], lane | 1);
+                    if ((j & 1) == h) {
+                        float tot = 0.f;
+#pragma unroll
+                        for (int w = 0; w < 2 * DV / 32; ++w) tot += ysum[j][w];
+                        const float rr = rsqrtf(tot / (float)DV + p.rms_eps);
+                        const float zv = to_f32(st_z[j][c]);
+                        out[(size_t)(bos + j) * hv_n * DV + (size_t)hv * DV + c] =
+                            from_f32<T>(oj * rr * rn * gatef_(zv, p.act));
+                    }
+                }
+        }
+        __syncthreads();  // the staging and z rows are the next item's
+    }
+
+    // no copy may be in flight when the CTA leaves (only after a give-up)
+    if (s_pending && tid == 0 && !tc::mbar_wait(&bar_s, s_phase)) atomicCAS(&g_rec_error, 0, 30);
+}
+
 // SMs of the current device, cached per device.
 static int rec_sm_count() {
     static std::atomic<int> cached[64];
@@ -414,10 +811,50 @@ static cudaError_t launch_rec_inst(const RecurrentArgs& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+template <int DK, int DV, typename T>
+static cudaError_t launch_ro_inst(const RecurrentArgs& p, cudaStream_t st) {
+    constexpr int kSmem = RoStage<DK, DV, T>::kBytes;
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load()) {
+        cudaError_t e = cudaFuncSetAttribute(verify_ro_kernel<DK, DV, T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(verify_ro_kernel<DK, DV, T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        attr_set[dev].store(true);
+    }
+    const int items = p.n_seq * p.n_v_heads;
+    const int grid = std::min(items, kRecCtasPerSm * rec_sm_count());
+    verify_ro_kernel<DK, DV, T><<<grid, kRecThreads, kSmem, st>>>(p);
+    return cudaGetLastError();
+}
+
+// A call the read-only kernel takes: no state written, a resident state read,
+// at most kRecSub tokens in every sequence, scalar decay, 16-byte aligned
+// inputs (its async copies), d_v <= 128.
+static bool read_only_call(const RecurrentArgs& p, int dv) {
+    const uintptr_t align = reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.z) |
+                            reinterpret_cast<uintptr_t>(p.conv_w) |
+                            reinterpret_cast<uintptr_t>(p.conv_state_in);
+    return !p.state_out && !p.inter && p.state_in && !p.per_channel && !p.cu_seqlens && p.uniform_T >= 1 &&
+           p.uniform_T <= kRecSub && dv <= 128 && (align & 15) == 0 && !std::getenv("GDN_VERIFY_TOKENWISE");
+}
+
 template <typename T>
 static cudaError_t launch_recurrent_t(const RecurrentArgs& p, int dk, int dv, cudaStream_t st) {
     // the bulk state copies read 16-byte aligned slabs
     if (p.state_in && reinterpret_cast<uintptr_t>(p.state_in) % 16) return cudaErrorInvalidValue;
+    if (read_only_call(p, dv)) {
+#define GDN_RO_CASE(A, B) \
+        if (dk == A && dv == B) return launch_ro_inst<A, B, T>(p, st);
+        GDN_RO_CASE(32, 32) GDN_RO_CASE(32, 64) GDN_RO_CASE(32, 128)
+        GDN_RO_CASE(64, 32) GDN_RO_CASE(64, 64) GDN_RO_CASE(64, 128)
+        GDN_RO_CASE(128, 32) GDN_RO_CASE(128, 64) GDN_RO_CASE(128, 128)
+#undef GDN_RO_CASE
+    }
 #define GDN_REC_CASE(A, B)                                                                         \
     if (dk == A && dv == B)                                                                        \
         return p.per_channel ? launch_rec_inst<A, B, T, true>(p, st) : launch_rec_inst<A, B, T, false>(p, st);

@@ -211,9 +211,10 @@ def test_decode_commit_keeps_accepted_prefix():
 
 
 @pytest.mark.parametrize("d_k", [128, 64])
-def test_verify_then_replay_gives_the_committed_state(d_k):
+def test_verify_then_replay_gives_the_committed_state(d_k, monkeypatch):
     """Rollback by replay: gdn_verify runs the drafts against a read-only state
-    (its outputs are gdn_decode's, and nothing else is written); replaying each
+    (its outputs are gdn_decode's up to rounding, bit for bit on the
+    token-by-token path, and nothing else is written); replaying each
     sequence's accepted prefix with gdn_prefill from the kept state and history
     (the token-recurrent path: every prefix is short) gives the state that
     gdn_decode wrote as an intermediate and the history gdn_decode_commit keeps,
@@ -229,9 +230,13 @@ def test_verify_then_replay_gives_the_committed_state(d_k):
     inter = torch.full((n, tt, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
     out_ref = gdn.decode(d, t["params"], x, z, a, b, st0.clone(), cs0.clone(), inter)
     st_v, cs_v = st0.clone(), cs0.clone()
-    out_v = gdn.verify(d, t["params"], x, z, a, b, st_v, conv_state=cs_v)
+    out_v = gdn.verify(d, t["params"], x, z, a, b, st_v, conv_state=cs_v)  # all drafts in one pass
+    monkeypatch.setenv("GDN_VERIFY_TOKENWISE", "1")
+    out_w = gdn.verify(d, t["params"], x, z, a, b, st_v, conv_state=cs_v)  # token by token
+    monkeypatch.delenv("GDN_VERIFY_TOKENWISE")
     torch.cuda.synchronize()
-    assert torch.equal(out_v, out_ref)
+    assert torch.equal(out_w, out_ref)
+    assert rel_err(out_v.reshape(n * tt, -1), run_oracle(case)["out"]) <= TOL["bf16"]
     assert torch.equal(st_v, st0) and torch.equal(cs_v, cs0)
     # replay: the accepted prefixes packed as one variable-length prefill
     cu = np.concatenate([[0], np.cumsum(accepted)]).astype(np.int32)
@@ -252,6 +257,42 @@ def test_verify_then_replay_gives_the_committed_state(d_k):
         sub.x, sub.z, sub.a, sub.b = sub.x[:j], sub.z[:j], sub.a[:j], sub.b[:j]
         ref = run_oracle(sub)
         assert rel_err(st_r[i], ref["state"][0]) <= TOL["bf16"]
+
+
+READ_ONLY_VERIFY_CASES = {
+    # d_k, d_v, tokens, conv_k, act, dtype, GQA (Hk, Hv), conv history given
+    "d128_T4": (128, 128, 4, 4, "silu", "bf16", (2, 4), True),
+    "d128_T3_sigmoid": (128, 128, 3, 4, "sigmoid", "bf16", (1, 3), True),
+    "d128_T1_no_history": (128, 128, 1, 4, "silu", "bf16", (2, 2), False),
+    "dk64_dv128_T2_K3": (64, 128, 2, 3, "silu", "bf16", (2, 4), True),
+    "dk128_dv64_T4_f32": (128, 64, 4, 4, "sigmoid", "f32", (1, 4), True),
+    "dk32_dv32_T4_K2": (32, 32, 4, 2, "silu", "bf16", (1, 8), True),
+    "dk128_dv32_T3_f32_K3": (128, 32, 3, 3, "silu", "f32", (2, 4), False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(READ_ONLY_VERIFY_CASES))
+def test_read_only_verify_matches_oracle(name):
+    """gdn_verify of up to four drafts takes all of them in one pass over the
+    state (unrolled form of the token rule): its outputs match the oracle's
+    decode of the same tokens, and neither the state nor the history moves."""
+    d_k, d_v, tt, k, act, dt, (hk, hv), hist = READ_ONLY_VERIFY_CASES[name]
+    n = 5
+    case = _gen("ro" + name, mode="decode", n_seq=n, tokens_per_seq=tt, d_k=d_k, d_v=d_v,
+                conv_k=k, act=act, dtype=dt, n_k_heads=hk, n_v_heads=hv, state_std=0.05,
+                conv_state_std=1.0 if hist else None, seed=41)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    t = upload(case)
+    x, z, a, b = (t[key].view(n, tt, -1) for key in ("x", "z", "a", "b"))
+    st = t["state"].clone()
+    cs = None if t["conv_state"] is None else t["conv_state"].clone()
+    out = gdn.verify(d, t["params"], x, z, a, b, st, conv_state=cs)
+    torch.cuda.synchronize()
+    assert rel_err(out.reshape(n * tt, -1), ref["out"]) <= TOL[dt]
+    assert torch.equal(st, t["state"])
+    if cs is not None:
+        assert torch.equal(cs, t["conv_state"])
 
 
 def test_decode_equals_prefill_of_same_tokens():
@@ -539,6 +580,22 @@ def test_full_size_decode_256():
     assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
     assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
+def test_full_size_read_only_verify_64x4():
+    """The speculative-verify workload through gdn_verify (one pass over each
+    state for all four drafts): outputs against the oracle, state untouched."""
+    case = workloads.config(4)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    t = upload(case)
+    n, tt = case.n_seq, case.tokens_per_seq
+    x, z, a, b = (t[key].view(n, tt, -1) for key in ("x", "z", "a", "b"))
+    st, cs = t["state"].clone(), t["conv_state"].clone()
+    out = gdn.verify(d, t["params"], x, z, a, b, st, conv_state=cs)
+    torch.cuda.synchronize()
+    assert rel_err(out.reshape(n * tt, -1), ref["out"]) <= TOL["bf16"]
+    assert torch.equal(st, t["state"]) and torch.equal(cs, t["conv_state"])
 
 
 def test_full_size_spec_verify_64x4():
