@@ -51,6 +51,9 @@ TRAFFIC = {
     ("decode", "recurrent"): ((139_134_208 + 73_977_088) * 4,
                               "ncu capture of the 64-sequence decode step, scaled x 256/64"),
     ("spec_verify", "recurrent"): (144_244_992 + 477_105_664, "ncu capture of this workload's launch"),
+    # the step's two launches under one name: the read-only verify and the replay
+    ("spec_replay", "recurrent"): (((143_898_112 + 3_576_832) + (140_742_912 + 74_456_320)) // 2,
+                                   "ncu captures of the step's two launches (verify, replay), averaged"),
     # 16 sequences of 128..1024 tokens (149 chunks); the traffic is per chunk: x 1015/149
     ("varlen", "chunk_scan"): (round((659_001_856 + 96_884_992) * 1015 / 149),
                                "ncu capture of a 149-chunk varlen case, scaled x 1015/149 chunks"),
