@@ -388,6 +388,26 @@ def test_decode_per_channel_decay_matches_oracle():
     assert rel_err(got["inter"], ref["inter"].reshape(n, tt, *ref["inter"].shape[1:])) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("options", ["tiled_coef", "per_channel"])
+def test_read_only_verify_options_match_oracle(options):
+    """gdn_verify with the checkpoint options: the tiled map with the decay
+    coefficient (the one-pass kernel takes them), and per-channel decay (which
+    it does not: the token-by-token kernel runs the call)."""
+    case = _gen("vo", mode="decode", n_seq=5, tokens_per_seq=4, n_k_heads=2, n_v_heads=6,
+                act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=30)
+    case = _with_options(case, "tiled", "coef") if options == "tiled_coef" else _per_channel(case, 93)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    t = upload(case)
+    n, tt = case.n_seq, case.tokens_per_seq
+    x, z, a, b = (t[key].view(n, tt, -1) for key in ("x", "z", "a", "b"))
+    st, cs = t["state"].clone(), t["conv_state"].clone()
+    out = gdn.verify(d, t["params"], x, z, a, b, st, conv_state=cs)
+    torch.cuda.synchronize()
+    assert rel_err(out.reshape(n * tt, -1), ref["out"]) <= TOL["bf16"]
+    assert torch.equal(st, t["state"]) and torch.equal(cs, t["conv_state"])
+
+
 TC_CASES = sorted(k for k in PREFILL_CASES if k.startswith("tc_"))
 
 
