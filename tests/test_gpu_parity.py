@@ -602,6 +602,24 @@ def test_full_size_decode_256():
     assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
 
 
+def test_read_only_verify_many_items_per_cta():
+    """More (sequence, value head) items than resident CTAs, so that each CTA
+    walks several items (its next state copy in flight while one computes):
+    600 sequences x 4 heads against at most two CTAs per SM."""
+    n, tt = 600, 3
+    case = _gen("rm", mode="decode", n_seq=n, tokens_per_seq=tt, n_k_heads=2, n_v_heads=4,
+                d_k=64, d_v=64, state_std=0.05, conv_state_std=1.0, seed=43)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    t = upload(case)
+    x, z, a, b = (t[key].view(n, tt, -1) for key in ("x", "z", "a", "b"))
+    st, cs = t["state"].clone(), t["conv_state"].clone()
+    out = gdn.verify(d, t["params"], x, z, a, b, st, conv_state=cs)
+    torch.cuda.synchronize()
+    assert rel_err(out.reshape(n * tt, -1), ref["out"]) <= TOL["bf16"]
+    assert torch.equal(st, t["state"]) and torch.equal(cs, t["conv_state"])
+
+
 def test_full_size_read_only_verify_64x4():
     """The speculative-verify workload through gdn_verify (one pass over each
     state for all four drafts): outputs against the oracle, state untouched."""
