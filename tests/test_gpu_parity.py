@@ -268,6 +268,7 @@ READ_ONLY_VERIFY_CASES = {
     "dk128_dv64_T4_f32": (128, 64, 4, 4, "sigmoid", "f32", (1, 4), True),
     "dk32_dv32_T4_K2": (32, 32, 4, 2, "silu", "bf16", (1, 8), True),
     "dk128_dv32_T3_f32_K3": (128, 32, 3, 3, "silu", "f32", (2, 4), False),
+    "d128_T2_f32": (128, 128, 2, 4, "silu", "f32", (2, 4), True),
 }
 
 
