@@ -23,6 +23,10 @@
 // a warp, then shared memory across warps.  The readout uses
 // o = e^g S^T q + (k.q) delta, which equals S'^T q for the written state S'
 // (S' = e^g S + k delta^T), so the state is read once per token.
+//
+// A second kernel, verify_ro_kernel, takes verify calls that write no state:
+// all of a sequence's drafts in one pass over the state (the rule unrolled
+// over up to four tokens), with no state update.
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
