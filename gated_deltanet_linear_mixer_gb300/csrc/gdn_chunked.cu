@@ -758,11 +758,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 //               it runs in the pipe while the state is updated.
 //   warps 10,11 the gate norm_w act(z) of each chunk, from its z rows, into
 //               shared memory for the output warps.
-// Split products: P4 and P7 (the chain) take the hi and lo halves of their B
-// operand side by side as one N=128 product, A_hi [B_hi | B_lo], plus
-// A_lo B_hi into the first half; the result is the sum of the accumulator's
-// two halves.  P6 (off the chain) is hi.hi + hi.lo + lo.hi into one N=64
-// accumulator.  Every wait is bounded (wait_or_dead).
+// Split products: every product is hi.hi + hi.lo + lo.hi.  P4 takes the hi
+// and lo halves of its B operand side by side as one N=128 product,
+// A_hi [B_hi | B_lo], plus A_lo B_hi into the first half; its result is the
+// sum of the accumulator's two halves.  P7 and P6 are three N=64 MMAs into one
+// accumulator, so that the state update reads one 32-column block.  Every
+// wait is bounded (wait_or_dead).
 constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;      // value lanes per CTA
 constexpr int kScanThreads = 384;     // 8 compute warps + a control warpgroup
@@ -781,8 +782,8 @@ constexpr uint32_t kScanZ = 212992;                         // z rows, bf16 64 x
 constexpr uint32_t kScanGc = 221184;                        // in-chunk cumulative log-decay, 2 x 64 fp32
 constexpr uint32_t kScanEnd = 221696;
 // tensor-memory columns: P4 in two 128-column slots (chunk c uses c%2), P7 in
-// 128 columns, P6 in two 64-column slots
-constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 384;
+// 64 columns, P6 in two 64-column slots
+constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 320;
 
 struct ScanSync {
     uint64_t a4, k, qk;        // TMA loads landed
@@ -926,7 +927,6 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             constexpr uint64_t kLo16 = 16384 >> 4, kLoA4 = 32768 >> 4;
             const uint32_t id128 = idesc_bf16_f32(128, 2 * kDS, false, true);
             const uint32_t id64 = idesc_bf16_f32(128, kDS, false, true);
-            const uint32_t id7_128 = idesc_bf16_f32(128, 2 * kDS, true, true);
             const uint32_t id7_64 = idesc_bf16_f32(128, kDS, true, true);
             uint32_t last = 0;  // (barrier index << 1) | parity of the last commit
             int commits = 0;
@@ -959,13 +959,13 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 }
                 mma_commit(&sy.p4);
                 last = (0u << 1) | (c & 1); ++commits;
-                // P7_c = K^T U'_c: K^T_hi [U'_hi | U'_lo] + K^T_lo U'_hi
+                // P7_c = K^T U'_c, three N=64 products into one accumulator
                 if (!wait_or_dead(&sy.u, c & 1, sy, 6) || !wait_or_dead(&sy.k, c & 1, sy, 5)) break;
                 tc_fence_after_sync();
-#pragma unroll
+#pragma unroll 1  // few registers: the control warps run at 96
                 for (int k = 0; k < 4; ++k) {
-                    mma_bf16(tmem + kTmDs, dK + k * 128, dUp + k * 128, id7_128, k > 0 ? 1u : 0u);
-                    mma_bf16(tmem + kTmDs, dK + kLo16 + k * 128, dUp + k * 128, id7_64, 1u);
+                    mma3(tmem + kTmDs, dK + k * 128, dK + kLo16 + k * 128, dUp + k * 128,
+                         dUp + (8192 >> 4) + k * 128, id7_64, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&sy.p7);
                 last = (1u << 1) | (c & 1); ++commits;
@@ -1283,11 +1283,11 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p7, c & 1, sy, 6));
             if (alive) {
                 tc_fence_after_sync();
-                float a[32], b[32];
+                float a[32];
                 const uint32_t ds = tmem + kTmDs + lane_off + cl;
-                tmem_ld32x2(ds, ds + 64, a, b);
+                tmem_ld32(ds, a);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], a[j] + b[j]);
+                for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], a[j]);
                 if (c + 1 < n_ch) {
                     store_s();
                     fence_proxy_async_smem();
