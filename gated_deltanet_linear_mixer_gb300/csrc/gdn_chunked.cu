@@ -829,7 +829,11 @@ __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, Sca
     }
 }
 
-// Value head h of sequence n, this CTA's half of the value lanes.
+// Value head h of sequence n, this CTA's half of the value lanes.  kSplitP4:
+// P4 as three N=64 products into one 64-column accumulator (its issue loop
+// rolled) instead of the N-stacked form; the two-kernel scan, which runs on
+// every SM at once and is slowed more by the longer U step, takes it.
+template <bool kSplitP4>
 __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
                                                 const CUtensorMap& map_kqh, const CUtensorMap& map_kql,
@@ -885,6 +889,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
     cluster_wait();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
+    constexpr uint32_t kP4Cols = kSplitP4 ? 64 : 128;  // tensor-memory columns of a P4 slot
     const uint32_t peer_dead = map_to_rank(smem_u32(&sy.dead), peer);
 
     auto wrow = [&](int c) { return ((c_begin + c) * hv_n + h) * kC; };
@@ -940,17 +945,30 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 // from it (the state rows 0..63 do not imply that)
                 if (c >= 2 && !wait_or_dead(&sy.d4free[c & 1], ((c - 2) >> 1) & 1, sy, 4)) break;
                 tc_fence_after_sync();
-                const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128;
+                const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * kP4Cols;
                 bool hi_ok = true;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (k == 4) {
-                        if (!(hi_ok = wait_or_dead(&sy.s_hi, c & 1, sy, 4))) break;
-                        tc_fence_after_sync();
+                if constexpr (kSplitP4) {
+#pragma unroll 1
+                    for (int k = 0; k < 8; ++k) {
+                        if (k == 4) {
+                            if (!(hi_ok = wait_or_dead(&sy.s_hi, c & 1, sy, 4))) break;
+                            tc_fence_after_sync();
+                        }
+                        const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                        mma3(d4, dA4 + ao, dA4 + kLoA4 + ao, dBs + k * 128, dBs + kLo16 + k * 128, id64,
+                             k > 0 ? 1u : 0u);
                     }
-                    const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma_bf16(d4, dA4 + ao, dBs + k * 128, id128, k > 0 ? 1u : 0u);
-                    mma_bf16(d4, dA4 + kLoA4 + ao, dBs + k * 128, id64, 1u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (k == 4) {
+                            if (!(hi_ok = wait_or_dead(&sy.s_hi, c & 1, sy, 4))) break;
+                            tc_fence_after_sync();
+                        }
+                        const uint64_t ao = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                        mma_bf16(d4, dA4 + ao, dBs + k * 128, id128, k > 0 ? 1u : 0u);
+                        mma_bf16(d4, dA4 + kLoA4 + ao, dBs + k * 128, id64, 1u);
+                    }
                 }
                 if (!hi_ok) {  // the MMAs already issued still complete before the unwind
                     mma_commit(&sy.p4);
@@ -1157,14 +1175,22 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                                                   wait_or_dead(&sy.gate, c & 1, sy, 9));
             if (!ok) return false;
             tc_fence_after_sync();
-            float a[32], b[32];
-            const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
-            tmem_ld32x3(d4, d4 + 64, tmem + kTmD6 + (uint32_t)(c & 1) * 64 + lane_off + cl, a, b, og);
+            float a[32];
+            const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * kP4Cols + lane_off + cl;
+            const uint32_t d6 = tmem + kTmD6 + (uint32_t)(c & 1) * 64 + lane_off + cl;
+            if constexpr (kSplitP4) {
+                tmem_ld32x2(d4, d6, a, og);
+            } else {
+                float b[32];
+                tmem_ld32x3(d4, d4 + 64, d6, a, b, og);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[j] += b[j];
+            }
             const float eg = __expf(gt_pend);
             oss = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                og[j] = fmaf(eg, a[j] + b[j], og[j]);
+                og[j] = fmaf(eg, a[j], og[j]);
                 oss = fmaf(og[j], og[j], oss);
             }
             const float* gb = reinterpret_cast<const float*>(smem + kScanGate) + t * kC;
@@ -1241,11 +1267,18 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 if (!(alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.p4, c & 1, sy, 5)))) break;
                 tc_fence_after_sync();
                 {
-                    float a[32], b[32];
-                    const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * 128 + lane_off + cl;
-                    tmem_ld32x2(d4, d4 + 64, a, b);
+                    float a[32];
+                    const uint32_t d4 = tmem + kTmD4 + (uint32_t)(c & 1) * kP4Cols + lane_off + cl;
+                    if constexpr (kSplitP4) {
+                        tmem_ld32(d4, a);
+                    } else {
+                        float b[32];
+                        tmem_ld32x2(d4, d4 + 64, a, b);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ut[j] -= a[j] + b[j];
+                        for (int j = 0; j < 32; ++j) a[j] += b[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ut[j] -= a[j];
                 }
                 // U' for P7_c (P7_{c-1} has read the last one), then U for P6_c
                 // (P6_{c-1} has read U_{c-1}): both readers are done once P4_c
@@ -1343,7 +1376,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                   const __grid_constant__ CUtensorMap map_z, ChunkArgs p) {
     // sequences with the most chunks start first: the last wave is shorter
-    chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
+    chunk_scan_body<true>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                     blockIdx.x / kSplit, p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y);
 }
 
@@ -1374,7 +1407,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_cons
                         blockIdx.x, n_prep);
     } else {
         const int s = ((int)blockIdx.x - n_prep) / kSplit;  // n_prep is even: clusters stay aligned
-        chunk_scan_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
+        chunk_scan_body<false>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                         s % p.n_v_heads, s / p.n_v_heads);
     }
 }

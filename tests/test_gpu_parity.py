@@ -416,18 +416,19 @@ TC_CASES = sorted(k for k in PREFILL_CASES if k.startswith("tc_"))
 def test_prefill_fused_and_two_kernel_launches_agree(name, monkeypatch):
     """Small batches run prep and scan as one launch (scan clusters wait on
     the prep CTAs' per-chunk flags); GDN_PREFILL_FUSED=0 forces the two-kernel
-    launch.  Both do the same arithmetic: results must be bit-identical, and the
-    two-kernel launch must meet the oracle on its own."""
+    launch.  The two differ only in how one split product's three terms are
+    summed (rounding): each meets the oracle, and their fp32 states agree to
+    1e-3 of the state's RMS (a stale or missing chunk row would be far off)."""
     case = PREFILL_CASES[name]()
     monkeypatch.setenv("GDN_PREFILL_FUSED", "0")
     two = gpu_prefill(case)
     monkeypatch.setenv("GDN_PREFILL_FUSED", "1")
     one = gpu_prefill(case)
-    assert torch.equal(one["out"], two["out"])
-    assert torch.equal(one["state"], two["state"])
     ref = run_oracle(case)
-    assert rel_err(two["out"], ref["out"]) <= TOL["bf16"]
-    assert rel_err(two["state"], ref["state"]) <= TOL["bf16"]
+    for got in (one, two):
+        assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+        assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(one["state"], two["state"].cpu().numpy()) <= 1e-3
 
 
 def _layer_inputs(case, hidden, seed, exact=False):
@@ -562,8 +563,8 @@ def test_decode_at_the_sequence_limit():
 def test_long_single_sequence_fused_launch():
     """One 32,768-token sequence (512 chunks, long-memory gates so that the state
     carries across every chunk) through the fused launch, whose scan waits on
-    prep's per-chunk flags 512 times; matches the oracle and the two-kernel
-    launch bit for bit."""
+    prep's per-chunk flags 512 times; matches the oracle, and so does the
+    two-kernel launch, their fp32 states within 1e-3 of the RMS."""
     case = _gen("long", n_k_heads=2, n_v_heads=4, lengths=[32768], state_std=0.05, seed=61,
                 slow_decay=True)
     t = upload(case)
@@ -577,7 +578,9 @@ def test_long_single_sequence_fused_launch():
         two = gpu_prefill(case, t)
     finally:
         del os.environ["GDN_PREFILL_FUSED"]
-    assert torch.equal(got["out"], two["out"]) and torch.equal(got["state"], two["state"])
+    assert rel_err(two["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(two["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["state"], two["state"].cpu().numpy()) <= 1e-3
     code = gdn.device_error()
     assert code == 0
 
