@@ -44,8 +44,8 @@ METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
 # by the units it processes, and the source says so.  An entry is removed when
 # its kernel changes, until it is captured again.
 TRAFFIC = {
-    ("prefill", "chunk_fused"): (216_812_288 + 193_505_536, "ncu capture of this workload's launch"),
-    ("layer", "chunk_fused"): (216_812_288 + 193_505_536,
+    ("prefill", "chunk_fused"): (213_410_304 + 193_265_664, "ncu capture of this workload's launch"),
+    ("layer", "chunk_fused"): (213_410_304 + 193_265_664,
                                "ncu capture of the same launch in the T=4096 prefill workload"),
     # 64-sequence decode step; the traffic is per sequence: x 256/64
     ("decode", "recurrent"): ((139_134_208 + 73_977_088) * 4,
@@ -55,7 +55,7 @@ TRAFFIC = {
     ("spec_replay", "recurrent"): (((143_898_112 + 3_576_832) + (140_742_912 + 74_456_320)) // 2,
                                    "ncu captures of the step's two launches (verify, replay), averaged"),
     # 16 sequences of 128..1024 tokens (149 chunks); the traffic is per chunk: x 1015/149
-    ("varlen", "chunk_scan"): (round((659_001_856 + 96_884_992) * 1015 / 149),
+    ("varlen", "chunk_scan"): (round((657_587_456 + 91_176_960) * 1015 / 149),
                                "ncu capture of a 149-chunk varlen case, scaled x 1015/149 chunks"),
 }
 UNIT = "tokens/s"
