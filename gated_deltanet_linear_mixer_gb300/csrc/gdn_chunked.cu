@@ -758,12 +758,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 //               it runs in the pipe while the state is updated.
 //   warps 10,11 the gate norm_w act(z) of each chunk, from its z rows, into
 //               shared memory for the output warps.
-// Split products: every product is hi.hi + hi.lo + lo.hi.  P4 takes the hi
-// and lo halves of its B operand side by side as one N=128 product,
-// A_hi [B_hi | B_lo], plus A_lo B_hi into the first half; its result is the
-// sum of the accumulator's two halves.  P7 and P6 are three N=64 MMAs into one
-// accumulator, so that the state update reads one 32-column block.  Every
-// wait is bounded (wait_or_dead).
+// Split products: every product is hi.hi + hi.lo + lo.hi.  In the fused
+// launch P4 takes the hi and lo halves of its B operand side by side as one
+// N=128 product, A_hi [B_hi | B_lo], plus A_lo B_hi into the first half, its
+// result the sum of the accumulator's two halves; in the two-kernel launch,
+// and for P7 and P6 in both, the three terms are N=64 MMAs into one
+// accumulator, so that a reader takes one 32-column block.  Every wait is
+// bounded (wait_or_dead).
 constexpr int kSplit = 2;
 constexpr int kDS = kD / kSplit;      // value lanes per CTA
 constexpr int kScanThreads = 384;     // 8 compute warps + a control warpgroup
@@ -781,8 +782,8 @@ constexpr uint32_t kScanUt = 196608;                        // U~ of the chunk, 
 constexpr uint32_t kScanZ = 212992;                         // z rows, bf16 64 x 64 (TMA, 128-byte swizzle)
 constexpr uint32_t kScanGc = 221184;                        // in-chunk cumulative log-decay, 2 x 64 fp32
 constexpr uint32_t kScanEnd = 221696;
-// tensor-memory columns: P4 in two 128-column slots (chunk c uses c%2), P7 in
-// 64 columns, P6 in two 64-column slots
+// tensor-memory columns: P4 in two slots (chunk c uses c%2) of 128 columns (64
+// in the two-kernel launch), P7 in 64 columns, P6 in two 64-column slots
 constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 320;
 
 struct ScanSync {
@@ -830,9 +831,12 @@ __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, Sca
 }
 
 // Value head h of sequence n, this CTA's half of the value lanes.  kSplitP4:
-// P4 as three N=64 products into one 64-column accumulator (its issue loop
-// rolled) instead of the N-stacked form; the two-kernel scan, which runs on
-// every SM at once and is slowed more by the longer U step, takes it.
+// P4 as three N=64 products into one 64-column accumulator from a rolled issue
+// loop, instead of the N-stacked form.  The two-kernel scan takes it: with the
+// scan on every SM at once, its shorter U step and smaller hot code (the
+// instruction cache) measured faster.  The fused launch keeps the stacked
+// form, where eight fewer MMAs on the chain count for more; the two launches
+// therefore differ in that product's rounding.
 template <bool kSplitP4>
 __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
