@@ -104,14 +104,13 @@ bool ranges_overlap(const void* a, const void* b, size_t bytes) {
     return x < y + bytes && y < x + bytes;
 }
 
-// The bf16 prefill takes the chunked tensor-core path unless every sequence
-// has at most kShortPrefill tokens (a replayed verify prefix, a batch of
+// The bf16 prefill (scalar or per-channel decay) takes the chunked
+// tensor-core path unless every sequence has at most kShortPrefill tokens (a replayed verify prefix, a batch of
 // decode-sized prompts): then the token-recurrent kernel, which streams each
 // state once and has no chunk to fill, is the faster one.
 constexpr int kShortPrefill = 16;
 bool use_chunked(const gdn_dims* d, int n_seq, const int32_t* cu_host) {
-    if (!gdn::chunked_supported(d->d_k, d->d_v, d->n_k_heads, d->n_v_heads, d->dtype == GDN_DTYPE_BF16) ||
-        d->decay_per_channel)
+    if (!gdn::chunked_supported(d->d_k, d->d_v, d->n_k_heads, d->n_v_heads, d->dtype == GDN_DTYPE_BF16))
         return false;
     for (int i = 0; i < n_seq; ++i)
         if (cu_host[i + 1] - cu_host[i] > kShortPrefill) return true;
@@ -352,7 +351,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
             return st;
         if (!use_chunked(dims, n_seq, cu_seqlens_host)) return GDN_OK;
         *bytes = gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads,
-                                              dims->n_v_heads, nullptr);
+                                              dims->n_v_heads, dims->decay_per_channel, nullptr);
     }
     g_err[0] = '\0';
     return GDN_OK;
@@ -375,6 +374,8 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
     if ((x && !aligned16(x)) || (z && !aligned16(z)) || (out && !aligned16(out)) ||
         (initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
         return fail(GDN_ERR_INVALID_ARG, fn, "x, z, out and the states must be 16-byte aligned");
+    if (dims->decay_per_channel && a && !aligned16(a))
+        return fail(GDN_ERR_INVALID_ARG, fn, "with per-channel decay, a must be 16-byte aligned");
     size_t need = 0;
     if ((st = gdn_prefill_workspace_size(dims, n_seq, cu_seqlens_host, &need)) != GDN_OK) return st;
     if (need > 0 && (!workspace || workspace_bytes < need))
@@ -394,6 +395,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         c.n_seq = n_seq; c.n_tokens = total; c.n_k_heads = dims->n_k_heads;
         c.n_v_heads = dims->n_v_heads; c.conv_k = dims->conv_k; c.act = dims->act;
         c.head_map = dims->head_map; c.decay_form = dims->decay_form;
+        c.per_channel = dims->decay_per_channel;
         c.l2_eps = dims->l2_eps; c.rms_eps = dims->rms_eps; c.cu_seqlens = cu_seqlens;
         c.x = x; c.z = z; c.a = a; c.b = b;
         c.conv_w = params->conv_w; c.A_log = params->A_log; c.dt_bias = params->dt_bias;
@@ -409,7 +411,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
             conv_done = true;
         }
         gdn::chunked_workspace_bytes(n_seq, cu_seqlens_host, dims->n_k_heads, dims->n_v_heads,
-                                     &c.layout);
+                                     dims->decay_per_channel, &c.layout);
         if ((st = cuda_status(gdn::launch_chunked_prefill(c, s), fn, "chunked prefill launch")) !=
             GDN_OK)
             return st;

@@ -37,6 +37,7 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_chunk_ops.cuh"
 #include "gdn_tc.cuh"
 #include "gdn_tma_host.h"
 
@@ -44,93 +45,11 @@ namespace gdn {
 
 using namespace tc;
 
-constexpr int kC = kChunkTokens;   // chunk length
-constexpr int kD = 128;            // d_k = d_v on this path
 constexpr int kChunkThreads = 256;
 
 __device__ int g_device_error = 0;
 
 __device__ __forceinline__ void report_error(int code) { atomicCAS(&g_device_error, 0, code); }
-
-__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float f) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16) * f;
-        const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * f;
-        w[i] = pack_bf16x2(lo, hi);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ void unpack_bf16x8(uint4 v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
-__device__ __forceinline__ uint4 pack_bf16x8(const float* f) {
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
-}
-
-// Uniform decision after a bounded wait: every thread learns whether any
-// thread's wait gave up.
-// Barriers of the prep role: named barrier 1 over its eight warps (256
-// threads), so that a launch may carry more warps than prep uses.
-__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// Every prep thread learns whether any of them passed v != 0.
-__device__ __forceinline__ bool prep_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 256, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(v ? 1u : 0u)
-        : "memory");
-    return r != 0;
-}
-// Uniform decision after a bounded wait: every prep thread learns whether any
-// thread's wait gave up.
-__device__ __forceinline__ bool prep_failed(bool ok) { return prep_any(!ok); }
-
-// Split arithmetic.  Every tensor-core operand is carried as a pair of bf16
-// tiles, hi = bf16(x) and lo = bf16(x - hi), which together hold ~16
-// significant bits; a product A.B is formed as hi.hi + hi.lo + lo.hi with
-// fp32 accumulation (the dropped lo.lo term is ~2^-16 relative).  The gated
-// outputs are heavy-tailed (up to ~50x their RMS), so plain bf16 operands
-// (2^-9 relative) would put the largest outputs' error far above 2e-2 of the
-// output RMS.
-__device__ __forceinline__ void split_store(const float* f, uint8_t* hi, uint8_t* lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // hi rounded once per pair; lo = the exact remainder, rounded
-        h[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-        l[i] = pack_bf16x2(f[2 * i] - __uint_as_float(h[i] << 16),
-                           f[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u));
-    }
-    *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-__device__ __forceinline__ void load_pair(const uint8_t* hi, const uint8_t* lo, float* f) {
-    float l[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(hi), f);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(lo), l);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] += l[e];
-}
-// D (+)= A.B with A, B given as (hi, lo) descriptor pairs.
-__device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
-                                     uint32_t idesc, uint32_t accumulate) {
-    mma_bf16(d, ah, bh, idesc, accumulate);
-    mma_bf16(d, ah, bl, idesc, 1u);
-    mma_bf16(d, al, bh, idesc, 1u);
-}
 
 // --------------------------------------------------------------- chunk_prep
 // One CTA per (chunk, key head); its R = Hv/Hk value heads are processed in
@@ -155,88 +74,6 @@ constexpr uint32_t kTpW = 0, kTpUa = 128, kTpUb = 256, kTpGram = 384;
 // (then dead) Q rows of the Gram operand, 32 rows per 8 KB piece.
 __device__ __forceinline__ float* prep_tf(uint8_t* smem, int hh, int row) {
     return reinterpret_cast<float*>(smem + kPrepAg + (hh * 2 + (row >> 5)) * 16384 + (row & 31) * 256);
-}
-
-// The solve's fp32 64 x 64 tiles (A, T) are row-major with their 16-byte
-// chunks XOR-swizzled by the row: chunk c of row r sits at chunk c ^ (r & 15).
-// Row vectors and the column reads of mma fragments are both free of bank
-// conflicts.  Offset (in floats) of column col within row r:
-__device__ __forceinline__ int swz_col(int r, int col) {
-    return (((col >> 2) ^ (r & 15)) << 2) + (col & 3);
-}
-
-// Warp-level bf16 tensor-core product (m16n8k16, fp32 accumulation) for the
-// 16 x 16 blocks of the triangular solve.  Operands are split like the
-// tcgen05 ones (hi = bf16(x), lo = bf16(x - hi)) and every product is
-// hi.hi + hi.lo + lo.hi.  Fragment layouts (lane = 4 g + q):
-//   A 16 x 16: a0 (g, 2q..2q+1), a1 (g+8, 2q..), a2 (g, 2q+8..), a3 (g+8, 2q+8..)
-//   B 16 x 8:  b0 (k = 2q..2q+1, n = g), b1 (k = 2q+8..2q+9, n = g)
-//   C 16 x 8:  c0, c1 (g, 2q..2q+1), c2, c3 (g+8, 2q..2q+1)
-// so the two C tiles of a 16 x 16 result are, element for element, the A
-// fragment of a following product.
-struct SplitA { uint32_t h[4], l[4]; };
-struct SplitB { uint32_t h[2], l[2]; };
-
-__device__ __forceinline__ void split2(float x, float y, uint32_t& h, uint32_t& l) {
-    h = pack_bf16x2(x, y);
-    l = pack_bf16x2(x - __uint_as_float(h << 16), y - __uint_as_float(h & 0xFFFF0000u));
-}
-__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// A fragment of block (bi, bj) of a swizzled tile given by its row pointers.
-template <class Rows>
-__device__ __forceinline__ SplitA solve_load_a(Rows rows, int bi, int bj, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-    SplitA a;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int r = 16 * bi + g + 8 * (k & 1), c = 16 * bj + 2 * q + 8 * (k >> 1);
-        const float2 v = *reinterpret_cast<const float2*>(rows(r) + swz_col(r, c));
-        split2(v.x, v.y, a.h[k], a.l[k]);
-    }
-    return a;
-}
-// D (16 x 16, two C tiles) = A B (+ D), B = block (bk, bn) of a swizzled tile.
-template <class Rows>
-__device__ __forceinline__ void solve_mma(float (*d)[4], const SplitA& a, Rows rows, int bk, int bn,
-                                          int lane) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int c = 16 * bn + 8 * nt + g;
-        SplitB b;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int r = 16 * bk + 2 * q + 8 * k;
-            split2(rows(r)[swz_col(r, c)], rows(r + 1)[swz_col(r + 1, c)], b.h[k], b.l[k]);
-        }
-        mma16816(d[nt], a.h, b.h[0], b.h[1]);
-        mma16816(d[nt], a.h, b.l[0], b.l[1]);
-        mma16816(d[nt], a.l, b.h[0], b.h[1]);
-    }
-}
-__device__ __forceinline__ SplitA solve_c_to_a(const float (*d)[4]) {
-    SplitA a;
-    split2(d[0][0], d[0][1], a.h[0], a.l[0]);
-    split2(d[0][2], d[0][3], a.h[1], a.l[1]);
-    split2(d[1][0], d[1][1], a.h[2], a.l[2]);
-    split2(d[1][2], d[1][3], a.h[3], a.l[3]);
-    return a;
-}
-
-// An item is published (p.ready non-null) once all of its workspace writes
-// have landed: the TMA stores completed, then a gpu-scope release that also
-// covers the other threads' stores (they precede it through the CTA barrier).
-__device__ __forceinline__ void publish_item(int* flag) {
-    bulk_wait_all();
-    fence_proxy_async_global();
-    __threadfence();
-    st_release_gpu(flag, 1);
 }
 
 // Items worker, worker + n_workers, ... (chunk-major).
@@ -492,79 +329,13 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
                 }
                 bulk_commit();
             }
-            // ---- phase B: T = (I + A)^-1 per head, by 16 x 16 blocks (4 warps a head)
-            // diagonal blocks T_ii = (I + A_ii)^-1 by forward substitution in fp32,
-            // one warp each; then with Y_ij = T_ii A_ij (i > j),
-            //   T_ij = -sum_{k=j}^{i-1} Y_ik T_kj
-            // one block distance i - j per step, on the warp tensor cores
+            // ---- phase B: T = (I + A)^-1 per head (four warps a head)
             {
-                const int hh = warp >> 2, w = warp & 3;
+                const int hh = warp >> 2;
                 if (hh < nb) {
                     float* sAf = reinterpret_cast<float*>(smem + kPrepT1 + hh * 16384);
-                    auto rowsA = [&](int r) { return sAf + r * kC; };
-                    auto rowsT = [&](int r) { return prep_tf(smem, hh, r); };
-                    const uint32_t bar = 2 + hh;  // named barrier of this head's four warps
-                    {   // T_ww, column j per lane (lanes 16..31 repeat lanes 0..15)
-                        const int i = w, j = lane & 15;
-                        float x[16];
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) {
-                            // row r of A_ii as 16-byte chunks (those left of the diagonal)
-                            const int row = 16 * i + r;
-                            float a16[16];
-#pragma unroll
-                            for (int c4 = 0; c4 < 4; ++c4) {
-                                if (4 * c4 < r) {
-                                    const float4 v4 = *reinterpret_cast<const float4*>(
-                                        rowsA(row) + (((4 * i + c4) ^ (row & 15)) << 2));
-                                    a16[4 * c4] = v4.x; a16[4 * c4 + 1] = v4.y;
-                                    a16[4 * c4 + 2] = v4.z; a16[4 * c4 + 3] = v4.w;
-                                }
-                            }
-                            float acc = r == j ? 1.f : 0.f;
-#pragma unroll
-                            for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-a16[s2], x[s2], acc);
-                            x[r] = acc;
-                            asm volatile("" ::: "memory");  // one row's loads at a time
-                        }
-                        if (lane < 16) {
-#pragma unroll
-                            for (int r = 0; r < 16; ++r) rowsT(16 * i + r)[swz_col(16 * i + r, 16 * i + j)] = x[r];
-                        }
-                    }
-                    group_sync(bar, 128);
-                    SplitA y[3];  // Y_wk, k < w
-                    if (w > 0) {
-                        const SplitA tw = solve_load_a(rowsT, w, w, lane);
-#pragma unroll
-                        for (int k = 0; k < 3; ++k) {
-                            if (k < w) {
-                                float d[2][4] = {};
-                                solve_mma(d, tw, rowsA, w, k, lane);
-                                y[k] = solve_c_to_a(d);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int dist = 1; dist < 4; ++dist) {
-                        if (dist > 1) group_sync(bar, 128);  // T blocks of distance < dist are stored
-                        if (w >= dist) {
-                            const int j = w - dist;
-                            float d[2][4] = {};
-#pragma unroll
-                            for (int k = 0; k < 3; ++k)
-                                if (k >= j && k < w) solve_mma(d, y[k], rowsT, k, j, lane);
-                            const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                const int r0 = 16 * w + g, c = 16 * j + 8 * nt + 2 * q;
-                                *reinterpret_cast<float2*>(rowsT(r0) + swz_col(r0, c)) =
-                                    make_float2(-d[nt][0], -d[nt][1]);
-                                *reinterpret_cast<float2*>(rowsT(r0 + 8) + swz_col(r0 + 8, c)) =
-                                    make_float2(-d[nt][2], -d[nt][3]);
-                            }
-                        }
-                    }
+                    solve_unit_lower([&](int r) { return sAf + r * kC; },
+                                     [&](int r) { return prep_tf(smem, hh, r); }, 2 + hh, warp & 3, lane);
                 }
             }
             if (tid == 64) bulk_wait_all();  // the QK^T tiles have landed (T2 is rewritten next)
@@ -782,6 +553,9 @@ constexpr uint32_t kScanUt = 196608;                        // U~ of the chunk, 
 constexpr uint32_t kScanZ = 212992;                         // z rows, bf16 64 x 64 (TMA, 128-byte swizzle)
 constexpr uint32_t kScanGc = 221184;                        // in-chunk cumulative log-decay, 2 x 64 fp32
 constexpr uint32_t kScanEnd = 221696;
+constexpr uint32_t kScanGl = kScanEnd;                      // per-channel decay: G_last per key
+                                                            //   channel, 2 x 128 fp32
+constexpr uint32_t kScanEndKda = kScanGl + 2 * 128 * 4;
 // tensor-memory columns: P4 in two slots (chunk c uses c%2) of 128 columns (64
 // in the two-kernel launch), P7 in 64 columns, P6 in two 64-column slots
 constexpr uint32_t kTmD4 = 0, kTmDs = 256, kTmD6 = 320;
@@ -837,7 +611,11 @@ __device__ __forceinline__ bool wait_or_dead(uint64_t* bar, uint32_t parity, Sca
 // instruction cache) measured faster.  The fused launch keeps the stacked
 // form, where eight fewer MMAs on the chain count for more; the two launches
 // therefore differ in that product's rounding.
-template <bool kSplitP4>
+// kKda: one decay per key channel.  The query rows of P4 are chunk_prep_kda's
+// Q o e^G (per value head, from the W arrays at row qt_row0 on), the keys of
+// P7 its K o e^{G_last - G} (per value head), so U' = U and the output takes
+// no e^{G_t} factor; the state decays by e^{G_last} per key row.
+template <bool kSplitP4, bool kKda>
 __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const CUtensorMap& map_ql,
                                                 const CUtensorMap& map_wh, const CUtensorMap& map_wl,
                                                 const CUtensorMap& map_kqh, const CUtensorMap& map_kql,
@@ -1033,14 +811,19 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 for (int b = 0; b < 2; ++b) {
                     tma_load_2d(smem + kScanA4H + b * 16384, &map_wh, &sy.a4, 64 * b, wrow(c));
                     tma_load_2d(smem + kScanA4L + b * 16384, &map_wl, &sy.a4, 64 * b, wrow(c));
-                    tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_qh, &sy.a4, qcol + 64 * b, tok0(c));
-                    tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_ql, &sy.a4, qcol + 64 * b, tok0(c));
+                    if constexpr (kKda) {
+                        tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_wh, &sy.a4, 64 * b, p.qt_row0 + wrow(c));
+                        tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_wl, &sy.a4, 64 * b, p.qt_row0 + wrow(c));
+                    } else {
+                        tma_load_2d(smem + kScanA4H + b * 16384 + 8192, &map_qh, &sy.a4, qcol + 64 * b, tok0(c));
+                        tma_load_2d(smem + kScanA4L + b * 16384 + 8192, &map_ql, &sy.a4, qcol + 64 * b, tok0(c));
+                    }
                 }
                 sy.n_a4 += 1;
             };
             auto issue_k = [&](int c) {  // key rows of the chunk, both key-lane blocks (MN-major A)
                 if (p.ready) fence_proxy_async_global();
-                const int krow = ((c_begin + c) * p.n_k_heads + hk) * kC;
+                const int krow = kKda ? wrow(c) : ((c_begin + c) * p.n_k_heads + hk) * kC;
                 mbar_arrive_expect_tx(&sy.k, 4 * 8192);
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
@@ -1060,10 +843,14 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             // 4-column groups) and its cumulative log-decay, into G buffer c%2
             auto issue_ug = [&](int c) {
                 if (p.ready) fence_proxy_async_global();
-                mbar_arrive_expect_tx(&sy.ug, 16384 + kC * 4);
+                mbar_arrive_expect_tx(&sy.ug, 16384 + (kKda ? kD : kC) * 4);
                 bulk_load_1d(smem + kScanUt, p.u_ws + (size_t)wrow(c) * kD + (size_t)(v0 >> 2) * kC * 4,
                              16384, &sy.ug);
-                bulk_load_1d(smem + kScanGc + (c & 1) * kC * 4, p.gcum_ws + wrow(c), kC * 4, &sy.ug);
+                if constexpr (kKda)
+                    bulk_load_1d(smem + kScanGl + (c & 1) * kD * 4,
+                                 p.gcum_ws + (size_t)((c_begin + c) * hv_n + h) * kD, kD * 4, &sy.ug);
+                else
+                    bulk_load_1d(smem + kScanGc + (c & 1) * kC * 4, p.gcum_ws + wrow(c), kC * 4, &sy.ug);
                 sy.n_ug += 1;
             };
             auto issue_z = [&](int c) {  // the chunk's z rows, this CTA's value lanes
@@ -1253,13 +1040,16 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             // their arrive for chunk c-1 lets the producer reuse this buffer)
             alive = __all_sync(0xffffffffu, alive && wait_or_dead(&sy.ug, c & 1, sy, 12));
             const float* gc = sGc + (c & 1) * kC;
-            const float gam = alive ? __expf(gc[chunk_len(c) - 1]) : 0.f;  // state decay over chunk c
+            // state decay over chunk c (of this thread's key row, per-channel decay)
+            const float gam = !alive ? 0.f
+                              : kKda ? __expf(reinterpret_cast<const float*>(smem + kScanGl)[(c & 1) * kD + row])
+                                     : __expf(gc[chunk_len(c) - 1]);
             float gt_next = 0.f;
-            if (!is_u && alive) gt_next = gc[row - 64];
+            if (!kKda && !is_u && alive) gt_next = gc[row - 64];
             bool out_ok = false;
             if (is_u) {
                 // U_c = U~ - W S_c (rows 0..63 of P4_c), U'_c = e^{G_last-G_t} U_c
-                const float eu = __expf(gc[chunk_len(c) - 1] - gc[row]);
+                const float eu = kKda ? 1.f : __expf(gc[chunk_len(c) - 1] - gc[row]);
                 float ut[32];
                 const float4* us4 = reinterpret_cast<const float4*>(smem + kScanUt) + ((cl >> 2) * kC + row);
 #pragma unroll
@@ -1380,8 +1170,19 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                   const __grid_constant__ CUtensorMap map_z, ChunkArgs p) {
     // sequences with the most chunks start first: the last wave is shorter
-    chunk_scan_body<true>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
+    chunk_scan_body<true, false>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                     blockIdx.x / kSplit, p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y);
+}
+
+// The scan of the per-channel decay form (after chunk_prep_kda_kernel).
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kScanThreads, 1)
+chunk_scan_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_constant__ CUtensorMap map_ql,
+                      const __grid_constant__ CUtensorMap map_wh, const __grid_constant__ CUtensorMap map_wl,
+                      const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
+                      const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
+                      const __grid_constant__ CUtensorMap map_z, ChunkArgs p) {
+    chunk_scan_body<true, true>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
+                                blockIdx.x / kSplit, p.seq_order ? p.seq_order[blockIdx.y] : (int)blockIdx.y);
 }
 
 // ------------------------------------------------------------- chunk_fused
@@ -1411,15 +1212,16 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_cons
                         blockIdx.x, n_prep);
     } else {
         const int s = ((int)blockIdx.x - n_prep) / kSplit;  // n_prep is even: clusters stay aligned
-        chunk_scan_body<false>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
+        chunk_scan_body<false, false>(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, map_z, p,
                         s % p.n_v_heads, s / p.n_v_heads);
     }
 }
 
 // ------------------------------------------------------------------- host
 size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads, int n_v_heads,
-                               ChunkLayout* lay) {
+                               int per_channel, ChunkLayout* lay) {
     ChunkLayout l{};
+    const size_t pc = per_channel ? 1 : 0;
     const int T = n_seq > 0 ? cu_host[n_seq] : 0;
     long long chunks = 0;
     for (int i = 0; i < n_seq; ++i) chunks += (cu_host[i + 1] - cu_host[i] + kC - 1) / kC;
@@ -1431,22 +1233,26 @@ size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads,
     // starts inside the batch stays inside the tensor (no out-of-bounds boxes).
     l.qkv_hi = off; off = up(off + ((size_t)T + kC) * cd * 2);
     l.qkv_lo = off; off = up(off + ((size_t)T + kC) * cd * 2);
-    l.g = off; off = up(off + (size_t)T * n_v_heads * 4);
+    l.g = off; off = up(off + (pc ? 0 : (size_t)T * n_v_heads * 4));  // per channel: formed by its prep
     l.beta = off; off = up(off + (size_t)T * n_v_heads * 4);
     l.cu_chunks = off; off = up(off + (size_t)(n_seq + 1) * 4);
     l.chunk_info = off; off = up(off + (size_t)chunks * 8);
     l.seq_order = off; off = up(off + (size_t)n_seq * 4);
-    l.w_hi = off; off = up(off + crow * kD * 2);
-    l.w_lo = off; off = up(off + crow * kD * 2);
+    // per-channel decay: W rows, then as many rows of Q o e^G
+    l.w_hi = off; off = up(off + (1 + pc) * crow * kD * 2);
+    l.w_lo = off; off = up(off + (1 + pc) * crow * kD * 2);
     l.u = off; off = up(off + crow * kD * 4);
     l.qk_hi = off; off = up(off + crow * kC * 2);
     l.qk_lo = off; off = up(off + crow * kC * 2);
-    l.kw_hi = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
-    l.kw_lo = off; off = up(off + (size_t)chunks * n_k_heads * kC * kD * 2);
-    l.gcum = off; off = up(off + crow * 4);
+    // key rows per key head (per value head, decayed, with per-channel decay)
+    const size_t krows = pc ? crow : (size_t)chunks * n_k_heads * kC;
+    l.kw_hi = off; off = up(off + krows * kD * 2);
+    l.kw_lo = off; off = up(off + krows * kD * 2);
+    l.gcum = off; off = up(off + (pc ? crow * 2 : crow) * 4);
     l.ready = off; off = up(off + ((size_t)chunks * n_k_heads + 1) * 4);  // + one never set (test hook)
     l.total = off;
     l.n_chunks = static_cast<int>(chunks);
+    l.per_channel = per_channel ? 1 : 0;
     if (lay) *lay = l;
     return off;
 }
@@ -1503,6 +1309,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     cv.d_k = kD; cv.d_v = kD; cv.conv_k = a.conv_k; cv.l2_eps = a.l2_eps;
     cv.cu_seqlens = a.cu_seqlens; cv.x = a.x; cv.a = a.a; cv.b = a.b;
     cv.decay_form = a.decay_form;
+    cv.per_channel = a.per_channel;
     cv.conv_w = a.conv_w; cv.A_log = a.A_log; cv.dt_bias = a.dt_bias;
     cv.conv_state_in = a.conv_state_in;
     cv.conv_state_out = a.conv_state_out;
@@ -1554,13 +1361,23 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     CUtensorMap m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z;
     std::memset(&m_qh, 0, sizeof(m_qh));
     m_ql = m_wh = m_wl = m_kqh = m_kql = m_kwh = m_kwl = m_z = m_qh;
-    const uint64_t krows = (uint64_t)l.n_chunks * hk_n * kC;
+    const bool pc = a.per_channel != 0;
     const uint64_t crow = (uint64_t)l.n_chunks * hv_n * kC;
+    const uint64_t krows = pc ? crow : (uint64_t)l.n_chunks * hk_n * kC;
+    if (pc) {
+        p.qt_row0 = static_cast<int>(crow);
+        p.gate_a = static_cast<const __nv_bfloat16*>(a.a);
+        p.A_log = a.A_log;
+        p.dt_bias = a.dt_bias;
+        p.decay_form = a.decay_form;
+        p.kw_hi = reinterpret_cast<__nv_bfloat16*>(ws + l.kw_hi);
+        p.kw_lo = reinterpret_cast<__nv_bfloat16*>(ws + l.kw_lo);
+    }
     if (l.n_chunks > 0) {
         if (!make_tma_map_bf16_2d(&m_qh, ws + l.qkv_hi, (uint64_t)T + kC, cd, cd, 64, 64) ||
             !make_tma_map_bf16_2d(&m_ql, ws + l.qkv_lo, (uint64_t)T + kC, cd, cd, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, crow, kD, kD, 64, 64) ||
-            !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_wh, ws + l.w_hi, (pc ? 2 : 1) * crow, kD, kD, 64, 64) ||
+            !make_tma_map_bf16_2d(&m_wl, ws + l.w_lo, (pc ? 2 : 1) * crow, kD, kD, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kqh, ws + l.qk_hi, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kql, ws + l.qk_lo, crow, kC, kC, 64, 64) ||
             !make_tma_map_bf16_2d(&m_kwh, ws + l.kw_hi, krows, kD, kD, 64, 64) ||
@@ -1571,6 +1388,7 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
 
     const size_t prep_smem = 1024 + kPrepVec + (size_t)R * 4 * kC * 4;
     const size_t scan_smem = 1024 + kScanEnd;
+    const size_t scan_smem_kda = 1024 + kScanEndKda;
     const size_t prep_smem_max = 1024 + kPrepVec + 8 * 4 * kC * 4;
     // the kernels' shared-memory opt-in is a per-device setting
     static std::atomic<bool> attrs_set[64];
@@ -1585,8 +1403,28 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         if (ae == cudaSuccess)
             ae = cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(std::max(prep_smem_max, scan_smem)));
+        if (ae == cudaSuccess)
+            ae = cudaFuncSetAttribute(chunk_scan_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(scan_smem_kda));
         if (ae != cudaSuccess) return ae;
         attrs_set[dev].store(true);
+    }
+    if (pc) {  // per-channel decay: its prep over (chunk, value head) items, then its scan
+        if (l.n_chunks > 0) {
+            const int n_kda = l.n_chunks * hv_n;
+            CUtensorMap m_a;  // the gate input, a [T, Hv*128] (bf16)
+            if (!make_tma_map_bf16_2d(&m_a, a.a, (uint64_t)T, (uint64_t)hv_n * kD, (uint64_t)hv_n * kD, 64, 64))
+                return cudaErrorInvalidValue;
+            e = timed_launch("chunk_prep_kda", st, [&] {
+                return launch_kda_prep(m_qh, m_ql, m_kqh, m_kql, m_a, p, std::min(n_kda, sm_count()), st);
+            });
+            if (e != cudaSuccess) return e;
+        }
+        return timed_launch("chunk_scan_kda", st, [&] {
+            chunk_scan_kda_kernel<<<dim3(hv_n * kSplit, a.n_seq), kScanThreads, scan_smem_kda, st>>>(
+                m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p);
+            return cudaGetLastError();
+        });
     }
     const int n_items = l.n_chunks * hk_n;
     // One fused launch when the scan's clusters leave at least 32 CTA slots
@@ -1632,10 +1470,13 @@ cudaError_t read_device_error(int* code, bool reset) {
         const int zero = 0;
         e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
     }
-    int gemm = 0, rec = 0;  // the projection GEMM's word (codes 20..23), the recurrent kernel's (30)
+    // the projection GEMM's word (codes 20..23), the recurrent kernel's (30),
+    // the per-channel prep's (13, 14)
+    int gemm = 0, rec = 0, kda = 0;
     if (e == cudaSuccess) e = read_gemm_error(&gemm, reset);
     if (e == cudaSuccess) e = read_rec_error(&rec, reset);
-    if (e == cudaSuccess && *code == 0) *code = gemm ? gemm : rec;
+    if (e == cudaSuccess) e = read_kda_error(&kda, reset);
+    if (e == cudaSuccess && *code == 0) *code = gemm ? gemm : rec ? rec : kda;
     return e;
 }
 

@@ -244,6 +244,8 @@ __device__ void chunk_table_cta(const ConvArgs& p) {
 // coalesced loads; per token the L2 norm of a q/k head is a full-warp
 // reduction.  Writes q|k|v as a (hi, lo) bf16 pair, g and beta like
 // conv_prologue_kernel; the first CTA of the gate row also builds the chunk table.
+// With per-channel decay the gate row writes only beta (the chunked prep forms
+// the decays from a itself).
 constexpr int kPro128Tok = 8;                   // tokens per warp
 constexpr int kPro128Tile = 8 * kPro128Tok;     // tokens per CTA
 
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(256, 4) conv_prologue_d128_kernel(ConvArgs p) 
             const int h = i % hv_n;
             if (t >= p.n_tokens) break;
             const size_t idx = (size_t)t * hv_n + h;
-            p.g_out[idx] = log_decay(__bfloat162float(a[idx]), p.A_log[h], p.dt_bias[h], p.decay_form);
+            if (!p.per_channel)
+                p.g_out[idx] = log_decay(__bfloat162float(a[idx]), p.A_log[h], p.dt_bias[h], p.decay_form);
             p.beta_out[idx] = sigmoidf_(__bfloat162float(b[idx]));
         }
         return;

@@ -2,6 +2,7 @@
 // kernels.  Host-visible plain structs; pointers are device pointers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -16,6 +17,8 @@ struct ConvArgs {
     int n_seq, n_tokens, n_k_heads, n_v_heads, d_k, d_v, conv_k;
     int decay_form;             // gdn_decay_form
     int per_channel;            // one decay per key channel: a [T, Hv*dk], g_out [T, Hv*dk]
+                                //   (the d=128 prologue writes only beta then: the
+                                //   chunked prep forms g itself)
     float l2_eps;
     const int32_t* cu_seqlens;  // [n_seq+1]
     const void* x;              // [T, CD]
@@ -94,18 +97,28 @@ struct ChunkArgs {
     const int32_t* seq_order;     // [n_seq] scan launch order (longest first), or null
     const __nv_bfloat16* qkv_hi;  // [T, CD] normalised q | k | v, hi part (workspace)
     const __nv_bfloat16* qkv_lo;  // [T, CD] lo part (workspace)
-    const float* g;               // [T, Hv] log-decay (workspace)
+    const float* g;               // [T, Hv] log-decay (workspace; not with per-channel decay)
     const float* beta;            // [T, Hv] (workspace)
     const __nv_bfloat16* z;       // [T, Hv*dv]
     const float* norm_w;          // [dv]
     const float* state_in;        // [N, Hv, dk, dv] or null
     float* state_out;             // or null
-    __nv_bfloat16* w_hi;          // [chunks, Hv, 64, dk] W (hi, lo)
-    __nv_bfloat16* w_lo;
+    __nv_bfloat16* w_hi;          // [chunks, Hv, 64, dk] W (hi, lo); per-channel decay: then
+    __nv_bfloat16* w_lo;          //   Q o e^G in the same layout from row qt_row0 on
+    int qt_row0;                  // chunks * Hv * 64 (per-channel decay), else 0
+    // Per-channel decay: its prep forms g = coef softplus(a + dt_bias) itself
+    // from the raw gate input (the prologue writes only beta).
+    const __nv_bfloat16* gate_a;  // [T, Hv*dk] (read through a tensor map: 16-byte aligned)
+    const float* A_log;           // [Hv] (or the coefficient, decay_form)
+    const float* dt_bias;         // [Hv*dk]
+    int decay_form;
+    __nv_bfloat16* kw_hi;         // per-channel decay: [chunks, Hv, 64, dk] K o e^{G_last-G}
+    __nv_bfloat16* kw_lo;         //   (hi, lo), written by its prep (else by TMA, unused here)
     float* u_ws;                  // [chunks, Hv, dv/4, 64, 4] U~ (fp32), 4-column groups
     __nv_bfloat16* qk_hi;         // [chunks, Hv, 64, 64] masked decayed Q K^T (hi, lo)
     __nv_bfloat16* qk_lo;
-    float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay
+    float* gcum_ws;               // [chunks, Hv, 64] in-chunk cumulative log-decay; per-channel
+                                  //   decay: [chunks, Hv, dk] G_last of each key channel
     __nv_bfloat16* out;           // [T, Hv*dv]
     int* ready;                   // [chunks, Hk] item done flags (fused launch), else null
     // Test hook (fused launch): when set, the scan waits on this flag, which
@@ -119,6 +132,7 @@ struct ChunkLayout {
     size_t qkv_hi, qkv_lo, g, beta, cu_chunks, chunk_info, seq_order, w_hi, w_lo, u, qk_hi, qk_lo,
         kw_hi, kw_lo, gcum, ready, total;
     int n_chunks;
+    int per_channel;
 };
 
 // Per-kernel timing hook (CUDA events on the launching stream when enabled).
@@ -135,6 +149,7 @@ cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
 struct ChunkLaunch {
     int n_seq, n_tokens, n_k_heads, n_v_heads, conv_k, act;
     int head_map, decay_form;
+    int per_channel;       // one decay per key channel (a [T, Hv*dk], dt_bias [Hv*dk])
     float l2_eps, rms_eps;
     const int32_t* cu_seqlens;
     const void *x, *z, *a, *b;
@@ -151,12 +166,20 @@ struct ChunkLaunch {
 
 // Workspace size (and layout) of the chunked path for this sequence layout.
 size_t chunked_workspace_bytes(int n_seq, const int32_t* cu_host, int n_k_heads, int n_v_heads,
-                               ChunkLayout* layout);
+                               int per_channel, ChunkLayout* layout);
 // Whether the chunked tensor-core path serves this geometry.
 inline bool chunked_supported(int d_k, int d_v, int n_k_heads, int n_v_heads, bool bf16) {
     return bf16 && d_k == 128 && d_v == 128 && n_v_heads / n_k_heads <= 8;
 }
 cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t stream);
+// The per-channel decay prep (gdn_chunked_kda.cu): n_ctas persistent CTAs over
+// the (chunk, value head) items; the maps are the q|k|v (hi, lo) tiles and the
+// M o QK^T rows (hi, lo) of the workspace, and the gate input a [T, Hv*128].
+cudaError_t launch_kda_prep(const CUtensorMap& map_qh, const CUtensorMap& map_ql, const CUtensorMap& map_kqh,
+                            const CUtensorMap& map_kql, const CUtensorMap& map_a, const ChunkArgs& p, int n_ctas,
+                            cudaStream_t stream);
+size_t kda_prep_smem_bytes();
+cudaError_t read_kda_error(int* code, bool reset);
 // Sticky device-side error word set by a kernel whose bounded wait gave up.
 cudaError_t read_device_error(int* code, bool reset);
 

@@ -34,7 +34,8 @@
  * - Errors: each call returns a gdn_status; on failure nothing was enqueued
  *   (or, for GDN_ERR_CUDA, a launch failed), and gdn_last_error() returns a
  *   message naming the call and the reason.  No call aborts the process.
- * - Buffers must be 16-byte aligned (x, z, out, states, qkv_out).
+ * - Buffers must be 16-byte aligned (x, z, out, states, qkv_out; with
+ *   per-channel decay, a as well in gdn_prefill).
  * - A call takes at most GDN_MAX_SEQUENCES sequences (kernels index them on
  *   the second grid dimension); larger batches are refused before any launch.
  * - Failure injection (testing a caller's failure path, as cortiq-engine
@@ -107,7 +108,9 @@ typedef struct gdn_dims {
      * pages' Kimi Delta Attention mixer, qwen.rs Mixer::Kda): S <- diag(e^g) S
      * with g [T, Hv, dk] = coef[h] softplus(a[t, h, i] + dt_bias[h, i]); the
      * gate input a is then [T, Hv*dk] and dt_bias [Hv*dk] (b stays [T, Hv]).
-     * Runs on the token-recurrent kernel; gdn_layer_prefill refuses it.
+     * A bf16 prefill with d_k = d_v = 128 runs it on the chunked tensor-core
+     * path, everything else on the token-recurrent kernel;
+     * gdn_layer_prefill refuses it.
      * 0 (one decay per value head) when zero-initialised. */
     int32_t decay_per_channel;
 } gdn_dims;
@@ -156,8 +159,8 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t n_seq,
  *   out [T, Hv*dv] in the activation dtype.
  *   workspace: at least gdn_prefill_workspace_size() bytes, 256-byte aligned.
  * bf16 activations run the chunked form on tensor cores (bf16 operands, fp32
- * accumulation and fp32 state); fp32 activations run the token recurrence in
- * fp32 on CUDA cores.
+ * accumulation and fp32 state), with scalar or per-channel decay; fp32
+ * activations run the token recurrence in fp32 on CUDA cores.
  */
 gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n_seq,
                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,

@@ -324,7 +324,9 @@ def test_invalid_arguments_raise():
 def _with_options(case, head_map="contiguous", decay_form="A_log"):
     """The ABI options of the pages' GGUF checkpoints on a generated case: the
     tiled value-to-key map, and the decay coefficient given instead of A_log
-    (rounded to fp32 first, so that both sides read the same values)."""
+    (rounded to fp32 first, so that both sides read the same values).  A copy:
+    the named workloads are cached and shared."""
+    case = copy.copy(case)
     case.head_map, case.decay_form = head_map, decay_form
     if decay_form == "coef":
         case.A_log = (-np.exp(case.A_log)).astype(np.float32).astype(np.float64)
@@ -358,7 +360,9 @@ def test_decode_tiled_head_map_and_decay_coef_match_oracle():
 
 def _per_channel(case, seed):
     """The case with one decay per key channel: gate inputs a [T, Hv*dk] ~N(0,1)
-    (bf16-rounded for bf16 cases) and dt_bias [Hv*dk] ~N(0, 0.1)."""
+    (bf16-rounded for bf16 cases) and dt_bias [Hv*dk] ~N(0, 0.1).  A copy: the
+    named workloads are cached and shared."""
+    case = copy.copy(case)
     rng = np.random.default_rng(seed)
     a = rng.normal(size=(case.a.shape[0], case.n_v_heads * case.d_k))
     case.a = workloads.round_bf16(a.astype(np.float32)).astype(np.float64) if case.dtype == "bf16" else a
@@ -370,13 +374,74 @@ def _per_channel(case, seed):
 @pytest.mark.parametrize("name", ["ragged_bf16_d128_states", "bf16_slow_decay_long",
                                   "f32_slow_decay", "tc_gqa_R8"])
 def test_prefill_per_channel_decay_matches_oracle(name):
-    """One decay per key channel (token-recurrent kernel, also for d=128 bf16)."""
+    """One decay per key channel: the token-recurrent kernel (fp32) and the
+    chunked tensor-core path (bf16, d_k = d_v = 128)."""
     case = _per_channel(PREFILL_CASES[name](), seed=91)
     ref = run_oracle(case)
     got = gpu_prefill(case)
     tol = TOL[case.dtype]
     assert rel_err(got["out"], ref["out"]) <= tol
     assert rel_err(got["state"], ref["state"]) <= tol
+
+
+KDA_TC_CASES = ["tc_mha_R1", "tc_gqa_R4", "tc_gqa_R3", "tc_many_short", "tc_slow_decay_g0"]
+
+
+def _chunked_per_channel(case, want_kernels=True):
+    """gpu_prefill of a per-channel case, checking that the chunked tensor-core
+    kernels of that form ran (not the token-recurrent one)."""
+    gdn.timing_enable(True)
+    try:
+        got = gpu_prefill(case)
+        names = gdn.timing_report()
+    finally:
+        gdn.timing_enable(False)
+    if want_kernels:
+        assert "chunk_prep_kda" in names and "chunk_scan_kda" in names, names
+        assert "recurrent" not in names, names
+    return got
+
+
+@pytest.mark.parametrize("name", KDA_TC_CASES)
+def test_chunked_per_channel_decay_matches_oracle(name):
+    """Per-channel decay on the chunked tensor-core path (bf16, d_k = d_v = 128):
+    GQA ratios 1, 3, 4, ragged and one-token chunks, many short sequences, a
+    1000-token slow-decay sequence; outputs, final states and conv history
+    against the oracle."""
+    case = _per_channel(PREFILL_CASES[name](), seed=94)
+    ref = run_oracle(case)
+    got = _chunked_per_channel(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
+def test_chunked_per_channel_decay_wide_spread():
+    """Channel decays that differ by orders of magnitude within a head: a ~ N(0, 3)
+    per channel, so per-token log-decays run from ~0 to about -150 and the
+    in-chunk sums of the fast channels reach thousands.  The block factors of
+    the Gram products stay <= 1 (nothing overflows) and the result meets the
+    oracle."""
+    case = _gen("kw", n_k_heads=2, n_v_heads=4, lengths=[300, 64, 17], state_std=0.05,
+                conv_state_std=1.0, seed=37)
+    case = _per_channel(case, seed=96)
+    rng = np.random.default_rng(97)
+    case.a = workloads.round_bf16(rng.normal(0.0, 3.0, case.a.shape).astype(np.float32)).astype(np.float64)
+    ref = run_oracle(case)
+    got = _chunked_per_channel(case)
+    assert torch.isfinite(got["out"].float()).all() and torch.isfinite(got["state"]).all()
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+
+
+def test_full_size_chunked_per_channel_decay_T4096():
+    """The 4,096-token Qwen3-Next-shaped prefill with one decay per key channel
+    (gate inputs a [T, 32 x 128] ~ N(0, 1), dt_bias [32 x 128] ~ N(0, 0.1))."""
+    case = _per_channel(workloads.config(1), seed=98)
+    ref = run_oracle(case)
+    got = _chunked_per_channel(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
 
 
 def test_decode_per_channel_decay_matches_oracle():
