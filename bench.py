@@ -54,6 +54,7 @@ TRAFFIC = {
     # the step's two launches under one name: the read-only verify and the replay
     ("spec_replay", "recurrent"): (((143_898_112 + 3_576_832) + (140_742_912 + 74_456_320)) // 2,
                                    "ncu captures of the step's two launches (verify, replay), averaged"),
+    ("kda_prefill", "chunk_prep_kda"): (168_566_528 + 245_094_400, "ncu capture of this workload's launch"),
     # 16 sequences of 128..1024 tokens (149 chunks); the traffic is per chunk: x 1015/149
     ("varlen", "chunk_scan"): (round((657_587_456 + 91_176_960) * 1015 / 149),
                                "ncu capture of a 149-chunk varlen case, scaled x 1015/149 chunks"),
@@ -81,7 +82,8 @@ def _peaks():
 
 def _act_bytes_per_token(c):
     cd, vd, hv = c.conv_dim, c.n_v_heads * c.d_v, c.n_v_heads
-    return 2 * (cd + vd + 2 * hv + vd)  # x, z, a, b in; out
+    gates = hv * (c.d_k if getattr(c, "per_channel_decay", False) else 1)  # a: per value head or channel
+    return 2 * (cd + vd + gates + hv + vd)  # x, z, a, b in; out
 
 
 def _state_bytes(c):
@@ -100,7 +102,9 @@ WORKLOADS = {
     "spec_verify": 4,
     "spec_replay": 4,   # the same drafts, verified read-only, accepted prefix replayed
     "layer": 1,         # the T=4096 prefill inside a whole layer: in_proj -> core -> out_proj
+    "kda_prefill": 1,   # the T=4096 prefill with one decay per key channel
 }
+KDA_SEED = 98           # gate draw of kda_prefill (a [T, Hv*dk], dt_bias [Hv*dk])
 LAYER_HIDDEN = 2048     # model width of the layer workload (Qwen3-Next's hidden size)
 REPLAY_ACCEPTED = 2     # tokens of every sequence's 4 drafts accepted in spec_replay
 
@@ -114,7 +118,8 @@ class Runner:
         self.key, self.case, self.dev = key, case, device
         self.gdn, self.torch = gdn, torch
         c = case
-        self.d = gdn.Dims(c.n_k_heads, c.n_v_heads, c.d_k, c.d_v, c.conv_k, torch.bfloat16, c.act)
+        self.d = gdn.Dims(c.n_k_heads, c.n_v_heads, c.d_k, c.d_v, c.conv_k, torch.bfloat16, c.act,
+                          per_channel_decay=getattr(c, "per_channel_decay", False))
         bf = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.bfloat16)  # noqa: E731
         f32 = lambda a: torch.from_numpy(a).to(device=device, dtype=torch.float32)  # noqa: E731
         self.x, self.z, self.a, self.b = bf(c.x), bf(c.z), bf(c.a), bf(c.b)
@@ -192,8 +197,8 @@ class Runner:
         c = self.case
         act = _act_bytes_per_token(c) * c.n_tokens
         n = c.n_seq
-        if self.key == "prefill":      # zero initial state (not read); final state + conv state out
-            return act + n * (_state_bytes(c) + _conv_state_bytes(c))
+        if self.key in ("prefill", "kda_prefill"):  # zero initial state (not read); final state +
+            return act + n * (_state_bytes(c) + _conv_state_bytes(c))  # conv state out
         if self.key == "layer":        # h in, h_out, the weights once, final state + conv state out
             vd = c.n_v_heads * c.d_v
             w = 2 * LAYER_HIDDEN * (c.conv_dim + 2 * vd + 2 * c.n_v_heads)
@@ -218,7 +223,7 @@ class Runner:
         c = self.case
         conv = c.n_seq * _conv_state_bytes(c)
         hist = {"prefill": conv, "varlen": conv, "decode": 2 * conv, "spec_verify": 0,
-                "spec_replay": 2 * conv, "layer": conv}[self.key]
+                "spec_replay": 2 * conv, "layer": conv, "kda_prefill": conv}[self.key]
         if name == "conv_state":
             return hist
         rest = self.algorithmic_bytes() - (hist if "conv_state" in kernels else 0)
@@ -240,6 +245,18 @@ class Runner:
             vd = c.n_v_heads * dv
             flops += 2 * c.n_tokens * LAYER_HIDDEN * (c.conv_dim + 2 * vd + 2 * c.n_v_heads)
         return flops
+
+    def kernel_flops(self, name, chunk=64):
+        """Useful flops of one launch of a chunked-form kernel that does part of
+        the contractions (the per-channel decay form's two launches): its prep
+        forms the Gram matrices, the solve and [W | U~] = T [K | V] (per token
+        and value head C (3 dk + dv) + C^2 / 3), its scan the state and output
+        products (6 dk dv + C dv); the two add up to useful_flops()."""
+        c = self.case
+        dk, dv = c.d_k, c.d_v
+        per = {"chunk_prep_kda": chunk * (3 * dk + dv) + chunk * chunk / 3,
+               "chunk_scan_kda": 6 * dk * dv + chunk * dv}[name]
+        return per * c.n_v_heads * c.n_tokens
 
     # -- end to end: pinned host buffers, H2D of the step's inputs, the call,
     # D2H of the step's outputs, pipelined as a serving loop runs them: the
@@ -478,12 +495,14 @@ def run_gpu(args):
     sampler = ClockSampler(index=local)
     sampler.start()
 
-    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify", "spec_replay", "layer")
-                          if k in args.extras]
+    keys = ["prefill"] + [k for k in ("decode", "varlen", "spec_verify", "spec_replay", "layer",
+                                      "kda_prefill") if k in args.extras]
     results = {}
     total_launches = 0
     for key in keys:
         case = workloads.config(WORKLOADS[key])
+        if key == "kda_prefill":
+            case = workloads.with_per_channel_decay(case, KDA_SEED)
         r = Runner(key, case, device)
         r.step()  # one untimed call: one-time costs (module loading, library setup) stay out
         torch.cuda.synchronize()
@@ -510,10 +529,11 @@ def run_gpu(args):
         dom_avg_ms = dom_ms / dom_n
         kb = r.kernel_bytes(dom_name, rep.keys())
         share = dom_ms / sum(v[1] for v in rep.values())
-        if dom_name == "chunk_fused":
-            # every tensor-core contraction of the chunked form runs in this one
-            # launch: a contraction, measured against the bf16 tensor peak
-            fl = r.useful_flops(with_proj=False)
+        if dom_name in ("chunk_fused", "chunk_prep_kda", "chunk_scan_kda"):
+            # the chunked form's tensor-core contractions (all of them in the
+            # fused launch, a kernel's share in the per-channel form's two):
+            # measured against the bf16 tensor peak
+            fl = r.useful_flops(with_proj=False) if dom_name == "chunk_fused" else r.kernel_flops(dom_name)
             achieved = fl / (dom_avg_ms / 1e3) / 1e12
             roof = {"bound": "tensor", "kernel": dom_name, "achieved": achieved,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -671,6 +691,8 @@ def run_profile(args):
         key = "varlen"
     else:
         case = workloads.config(WORKLOADS[key])
+        if key == "kda_prefill":
+            case = workloads.with_per_channel_decay(case, KDA_SEED)
     r = Runner(key, case, torch.device("cuda", 0))
     for _ in range(2):
         r.step()
@@ -686,7 +708,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
-    ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay,layer",
+    ap.add_argument("--extras", default="decode,varlen,spec_verify,spec_replay,layer,kda_prefill",
                     help="comma list of extra workloads in the same line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=sorted(WORKLOADS) + ["decode64", "varlen_small"],

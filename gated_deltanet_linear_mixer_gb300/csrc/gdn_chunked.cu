@@ -508,7 +508,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
 //
 // Warp roles (12 warps launched at 168 registers a thread; a register split
 // gives the eight compute warps 200 and the control warpgroup 96: 256 x 200 +
-// 128 x 96 = 63,488, within the launch's 384 x 168 = 64,512):
+// 128 x 96 = 63,488, within the launch's 384 x 168 = 64,512; 176 and 120 in
+// the per-channel decay instance):
 //   warps 0..7  compute.  Thread (warp w, lane l) owns key lane 32 (w%4) + l
 //               of the state and value lanes 32 (w/4) .. +31 of this CTA's
 //               slice, which is exactly the part of the tensor-memory
@@ -701,7 +702,9 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
 
     if (warp >= 8) {
         // ------------------------------------------------ control warpgroup
-        regs_dec<96>();
+        // per-channel decay: 120 / 176 (its control code needs more; spills
+        // measured 6% slower at 96 / 200); 128 x 120 + 256 x 176 = 60,416
+        regs_dec<kKda ? 120 : 96>();
         if (warp == 8 && lane == 0 && n_ch > 0) {
             // MMA issuer.  Shared-memory descriptors, computed once: a
             // descriptor for address a + o is the one for a plus o >> 4 (the
@@ -914,7 +917,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
         __syncwarp();
     } else {
         // ------------------------------------------------------ compute warps
-        regs_inc<200>();
+        regs_inc<kKda ? 176 : 200>();
         const int q = warp & 3, half = warp >> 2;
         const int row = 32 * q + lane;       // accumulator lane: key lane / token row
         const int cl = 32 * half;            // first of this thread's 32 value lanes in the slice

@@ -20,6 +20,7 @@ activations (x, z, a, b, conv state) are float32 or bf16-valued float32.
 """
 from __future__ import annotations
 
+import copy
 import functools
 from dataclasses import dataclass, field
 
@@ -194,3 +195,18 @@ def config(i: int, *, slow_decay: bool = False) -> Case:
                         dtype="bf16", act="sigmoid", seed=4, state_std=0.05,
                         conv_state_std=1.0, want_inter=True, slow_decay=slow_decay, **big)
     raise ValueError(f"no workload {i}")
+
+
+def with_per_channel_decay(case: Case, seed: int) -> Case:
+    """A copy of `case` with one decay per key channel (the per-channel decayed
+    rule): gate inputs a [T, Hv*dk] ~N(0,1) (bf16-rounded for bf16 cases) and
+    dt_bias [Hv*dk] ~N(0, 0.1), drawn from `seed`.  A copy because the named
+    workloads are cached and shared."""
+    c = copy.copy(case)
+    rng = np.random.default_rng(seed)
+    a = rng.normal(size=(case.a.shape[0], case.n_v_heads * case.d_k))
+    c.a = round_bf16(a.astype(np.float32)).astype(np.float64) if case.dtype == "bf16" else a
+    c.dt_bias = rng.normal(0, 0.1, case.n_v_heads * case.d_k)
+    c.per_channel_decay = True
+    c.name = case.name + "_per_channel_decay"
+    return c

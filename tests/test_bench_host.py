@@ -89,3 +89,28 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["warmup"] >= 3
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def _kda_runner():
+    r = bench.Runner.__new__(bench.Runner)
+    r.key = "kda_prefill"
+    r.case = workloads.with_per_channel_decay(workloads.config(bench.WORKLOADS["kda_prefill"]), bench.KDA_SEED)
+    return r
+
+
+def test_kda_prefill_bytes():
+    """Per-channel decay: the gate input a is [T, Hv*dk] instead of [T, Hv]."""
+    r = _kda_runner()
+    act = ACT + 2 * HV * (DK - 1)
+    assert act == 41_024
+    assert r.algorithmic_bytes() == 4096 * act + STATE + CONV
+
+
+def test_kda_kernel_flops_split_the_chunked_form():
+    """The prep's and the scan's shares of the contractions add up to the
+    chunked form's useful flops."""
+    r = _kda_runner()
+    prep, scan = r.kernel_flops("chunk_prep_kda"), r.kernel_flops("chunk_scan_kda")
+    assert prep == pytest.approx((64 * (3 * DK + DV) + 64 * 64 / 3) * HV * 4096)
+    assert scan == pytest.approx((6 * DK * DV + 64 * DV) * HV * 4096)
+    assert prep + scan == pytest.approx(r.useful_flops())

@@ -359,16 +359,8 @@ def test_decode_tiled_head_map_and_decay_coef_match_oracle():
 
 
 def _per_channel(case, seed):
-    """The case with one decay per key channel: gate inputs a [T, Hv*dk] ~N(0,1)
-    (bf16-rounded for bf16 cases) and dt_bias [Hv*dk] ~N(0, 0.1).  A copy: the
-    named workloads are cached and shared."""
-    case = copy.copy(case)
-    rng = np.random.default_rng(seed)
-    a = rng.normal(size=(case.a.shape[0], case.n_v_heads * case.d_k))
-    case.a = workloads.round_bf16(a.astype(np.float32)).astype(np.float64) if case.dtype == "bf16" else a
-    case.dt_bias = rng.normal(0, 0.1, case.n_v_heads * case.d_k)
-    case.per_channel_decay = True
-    return case
+    """The case with one decay per key channel (a copy; see the workloads module)."""
+    return workloads.with_per_channel_decay(case, seed)
 
 
 @pytest.mark.parametrize("name", ["ragged_bf16_d128_states", "bf16_slow_decay_long",
