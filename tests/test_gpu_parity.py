@@ -426,6 +426,34 @@ def test_chunked_per_channel_decay_wide_spread():
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("name", ["tc_gqa_R4", "tc_mha_R1"])
+def test_chunked_per_channel_decay_with_checkpoint_options(name):
+    """Per-channel decay on the chunked path with the tiled value-to-key map and
+    the decay coefficient given directly (the prep and the scan both look up a
+    value head's key head, and the prep forms the decays from the coefficient)."""
+    case = _per_channel(_with_options(PREFILL_CASES[name](), "tiled", "coef"), seed=99)
+    ref = run_oracle(case)
+    got = _chunked_per_channel(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+
+
+def test_chunked_per_channel_decay_in_place_states():
+    """Final state over the initial one, new conv history over the old one."""
+    case = _per_channel(PREFILL_CASES["ragged_bf16_d128_states"](), seed=100)
+    ref = run_oracle(case)
+    gdn.timing_enable(True)
+    try:
+        got = gpu_prefill(case, in_place=True)
+        names = gdn.timing_report()
+    finally:
+        gdn.timing_enable(False)
+    assert "chunk_prep_kda" in names
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
 def test_full_size_chunked_per_channel_decay_T4096():
     """The 4,096-token Qwen3-Next-shaped prefill with one decay per key channel
     (gate inputs a [T, 32 x 128] ~ N(0, 1), dt_bias [32 x 128] ~ N(0, 0.1))."""

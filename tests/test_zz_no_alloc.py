@@ -127,6 +127,20 @@ def test_noalloc_call_allocates_no_device_memory():
     assert rel_err(st_out, ref_st.cpu().numpy()) < TOL["bf16"]
 
 
+def test_noalloc_per_channel_decay_matches_the_oracle():
+    """Per-channel decay through the entry point that allocates nothing: its
+    chunked form (its own prep, wider workspace rows) on the built-in array."""
+    case = workloads.with_per_channel_decay(_case(46, [150, 33]), seed=47)
+    t = upload(case)
+    status, out, st, cs = _noalloc(case, t)
+    assert status == gdn.GDN_OK, gdn.load().gdn_last_error().decode()
+    ref = run_oracle(case)
+    assert rel_err(out, ref["out"]) <= TOL["bf16"]
+    assert rel_err(st, ref["state"]) <= TOL["bf16"]
+    assert rel_err(cs.float(), ref["conv_state"]) == 0.0
+    assert gdn.device_error(reset=True) == 0
+
+
 def test_noalloc_refuses_a_layout_beyond_its_scratch():
     lib = gdn.load()
     limit = int(lib.gdn_prefill_noalloc_scratch_bytes())
