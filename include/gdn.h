@@ -309,7 +309,9 @@ size_t gdn_timing_report(char* buf, size_t buf_len);
  * whose waits are bounded (the tensor-core prefill waits on its own TMA copies
  * and MMAs) give up after ~2 s instead of hanging, store a nonzero code here
  * (1..12 name the tensor-core prefill's wait that gave up, 11 being a fused
- * launch's wait for a chunk's prep rows; 20..23 the projection GEMM's; 30 the
+ * launch's wait for a chunk's prep rows; 13 and 14 its per-channel decay prep's
+ * waits for its tiles, and for its v tile, products and the next item's tiles;
+ * 20..23 the projection GEMM's; 30 the
  * token-recurrent kernel's wait for a state copy) and exit cleanly; their
  * outputs are then invalid.  Waits for the device (cudaMemcpyFromSymbol), writes the code to
  * *code (0 = no error) and clears it when reset != 0.
