@@ -682,6 +682,18 @@ def test_full_size_varlen_prefill_all_sequences(slow):
     assert rel_err(got["conv_state"].float(), ref["conv_state"]) == 0.0
 
 
+def test_full_size_varlen_per_channel_decay():
+    """The 16-sequence workload with one decay per key channel: 32,480 (chunk,
+    value head) items, about 214 for each of the prep's persistent CTAs, then
+    the per-channel scan; every sequence against the oracle."""
+    case = _per_channel(workloads.config(3), seed=101)
+    got = _chunked_per_channel(case)
+    ref = run_oracle(case)
+    assert rel_err(got["out"], ref["out"]) <= TOL["bf16"]
+    assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
+    assert rel_err(got["conv_state"].float(), ref["conv_state"]) == 0.0
+
+
 def test_full_size_decode_256():
     case = workloads.config(2)
     ref = run_oracle(case)
