@@ -436,6 +436,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_params* params, int32_t n
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
         c.cu_seqlens = cu_seqlens; c.x = x; c.conv_state_in = conv_state_in;
         c.conv_state_out = conv_state_out;
+        c.pdl = 1;  // after the recurrent kernel: starts in its tail
         if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
             return st;
     }
@@ -487,6 +488,7 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_params* params, int32_t n_
         c.d_k = dims->d_k; c.d_v = dims->d_v; c.conv_k = dims->conv_k;
         c.cu_seqlens = nullptr; c.uniform_T = T; c.x = x;
         c.conv_state_in = conv_state; c.conv_state_out = conv_state;
+        c.pdl = 1;  // starts in the recurrent kernel's tail
         if ((st = cuda_status(timed_launch("conv_state", s, [&] { return gdn::launch_conv_state(c, bf16, s); }), fn, "conv state launch")) != GDN_OK)
             return st;
     }

@@ -478,6 +478,9 @@ __global__ void conv_state_vec_kernel(ConvStateArgs p) {
                 nw.v[e * KEEP + s] = j == 0 ? old.v[e * KEEP] : (j == 1 ? old.v[e * KEEP + 1] : old.v[e * KEEP + 2]);
         }
     }
+    // a programmatic dependent stores only once the preceding grid, which may
+    // still read the old history, has completed
+    if (p.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
     uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.conv_state_out) + blk);
 #pragma unroll
     for (int i = 0; i < KEEP; ++i) dst[i] = nw.u[i];
@@ -491,11 +494,19 @@ cudaError_t launch_conv_state(const ConvStateArgs& p, bool bf16, cudaStream_t st
     if (p.conv_k == 4 && cd % vec == 0 && al16(p.x) && al16(p.conv_state_out) &&
         (!p.conv_state_in || al16(p.conv_state_in))) {
         dim3 grid((cd / vec + 255) / 256, p.n_seq);
-        if (bf16)
-            conv_state_vec_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
-        else
-            conv_state_vec_kernel<float><<<grid, 256, 0, stream>>>(p);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        if (p.pdl) {
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+        }
+        return bf16 ? cudaLaunchKernelEx(&cfg, conv_state_vec_kernel<__nv_bfloat16>, p)
+                    : cudaLaunchKernelEx(&cfg, conv_state_vec_kernel<float>, p);
     }
     dim3 grid((cd + 255) / 256, p.n_seq);
     if (bf16)

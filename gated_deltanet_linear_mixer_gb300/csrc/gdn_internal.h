@@ -54,6 +54,10 @@ struct ConvStateArgs {
     const void* x;
     const void* conv_state_in;  // or null (zeros)
     void* conv_state_out;
+    // Launched as the programmatic dependent of the preceding kernel (which may
+    // let it start early): its loads come first, its stores after that kernel
+    // has completed.
+    int pdl;
 };
 
 struct RecurrentArgs {

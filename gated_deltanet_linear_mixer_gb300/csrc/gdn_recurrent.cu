@@ -73,6 +73,10 @@ recurrent_kernel(RecurrentArgs p) {
     constexpr int CH = 2 * DK + DV;      // channels this head reads: q | k | v
     constexpr int NW = kRecThreads / 32;
     static_assert(DK % RG == 0 && RPT >= 1, "unsupported head dims");
+    // A conv-history update launched after this kernel as its programmatic
+    // dependent may start on SMs this grid leaves free: it only reads what this
+    // kernel reads before waiting for the grid's completion to store.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     __shared__ float cbuf[kRecTokBlock][CH];
     __shared__ float gam[kRecTokBlock], bet[kRecTokBlock], kqs[kRecTokBlock];
