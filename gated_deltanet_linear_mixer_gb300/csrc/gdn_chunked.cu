@@ -493,6 +493,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_const
                   const __grid_constant__ CUtensorMap map_kqh, const __grid_constant__ CUtensorMap map_kql,
                   const __grid_constant__ CUtensorMap map_kwh, const __grid_constant__ CUtensorMap map_kwl,
                   ChunkArgs p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the scan may start in our tail
     chunk_prep_body(map_qh, map_ql, map_wh, map_wl, map_kqh, map_kql, map_kwh, map_kwl, p,
                     blockIdx.x, gridDim.x);
 }
@@ -881,6 +882,16 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
                 sy.n_p6 += 1;
                 return true;
             };
+            // Two-kernel launch of the scalar form: this scan is the prep's
+            // programmatic dependent and may start in the prep's tail; its
+            // first copy of prep rows waits for the prep grid's completion (and
+            // its writes).  Nothing else this CTA reads before then is written
+            // by the prep.  (Without a pending prerequisite the wait returns at
+            // once: the per-channel scan is launched after its prep.)
+            if (!p.ready) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                fence_proxy_async_global();  // the rows are read by TMA (the async proxy)
+            }
             bool ok = wait_chunk(0);
             if (ok) {
                 issue_ug(0);
@@ -1298,6 +1309,24 @@ static int sm_count() {
     return cached[dev].load();
 }
 
+// A scan launch as the programmatic dependent of the prep kernel before it
+// (which triggers at its start): its CTAs may start setting up on SMs the prep
+// has left; the copy lane waits for the prep grid before reading its rows.
+template <typename Kernel, typename... Args>
+static cudaError_t launch_after_prep(Kernel kernel, dim3 grid, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kScanThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
     const ChunkLayout& l = a.layout;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -1424,6 +1453,9 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
             if (e != cudaSuccess) return e;
         }
         return timed_launch("chunk_scan_kda", st, [&] {
+            // launched after its prep completes: as a dependent starting in the
+            // prep's tail, its 64 CTAs measured slower (641 -> 650 us a step),
+            // all placed on the SMs that happened to finish first
             chunk_scan_kda_kernel<<<dim3(hv_n * kSplit, a.n_seq), kScanThreads, scan_smem_kda, st>>>(
                 m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p);
             return cudaGetLastError();
@@ -1460,9 +1492,8 @@ cudaError_t launch_chunked_prefill(const ChunkLaunch& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     e = timed_launch("chunk_scan", st, [&] {
-        chunk_scan_kernel<<<dim3(hv_n * kSplit, a.n_seq), kScanThreads, scan_smem, st>>>(
-            m_qh, m_ql, m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p);
-        return cudaGetLastError();
+        return launch_after_prep(chunk_scan_kernel, dim3(hv_n * kSplit, a.n_seq), scan_smem, st, m_qh, m_ql,
+                                 m_wh, m_wl, m_kqh, m_kql, m_kwh, m_kwl, m_z, p);
     });
     return e;
 }
