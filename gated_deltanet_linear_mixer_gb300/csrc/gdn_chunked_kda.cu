@@ -27,7 +27,10 @@
 //   Gram    A and M o QK^T as above; M -> workspace
 //   solve   T = (I + A)^-1 (fp32, blocked)
 //   [W | U~] = (T diag(beta)) [K o e^G | V] on tcgen05 -> workspace
-// Barriers are CTA-wide (__syncthreads), the solve's its own (four warps).
+// Barriers are CTA-wide (__syncthreads) up to the Gram; from the solve to the
+// item's end two groups of four warps run apart (named barriers 2 and 3): one
+// solves, issues the products and writes W and U~ out, the other forms the
+// next item's decays.
 #include <algorithm>
 #include <atomic>
 
@@ -131,14 +134,14 @@ __device__ __forceinline__ float softplus_fast(float x) {
 //   M_ts += sum_i (q_t,i e^{G_t,i-G_r,i}) (k_s,i e^{G_r,i-G_s,i})
 // as m16n8k16 products of split operands (the row operands formed once for
 // all the tiles); A (times beta_t) and M are stored.
-constexpr int NT = 4;  // at most four tiles a warp; n of them used
-__device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const int (&cols)[NT], int n, int lane) {
+constexpr int kKdaTiles = 4;  // column tiles a warp takes at most (n of them used)
+__device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const int (&cols)[kKdaTiles], int n, int lane) {
     const float* sG = reinterpret_cast<const float*>(smem + kKg);
     const float* sBeta = reinterpret_cast<const float*>(smem + kKb);
     float* sA = reinterpret_cast<float*>(smem + kKa);
     const int g = lane >> 2, q = lane & 3;
     const int r = 16 * bt, ta = r + g, tb = ta + 8;
-    float dA[NT][4] = {}, dM[NT][4] = {};
+    float dA[kKdaTiles][4] = {}, dM[kKdaTiles][4] = {};
 #pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
         const int i0 = 16 * kk + 2 * q, i1 = i0 + 8;
@@ -158,7 +161,7 @@ __device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const in
         left(ta, i1, gr1, 2);
         left(tb, i1, gr1, 3);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
+        for (int j = 0; j < kKdaTiles; ++j) {
             if (j >= n) break;
             const int s = cols[j] + g;
             const float2 gs0 = *reinterpret_cast<const float2*>(sG + kda_g(s, i0));
@@ -177,7 +180,7 @@ __device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const in
     }
     const float ba = sBeta[ta], bb = sBeta[tb];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
+    for (int j = 0; j < kKdaTiles; ++j) {
         if (j >= n) break;
         const int c0 = cols[j] + 2 * q;
         *reinterpret_cast<float2*>(sA + ta * kC + swz_col(ta, c0)) = make_float2(ba * dA[j][0], ba * dA[j][1]);
@@ -446,7 +449,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
             // 8-column tiles of the blocks before it), then the diagonal blocks
             // on every warp (one row pair of each block)
             if (warp < 4) {
-                int cols[NT] = {8 * (warp & 1), 16 + 8 * (warp & 1), 32 + 8 * (warp & 1), 0};
+                int cols[kKdaTiles] = {8 * (warp & 1), 16 + 8 * (warp & 1), 32 + 8 * (warp & 1), 0};
                 if (warp == 2) cols[0] = 0, cols[1] = 8, cols[2] = 16, cols[3] = 24;
                 if (warp == 3) cols[0] = 0, cols[1] = 8;
                 kda_gram_offdiag(smem, warp < 2 ? 3 : warp == 2 ? 2 : 1, cols, warp < 2 ? 3 : warp == 2 ? 4 : 2,
