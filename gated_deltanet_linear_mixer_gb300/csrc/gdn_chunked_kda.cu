@@ -117,6 +117,25 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     }
     return v[0];
 }
+// The special functions of this kernel: the approximate exponential, base-2
+// logarithm and reciprocal in their flush-to-zero forms.  Their non-flushing
+// forms measured 13% slower over the prep (results that would be subnormal,
+// below 1.2e-38, become 0: nothing here is that small and still counts).
+__device__ __forceinline__ float exp_ftz(float x) {  // e^x = 2^(x log2 e)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+__device__ __forceinline__ float log_ftz(float x) {  // ln x = log2 x ln 2
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y * 0.6931471805599453f;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // softplus(x) = log(1 + e^x) with the fast exponential and logarithm: log1p
 // by Kahan's identity log1p(y) = y log(u) / (u - 1), u = fl(1 + y) (Goldberg,
 // "What every computer scientist should know about floating-point arithmetic",
@@ -124,8 +143,8 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
 // identity x above 20, as for the scalar gates.  About 1e-6 relative.
 __device__ __forceinline__ float softplus_fast(float x) {
     if (x > 20.f) return x;
-    const float y = __expf(x), u = 1.f + y;
-    return u == 1.f ? y : __logf(u) * __fdividef(y, u - 1.f);
+    const float y = exp_ftz(x), u = 1.f + y;
+    return u == 1.f ? y : log_ftz(u) * (y * rcp_ftz(u - 1.f));
 }
 
 // Off-diagonal Gram blocks of key block b_t against n <= 4 8-column tiles cols[j]
@@ -150,7 +169,7 @@ __device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const in
         SplitA aq, ak;
         auto left = [&](int t, int i, float2 gr, int slot) {
             const float2 gt = *reinterpret_cast<const float2*>(sG + kda_g(t, i));
-            const float e0 = __expf(gt.x - gr.x), e1 = __expf(gt.y - gr.y);
+            const float e0 = exp_ftz(gt.x - gr.x), e1 = exp_ftz(gt.y - gr.y);
             const uint32_t o = kda_el(t, i);
             const float2 qv = kda_ld2(smem + kKq, o), kv = kda_ld2(smem + kKk, o);
             split2(qv.x * e0, qv.y * e1, aq.h[slot], aq.l[slot]);
@@ -168,8 +187,8 @@ __device__ __forceinline__ void kda_gram_offdiag(uint8_t* smem, int bt, const in
             const float2 gs1 = *reinterpret_cast<const float2*>(sG + kda_g(s, i1));
             const float2 k0 = kda_ld2(smem + kKk, kda_el(s, i0)), k1 = kda_ld2(smem + kKk, kda_el(s, i1));
             SplitB b;
-            split2(k0.x * __expf(gr0.x - gs0.x), k0.y * __expf(gr0.y - gs0.y), b.h[0], b.l[0]);
-            split2(k1.x * __expf(gr1.x - gs1.x), k1.y * __expf(gr1.y - gs1.y), b.h[1], b.l[1]);
+            split2(k0.x * exp_ftz(gr0.x - gs0.x), k0.y * exp_ftz(gr0.y - gs0.y), b.h[0], b.l[0]);
+            split2(k1.x * exp_ftz(gr1.x - gs1.x), k1.y * exp_ftz(gr1.y - gs1.y), b.h[1], b.l[1]);
             mma16816(dA[j], ak.h, b.h[0], b.h[1]);
             mma16816(dA[j], ak.h, b.l[0], b.l[1]);
             mma16816(dA[j], ak.l, b.h[0], b.h[1]);
@@ -227,7 +246,7 @@ __device__ __forceinline__ void kda_gram_diag(uint8_t* smem, int b, int w, int l
         float pa = 0.f, pm = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float x = ks[e] * __expf((ra ? ga[e] : gb[e]) - gsv[e]);
+            const float x = ks[e] * exp_ftz((ra ? ga[e] : gb[e]) - gsv[e]);
             pa = fmaf(ra ? ka[e] : kb[e], x, pa);
             pm = fmaf(ra ? qa[e] : qb[e], x, pm);
         }
@@ -273,7 +292,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar_qk, bar_v, bar_mma;
+    __shared__ __align__(8) uint64_t bar_qk, bar_v, bar_a, bar_mma;
     __shared__ uint32_t tmem_slot;
     float* sG = reinterpret_cast<float*>(smem + kKg);
     float* sBeta = reinterpret_cast<float*>(smem + kKb);
@@ -288,6 +307,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
     if (tid == 0) {
         mbar_init(&bar_qk, 1);
         mbar_init(&bar_v, 1);
+        mbar_init(&bar_a, 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
         for (const CUtensorMap* m : {&map_qh, &map_ql, &map_kqh, &map_kql, &map_a}) tma_prefetch_desc(m);
@@ -297,17 +317,14 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;  // W in columns 0..127, U~ in 128..255
-    uint32_t qk_phase = 0, v_phase = 0, mma_phase = 0;
-    bool qk_pending = false, v_pending = false, mma_pending = false;
+    uint32_t qk_phase = 0, v_phase = 0, a_phase = 0, mma_phase = 0;
+    bool qk_pending = false, v_pending = false, a_pending = false, mma_pending = false;
 
-    // q, k tiles of item it's key head and the gate input of its value head;
-    // the v tile
+    // q, k tiles of item it's key head; the v tile and the gate input of its
+    // value head
     auto issue_qk = [&](int it) {
         const int t0i = p.chunk_info[it / hv_n].x, hk = key_head(it % hv_n, R, hk_n, p.head_map);
-        mbar_arrive_expect_tx(&bar_qk, 10 * 8192);
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-            tma_load_2d(smem + kKgate + b * 8192, &map_a, &bar_qk, (it % hv_n) * kD + 64 * b, t0i);
+        mbar_arrive_expect_tx(&bar_qk, 8 * 8192);
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -316,6 +333,13 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
                 tma_load_2d(smem + kKq + m * 32768 + b * 8192, &map_qh, &bar_qk, col, t0i);
                 tma_load_2d(smem + kKq + m * 32768 + 16384 + b * 8192, &map_ql, &bar_qk, col, t0i);
             }
+    };
+    auto issue_gate = [&](int it) {
+        const int t0i = p.chunk_info[it / hv_n].x;
+        mbar_arrive_expect_tx(&bar_a, 2 * 8192);
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            tma_load_2d(smem + kKgate + b * 8192, &map_a, &bar_a, (it % hv_n) * kD + 64 * b, t0i);
     };
     auto issue_v = [&](int it) {
         const int t0i = p.chunk_info[it / hv_n].x, col = 2 * hk_n * kD + (it % hv_n) * kD;
@@ -328,10 +352,11 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
     };
     if ((int)blockIdx.x < n_items) {
         if (tid == 0) {
+            issue_gate(blockIdx.x);
             issue_qk(blockIdx.x);
             issue_v(blockIdx.x);
         }
-        qk_pending = v_pending = true;
+        qk_pending = v_pending = a_pending = true;
     }
     // rows past the chunk (another sequence's, or padding) of nb 8 KB blocks from base: zero
     auto zero_tail_rows = [&](uint32_t base, int nb, int L) {
@@ -387,8 +412,22 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
             qk_pending = false;
             qk_phase ^= 1;
             if (item == (int)blockIdx.x) {  // the first item's raw decays (later ones: during a solve)
+                const bool got_a = mbar_wait(&bar_a, a_phase);
+                if (kda_any(!got_a)) {
+                    if (tid == 0) report_kda_error(13);
+                    failed = true;
+                    break;
+                }
+                a_phase ^= 1;
+                a_pending = false;
                 raw_g(item, tid);
                 __syncthreads();
+            }
+            // the gate tile has been read: the next item's may land now (its
+            // raw decays are formed once the Gram has released the G tile)
+            if (next < n_items) {
+                if (tid == 0) issue_gate(next);
+                a_pending = true;
             }
             if (L < kC) zero_tail_rows(kKq, 8, L);
             // G: per-channel prefix sums of the raw decays, the second half of
@@ -434,10 +473,10 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
                 float ke[8], qe[8], kl[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float eg = __expf(gt[e]);
+                    const float eg = exp_ftz(gt[e]);
                     ke[e] = k8[e] * eg;
                     qe[e] = q8[e] * eg;
-                    kl[e] = k8[e] * __expf(gl[e] - gt[e]);
+                    kl[e] = k8[e] * exp_ftz(gl[e] - gt[e]);
                 }
                 split_store(ke, smem + kKe + off, smem + kKe + 16384 + off);
                 const size_t qrow = ((size_t)p.qt_row0 + wr + t) * kD + 8 * c8;
@@ -470,7 +509,8 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
             // 0, 1, 4, 5 (the accumulator lanes 0..63 are theirs) solve, split T,
             // issue the products and write W and U~ out, on named barriers 2
             // and 3; warps 2, 3, 6, 7 form the next item's raw decays (the G tile
-            // is no longer read) once its tiles, gate input included, land.
+            // is no longer read) once its gate tile, issued at this item's
+            // start, has landed.
             bool ok = true;
             if ((warp & 3) < 2) {
                 const int w4 = (warp & 1) | ((warp >> 2) << 1), c128 = 32 * w4 + lane;
@@ -555,7 +595,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
                 }
             } else if (next < n_items) {
                 const int j0 = 32 * ((warp & 1) | ((warp >> 2) << 1)) + lane;
-                ok = mbar_wait(&bar_qk, qk_phase);
+                ok = mbar_wait(&bar_a, a_phase);
                 if (ok) {
                     raw_g(next, j0);
                     raw_g(next, j0 + 128);
@@ -567,6 +607,10 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
                 failed = true;
                 break;
             }
+            if (next < n_items) {  // the raw-decay warps took the next item's gate tile
+                a_phase ^= 1;
+                a_pending = false;
+            }
         } while (false);
         if (failed) break;
     }
@@ -574,6 +618,7 @@ chunk_prep_kda_kernel(const __grid_constant__ CUtensorMap map_qh, const __grid_c
     // Unwind (also after a give-up): in-flight copies and MMAs land first.
     if (tid == 0) {
         if (qk_pending) mbar_wait(&bar_qk, qk_phase);
+        if (a_pending) mbar_wait(&bar_a, a_phase);
         if (v_pending) mbar_wait(&bar_v, v_phase);
     }
     if (kda_any(mma_pending) && tid == 0) mbar_wait(&bar_mma, mma_phase);
