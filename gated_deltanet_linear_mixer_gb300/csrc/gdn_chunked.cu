@@ -199,8 +199,8 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
         sG[warp * kC + s1] = excl + g0 + g1;
         sBeta[warp * kC + s0] = b0;
         sBeta[warp * kC + s1] = b1;
-        sCs1[warp * kC + s0] = b0 * __expf(excl + g0);
-        sCs1[warp * kC + s1] = b1 * __expf(excl + g0 + g1);
+        sCs1[warp * kC + s0] = b0 * exp_ftz(excl + g0);
+        sCs1[warp * kC + s1] = b1 * exp_ftz(excl + g0 + g1);
         sCs2[warp * kC + s0] = b0;
         sCs2[warp * kC + s1] = b1;
     }
@@ -296,7 +296,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int s = q8 * 8 + e;
-                                f[e] = s <= t ? __expf(Gt - Gr[s]) * v[s] : 0.f;
+                                f[e] = s <= t ? exp_ftz(Gt - Gr[s]) * v[s] : 0.f;
                             }
                             const uint32_t o = sw128_offset(t, q8);
                             split_store(f, st + o, st + 8192 + o);
@@ -311,7 +311,7 @@ __device__ __forceinline__ void chunk_prep_body(const CUtensorMap& map_qh, const
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const int s = 4 * c4 + e;
-                                f[e] = s < t ? bt * __expf(Gt - Gr[s]) * v[s] : 0.f;
+                                f[e] = s < t ? bt * exp_ftz(Gt - Gr[s]) * v[s] : 0.f;
                             }
                             *reinterpret_cast<float4*>(sA + ((c4 ^ (t & 15)) << 2)) =
                                 make_float4(f[0], f[1], f[2], f[3]);
@@ -991,7 +991,7 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
 #pragma unroll
                 for (int j = 0; j < 32; ++j) a[j] += b[j];
             }
-            const float eg = __expf(gt_pend);
+            const float eg = exp_ftz(gt_pend);
             oss = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -1056,14 +1056,14 @@ __device__ __forceinline__ void chunk_scan_body(const CUtensorMap& map_qh, const
             const float* gc = sGc + (c & 1) * kC;
             // state decay over chunk c (of this thread's key row, per-channel decay)
             const float gam = !alive ? 0.f
-                              : kKda ? __expf(reinterpret_cast<const float*>(smem + kScanGl)[(c & 1) * kD + row])
-                                     : __expf(gc[chunk_len(c) - 1]);
+                              : kKda ? exp_ftz(reinterpret_cast<const float*>(smem + kScanGl)[(c & 1) * kD + row])
+                                     : exp_ftz(gc[chunk_len(c) - 1]);
             float gt_next = 0.f;
             if (!kKda && !is_u && alive) gt_next = gc[row - 64];
             bool out_ok = false;
             if (is_u) {
                 // U_c = U~ - W S_c (rows 0..63 of P4_c), U'_c = e^{G_last-G_t} U_c
-                const float eu = kKda ? 1.f : __expf(gc[chunk_len(c) - 1] - gc[row]);
+                const float eu = kKda ? 1.f : exp_ftz(gc[chunk_len(c) - 1] - gc[row]);
                 float ut[32];
                 const float4* us4 = reinterpret_cast<const float4*>(smem + kScanUt) + ((cl >> 2) * kC + row);
 #pragma unroll

@@ -117,25 +117,6 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     }
     return v[0];
 }
-// The special functions of this kernel: the approximate exponential, base-2
-// logarithm and reciprocal in their flush-to-zero forms.  Their non-flushing
-// forms measured 13% slower over the prep (results that would be subnormal,
-// below 1.2e-38, become 0: nothing here is that small and still counts).
-__device__ __forceinline__ float exp_ftz(float x) {  // e^x = 2^(x log2 e)
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
-    return y;
-}
-__device__ __forceinline__ float log_ftz(float x) {  // ln x = log2 x ln 2
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y * 0.6931471805599453f;
-}
-__device__ __forceinline__ float rcp_ftz(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 // softplus(x) = log(1 + e^x) with the fast exponential and logarithm: log1p
 // by Kahan's identity log1p(y) = y log(u) / (u - 1), u = fl(1 + y) (Goldberg,
 // "What every computer scientist should know about floating-point arithmetic",

@@ -71,13 +71,31 @@ template <> struct Vec16<__nv_bfloat16> {
 
 // ------------------------------------------------------------- the method's
 // scalar functions (qwen.rs DeltaRule::run / gdn_forward; cpu.rs deltanet)
-// sigmoid and SiLU use the hardware exponential and an approximate divide
-// (__expf, __fdividef): relative error ~1e-6 over the range the gates see,
-// far below both tolerances, at a fraction of the precise functions' cost.
-// For x below about -87 the divisor overflows and __fdividef returns 0 (the
-// exact values are below 1e-37 there).
-__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// The hardware's approximate exponential, base-2 logarithm and reciprocal, in
+// their flush-to-zero forms: the non-flushing forms (what __expf, __logf and
+// __fdividef compile to) measured slower in the exponential-heavy kernels.
+// Results that would be subnormal (below 1.2e-38) become 0.
+__device__ __forceinline__ float exp_ftz(float x) {  // e^x = 2^(x log2 e)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+__device__ __forceinline__ float log_ftz(float x) {  // ln x = log2 x ln 2
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y * 0.6931471805599453f;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// sigmoid and SiLU with those: relative error ~1e-6 over the range the gates
+// see, far below both tolerances, at a fraction of the precise functions'
+// cost.  For x below about -88 e^-x overflows and the reciprocal is 0 (the
+// exact values are below 1e-38 there).
+__device__ __forceinline__ float sigmoidf_(float x) { return rcp_ftz(1.0f + exp_ftz(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x * rcp_ftz(1.0f + exp_ftz(-x)); }
 // softplus: identity above 20, else ln(1 + e^x)
 __device__ __forceinline__ float softplusf_(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 __device__ __forceinline__ float gatef_(float z, int act) {
