@@ -44,19 +44,19 @@ METRIC = "GDN prefill tokens/s and decode tokens/s (1 GB300) + % of roofline"
 # by the units it processes, and the source says so.  An entry is removed when
 # its kernel changes, until it is captured again.
 TRAFFIC = {
-    ("prefill", "chunk_fused"): (214_530_000 + 192_850_000, "ncu capture of this workload's launch"),
-    ("layer", "chunk_fused"): (214_530_000 + 192_850_000,
+    ("prefill", "chunk_fused"): (259_900_000 + 202_250_000, "ncu capture of this workload's launch"),
+    ("layer", "chunk_fused"): (259_900_000 + 202_250_000,
                                "ncu capture of the same launch in the T=4096 prefill workload"),
     # 64-sequence decode step; the traffic is per sequence: x 256/64
-    ("decode", "recurrent"): ((139_130_000 + 72_580_000) * 4,
+    ("decode", "recurrent"): ((139_130_000 + 72_380_000) * 4,
                               "ncu capture of the 64-sequence decode step, scaled x 256/64"),
-    ("spec_verify", "recurrent"): (144_210_000 + 476_380_000, "ncu capture of this workload's launch"),
+    ("spec_verify", "recurrent"): (144_420_000 + 476_470_000, "ncu capture of this workload's launch"),
     # the step's two launches under one name: the read-only verify and the replay
-    ("spec_replay", "recurrent"): (((143_890_000 + 3_270_000) + (140_710_000 + 72_830_000)) // 2,
+    ("spec_replay", "recurrent"): (((143_920_000 + 3_660_000) + (140_710_000 + 73_090_000)) // 2,
                                    "ncu captures of the step's two launches (verify, replay), averaged"),
-    ("kda_prefill", "chunk_prep_kda"): (168_566_528 + 245_094_400, "ncu capture of this workload's launch"),
+    ("kda_prefill", "chunk_prep_kda"): (168_550_000 + 244_610_000, "ncu capture of this workload's launch"),
     # 16 sequences of 128..1024 tokens (149 chunks); the traffic is per chunk: x 1015/149
-    ("varlen", "chunk_scan"): (round((657_540_000 + 91_300_000) * 1015 / 149),
+    ("varlen", "chunk_scan"): (round((657_530_000 + 91_200_000) * 1015 / 149),
                                "ncu capture of a 149-chunk varlen case, scaled x 1015/149 chunks"),
 }
 UNIT = "tokens/s"
