@@ -367,10 +367,20 @@ def _per_channel(case, seed):
                                   "f32_slow_decay", "tc_gqa_R8"])
 def test_prefill_per_channel_decay_matches_oracle(name):
     """One decay per key channel: the token-recurrent kernel (fp32) and the
-    chunked tensor-core path (bf16, d_k = d_v = 128)."""
+    chunked tensor-core path (bf16, d_k = d_v = 128); the kernels that ran are
+    checked, then the results against the oracle."""
     case = _per_channel(PREFILL_CASES[name](), seed=91)
     ref = run_oracle(case)
-    got = gpu_prefill(case)
+    gdn.timing_enable(True)
+    try:
+        got = gpu_prefill(case)
+        names = gdn.timing_report()
+    finally:
+        gdn.timing_enable(False)
+    if case.dtype == "bf16" and case.d_k == 128 and case.d_v == 128:
+        assert "chunk_prep_kda" in names and "chunk_scan_kda" in names and "recurrent" not in names, names
+    else:
+        assert "recurrent" in names and "chunk_prep_kda" not in names, names
     tol = TOL[case.dtype]
     assert rel_err(got["out"], ref["out"]) <= tol
     assert rel_err(got["state"], ref["state"]) <= tol
