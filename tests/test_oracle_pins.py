@@ -299,6 +299,27 @@ def test_recurrence_equals_independent_chunked_form(chunk, slow):
     assert np.max(np.abs(s1 - s2)) / np.sqrt(np.mean(s1 ** 2)) < 1e-10
 
 
+@pytest.mark.parametrize("chunk", [4, 16])
+@pytest.mark.parametrize("spread", [1.0, 30.0])
+def test_per_channel_recurrence_equals_independent_chunked_form(chunk, spread):
+    """One decay per key channel: the token recurrence against the chunked form
+    with per-channel pairwise decay factors (oracle/chunked.py), on decays of
+    ordinary size and on decays spread over orders of magnitude between the
+    channels (per-token log-decays down to -spread)."""
+    d = oracle.Dims(2, 4, 8, 6, 4, "silu", per_channel_decay=True)
+    rng = np.random.default_rng(int(chunk + spread))
+    cu = [0, 37, 53, 54, 77]
+    t = cu[-1]
+    q = rng.normal(size=(t, 2, 8)); k = _unit_rows(rng, t, 2, 8); v = rng.normal(size=(t, 4, 6))
+    g = -spread * rng.uniform(0, 1, size=(t, 4, 8)) ** 3
+    beta = rng.uniform(0, 1, size=(t, 4))
+    s0 = rng.normal(size=(4, 4, 8, 6))
+    o, s1, _ = oracle.recurrence(d, cu, q, k, v, g, beta, s0)
+    o2, s2 = chunked.recurrence_chunked(cu, q, k, v, g, beta, s0, chunk=chunk)
+    assert np.max(np.abs(o - o2)) / np.sqrt(np.mean(o ** 2)) < 1e-10
+    assert np.max(np.abs(s1 - s2)) / np.sqrt(np.mean(s1 ** 2)) < 1e-10
+
+
 def test_recurrence_is_jointly_linear_in_state_and_values():
     d = _dims(hk=2, hv=4, dk=8, dv=6)
     rng = np.random.default_rng(41)
