@@ -83,7 +83,7 @@ def run_oracle(case, want_inter=False, want_stages=False):
                       want_inter=want_inter, want_stages=want_stages)
 
 
-def gpu_prefill(case, t=None, in_place=False):
+def gpu_prefill(case, t=None, in_place=False, workspace=None):
     d, _ = dims(case)
     t = t or upload(case)
     n = case.n_seq
@@ -103,7 +103,7 @@ def gpu_prefill(case, t=None, in_place=False):
     out = torch.full((case.n_tokens, d.n_v_heads * d.d_v), float("nan"), dtype=d.dtype, device=dev)
     gdn.prefill(d, t["params"], case.cu_seqlens, t["x"], t["z"], t["a"], t["b"],
                 initial_state=st_in, final_state=st_out, conv_state_in=cs_in,
-                conv_state_out=cs_out, out=out)
+                conv_state_out=cs_out, out=out, workspace=workspace)
     torch.cuda.synchronize()
     return {"out": out, "state": st_out, "conv_state": cs_out}
 

@@ -110,6 +110,41 @@ def test_prefill_in_place_states(name):
     assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
 
 
+POISON_CASES = ["ragged_bf16_d128_states", "tc_many_short", "tc_gqa_R3", "tc_mha_R1",
+                "bf16_slow_decay_long"]
+
+
+@pytest.mark.parametrize("mode", ["fused", "two_kernel", "per_channel"])
+@pytest.mark.parametrize("name", POISON_CASES)
+def test_prefill_ignores_stale_workspace(name, mode, monkeypatch):
+    """A workspace whose every byte is 0xFF (NaN in bf16 and fp32, -1 in the
+    chunk table and the item flags) gives the oracle's results on the fused
+    launch, the two-kernel launch and the per-channel decay form: nothing in it
+    is read before this call writes it, and no padding row or masked tile entry
+    reaches an output (a NaN there would survive a multiply by zero)."""
+    monkeypatch.setenv("GDN_PREFILL_FUSED", "0" if mode == "two_kernel" else "1")
+    case = PREFILL_CASES[name]()
+    if mode == "per_channel":
+        case = _per_channel(case, seed=95)
+    ref = run_oracle(case)
+    d, _ = dims(case)
+    need = gdn.prefill_workspace_size(d, case.cu_seqlens)
+    assert need > 0  # the chunked tensor-core path
+    ws = torch.full((need,), 255, dtype=torch.uint8, device="cuda")
+    gdn.timing_enable(True)
+    try:
+        got = gpu_prefill(case, workspace=ws)
+        names = gdn.timing_report()
+    finally:
+        gdn.timing_enable(False)
+    want = {"fused": "chunk_fused", "two_kernel": "chunk_scan", "per_channel": "chunk_scan_kda"}[mode]
+    assert want in names, names
+    tol = TOL[case.dtype]
+    assert rel_err(got["out"], ref["out"]) <= tol
+    assert rel_err(got["state"], ref["state"]) <= tol
+    assert rel_err(got["conv_state"], ref["conv_state"]) == 0.0
+
+
 def test_prefill_without_optional_states():
     """NULL initial state / conv state in, no outputs for them: out still matches."""
     case = _gen("r7", lengths=[50, 3], seed=17)
