@@ -593,7 +593,7 @@ def _layer_inputs(case, hidden, seed, exact=False):
     return h, w
 
 
-def _layer_check(case, hidden, seed, exact=False):
+def _layer_check(case, hidden, seed, exact=False, poison=False):
     d, od = dims(case)
     t = upload(case)
     h, w = _layer_inputs(case, hidden, seed, exact)
@@ -601,9 +601,15 @@ def _layer_check(case, hidden, seed, exact=False):
     n = case.n_seq
     st = torch.full((n, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
     cs = torch.full((n, d.conv_dim, d.conv_k - 1), float("nan"), dtype=d.dtype, device="cuda")
+    out = torch.full((case.n_tokens, hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = None
+    if poison:  # every byte 0xFF: NaN in the bf16/fp32 intermediates, -1 in the tables
+        need = gdn.layer_prefill_workspace_size(d, hidden, case.cu_seqlens)
+        ws = torch.full((need,), 255, dtype=torch.uint8, device="cuda")
     got = gdn.layer_prefill(d, t["params"], proj, case.cu_seqlens, h.cuda(),
                             initial_state=t["state"], final_state=st,
-                            conv_state_in=t["conv_state"], conv_state_out=cs)
+                            conv_state_in=t["conv_state"], conv_state_out=cs, out=out,
+                            workspace=ws)
     torch.cuda.synchronize()
     f = lambda u: u.float().numpy()  # noqa: E731
     ref = oracle.layer(od, case.cu_seqlens, f(h), f(w["w_qkv"]), f(w["w_z"]), f(w["w_a"]),
@@ -620,6 +626,15 @@ def test_layer_prefill_matches_oracle(lengths):
     projections; [5, 9, 16] takes the short-sequence (token-recurrent) core."""
     case = _gen("ly", lengths=lengths, state_std=0.05, conv_state_std=1.0, seed=41)
     _layer_check(case, hidden=256, seed=141)
+
+
+@pytest.mark.parametrize("lengths", [[150, 70, 1], [5, 9, 16]])
+def test_layer_prefill_ignores_stale_workspace(lengths):
+    """The layer from a workspace of 0xFF bytes: the projections' outputs, the
+    core's workspace and the gated-norm rows are all written before they are
+    read, on the tensor-core and the token-recurrent core."""
+    case = _gen("ly", lengths=lengths, state_std=0.05, conv_state_std=1.0, seed=43)
+    _layer_check(case, hidden=256, seed=143, poison=True)
 
 
 def test_layer_prefill_qwen3_next_width():
