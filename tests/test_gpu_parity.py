@@ -655,6 +655,62 @@ def test_full_size_prefill_T4096():
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_max_size_64bit_offsets(per_channel):
+    """One 600,000-token sequence, then a 1,000-token one: the second sequence's
+    element offsets into x (4.9e9), out (2.5e9) and the workspace's U~ rows
+    (2.5e9) pass 2^31, about 70 GB on the device (about 110 GB at the peak with
+    per-channel decay). The oracle checks the short sequence (out, final state,
+    conv history) and the long one's first 200 outputs (they depend only on its
+    first 200 tokens)."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < (150 if per_channel else 100) * 2 ** 30:
+        pytest.skip("not enough free device memory")
+    small = _gen("mx", n_k_heads=16, n_v_heads=32, lengths=[200, 1000], state_std=0.05,
+                 conv_state_std=1.0, seed=47)
+    if per_channel:
+        small = _per_channel(small, seed=96)
+    ref = run_oracle(small)
+    d, _ = dims(small)
+    t_small = upload(small)
+    long_len = 600000
+    total = long_len + 1000
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(47)
+
+    def big(name, width):
+        v = torch.randn((total, width), generator=gen, device="cuda").to(torch.bfloat16)
+        v[:200] = t_small[name][:200]
+        v[long_len:] = t_small[name][200:]
+        return v
+
+    x = big("x", d.conv_dim)
+    z = big("z", d.n_v_heads * d.d_v)
+    a = big("a", d.gate_width)
+    b = big("b", d.n_v_heads)
+    cu = np.array([0, long_len, total], dtype=np.int32)
+    st_out = torch.full((2, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
+    cs_out = torch.full((2, d.conv_dim, d.conv_k - 1), float("nan"), dtype=d.dtype, device="cuda")
+    gdn.timing_enable(True)
+    try:
+        out = gdn.prefill(d, t_small["params"], cu, x, z, a, b, initial_state=t_small["state"],
+                          final_state=st_out, conv_state_in=t_small["conv_state"],
+                          conv_state_out=cs_out)
+        torch.cuda.synchronize()
+        names = gdn.timing_report()
+    finally:
+        gdn.timing_enable(False)
+    del x, z, a, b
+    # two sequences take the scalar form's two-kernel launch (their 128 scan CTAs
+    # leave too few of the 152 slots for a fused prep)
+    assert ("chunk_scan_kda" if per_channel else "chunk_scan") in names, names
+    assert rel_err(out[long_len:], ref["out"][200:]) <= TOL["bf16"]
+    assert rel_err(out[:200], ref["out"][:200]) <= TOL["bf16"]
+    assert rel_err(st_out[1], ref["state"][1]) <= TOL["bf16"]
+    assert torch.isfinite(st_out[0]).all()
+    assert rel_err(cs_out[1], ref["conv_state"][1]) == 0.0
+
+
 def test_full_size_prefill_T4096_slow_decay():
     case = workloads.config(1, slow_decay=True)
     ref = run_oracle(case)
