@@ -711,6 +711,44 @@ def test_max_size_64bit_offsets(per_channel):
     assert rel_err(cs_out[1], ref["conv_state"][1]) == 0.0
 
 
+def test_max_size_decode_64bit_state_offsets():
+    """One decode step of 20,000 sequences (a 42 GB fp32 state, updated in
+    place): the last sequences' state offsets (1.05e10 elements) pass 2^31. The
+    oracle checks two sequences at each end of the batch."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < 80 * 2 ** 30:
+        pytest.skip("not enough free device memory")
+    small = _gen("md", mode="decode", n_seq=4, tokens_per_seq=1, n_k_heads=16, n_v_heads=32,
+                 act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=48)
+    ref = run_oracle(small)
+    d, _ = dims(small)
+    ts = upload(small)
+    n = 20000
+    pick = [0, 1, n - 2, n - 1]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(48)
+
+    def big(src, shape, std=1.0):
+        v = torch.randn(shape, generator=gen, device="cuda")
+        v = v.mul_(std) if src.dtype == torch.float32 else v.to(src.dtype)
+        v[pick] = src.reshape(4, *shape[1:])
+        return v
+
+    vd = d.n_v_heads * d.d_v
+    x = big(ts["x"], (n, 1, d.conv_dim))
+    z = big(ts["z"], (n, 1, vd))
+    a = big(ts["a"], (n, 1, d.gate_width))
+    b = big(ts["b"], (n, 1, d.n_v_heads))
+    state = big(ts["state"], (n, d.n_v_heads, d.d_k, d.d_v), std=0.05)
+    cs = big(ts["conv_state"], (n, d.conv_dim, d.conv_k - 1))
+    out = torch.full((n, 1, vd), float("nan"), dtype=d.dtype, device="cuda")
+    gdn.decode(d, ts["params"], x, z, a, b, state, cs, None, out)
+    torch.cuda.synchronize()
+    assert rel_err(out[pick].reshape(4, vd), ref["out"]) <= TOL["bf16"]
+    assert rel_err(state[pick], ref["state"]) <= TOL["bf16"]
+    assert rel_err(cs[pick], ref["conv_state"]) == 0.0
+
+
 def test_full_size_prefill_T4096_slow_decay():
     case = workloads.config(1, slow_decay=True)
     ref = run_oracle(case)
