@@ -749,6 +749,48 @@ def test_max_size_decode_64bit_state_offsets():
     assert rel_err(cs[pick], ref["conv_state"]) == 0.0
 
 
+def test_max_size_verify_64bit_inter_offsets():
+    """Speculative verify of 2,048 sequences x 4 drafts writing every
+    intermediate state (17 GB): the last sequences' offsets into the
+    intermediates (4.3e9 elements) pass 2^31. The oracle checks two sequences at
+    each end; the resident state and conv history stay as they were."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < 60 * 2 ** 30:
+        pytest.skip("not enough free device memory")
+    small = _gen("mv", mode="decode", n_seq=4, tokens_per_seq=4, n_k_heads=16, n_v_heads=32,
+                 act="sigmoid", state_std=0.05, conv_state_std=1.0, seed=49, want_inter=True)
+    ref = run_oracle(small, want_inter=True)
+    d, _ = dims(small)
+    ts = upload(small)
+    n, tt = 2048, 4
+    pick = [0, 1, n - 2, n - 1]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(49)
+
+    def big(src, shape, std=1.0):
+        v = torch.randn(shape, generator=gen, device="cuda")
+        v = v.mul_(std) if src.dtype == torch.float32 else v.to(src.dtype)
+        v[pick] = src.reshape(4, *shape[1:])
+        return v
+
+    vd = d.n_v_heads * d.d_v
+    x = big(ts["x"], (n, tt, d.conv_dim))
+    z = big(ts["z"], (n, tt, vd))
+    a = big(ts["a"], (n, tt, d.gate_width))
+    b = big(ts["b"], (n, tt, d.n_v_heads))
+    state = big(ts["state"], (n, d.n_v_heads, d.d_k, d.d_v), std=0.05)
+    cs = big(ts["conv_state"], (n, d.conv_dim, d.conv_k - 1))
+    inter = torch.full((n, tt, d.n_v_heads, d.d_k, d.d_v), float("nan"), device="cuda")
+    out = torch.full((n, tt, vd), float("nan"), dtype=d.dtype, device="cuda")
+    gdn.decode(d, ts["params"], x, z, a, b, state, cs, inter, out)
+    torch.cuda.synchronize()
+    assert rel_err(out[pick].reshape(4 * tt, vd), ref["out"]) <= TOL["bf16"]
+    inter_ref = ref["inter"].reshape(4, tt, *ref["inter"].shape[1:])
+    assert rel_err(inter[pick], inter_ref) <= TOL["bf16"]
+    assert rel_err(state[pick], small.state) == 0.0
+    assert rel_err(cs[pick], small.conv_state) == 0.0
+
+
 def test_full_size_prefill_T4096_slow_decay():
     case = workloads.config(1, slow_decay=True)
     ref = run_oracle(case)
