@@ -647,6 +647,14 @@ def test_layer_prefill_qwen3_next_width():
 
 # ---------------------------------------------------------------- full sizes
 
+@pytest.fixture
+def _release_memory():
+    """The maximum-size tests hold 20-110 GB; hand it back to the device after
+    each, so that the tests after them see the memory free."""
+    yield
+    torch.cuda.empty_cache()
+
+
 def test_full_size_prefill_T4096():
     case = workloads.config(1)
     ref = run_oracle(case)
@@ -655,6 +663,7 @@ def test_full_size_prefill_T4096():
     assert rel_err(got["state"], ref["state"]) <= TOL["bf16"]
 
 
+@pytest.mark.usefixtures("_release_memory")
 @pytest.mark.parametrize("per_channel", [False, True])
 def test_max_size_64bit_offsets(per_channel):
     """One 600,000-token sequence, then a 1,000-token one: the second sequence's
@@ -711,6 +720,7 @@ def test_max_size_64bit_offsets(per_channel):
     assert rel_err(cs_out[1], ref["conv_state"][1]) == 0.0
 
 
+@pytest.mark.usefixtures("_release_memory")
 def test_max_size_decode_64bit_state_offsets():
     """One decode step of 20,000 sequences (a 42 GB fp32 state, updated in
     place): the last sequences' state offsets (1.05e10 elements) pass 2^31. The
@@ -749,6 +759,7 @@ def test_max_size_decode_64bit_state_offsets():
     assert rel_err(cs[pick], ref["conv_state"]) == 0.0
 
 
+@pytest.mark.usefixtures("_release_memory")
 def test_max_size_verify_64bit_inter_offsets():
     """Speculative verify of 2,048 sequences x 4 drafts writing every
     intermediate state (17 GB): the last sequences' offsets into the
